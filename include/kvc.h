@@ -1,0 +1,258 @@
+/*
+ * kvc.h -- C ABI of libkvc: KV-cache compression and decode attention over the compressed cache
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [KVC]  "Compressão e Poda Dinâmica de KV Cache: StreamingLLM, SnapKV, PyramidKV e
+ *          DuoAttention" (produtoramaxvision.com.br blog)
+ *   [SINK] "attention sinks" encyclopedia entry (tonho.wtf diário)
+ *   [KVCL] "O KV cache", lesson 7.2 of llmdeepdive, section "01 · Conceito"
+ *
+ * Conventions shared by every entry point
+ *   - Plain C types only.  Every tensor argument is a DEVICE pointer owned by the caller unless
+ *     the comment says "host".  The library never allocates device memory; operations that
+ *     need scratch take a caller-owned workspace whose size is given by a *_workspace_bytes
+ *     query.  Workspaces must be 256-byte aligned.
+ *   - All work is enqueued on the caller's CUDA stream (`stream`, a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  No entry point synchronises except
+ *     kvc_device_status.  Entry points can be captured into a CUDA graph.
+ *   - Every entry point validates its arguments on the host before launching anything and
+ *     returns a kvc_status; on error nothing is launched and kvc_last_error() describes why.
+ *     Values that only exist on the device (lengths, slots, positions) are range-checked by the
+ *     kernels: an out-of-range value skips the access and records a code that
+ *     kvc_device_status() returns.
+ *   - A cache is [batch][n_heads_kv][cap][d_head] with d_head contiguous (see kvc_cache).
+ *     d_head is 64, 128 or 256; base pointers are 16-byte aligned and every stride is a
+ *     multiple of 16 bytes.  Query head h reads KV head h / (n_heads_q / n_heads_kv)
+ *     (grouped-query attention, [KVCL] "01 · Conceito"; [KVC] "O gargalo de memória...").
+ *   - Element types: KVC_F32 (fp32 storage and arithmetic) or KVC_BF16 (bf16 storage, fp32
+ *     arithmetic).  Queries and new keys/values use the cache's type; outputs are fp32.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum value               */
+    KVC_ERR_SHAPE = 2,         /* unsupported or inconsistent sizes (d_head, head groups)    */
+    KVC_ERR_ALIGN = 3,         /* pointer or stride not 16-byte aligned                      */
+    KVC_ERR_CAPACITY = 4,      /* a cache or output is too small for the request             */
+    KVC_ERR_CUDA = 5,          /* a CUDA runtime call failed (message in kvc_last_error)     */
+    KVC_ERR_WORKSPACE = 6,     /* workspace missing, too small or misaligned                 */
+    KVC_ERR_DEVICE = 7         /* a kernel's own range check fired (see kvc_device_status)   */
+} kvc_status;
+
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1 } kvc_dtype;
+
+/* Device-side range-check codes recorded by kernels (first one wins until read). */
+enum {
+    KVC_DEV_OK = 0,
+    KVC_DEV_TAIL_FULL = 1,      /* append at len >= cap                                       */
+    KVC_DEV_BAD_SLOT = 2,       /* free slot outside [0, cap)                                 */
+    KVC_DEV_BAD_INDEX = 3,      /* gather index outside [0, src cap)                          */
+    KVC_DEV_BAD_POSITION = 4,   /* negative text position                                     */
+    KVC_DEV_BAD_LENGTH = 5,     /* len outside [0, cap]                                       */
+    KVC_DEV_NO_CANDIDATE = 6    /* H2O: cache over budget but no historical token to evict    */
+};
+
+/* A KV cache (or a prompt's keys/values) in device memory.
+ * Element (b, h, slot, d) of K is at k + b*stride_b + h*stride_h + slot*stride_slot + d
+ * (strides in elements).  v follows the same strides; v may be NULL where only keys are read. */
+typedef struct {
+    void *k;
+    void *v;
+    int32_t dtype;          /* kvc_dtype */
+    int32_t batch;
+    int32_t n_heads_kv;
+    int32_t cap;            /* slots per (batch, head) */
+    int32_t d_head;
+    int32_t reserved;
+    int64_t stride_b;
+    int64_t stride_h;
+    int64_t stride_slot;
+} kvc_cache;
+
+/* RoPE at in-cache positions for a StreamingLLM cache ([SINK] "como funciona"; [KVC]
+ * "Attention Sinks e o StreamingLLM..."): slots 0..n_sink-1 hold the sinks (text positions
+ * 0..n_sink-1), slots n_sink..n_sink+window form a ring of window+1 slots in which token
+ * a >= n_sink lives at slot n_sink + (a - n_sink) mod (window + 1).  When the token at text
+ * position *t is decoded it attends to the sinks and to tokens max(n_sink, t-window) .. t;
+ * each attended token's in-cache position is its rank in that set and the query's is
+ * min(t, n_sink + window).  Keys are stored before rotation and rotated at those positions on
+ * every call.  Pairing: dimension i with i + d_head/2, angle position * theta^(-2i/d_head).  */
+typedef struct {
+    int32_t n_sink;         /* S  (4 in the pages' configuration)                            */
+    int32_t window;         /* W                                                             */
+    const int64_t *t;       /* device scalar: text position of the token being decoded       */
+    const float *cos_sin;   /* device [n_pos][d_head/2][2] = (cos, sin), see kvc_rope_table  */
+    int32_t n_pos;          /* rows of cos_sin; must be >= n_sink + window + 1               */
+    int32_t reserved;
+} kvc_rope;
+
+/* ---------------------------------------------------------------------------------------- */
+/* Diagnostics                                                                               */
+
+/* Message for the last non-OK status returned on the calling thread ("" if none). */
+const char *kvc_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the device range-check code of the current
+ * device into *code (KVC_DEV_*).  Returns KVC_ERR_DEVICE if a code was set, else KVC_OK. */
+kvc_status kvc_device_status(void *stream, int32_t *code);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Host-side sizing                                                                          */
+
+/* Bytes of an uncompressed KV cache: 2 * n_layers * n_heads_kv * d_head * seq_len *
+ * bytes_per_elem * batch.  [KVC] "O gargalo de memória do KV Cache em contextos longos",
+ * equation Memoria_KV; [KVCL] "01 · Conceito".  Pure host arithmetic. */
+uint64_t kvc_kv_bytes(uint64_t n_layers, uint64_t n_heads_kv, uint64_t d_head, uint64_t seq_len,
+                      uint64_t bytes_per_elem, uint64_t batch);
+
+/* PyramidKV per-layer budgets, host.  [KVC] "Alocação piramidal com o PyramidKV":
+ * B_l = B_base + dB*(N_L-1-l)/(N_L-1) with sum_l B_l = N_L*b_target.  The ramp's steepness is
+ * the ratio B_0/B_{N_L-1} = ratio_num/ratio_den (4/1 for a 2x-to-0.5x ramp).  Budgets are
+ * floored and the remaining slots go to the largest remainders (lower layer first on ties),
+ * so the total is exact.  out: host int64[n_layers]. */
+kvc_status kvc_pyramid_budgets(int32_t n_layers, int64_t b_target, int64_t ratio_num,
+                               int64_t ratio_den, int64_t *out);
+
+/* RoPE table, host: out[p][i][0] = cos(p*theta^(-2i/d_head)), out[p][i][1] = sin(...) for
+ * p < n_pos, i < d_head/2, computed in double and rounded to fp32.  out: host
+ * float[n_pos * d_head]; the caller uploads it for kvc_rope.cos_sin. */
+kvc_status kvc_rope_table(int32_t n_pos, int32_t d_head, double theta, float *out);
+
+/* ---------------------------------------------------------------------------------------- */
+/* SnapKV prefill selection.  [KVC] "SnapKV e a seleção de contexto no prefill", steps 1-4:
+ *   1. the last L_obs prompt queries (observation window) attend causally to all seq_len
+ *      prompt keys (scale * q.k, softmax per query);
+ *   2. s_h[i] = (1/L_obs) * sum over the window of the attention to key i, per query head;
+ *   3. average pooling of s_h over the prefix i < seq_len-L_obs, kernel pool_k (odd), stride 1,
+ *      zero padding, divisor pool_k; then max over the query heads of each KV head;
+ *   4. the budget-L_obs prefix positions with the largest pooled score are kept (equal scores
+ *      keep the lower index), in ascending order, followed by the window
+ *      seq_len-L_obs .. seq_len-1 (always kept).  budget >= seq_len keeps every position.
+ * q_obs:  [batch][n_heads_q][L_obs][d_head], prompt->dtype, contiguous.
+ * prompt: the prompt keys (prompt->k; prompt->v unused), cap >= seq_len.
+ * idx_out: [batch][n_heads_kv][min(budget, seq_len)] int32.
+ * scores_out (nullable): [batch][n_heads_q][seq_len-L_obs] fp32, the step-2 column means.
+ * bf16 inputs use the tensor cores (fp32 accumulation); fp32 inputs use fp32 FMA.
+ * Workspace: kvc_snapkv_select_workspace_bytes(). */
+size_t kvc_snapkv_select_workspace_bytes(int32_t batch, int32_t n_heads_q, int32_t n_heads_kv,
+                                         int32_t d_head, int32_t seq_len, int32_t L_obs);
+kvc_status kvc_snapkv_select(const void *q_obs, const kvc_cache *prompt, int32_t n_heads_q,
+                             int32_t seq_len, int32_t L_obs, int32_t pool_k, int32_t budget,
+                             float scale, int32_t *idx_out, float *scores_out, void *ws,
+                             size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Gather / compaction of retained rows.  [KVC] H2O "Poda e Desalocação" (the discarded
+ * tokens' tensors leave physical memory) and "Implementação prática em vLLM e SGLang"
+ * (aligned, dense rows).  Out of place: for every (b, h) and j < n_keep,
+ *   dst.K[b,h,j] = src.K[b,h,idx[b,h,j]], dst.V[b,h,j] = src.V[b,h,idx[b,h,j]],
+ *   pos_dst[b,h,j] = idx[b,h,j] (if pos_dst), len_dst[b*H+h] = n_keep (if len_dst).
+ * idx: [batch][n_heads_kv][idx_stride] int32.  Copies are bit exact.  src and dst must not
+ * overlap and must agree in dtype, batch, n_heads_kv and d_head; dst->cap >= n_keep. */
+kvc_status kvc_compact_gather(const kvc_cache *src, const int32_t *idx, int64_t idx_stride,
+                              int32_t n_keep, const kvc_cache *dst, int32_t *pos_dst,
+                              int64_t pos_stride, int32_t *len_dst, void *stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Append one new token's key and value per (batch, KV head).
+ * k_new, v_new: [batch][n_heads_kv][d_head], cache dtype, contiguous.  Keys are stored as
+ * given (pre-rotation in the StreamingLLM case, [SINK] "como funciona").
+ *   KVC_APPEND_TAIL:      slot = len[b*H+h]; then len[b*H+h] += 1 (device int32[batch*H]).
+ *                         A full cache (len >= cap) skips the row and records
+ *                         KVC_DEV_TAIL_FULL.
+ *   KVC_APPEND_RING:      slot of text position *t in the sink + ring layout of kvc_rope
+ *                         ([KVC] "Janela Móvel ... buffer circular"); cap >= n_sink+window+1.
+ *   KVC_APPEND_FREE_SLOT: slot = free_slot[b*H+h] (set by kvc_h2o_accumulate_evict).
+ * t: device int64 scalar, text position of the new token (required for RING, FREE_SLOT and
+ * whenever pos is given).  pos (nullable): pos[(b*H+h)*pos_stride + slot] = *t.
+ * score (nullable): score[(b*H+h)*score_stride + slot] = 0 (H2O: a new token has s = 0). */
+typedef enum {
+    KVC_APPEND_TAIL = 0,
+    KVC_APPEND_RING = 1,
+    KVC_APPEND_FREE_SLOT = 2
+} kvc_append_policy;
+
+kvc_status kvc_stream_append(const kvc_cache *cache, int32_t policy, const void *k_new,
+                             const void *v_new, const int64_t *t, int32_t *len, int32_t n_sink,
+                             int32_t window, const int32_t *free_slot, int32_t *pos,
+                             int64_t pos_stride, float *score, int64_t score_stride,
+                             void *stream);
+
+/* Adds delta to the device int64 scalar *t (the decode position shared by the calls above),
+ * on the stream, so a captured decode step can be replayed. */
+kvc_status kvc_position_advance(int64_t *t, int64_t delta, void *stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Decode attention over the retained slots: for every query head h of every batch row,
+ *   out[b,h] = sum_j softmax_j(scale * q[b,h].k_j) v_j
+ * over the valid slots j of KV head h/G (the token being decoded is among them once
+ * appended).  [KVCL] "01 · Conceito" (the new query attends to the cached keys and mixes the
+ * cached values: exact causal attention); [KVC] "O gargalo de memória..." (a GEMV over the
+ * whole cache, 1-2 FLOP per byte) and "Implementação prática..." (FlashDecoding parallelises
+ * over the time axis: the slots are split across thread blocks and the partial softmax states
+ * are merged by log-sum-exp).
+ * Valid slots: with rope == NULL, slots 0..len[b*H+h]-1 (or 0..n_valid-1 when len is NULL);
+ * with rope, the sink + ring slots of kvc_rope at the decode position *rope->t.
+ * q: [batch][n_heads_q][d_head] cache dtype (pre-rotation when rope is given).
+ * out: [batch][n_heads_q][d_head] fp32.
+ * logits (nullable): logits[(b*n_heads_q+h)*logits_stride + slot] = scale*q.k_slot for valid
+ * slots (rotated keys with rope).  lse (nullable): [batch][n_heads_q] log-sum-exp of the
+ * logits.  A row with no valid slot gets out = 0 and lse = -inf.
+ * Workspace: kvc_decode_attn_workspace_bytes(); it must be zero-filled once before its first
+ * use (the kernel leaves it zeroed again), and calls sharing a workspace must not overlap on
+ * the GPU. */
+size_t kvc_decode_attn_workspace_bytes(int32_t batch, int32_t n_heads_q, int32_t n_heads_kv,
+                                       int32_t d_head, int32_t cap);
+kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                           const int32_t *len, int32_t n_valid, const kvc_rope *rope,
+                           float scale, float *out, float *logits, int64_t logits_stride,
+                           float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* H2O score accumulation and eviction for one decode step.  [KVC] "Heavy-Hitter Oracle (H2O)
+ * e a esparsidade de cauda pesada": s_j = sum_t alpha_{t,j}; when the cache is over its
+ * budget K, the L_local newest tokens are kept (recent quota) and, among the older tokens,
+ * the one with the smallest s is evicted so that only the K_HH largest remain.
+ * For every (b, h), h a head of an MHA cache (n_heads_q == n_heads_kv):
+ *   score[j] += exp(logits[j] - lse)   for j < n_slots (alpha of this step, from
+ *                                      kvc_decode_attn's logits and lse);
+ *   if n_slots > budget: among slots with pos[j] <= *t - L_local, the smallest score is
+ *   evicted (equal scores: the larger position), free_slot[b*H+h] = that slot.
+ * score, pos: [batch][n_heads][stride] (fp32, int32); logits: [batch][n_heads][logits_stride];
+ * lse: [batch][n_heads]; free_slot: device int32[batch*n_heads]. */
+kvc_status kvc_h2o_accumulate_evict(const float *logits, int64_t logits_stride, const float *lse,
+                                    float *score, int32_t *pos, int64_t stride,
+                                    int32_t *free_slot, int32_t batch, int32_t n_heads,
+                                    int32_t n_slots, const int64_t *t, int32_t L_local,
+                                    int32_t budget, void *stream);
+
+/* H2O at the end of the prompt: full causal attention of the prompt (every query row), the
+ * column sums s_j = sum_t alpha_{t,j}, then the one-shot compression to the budget: the
+ * L_local newest positions plus the K_hh largest s among the older ones (equal scores keep
+ * the lower position), ascending.
+ * q: [batch][n_heads][seq_len][d_head] (prompt->dtype); prompt: keys (cap >= seq_len), MHA.
+ * idx_out: [batch][n_heads][n_keep] int32 and score_out: [batch][n_heads][n_keep] fp32 (the
+ * kept tokens' s), n_keep = min(seq_len, K_hh + L_local).  s_full (nullable):
+ * [batch][n_heads][seq_len] fp32.  Workspace: kvc_h2o_prefill_workspace_bytes(). */
+size_t kvc_h2o_prefill_workspace_bytes(int32_t batch, int32_t n_heads, int32_t d_head,
+                                       int32_t seq_len);
+kvc_status kvc_h2o_prefill_select(const void *q, const kvc_cache *prompt, int32_t seq_len,
+                                  int32_t L_local, int32_t K_hh, float scale, int32_t *idx_out,
+                                  float *score_out, float *s_full, void *ws, size_t ws_bytes,
+                                  void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

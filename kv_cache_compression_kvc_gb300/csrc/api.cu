@@ -1,0 +1,592 @@
+// api.cu -- the C ABI of libkvc (include/kvc.h): argument validation, planning, dispatch.
+//
+// Every entry point validates on the host and returns a kvc_status before launching anything;
+// nothing here allocates device memory or synchronises (except kvc_device_status).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/kvc.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Device-side range-check code (KVC_DEV_*); kernels receive its address.
+__device__ int32_t g_dev_code;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+int32_t *g_code_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+kvc_status fail(kvc_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+kvc_status fail(kvc_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+kvc_status ok()
+{
+    g_last_error.clear();
+    return KVC_OK;
+}
+
+kvc_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(KVC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Per-device facts, looked up once per device.
+kvc_status device_info(int32_t **code_ptr, int *n_sm)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(KVC_ERR_CUDA, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_code_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dev_code);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device code)");
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_code_ptr[dev] = static_cast<int32_t *>(p);
+        g_sm_count[dev] = sms;
+    }
+    if (code_ptr) *code_ptr = g_code_ptr[dev];
+    if (n_sm) *n_sm = g_sm_count[dev];
+    return KVC_OK;
+}
+
+// SM count for workspace sizing; 152 (GB300) when no device is usable from this thread.
+int sm_count_or_default()
+{
+    int n_sm = 0;
+    if (device_info(nullptr, &n_sm) != KVC_OK || n_sm <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n_sm;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == KVC_BF16 ? 2 : 4; }
+
+kvc_status check_cache(const kvc_cache *c, const char *name, bool need_v)
+{
+    if (c == nullptr) return fail(KVC_ERR_INVALID_ARG, "%s: null cache descriptor", name);
+    if (c->k == nullptr || (need_v && c->v == nullptr))
+        return fail(KVC_ERR_INVALID_ARG, "%s: null k/v pointer", name);
+    if (c->dtype != KVC_F32 && c->dtype != KVC_BF16)
+        return fail(KVC_ERR_INVALID_ARG, "%s: dtype %d", name, c->dtype);
+    if (c->batch <= 0 || c->n_heads_kv <= 0 || c->cap < 0)
+        return fail(KVC_ERR_SHAPE, "%s: batch %d heads %d cap %d", name, c->batch,
+                    c->n_heads_kv, c->cap);
+    if (c->d_head != 64 && c->d_head != 128 && c->d_head != 256)
+        return fail(KVC_ERR_SHAPE, "%s: d_head %d (supported: 64, 128, 256)", name, c->d_head);
+    if (c->stride_slot < c->d_head || c->stride_b < 0 || c->stride_h < 0)
+        return fail(KVC_ERR_SHAPE, "%s: strides", name);
+    const int64_t eb = elem_bytes(c->dtype);
+    if (!aligned16(c->k) || (need_v && !aligned16(c->v)) || (c->stride_slot * eb) % 16 ||
+        (c->stride_h * eb) % 16 || (c->stride_b * eb) % 16)
+        return fail(KVC_ERR_ALIGN, "%s: pointers and strides must be 16-byte aligned", name);
+    return KVC_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+namespace kvc {
+
+DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm)
+{
+    DecodePlan pl{};
+    const long long pairs = (long long)B * Hkv;
+    const long long target = 8LL * (n_sm > 0 ? n_sm : 152);
+    const int min_chunk = 64;
+    long long max_splits = cap > 0 ? (cap + min_chunk - 1) / min_chunk : 1;
+    long long n_splits = (target + pairs - 1) / pairs;
+    n_splits = std::max(1LL, std::min(n_splits, max_splits));
+    long long chunk = cap > 0 ? (cap + n_splits - 1) / n_splits : 0;
+    chunk = (chunk + 15) / 16 * 16;
+    if (chunk > 0) n_splits = (cap + chunk - 1) / chunk;
+    if (n_splits < 1) n_splits = 1;
+    pl.n_splits = (int)n_splits;
+    pl.chunk = (int)std::max(chunk, 16LL);
+    if (pl.n_splits == 1) {
+        pl.chunk = std::max(cap, 1);
+        return pl;   // no workspace: the single block writes the output
+    }
+    const size_t rows = (size_t)B * Hq;
+    pl.off_o = 0;
+    pl.off_ml = align256(pl.off_o + rows * n_splits * D * sizeof(float));
+    pl.off_cnt = align256(pl.off_ml + rows * n_splits * 2 * sizeof(float));
+    pl.bytes = align256(pl.off_cnt + (size_t)pairs * sizeof(int32_t));
+    return pl;
+}
+
+}  // namespace kvc
+
+// ==========================================================================================
+extern "C" {
+
+const char *kvc_last_error(void) { return g_last_error.c_str(); }
+
+kvc_status kvc_device_status(void *stream, int32_t *code)
+{
+    if (code == nullptr) return fail(KVC_ERR_INVALID_ARG, "kvc_device_status: null code");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    kvc_status st = device_info(nullptr, nullptr);
+    if (st != KVC_OK) return st;
+    int32_t v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_dev_code, sizeof(v));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+    const int32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_code, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    *code = v;
+    if (v != 0) return fail(KVC_ERR_DEVICE, "device range check fired: code %d", v);
+    return ok();
+}
+
+uint64_t kvc_kv_bytes(uint64_t n_layers, uint64_t n_heads_kv, uint64_t d_head, uint64_t seq_len,
+                      uint64_t bytes_per_elem, uint64_t batch)
+{
+    // Keys and values (factor 2) for every layer, KV head, head dimension, position, batch row.
+    return 2ull * n_layers * n_heads_kv * d_head * seq_len * bytes_per_elem * batch;
+}
+
+kvc_status kvc_pyramid_budgets(int32_t n_layers, int64_t b_target, int64_t ratio_num,
+                               int64_t ratio_den, int64_t *out)
+{
+    if (out == nullptr || n_layers <= 0 || b_target < 0 || ratio_num <= 0 || ratio_den <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_pyramid_budgets: invalid arguments");
+    if (n_layers == 1) {
+        out[0] = b_target;
+        return ok();
+    }
+    // B_l * (num+den)*(N_L-1) = 2*b_target*(num*(N_L-1-l) + den*l), exact in integers.
+    const int64_t last = n_layers - 1;
+    const int64_t denom = (ratio_num + ratio_den) * last;
+    std::vector<std::pair<int64_t, int32_t>> frac(n_layers);
+    int64_t assigned = 0;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        const int64_t numer = 2 * b_target * (ratio_num * (last - l) + ratio_den * l);
+        out[l] = numer / denom;
+        frac[l] = {numer % denom, l};
+        assigned += out[l];
+    }
+    std::sort(frac.begin(), frac.end(), [](const auto &a, const auto &b) {
+        return a.first != b.first ? a.first > b.first : a.second < b.second;
+    });
+    const int64_t missing = (int64_t)n_layers * b_target - assigned;
+    for (int64_t i = 0; i < missing; ++i) out[frac[(size_t)i].second] += 1;
+    return ok();
+}
+
+kvc_status kvc_rope_table(int32_t n_pos, int32_t d_head, double theta, float *out)
+{
+    if (out == nullptr || n_pos < 0 || d_head <= 0 || (d_head % 2) || !(theta > 0))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_rope_table: invalid arguments");
+    const int half = d_head / 2;
+    std::vector<double> inv_freq(half);
+    for (int i = 0; i < half; ++i) inv_freq[i] = std::pow(theta, -2.0 * i / d_head);
+    for (int32_t p = 0; p < n_pos; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double a = (double)p * inv_freq[i];
+            out[((size_t)p * half + i) * 2] = (float)std::cos(a);
+            out[((size_t)p * half + i) * 2 + 1] = (float)std::sin(a);
+        }
+    return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+size_t kvc_decode_attn_workspace_bytes(int32_t batch, int32_t n_heads_q, int32_t n_heads_kv,
+                                       int32_t d_head, int32_t cap)
+{
+    if (batch <= 0 || n_heads_q <= 0 || n_heads_kv <= 0 || d_head <= 0 || cap < 0) return 0;
+    return kvc::decode_plan(batch, n_heads_q, n_heads_kv, d_head, cap, sm_count_or_default())
+        .bytes;
+}
+
+kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                           const int32_t *len, int32_t n_valid, const kvc_rope *rope,
+                           float scale, float *out, float *logits, int64_t logits_stride,
+                           float *lse, void *ws, size_t ws_bytes, void *stream)
+{
+    kvc_status st = check_cache(cache, "kvc_decode_attn", true);
+    if (st != KVC_OK) return st;
+    if (q == nullptr || out == nullptr) return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: null q/out");
+    if (!aligned16(q)) return fail(KVC_ERR_ALIGN, "kvc_decode_attn: q must be 16-byte aligned");
+    if (n_heads_q <= 0 || n_heads_q % cache->n_heads_kv)
+        return fail(KVC_ERR_SHAPE, "kvc_decode_attn: n_heads_q %d not a multiple of n_heads_kv %d",
+                    n_heads_q, cache->n_heads_kv);
+    const int G = n_heads_q / cache->n_heads_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 6 && G != 8)
+        return fail(KVC_ERR_SHAPE, "kvc_decode_attn: group size %d (supported: 1,2,4,6,8)", G);
+    if (!std::isfinite(scale)) return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: scale");
+    int slots_max = cache->cap;
+    if (rope != nullptr) {
+        if (rope->t == nullptr || rope->cos_sin == nullptr || rope->n_sink < 0 || rope->window < 0)
+            return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: rope descriptor");
+        const long long ring = (long long)rope->n_sink + rope->window + 1;
+        if (ring > cache->cap)
+            return fail(KVC_ERR_CAPACITY, "kvc_decode_attn: cap %d < n_sink + window + 1 = %lld",
+                        cache->cap, ring);
+        if (rope->n_pos < ring)
+            return fail(KVC_ERR_CAPACITY, "kvc_decode_attn: rope table has %d rows, needs %lld",
+                        rope->n_pos, ring);
+        if (!aligned16(rope->cos_sin))
+            return fail(KVC_ERR_ALIGN, "kvc_decode_attn: cos_sin must be 16-byte aligned");
+        slots_max = (int)ring;
+    } else if (len == nullptr && (n_valid < 0 || n_valid > cache->cap)) {
+        return fail(KVC_ERR_CAPACITY, "kvc_decode_attn: n_valid %d outside [0, cap %d]", n_valid,
+                    cache->cap);
+    }
+    if (logits != nullptr && logits_stride < slots_max)
+        return fail(KVC_ERR_CAPACITY, "kvc_decode_attn: logits_stride %lld < %d slots",
+                    (long long)logits_stride, slots_max);
+    int32_t *code = nullptr;
+    int n_sm = 0;
+    st = device_info(&code, &n_sm);
+    if (st != KVC_OK) return st;
+    const kvc::DecodePlan pl = kvc::decode_plan(cache->batch, n_heads_q, cache->n_heads_kv,
+                                                cache->d_head, cache->cap, n_sm);
+    if (pl.bytes > 0) {
+        if (ws == nullptr || ws_bytes < pl.bytes)
+            return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn: workspace needs %zu bytes, got %zu",
+                        pl.bytes, ws_bytes);
+        if (!aligned256(ws)) return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn: workspace alignment");
+    }
+    kvc::DecodeParams p{};
+    p.q = q;
+    p.k = cache->k;
+    p.v = cache->v;
+    p.sb = cache->stride_b; p.sh = cache->stride_h; p.ss = cache->stride_slot;
+    p.B = cache->batch; p.Hq = n_heads_q; p.Hkv = cache->n_heads_kv; p.cap = cache->cap;
+    p.len = len;
+    p.n_valid = n_valid;
+    if (rope != nullptr) {
+        p.rope = 1; p.S = rope->n_sink; p.W = rope->window; p.t = rope->t;
+        p.cos_sin = rope->cos_sin;
+    }
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out; p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;
+    char *wsb = static_cast<char *>(ws);
+    p.ws_o = pl.bytes ? reinterpret_cast<float *>(wsb + pl.off_o) : nullptr;
+    p.ws_ml = pl.bytes ? reinterpret_cast<float *>(wsb + pl.off_ml) : nullptr;
+    p.ws_cnt = pl.bytes ? reinterpret_cast<int32_t *>(wsb + pl.off_cnt) : nullptr;
+    p.n_splits = pl.n_splits;
+    p.chunk = pl.chunk;
+    p.dev_code = code;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cache->dtype == KVC_BF16
+                        ? kvc::launch_decode_attn_bf16(p, cache->d_head, G, s)
+                        : kvc::launch_decode_attn_f32(p, cache->d_head, G, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+kvc_status kvc_stream_append(const kvc_cache *cache, int32_t policy, const void *k_new,
+                             const void *v_new, const int64_t *t, int32_t *len, int32_t n_sink,
+                             int32_t window, const int32_t *free_slot, int32_t *pos,
+                             int64_t pos_stride, float *score, int64_t score_stride,
+                             void *stream)
+{
+    kvc_status st = check_cache(cache, "kvc_stream_append", true);
+    if (st != KVC_OK) return st;
+    if (k_new == nullptr || v_new == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_stream_append: null k_new/v_new");
+    if (!aligned16(k_new) || !aligned16(v_new))
+        return fail(KVC_ERR_ALIGN, "kvc_stream_append: k_new/v_new must be 16-byte aligned");
+    if (policy == KVC_APPEND_TAIL) {
+        if (len == nullptr) return fail(KVC_ERR_INVALID_ARG, "kvc_stream_append: TAIL needs len");
+    } else if (policy == KVC_APPEND_RING) {
+        if (t == nullptr || n_sink < 0 || window < 0)
+            return fail(KVC_ERR_INVALID_ARG, "kvc_stream_append: RING needs t, n_sink, window");
+        if ((long long)n_sink + window + 1 > cache->cap)
+            return fail(KVC_ERR_CAPACITY, "kvc_stream_append: cap %d < n_sink + window + 1",
+                        cache->cap);
+    } else if (policy == KVC_APPEND_FREE_SLOT) {
+        if (t == nullptr || free_slot == nullptr)
+            return fail(KVC_ERR_INVALID_ARG, "kvc_stream_append: FREE_SLOT needs t and free_slot");
+    } else {
+        return fail(KVC_ERR_INVALID_ARG, "kvc_stream_append: policy %d", policy);
+    }
+    if ((pos != nullptr && (t == nullptr || pos_stride < cache->cap)) ||
+        (score != nullptr && score_stride < cache->cap))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_stream_append: pos needs t; strides >= cap");
+    int32_t *code = nullptr;
+    st = device_info(&code, nullptr);
+    if (st != KVC_OK) return st;
+    kvc::AppendParams p{};
+    p.k = cache->k; p.v = cache->v;
+    p.sb = cache->stride_b; p.sh = cache->stride_h; p.ss = cache->stride_slot;
+    p.B = cache->batch; p.H = cache->n_heads_kv; p.cap = cache->cap; p.D = cache->d_head;
+    p.policy = policy;
+    p.k_new = k_new; p.v_new = v_new; p.t = t; p.len = len;
+    p.S = n_sink; p.W = window; p.free_slot = free_slot;
+    p.pos = pos; p.pos_stride = pos_stride; p.score = score; p.score_stride = score_stride;
+    p.dev_code = code;
+    cudaError_t e = kvc::launch_append(p, elem_bytes(cache->dtype), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return ok();
+}
+
+kvc_status kvc_position_advance(int64_t *t, int64_t delta, void *stream)
+{
+    if (t == nullptr) return fail(KVC_ERR_INVALID_ARG, "kvc_position_advance: null t");
+    cudaError_t e = kvc::launch_position_advance(t, delta, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "position advance launch");
+    return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+kvc_status kvc_compact_gather(const kvc_cache *src, const int32_t *idx, int64_t idx_stride,
+                              int32_t n_keep, const kvc_cache *dst, int32_t *pos_dst,
+                              int64_t pos_stride, int32_t *len_dst, void *stream)
+{
+    kvc_status st = check_cache(src, "kvc_compact_gather(src)", true);
+    if (st != KVC_OK) return st;
+    st = check_cache(dst, "kvc_compact_gather(dst)", true);
+    if (st != KVC_OK) return st;
+    if (idx == nullptr || n_keep < 0 || idx_stride < n_keep)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact_gather: idx / n_keep / idx_stride");
+    if (src->dtype != dst->dtype || src->batch != dst->batch ||
+        src->n_heads_kv != dst->n_heads_kv || src->d_head != dst->d_head)
+        return fail(KVC_ERR_SHAPE, "kvc_compact_gather: src and dst disagree in shape or dtype");
+    if (dst->cap < n_keep)
+        return fail(KVC_ERR_CAPACITY, "kvc_compact_gather: dst cap %d < n_keep %d", dst->cap, n_keep);
+    if (src->k == dst->k || src->v == dst->v || src->k == dst->v || src->v == dst->k)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact_gather: out of place only");
+    if (pos_dst != nullptr && pos_stride < n_keep)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact_gather: pos_stride < n_keep");
+    int32_t *code = nullptr;
+    st = device_info(&code, nullptr);
+    if (st != KVC_OK) return st;
+    kvc::GatherParams p{};
+    p.sk = src->k; p.sv = src->v;
+    p.s_sb = src->stride_b; p.s_sh = src->stride_h; p.s_ss = src->stride_slot; p.s_cap = src->cap;
+    p.dk = dst->k; p.dv = dst->v;
+    p.d_sb = dst->stride_b; p.d_sh = dst->stride_h; p.d_ss = dst->stride_slot;
+    p.B = src->batch; p.H = src->n_heads_kv; p.D = src->d_head;
+    p.idx = idx; p.idx_stride = idx_stride; p.n_keep = n_keep;
+    p.pos_dst = pos_dst; p.pos_stride = pos_stride; p.len_dst = len_dst;
+    p.dev_code = code;
+    cudaError_t e = kvc::launch_gather(p, elem_bytes(src->dtype), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+// SnapKV workspace: [s (G heads, prefix columns)] [pooled score] [row states] [row lse].
+static void snapkv_layout(int B, int Hq, int Hkv, int N, int L_obs, int n_sm, size_t *off_s,
+                          size_t *off_score, kvc::ScorePlan *pl)
+{
+    const size_t n = (size_t)(N - L_obs);
+    *off_s = 0;
+    *off_score = align256((size_t)B * Hq * n * sizeof(float));
+    const size_t base = align256(*off_score + (size_t)B * Hkv * n * sizeof(float));
+    *pl = kvc::score_plan(B, Hkv, Hq / Hkv, N, L_obs, n_sm, base);
+}
+
+size_t kvc_snapkv_select_workspace_bytes(int32_t batch, int32_t n_heads_q, int32_t n_heads_kv,
+                                         int32_t d_head, int32_t seq_len, int32_t L_obs)
+{
+    (void)d_head;
+    if (batch <= 0 || n_heads_kv <= 0 || n_heads_q <= 0 || n_heads_q % n_heads_kv ||
+        L_obs <= 0 || seq_len < L_obs)
+        return 0;
+    size_t off_s, off_score;
+    kvc::ScorePlan pl;
+    snapkv_layout(batch, n_heads_q, n_heads_kv, seq_len, L_obs, sm_count_or_default(), &off_s,
+                  &off_score, &pl);
+    return pl.bytes;
+}
+
+kvc_status kvc_snapkv_select(const void *q_obs, const kvc_cache *prompt, int32_t n_heads_q,
+                             int32_t seq_len, int32_t L_obs, int32_t pool_k, int32_t budget,
+                             float scale, int32_t *idx_out, float *scores_out, void *ws,
+                             size_t ws_bytes, void *stream)
+{
+    kvc_status st = check_cache(prompt, "kvc_snapkv_select", false);
+    if (st != KVC_OK) return st;
+    if (q_obs == nullptr || idx_out == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_snapkv_select: null q_obs/idx_out");
+    if (n_heads_q <= 0 || n_heads_q % prompt->n_heads_kv)
+        return fail(KVC_ERR_SHAPE, "kvc_snapkv_select: n_heads_q %d vs n_heads_kv %d", n_heads_q,
+                    prompt->n_heads_kv);
+    if (L_obs <= 0 || seq_len < L_obs || seq_len > prompt->cap)
+        return fail(KVC_ERR_SHAPE, "kvc_snapkv_select: need 0 < L_obs <= seq_len <= cap");
+    if (pool_k <= 0 || pool_k % 2 == 0)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_snapkv_select: pool_k %d must be odd", pool_k);
+    if (budget < L_obs)
+        return fail(KVC_ERR_CAPACITY, "kvc_snapkv_select: budget %d < L_obs %d", budget, L_obs);
+    if (!std::isfinite(scale)) return fail(KVC_ERR_INVALID_ARG, "kvc_snapkv_select: scale");
+    int32_t *code = nullptr;
+    int n_sm = 0;
+    st = device_info(&code, &n_sm);
+    if (st != KVC_OK) return st;
+    const int B = prompt->batch, Hkv = prompt->n_heads_kv, G = n_heads_q / Hkv;
+    size_t off_s, off_score;
+    kvc::ScorePlan pl;
+    snapkv_layout(B, n_heads_q, Hkv, seq_len, L_obs, n_sm, &off_s, &off_score, &pl);
+    if (ws == nullptr || ws_bytes < pl.bytes || !aligned256(ws))
+        return fail(KVC_ERR_WORKSPACE, "kvc_snapkv_select: workspace needs %zu aligned bytes",
+                    pl.bytes);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int n = seq_len - L_obs;
+    const int n_keep = std::min(budget, seq_len);
+    if (budget >= seq_len && scores_out == nullptr) {
+        cudaError_t e = kvc::launch_iota_rows(idx_out, n_keep, B * Hkv, n_keep, s);
+        if (e != cudaSuccess) return cuda_fail(e, "iota launch");
+        return ok();
+    }
+    char *wsb = static_cast<char *>(ws);
+    float *s_cols = scores_out ? scores_out : reinterpret_cast<float *>(wsb + off_s);
+    float *pooled = reinterpret_cast<float *>(wsb + off_score);
+    kvc::ScoreParams sp{};
+    sp.q = q_obs; sp.k = prompt->k;
+    sp.sb = prompt->stride_b; sp.sh = prompt->stride_h; sp.ss = prompt->stride_slot;
+    sp.B = B; sp.Hq = n_heads_q; sp.Hkv = Hkv; sp.G = G; sp.D = prompt->d_head; sp.N = seq_len;
+    sp.L_obs = L_obs;
+    sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.n_cols = n;
+    sp.col_mult = 1.0f / (float)L_obs;
+    sp.s_out = s_cols;
+    sp.row_ml = reinterpret_cast<float *>(wsb + pl.off_ml);
+    sp.row_lse2 = reinterpret_cast<float *>(wsb + pl.off_lse);
+    sp.n_chunks = pl.n_chunks;
+    sp.chunk = pl.chunk;
+    cudaError_t e = kvc::launch_obs_scores(sp, prompt->dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "observation scores launch");
+    if (budget >= seq_len) {
+        e = kvc::launch_iota_rows(idx_out, n_keep, B * Hkv, n_keep, s);
+        if (e != cudaSuccess) return cuda_fail(e, "iota launch");
+        return ok();
+    }
+    e = kvc::launch_pool_groupmax(s_cols, n, pooled, B * Hkv, G, n, pool_k, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pool launch");
+    e = kvc::launch_topk_rows(pooled, n, B * Hkv, n, budget - L_obs, L_obs, idx_out, budget, s);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+kvc_status kvc_h2o_accumulate_evict(const float *logits, int64_t logits_stride, const float *lse,
+                                    float *score, int32_t *pos, int64_t stride,
+                                    int32_t *free_slot, int32_t batch, int32_t n_heads,
+                                    int32_t n_slots, const int64_t *t, int32_t L_local,
+                                    int32_t budget, void *stream)
+{
+    if (logits == nullptr || lse == nullptr || score == nullptr || pos == nullptr ||
+        free_slot == nullptr || t == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_h2o_accumulate_evict: null pointer");
+    if (batch <= 0 || n_heads <= 0 || n_slots < 0 || L_local < 0 || budget < 0 ||
+        logits_stride < n_slots || stride < n_slots)
+        return fail(KVC_ERR_SHAPE, "kvc_h2o_accumulate_evict: sizes");
+    int32_t *code = nullptr;
+    kvc_status st = device_info(&code, nullptr);
+    if (st != KVC_OK) return st;
+    kvc::H2OParams p{};
+    p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;
+    p.score = score; p.pos = pos; p.stride = stride; p.free_slot = free_slot;
+    p.rows = batch * n_heads; p.n_slots = n_slots; p.L_local = L_local; p.budget = budget;
+    p.t = t; p.dev_code = code;
+    cudaError_t e = kvc::launch_h2o_accumulate_evict(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "H2O launch");
+    return ok();
+}
+
+// H2O prefill workspace: [s_full] [row states] [row lse].
+static void h2o_layout(int B, int H, int N, int n_sm, size_t *off_s, kvc::ScorePlan *pl)
+{
+    *off_s = 0;
+    const size_t base = align256((size_t)B * H * N * sizeof(float));
+    *pl = kvc::score_plan(B, H, 1, N, N, n_sm, base);
+}
+
+size_t kvc_h2o_prefill_workspace_bytes(int32_t batch, int32_t n_heads, int32_t d_head,
+                                       int32_t seq_len)
+{
+    (void)d_head;
+    if (batch <= 0 || n_heads <= 0 || seq_len <= 0) return 0;
+    size_t off_s;
+    kvc::ScorePlan pl;
+    h2o_layout(batch, n_heads, seq_len, sm_count_or_default(), &off_s, &pl);
+    return pl.bytes;
+}
+
+kvc_status kvc_h2o_prefill_select(const void *q, const kvc_cache *prompt, int32_t seq_len,
+                                  int32_t L_local, int32_t K_hh, float scale, int32_t *idx_out,
+                                  float *score_out, float *s_full, void *ws, size_t ws_bytes,
+                                  void *stream)
+{
+    kvc_status st = check_cache(prompt, "kvc_h2o_prefill_select", false);
+    if (st != KVC_OK) return st;
+    if (q == nullptr || idx_out == nullptr || score_out == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_h2o_prefill_select: null pointer");
+    if (seq_len <= 0 || seq_len > prompt->cap || L_local < 0 || K_hh < 0)
+        return fail(KVC_ERR_SHAPE, "kvc_h2o_prefill_select: sizes");
+    if (!std::isfinite(scale)) return fail(KVC_ERR_INVALID_ARG, "kvc_h2o_prefill_select: scale");
+    int32_t *code = nullptr;
+    int n_sm = 0;
+    st = device_info(&code, &n_sm);
+    if (st != KVC_OK) return st;
+    const int B = prompt->batch, H = prompt->n_heads_kv, N = seq_len;
+    size_t off_s;
+    kvc::ScorePlan pl;
+    h2o_layout(B, H, N, n_sm, &off_s, &pl);
+    if (ws == nullptr || ws_bytes < pl.bytes || !aligned256(ws))
+        return fail(KVC_ERR_WORKSPACE, "kvc_h2o_prefill_select: workspace needs %zu aligned bytes",
+                    pl.bytes);
+    char *wsb = static_cast<char *>(ws);
+    float *sf = s_full ? s_full : reinterpret_cast<float *>(wsb + off_s);
+    kvc::ScoreParams sp{};
+    sp.q = q; sp.k = prompt->k;
+    sp.sb = prompt->stride_b; sp.sh = prompt->stride_h; sp.ss = prompt->stride_slot;
+    sp.B = B; sp.Hq = H; sp.Hkv = H; sp.G = 1; sp.D = prompt->d_head; sp.N = N; sp.L_obs = N;
+    sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.n_cols = N;
+    sp.col_mult = 1.0f;
+    sp.s_out = sf;
+    sp.row_ml = reinterpret_cast<float *>(wsb + pl.off_ml);
+    sp.row_lse2 = reinterpret_cast<float *>(wsb + pl.off_lse);
+    sp.n_chunks = pl.n_chunks;
+    sp.chunk = pl.chunk;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = kvc::launch_obs_scores(sp, prompt->dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prompt scores launch");
+    const long long keep_ll = (long long)K_hh + L_local;
+    const int n_keep = (int)std::min<long long>(N, keep_ll);
+    if (N <= keep_ll) {
+        e = kvc::launch_iota_rows(idx_out, n_keep, B * H, n_keep, s);
+    } else {
+        e = kvc::launch_topk_rows(sf, N, B * H, N - L_local, K_hh, L_local, idx_out, n_keep, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "H2O selection launch");
+    e = kvc::launch_gather_scores(sf, N, idx_out, n_keep, B * H, n_keep, score_out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "score gather launch");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// common.cuh -- small device helpers shared by libkvc's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvc {
+
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLog2e = 1.442695040888963407f;
+// Finite "minus infinity" for running maxima: exp2(x - kNegBig) never produces NaN.
+constexpr float kNegBig = -1.0e30f;
+
+__device__ __forceinline__ void record_code(int32_t *code, int32_t c)
+{
+    if (code != nullptr) atomicCAS(code, 0, c);
+}
+
+// bf16 stored in the low / high half of a 32-bit word (element 2i in the low half).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Streaming 16/8-byte global loads that do not allocate in L1 (each KV byte is read once).
+__device__ __forceinline__ uint4 ld_stream_16(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_stream_8(const void *p)
+{
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p));
+    return r;
+}
+
+// A vector of VW consecutive elements of type T held as raw 32-bit words.
+template <typename T, int VW>
+struct RawVec;
+
+template <>
+struct RawVec<float, 4> {
+    uint4 w;
+    __device__ __forceinline__ void load(const float *p) { w = ld_stream_16(p); }
+    __device__ __forceinline__ void zero() { w = make_uint4(0, 0, 0, 0); }
+    __device__ __forceinline__ void to_float(float *f) const
+    {
+        f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+        f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+    }
+};
+template <>
+struct RawVec<__nv_bfloat16, 8> {
+    uint4 w;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { w = ld_stream_16(p); }
+    __device__ __forceinline__ void zero() { w = make_uint4(0, 0, 0, 0); }
+    __device__ __forceinline__ void to_float(float *f) const
+    {
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+    }
+};
+template <>
+struct RawVec<__nv_bfloat16, 4> {
+    uint2 w;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { w = ld_stream_8(p); }
+    __device__ __forceinline__ void zero() { w = make_uint2(0, 0); }
+    __device__ __forceinline__ void to_float(float *f) const
+    {
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    }
+};
+
+// Plain (cached) load of VW elements of T into floats: used for small, reused operands.
+template <typename T, int VW>
+__device__ __forceinline__ void load_cached(const T *p, float *f)
+{
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int i = 0; i < VW; i += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(p + i);
+            f[i] = x.x; f[i + 1] = x.y; f[i + 2] = x.z; f[i + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < VW; i += 2) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(p + i);
+            f[i] = bf16_lo(w); f[i + 1] = bf16_hi(w);
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace kvc

@@ -1,0 +1,9 @@
+// decode_bf16.cu -- bf16-storage instantiations of the decode attention kernel.
+#include "decode_attn.cuh"
+
+namespace kvc {
+cudaError_t launch_decode_attn_bf16(const DecodeParams &p, int D, int G, cudaStream_t stream)
+{
+    return launch_decode_dtype<__nv_bfloat16>(p, D, G, stream);
+}
+}  // namespace kvc

@@ -1,0 +1,145 @@
+// internal.h -- launch-parameter structs and launcher declarations shared by libkvc's own
+// translation units.  Not part of the public ABI (include/kvc.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvc {
+
+// ------------------------------------------------------------------------------------------
+// Decode attention (split over slots, log-sum-exp merge by the last block of each KV head).
+struct DecodeParams {
+    const void *q;
+    const void *k;
+    const void *v;
+    int64_t sb, sh, ss;          // cache strides, elements
+    int32_t B, Hq, Hkv, cap;
+    const int32_t *len;          // device [B*Hkv] or nullptr
+    int32_t n_valid;             // used when len == nullptr
+    // RoPE / StreamingLLM layout (rope != 0)
+    int32_t rope, S, W;
+    const int64_t *t;
+    const float *cos_sin;        // [n_pos][D/2][2]
+    float scale_log2;            // scale * log2(e)
+    float *out;                  // [B][Hq][D]
+    float *logits;               // nullable, [B*Hq][logits_stride]
+    int64_t logits_stride;
+    float *lse;                  // nullable, [B*Hq]
+    float *ws_o;                 // [B*Hq][n_splits][D]
+    float *ws_ml;                // [B*Hq][n_splits][2]
+    int32_t *ws_cnt;             // [B*Hkv], zero between calls
+    int32_t n_splits;
+    int32_t chunk;               // slots per split
+    int32_t *dev_code;
+};
+
+struct DecodePlan {
+    int32_t n_splits;
+    int32_t chunk;
+    size_t off_o, off_ml, off_cnt, bytes;
+};
+
+DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm);
+cudaError_t launch_decode_attn_f32(const DecodeParams &p, int D, int G, cudaStream_t stream);
+cudaError_t launch_decode_attn_bf16(const DecodeParams &p, int D, int G, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// Append, gather, position advance.
+struct AppendParams {
+    void *k;
+    void *v;
+    int64_t sb, sh, ss;
+    int32_t B, H, cap, D;
+    int32_t policy;
+    const void *k_new;
+    const void *v_new;
+    const int64_t *t;
+    int32_t *len;
+    int32_t S, W;
+    const int32_t *free_slot;
+    int32_t *pos;
+    int64_t pos_stride;
+    float *score;
+    int64_t score_stride;
+    int32_t *dev_code;
+};
+cudaError_t launch_append(const AppendParams &p, int elem_bytes, cudaStream_t stream);
+
+struct GatherParams {
+    const void *sk;
+    const void *sv;
+    int64_t s_sb, s_sh, s_ss;
+    int32_t s_cap;
+    void *dk;
+    void *dv;
+    int64_t d_sb, d_sh, d_ss;
+    int32_t B, H, D;
+    const int32_t *idx;
+    int64_t idx_stride;
+    int32_t n_keep;
+    int32_t *pos_dst;
+    int64_t pos_stride;
+    int32_t *len_dst;
+    int32_t *dev_code;
+};
+cudaError_t launch_gather(const GatherParams &p, int elem_bytes, cudaStream_t stream);
+cudaError_t launch_position_advance(int64_t *t, int64_t delta, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// Observation-window scoring (SnapKV steps 1-2; H2O prompt column sums).
+// Rows r = g*L_obs + w of KV head kh are the window queries of q-head kh*G+g; the query at
+// window index w sits at text position N - L_obs + w and sees keys 0 .. N - L_obs + w.
+struct ScoreParams {
+    const void *q;               // [B][Hq][L_obs][D] contiguous
+    const void *k;               // prompt keys (cache strides)
+    int64_t sb, sh, ss;
+    int32_t B, Hq, Hkv, G, D, N, L_obs;
+    float scale_log2;            // scale * log2(e)
+    int32_t n_cols;              // columns written: N - L_obs (SnapKV) or N (H2O)
+    float col_mult;              // 1/L_obs (mean) or 1 (sum)
+    float *s_out;                // [B][Hq][n_cols]
+    float *row_ml;               // workspace [B*Hkv][n_chunks][R][2]
+    float *row_lse2;             // workspace [B*Hkv][R] (log2 units)
+    int32_t n_chunks;
+    int32_t chunk;
+};
+struct ScorePlan {
+    int32_t n_chunks, chunk;
+    size_t off_ml, off_lse, bytes;
+};
+ScorePlan score_plan(int B, int Hkv, int G, int N, int L_obs, int n_sm, size_t base_off);
+cudaError_t launch_obs_scores(const ScoreParams &p, int dtype, cudaStream_t stream);
+
+// Pool (kernel pool_k, zero padding, divisor pool_k, sum left to right) + max over the G heads.
+cudaError_t launch_pool_groupmax(const float *s, int64_t s_row_stride, float *score, int BH,
+                                 int G, int n, int pool_k, cudaStream_t stream);
+
+// Exact top-k per row (ties: lower index), ascending emission, then `tail` indices
+// n .. n+tail-1 appended.  idx row stride = k + tail.
+cudaError_t launch_topk_rows(const float *score, int64_t score_stride, int rows, int n, int k,
+                             int tail, int32_t *idx, int64_t idx_stride, cudaStream_t stream);
+cudaError_t launch_iota_rows(int32_t *idx, int64_t idx_stride, int rows, int n,
+                             cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// H2O.
+struct H2OParams {
+    const float *logits;
+    int64_t logits_stride;
+    const float *lse;
+    float *score;
+    int32_t *pos;
+    int64_t stride;
+    int32_t *free_slot;
+    int32_t rows, n_slots, L_local, budget;
+    const int64_t *t;
+    int32_t *dev_code;
+};
+cudaError_t launch_h2o_accumulate_evict(const H2OParams &p, cudaStream_t stream);
+cudaError_t launch_gather_scores(const float *s_full, int64_t s_stride, const int32_t *idx,
+                                 int64_t idx_stride, int rows, int n_keep, float *out,
+                                 cudaStream_t stream);
+
+}  // namespace kvc

@@ -1,0 +1,107 @@
+"""The C ABI library builds, loads and exports every symbol include/kvc.h declares; its host-only
+entry points agree with the oracle; argument validation rejects bad calls before any launch.
+No GPU needed: nothing here launches a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    from kv_cache_compression_kvc_gb300 import build, kvc as k
+    build.build()
+    k.load()
+    return k
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_symbols()
+    for n in ("kvc_snapkv_select", "kvc_compact_gather", "kvc_stream_append",
+              "kvc_h2o_accumulate_evict", "kvc_decode_attn"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kvc):
+    lib = ctypes.CDLL(kvc.library_path())
+    missing = [n for n in _declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding declares a signature for each of them, no more, no less
+    assert sorted(kvc.SIGNATURES) == _declared_symbols()
+
+
+def test_kv_bytes_matches_oracle(kvc):
+    for args in [(64, 4, 256, 262144, 2, 1), (16, 4, 256, 262144, 2, 1), (32, 32, 128, 2049, 2, 16),
+                 (1, 1, 64, 1, 4, 1)]:
+        assert kvc.kvc_kv_bytes(*args) == oracle.kv_bytes(*args)
+
+
+@pytest.mark.parametrize("n_layers,target,num,den", [(16, 8192, 4, 1), (32, 5243, 4, 1),
+                                                     (3, 1, 3, 1), (7, 1001, 1, 4), (1, 9, 4, 1),
+                                                     (40, 123457, 7, 3)])
+def test_pyramid_budgets_match_oracle(kvc, n_layers, target, num, den):
+    assert kvc.kvc_pyramid_budgets(n_layers, target, num, den) == \
+        [int(x) for x in oracle.pyramid_budgets(n_layers, target, num, den)]
+
+
+def test_rope_table_matches_oracle_rotation(kvc):
+    D, n = 128, 300
+    tab = kvc.kvc_rope_table(n, D, 10000.0).numpy().astype(np.float64)
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(D)
+    for p in (0, 1, 17, 299):
+        c, s = tab[p, :, 0], tab[p, :, 1]
+        y = np.concatenate([x[:D // 2] * c - x[D // 2:] * s, x[:D // 2] * s + x[D // 2:] * c])
+        assert np.max(np.abs(y - oracle.rope(x, p))) < 1e-5   # fp32 table entries
+
+
+def test_validation_rejects_bad_calls_before_launch(kvc):
+    lib = kvc.load()
+    c = kvc.kvc_cache()
+    c.k = c.v = 4096
+    c.dtype, c.batch, c.n_heads_kv, c.cap, c.d_head = kvc.KVC_BF16, 1, 1, 16, 96
+    c.stride_b, c.stride_h, c.stride_slot = 16 * 96, 16 * 96, 96
+    st = lib.kvc_decode_attn(4096, 1, ctypes.byref(c), None, 4, None, 1.0, 4096, None, 0, None,
+                             None, 0, None)
+    assert st == 2 and "d_head" in kvc.kvc_last_error()           # KVC_ERR_SHAPE
+    c.d_head, c.stride_slot = 128, 128
+    st = lib.kvc_decode_attn(4096, 3, ctypes.byref(c), None, 4, None, 1.0, 4096, None, 0, None,
+                             None, 0, None)
+    assert st == 2                                                 # group size 3 unsupported
+    c.k = 4100
+    st = lib.kvc_decode_attn(4096, 1, ctypes.byref(c), None, 4, None, 1.0, 4096, None, 0, None,
+                             None, 0, None)
+    assert st == 3                                                 # KVC_ERR_ALIGN
+    c.k = 4096
+    st = lib.kvc_decode_attn(4096, 1, ctypes.byref(c), None, 17, None, 1.0, 4096, None, 0, None,
+                             None, 0, None)
+    assert st == 4                                                 # n_valid > cap
+    st = lib.kvc_stream_append(ctypes.byref(c), 7, 4096, 4096, None, None, 0, 0, None, None, 0,
+                               None, 0, None)
+    assert st == 1                                                 # bad policy
+    st = lib.kvc_stream_append(ctypes.byref(c), kvc.KVC_APPEND_RING, 4096, 4096, 4096, None, 4,
+                               20, None, None, 0, None, 0, None)
+    assert st == 4                                                 # ring does not fit cap 16
+    st = lib.kvc_snapkv_select(4096, ctypes.byref(c), 1, 16, 8, 4, 20, 1.0, 4096, None, None, 0,
+                               None)
+    assert st == 1                                                 # even pool kernel
+    st = lib.kvc_snapkv_select(4096, ctypes.byref(c), 1, 16, 8, 5, 7, 1.0, 4096, None, None, 0,
+                               None)
+    assert st == 4                                                 # budget < L_obs
+    d = kvc.kvc_cache.from_buffer_copy(c)
+    st = lib.kvc_compact_gather(ctypes.byref(c), 4096, 8, 8, ctypes.byref(d), None, 0, None, None)
+    assert st == 1                                                 # in place is refused
+    assert lib.kvc_pyramid_budgets(0, 10, 4, 1, None) == 1
+    assert kvc.kvc_last_error() != ""

@@ -1,0 +1,185 @@
+"""GPU parity: decode attention, append and the StreamingLLM ring, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import TOL, assert_close, cuda_or_skip, f64, lib
+from kv_cache_compression_kvc_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_decode(q, K, V, lens, scale, G):
+    B, Hq, D = q.shape
+    out = np.zeros((B, Hq, D))
+    logits = {}
+    lse = np.zeros((B, Hq))
+    for b in range(B):
+        for h in range(Hq):
+            n = int(lens[b, h // G])
+            o, lg, ls = oracle.attend(f64(q[b, h]), f64(K[b, h // G, :n]), f64(V[b, h // G, :n]),
+                                      scale)
+            out[b, h], lse[b, h], logits[(b, h)] = o, ls, lg
+    return out, logits, lse
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("D,G", [(64, 4), (128, 1), (128, 2), (256, 6), (128, 8), (64, 1)])
+def test_decode_matches_oracle_ragged(dtype, D, G):
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv, cap = 2, 2, 1040
+    Hq = Hkv * G
+    K = I.randn((B, Hkv, cap, D), 11 + D + G, dev, dtype)
+    V = I.randn((B, Hkv, cap, D), 12 + D + G, dev, dtype)
+    q = I.randn((B, Hq, D), 13 + D + G, dev, dtype)
+    lens = torch.tensor([[1037, 1], [300, 64]], dtype=torch.int32, device=dev)
+    scale = 1 / math.sqrt(D)
+    logits = torch.full((B, Hq, cap), float("nan"), device=dev)
+    lse = torch.empty((B, Hq), device=dev)
+    out = kvc.kvc_decode_attn(q, K, V, scale=scale, len=lens.flatten(), logits=logits, lse=lse)
+    assert kvc.kvc_device_status() == 0
+    ref, ref_lg, ref_lse = _oracle_decode(q, K, V, lens.cpu().numpy(), scale, G)
+    assert_close(out.cpu(), ref, TOL[dtype], "decode out")
+    assert_close(lse.cpu(), ref_lse, 1e-4, "lse")
+    lg = logits.cpu().numpy()
+    for (b, h), r in ref_lg.items():
+        assert_close(lg[b, h, :len(r)], r, 1e-4, f"logits {b},{h}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_decode_host_n_valid_and_empty(dtype):
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv, G, D, cap = 3, 1, 2, 128, 700
+    K = I.randn((B, Hkv, cap, D), 21, dev, dtype)
+    V = I.randn((B, Hkv, cap, D), 22, dev, dtype)
+    q = I.randn((B, Hkv * G, D), 23, dev, dtype)
+    scale = 1 / math.sqrt(D)
+    for n in (0, 1, 129, 700):
+        lse = torch.empty((B, Hkv * G), device=dev)
+        out = kvc.kvc_decode_attn(q, K, V, scale=scale, n_valid=n, lse=lse)
+        ref, _, ref_lse = _oracle_decode(q, K, V, np.full((B, Hkv), n), scale, G)
+        assert_close(out.cpu(), ref, TOL[dtype], f"n_valid={n}")
+        if n == 0:
+            assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_decode_strided_cache_view():
+    """A cache that is a slice of a larger buffer (slot stride > d_head, capacity padding)."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv, G, D = 2, 3, 2, 64
+    big_k = I.randn((B, Hkv, 900, 2 * D), 31, dev, torch.bfloat16)
+    big_v = I.randn((B, Hkv, 900, 2 * D), 32, dev, torch.bfloat16)
+    K, V = big_k[:, :, 100:800, D:], big_v[:, :, 100:800, D:]
+    q = I.randn((B, Hkv * G, D), 33, dev, torch.bfloat16)
+    out = kvc.kvc_decode_attn(q, K, V, scale=0.125, n_valid=650)
+    ref, _, _ = _oracle_decode(q, K, V, np.full((B, Hkv), 650), 0.125, G)
+    assert_close(out.cpu(), ref, TOL[torch.bfloat16], "strided")
+
+
+def test_append_tail_and_free_slot_layout():
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, H, cap, D = 2, 3, 10, 64
+    K = torch.zeros((B, H, cap, D), device=dev, dtype=torch.bfloat16)
+    V = torch.zeros_like(K)
+    lens = torch.tensor([0, 3, 9, 5, 2, 0], dtype=torch.int32, device=dev)
+    kn = I.randn((B, H, D), 41, dev, torch.bfloat16)
+    vn = I.randn((B, H, D), 42, dev, torch.bfloat16)
+    t = torch.tensor([77], dtype=torch.int64, device=dev)
+    pos = torch.full((B, H, cap), -1, dtype=torch.int32, device=dev)
+    kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_TAIL, kn, vn, t=t, len=lens, pos=pos)
+    assert kvc.kvc_device_status() == 0
+    before = [0, 3, 9, 5, 2, 0]
+    assert lens.cpu().tolist() == [x + 1 for x in before]
+    for r, s in enumerate(before):
+        b, h = divmod(r, H)
+        assert torch.equal(K[b, h, s], kn[b, h]) and torch.equal(V[b, h, s], vn[b, h])
+        assert int(pos[b, h, s]) == 77
+    # a full row records KVC_DEV_TAIL_FULL and is left untouched
+    lens2 = torch.tensor([cap, 0, 0, 0, 0, 0], dtype=torch.int32, device=dev)
+    snapshot = K.clone()
+    kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_TAIL, kn, vn, len=lens2)
+    assert kvc.kvc_device_status() == 1
+    assert torch.equal(K[0, 0], snapshot[0, 0]) and int(lens2[0]) == cap
+    # FREE_SLOT writes at the given slot, sets pos = t and score = 0
+    free = torch.tensor([4, 0, 9, 1, 1, 7], dtype=torch.int32, device=dev)
+    score = torch.ones((B, H, cap), device=dev)
+    kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_FREE_SLOT, kn, vn, t=t, free_slot=free, pos=pos,
+                          score=score)
+    assert kvc.kvc_device_status() == 0
+    for r, s in enumerate(free.cpu().tolist()):
+        b, h = divmod(r, H)
+        assert torch.equal(K[b, h, s], kn[b, h]) and float(score[b, h, s]) == 0.0
+        assert int(pos[b, h, s]) == 77
+
+
+@pytest.mark.parametrize("dtype,D,G,S,W", [(torch.float32, 64, 1, 4, 20),
+                                           (torch.bfloat16, 128, 2, 4, 37),
+                                           (torch.bfloat16, 64, 1, 0, 9),
+                                           (torch.float32, 256, 4, 2, 130)])
+def test_streaming_ring_rope_matches_oracle_every_step(dtype, D, G, S, W):
+    """Token by token from an empty cache: ring append then decode with RoPE at in-cache
+    positions; every step against the oracle's StreamingLLM decode from the full history."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv = 2, 2
+    Hq = Hkv * G
+    T = S + 3 * (W + 1) + 5
+    cap = S + W + 1 + 3                        # extra slots past the ring are never used
+    K = torch.zeros((B, Hkv, cap, D), device=dev, dtype=dtype)
+    V = torch.zeros_like(K)
+    qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, T, 50 + D + W, dev, dtype)
+    table = kvc.kvc_rope_table(S + W + 1, D, 10000.0).to(dev)
+    t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    rope = kvc.make_rope(S, W, t_dev, table)
+    scale = 1 / math.sqrt(D)
+    hk, hv = f64(ks), f64(vs)
+    for t in range(T):
+        t_dev.fill_(t)
+        kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_RING, ks[t], vs[t], t=t_dev, n_sink=S,
+                              window=W)
+        out = kvc.kvc_decode_attn(qs[t], K, V, scale=scale, rope=rope).cpu().numpy()
+        for b in range(B):
+            for h in range(Hq):
+                ref = oracle.stream_decode(t, S, W, f64(qs[t, b, h]), hk[:t + 1, b, h // G],
+                                           hv[:t + 1, b, h // G], scale)
+                assert_close(out[b, h], ref, TOL[dtype], f"t={t} b={b} h={h}")
+    assert kvc.kvc_device_status() == 0
+    # sinks never move once written
+    for a in range(min(S, T)):
+        assert torch.equal(K[:, :, a], ks[a]), "sink slot overwritten"
+
+
+def test_streaming_worked_example_positions():
+    """The pages' example: cache [0,1,2,3,6,7,8] decoding the next token uses positions 0..7.
+    With values one-hot per token, the output mixes exactly the tokens 0,1,2,3,6,7,8,9, and the
+    logits (rotated at cache positions) equal the oracle's."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    S, W, D = 4, 3, 64
+    K = torch.zeros((1, 1, S + W + 1, D), device=dev)
+    V = torch.zeros_like(K)
+    ks = I.randn((10, 1, 1, D), 61, dev)
+    vs = torch.zeros((10, 1, 1, D), device=dev)
+    for a in range(10):
+        vs[a, 0, 0, a] = 1.0
+    q = I.randn((1, 1, D), 62, dev)
+    table = kvc.kvc_rope_table(S + W + 1, D).to(dev)
+    t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    for t in range(10):
+        t_dev.fill_(t)
+        kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_RING, ks[t], vs[t], t=t_dev, n_sink=S, window=W)
+    logits = torch.zeros((1, 1, S + W + 1), device=dev)
+    out = kvc.kvc_decode_attn(q, K, V, scale=0.125, rope=kvc.make_rope(S, W, t_dev, table),
+                              logits=logits)[0, 0].cpu().numpy()
+    assert np.all(out[[4, 5]] == 0) and np.all(out[[0, 1, 2, 3, 6, 7, 8, 9]] > 0)
+    tok, cpos, qpos = oracle.stream_window(9, S, W)
+    assert list(cpos) == list(range(8)) and qpos == 7
+    ref = oracle.stream_decode(9, S, W, f64(q[0, 0]), f64(ks[:, 0, 0]), f64(vs[:, 0, 0]), 0.125)
+    assert_close(out, ref, 1e-5, "worked example")

@@ -1,0 +1,248 @@
+"""GPU parity: SnapKV selection, compaction and H2O, through the C ABI.
+
+Index contract.  Stage-exact: given the GPU's own fp32 window means (scores_out), the oracle's
+fp32 replay of pooling + group max + top-k must give bit-identical indices.  End-to-end: the GPU
+index set may differ from the fp64 oracle's only at positions whose oracle score is within a
+relative 1e-4 of the k-th threshold.  H2O is checked teacher-forced: every step starts the oracle
+from the GPU's state.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (TOL, assert_close, assert_rel, cuda_or_skip, f64, lib,
+                         topk_sets_agree)
+from kv_cache_compression_kvc_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_snapkv(q_obs, K, seq_len, L_obs, budget, pool_k, scale, kvc, pairs=None,
+                  rtol=1e-4):
+    dev = q_obs.device
+    B, Hq = q_obs.shape[:2]
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    n = seq_len - L_obs
+    scores = torch.empty((B, Hq, n), device=dev)
+    idx = kvc.kvc_snapkv_select(q_obs, K, seq_len=seq_len, L_obs=L_obs, budget=budget,
+                                scale=scale, pool_k=pool_k, scores_out=scores)
+    assert kvc.kvc_device_status() == 0
+    idx = idx.cpu().numpy()
+    s_gpu = scores.cpu().numpy()
+    n_keep = min(budget, seq_len)
+    assert idx.shape == (B, Hkv, n_keep)
+    pairs = pairs or [(b, h) for b in range(B) for h in range(Hkv)]
+    for b, h in pairs:
+        row = idx[b, h]
+        assert np.all(np.diff(row) > 0), "indices ascending"
+        ref_idx, ref_s, ref_score = oracle.snapkv_select(
+            f64(q_obs[b, h * G:(h + 1) * G]), f64(K[b, h, :seq_len]), budget, scale, pool_k)
+        # window means: fp32 (tensor-core or FMA) against fp64
+        assert_rel(s_gpu[b, h * G:(h + 1) * G], ref_s[:, :n], rtol, 1e-7, f"s {b},{h}")
+        # stage-exact replay from the GPU's own scores
+        replay = oracle.snapkv_stage_f32(s_gpu[b, h * G:(h + 1) * G], L_obs, budget, pool_k)
+        assert np.array_equal(replay, row), f"stage-exact indices differ at ({b},{h})"
+        # end-to-end against fp64
+        if budget < seq_len:
+            assert list(row[budget - L_obs:]) == list(range(n, seq_len)), "window kept"
+            topk_sets_agree(row[:budget - L_obs], ref_idx[:budget - L_obs], ref_score,
+                            budget - L_obs)
+        else:
+            assert list(row) == list(range(seq_len))
+    return idx
+
+
+def test_snapkv_tiny_workload_fp32():
+    """The tiny workload: fp32, Hq=8, Hkv=2, D=64, N=512, L_obs=32, pool 5, budget 128."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    w = I.WORKLOADS["tiny"]
+    q, k, v = I.prompt_qkv(1, 8, 2, 512, 64, w.seed, dev, torch.float32)
+    _check_snapkv(q[:, :, -32:].contiguous(), k, 512, 32, 128, 5, w.scale, kvc)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("B,Hq,Hkv,D,N,L_obs,budget", [
+    (2, 4, 2, 128, 1000, 20, 200),      # ragged N, window not a multiple of 32
+    (1, 6, 1, 256, 777, 64, 300),       # G = 6, D = 256, two tiles per head
+    (1, 2, 2, 64, 300, 7, 300),         # budget = N: identity
+    (1, 4, 1, 64, 130, 3, 9),           # tiny budget, pool edges
+])
+def test_snapkv_select_ragged(dtype, B, Hq, Hkv, D, N, L_obs, budget):
+    dev = cuda_or_skip()
+    kvc = lib()
+    q = I.randn((B, Hq, L_obs, D), 70 + N, dev, dtype)
+    K = I.randn((B, Hkv, N + 5, D), 71 + N, dev, dtype)      # cap > seq_len
+    _check_snapkv(q, K, N, L_obs, budget, 5, 1 / math.sqrt(D), kvc)
+
+
+def test_snapkv_exact_ties_keep_lowest_index():
+    """Identical keys give identical scores: the lower index must win every tie."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    D, N, L_obs = 64, 400, 16
+    K = I.randn((1, 1, N, D), 81, dev)
+    K[0, 0, :N - L_obs] = K[0, 0, 5]          # every prefix key the same: all scores tie
+    q = I.randn((1, 2, L_obs, D), 82, dev)
+    idx = _check_snapkv(q, K, N, L_obs, 50, 5, 0.125, kvc)
+    # interior pooled scores tie exactly; the two ends lose mass to zero padding
+    assert list(idx[0, 0, :34]) == list(range(2, 36))
+
+
+def test_compact_gather_bit_exact():
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, H, N, D, keep = 2, 3, 500, 128, 77
+    K = I.randn((B, H, N, D), 91, dev, torch.bfloat16)
+    V = I.randn((B, H, N, D), 92, dev, torch.bfloat16)
+    g = torch.Generator().manual_seed(93)
+    idx = torch.stack([torch.sort(torch.randperm(N, generator=g)[:keep]).values
+                       for _ in range(B * H)]).reshape(B, H, keep).to(torch.int32).to(dev)
+    Kd = torch.zeros((B, H, keep + 10, D), device=dev, dtype=torch.bfloat16)
+    Vd = torch.zeros_like(Kd)
+    pos = torch.zeros((B, H, keep + 10), dtype=torch.int32, device=dev)
+    lens = torch.zeros(B * H, dtype=torch.int32, device=dev)
+    kvc.kvc_compact_gather(K, V, idx, keep, Kd, Vd, pos_dst=pos, len_dst=lens)
+    assert kvc.kvc_device_status() == 0
+    il = idx.long()
+    assert torch.equal(Kd[:, :, :keep], torch.gather(K, 2, il[..., None].expand(-1, -1, -1, D)))
+    assert torch.equal(Vd[:, :, :keep], torch.gather(V, 2, il[..., None].expand(-1, -1, -1, D)))
+    assert torch.equal(pos[:, :, :keep], idx) and lens.tolist() == [keep] * (B * H)
+    bad = idx.clone()
+    bad[1, 2, 5] = N + 3
+    kvc.kvc_compact_gather(K, V, bad, keep, Kd, Vd)
+    assert kvc.kvc_device_status() == 3      # KVC_DEV_BAD_INDEX, row skipped
+
+
+def test_snapkv_then_decode_tiny():
+    """Select -> compact -> TAIL appends -> decode, against the oracle on the same kept rows."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    w = I.WORKLOADS["tiny"]
+    B, Hq, Hkv, D, N = 1, 8, 2, 64, 512
+    q, k, v = I.prompt_qkv(B, Hq, Hkv, N, D, w.seed, dev, torch.float32)
+    idx = kvc.kvc_snapkv_select(q[:, :, -32:].contiguous(), k, seq_len=N, L_obs=32, budget=128,
+                                scale=w.scale)
+    cap = 128 + w.steps
+    Kc = torch.zeros((B, Hkv, cap, D), device=dev)
+    Vc = torch.zeros_like(Kc)
+    lens = torch.zeros(B * Hkv, dtype=torch.int32, device=dev)
+    kvc.kvc_compact_gather(k, v, idx, 128, Kc, Vc, len_dst=lens)
+    qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, w.steps, w.seed, dev)
+    kept = idx.cpu().numpy()
+    for step in range(w.steps):
+        kvc.kvc_stream_append(Kc, Vc, kvc.KVC_APPEND_TAIL, ks[step], vs[step], len=lens)
+        out = kvc.kvc_decode_attn(qs[step], Kc, Vc, scale=w.scale, len=lens).cpu().numpy()
+        if step % 16 == 15 or step == 0:
+            for h in range(Hq):
+                kh = h // 4
+                Kr = np.concatenate([f64(k[0, kh])[kept[0, kh]], f64(ks[:step + 1, 0, kh])])
+                Vr = np.concatenate([f64(v[0, kh])[kept[0, kh]], f64(vs[:step + 1, 0, kh])])
+                ref, _, _ = oracle.attend(f64(qs[step, 0, h]), Kr, Vr, w.scale)
+                assert_close(out[0, h], ref, TOL[torch.float32], f"step {step} head {h}")
+    assert lens.tolist() == [128 + w.steps] * Hkv
+    assert kvc.kvc_device_status() == 0
+
+
+# --------------------------------------------------------------------------------- H2O
+def _h2o_run(B, H, N, D, budget, L_local, steps, dtype, seed, kvc, dev, check_every=1):
+    K_hh = budget - L_local
+    q, k, v = I.prompt_qkv(B, H, H, N, D, seed, dev, dtype)
+    scale = 1 / math.sqrt(D)
+    s_full = torch.empty((B, H, N), device=dev)
+    idx, score = kvc.kvc_h2o_prefill_select(q, k, seq_len=N, L_local=L_local, K_hh=K_hh,
+                                            scale=scale, s_full=s_full)
+    assert kvc.kvc_device_status() == 0
+    sf = s_full.cpu().numpy()
+    ix = idx.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            ref = oracle.h2o_prompt_scores(f64(q[b, h]), f64(k[b, h]), scale)
+            assert_rel(sf[b, h], ref, 1e-4, 1e-6, f"prompt scores {b},{h}")
+            assert abs(sf[b, h].sum() - N) < 1e-3 * N
+            assert np.array_equal(oracle.h2o_prompt_select(sf[b, h].astype(np.float64), L_local,
+                                                           K_hh), ix[b, h]), "stage-exact"
+            ref_idx = oracle.h2o_prompt_select(ref, L_local, K_hh)
+            topk_sets_agree(ix[b, h][:K_hh], ref_idx[:K_hh], ref[:N - L_local], K_hh)
+    assert np.allclose(score.cpu().numpy(), np.take_along_axis(sf, ix.astype(np.int64), 2))
+
+    cap = budget + 1
+    Kc = torch.zeros((B, H, cap, D), device=dev, dtype=dtype)
+    Vc = torch.zeros_like(Kc)
+    pos = torch.full((B, H, cap), -1, dtype=torch.int32, device=dev)
+    sc = torch.zeros((B, H, cap), device=dev)
+    kvc.kvc_compact_gather(k, v, idx, budget, Kc, Vc, pos_dst=pos)
+    sc[:, :, :budget] = score
+    free = torch.full((B * H,), budget, dtype=torch.int32, device=dev)
+    t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    qs, ks, vs = I.decode_qkv(B, H, H, D, steps, seed + 1, dev, dtype)
+    logits = torch.empty((B, H, cap), device=dev)
+    lse = torch.empty((B, H), device=dev)
+    for step in range(steps):
+        t = N + step
+        t_dev.fill_(t)
+        kvc.kvc_stream_append(Kc, Vc, kvc.KVC_APPEND_FREE_SLOT, ks[step], vs[step], t=t_dev,
+                              free_slot=free, pos=pos, score=sc)
+        check = step % check_every == 0 or step == steps - 1
+        if check:
+            K0, V0 = f64(Kc), f64(Vc)
+            pos0, s0 = pos.cpu().numpy().astype(np.int64), sc.cpu().numpy().astype(np.float64)
+        out = kvc.kvc_decode_attn(qs[step], Kc, Vc, scale=scale, n_valid=cap, logits=logits,
+                                  lse=lse)
+        kvc.kvc_h2o_accumulate_evict(logits, lse, sc, pos, free, n_slots=cap, t=t_dev,
+                                     L_local=L_local, budget=budget)
+        if not check:
+            continue
+        o_gpu, s_gpu, f_gpu = out.cpu().numpy(), sc.cpu().numpy(), free.cpu().numpy()
+        for b in range(B):
+            for h in range(H):
+                o_ref, s_ref, _, ev_ref = oracle.h2o_step(
+                    f64(qs[step, b, h]), K0[b, h], V0[b, h], pos0[b, h], s0[b, h], t, L_local,
+                    budget, scale)
+                assert_close(o_gpu[b, h], o_ref, TOL[dtype], f"H2O out step {step}")
+                assert_rel(s_gpu[b, h], s_ref, 1e-4, 1e-6, f"H2O s step {step}")
+                ev = oracle.h2o_evict_f32(s_gpu[b, h], pos0[b, h], t, L_local)
+                assert ev == int(f_gpu[b * H + h]), f"evictee step {step} ({b},{h})"
+                kept_pos = set(pos0[b, h]) - {pos0[b, h][ev]}
+                assert set(range(t - L_local + 1, t + 1)) <= kept_pos, "recent quota kept"
+    assert kvc.kvc_device_status() == 0
+
+
+def test_h2o_tiny_workload_teacher_forced():
+    """The tiny H2O run: fp32, 8 heads, N=512, budget 102 (51 recent + 51 heavy), 64 steps."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    _h2o_run(1, 8, 512, 64, 102, 51, 64, torch.float32, I.WORKLOADS["tiny"].seed + 7, kvc, dev)
+
+
+def test_h2o_bf16_ragged():
+    dev = cuda_or_skip()
+    kvc = lib()
+    _h2o_run(2, 3, 333, 128, 70, 35, 40, torch.bfloat16, 4321, kvc, dev, check_every=3)
+
+
+def test_h2o_evict_candidates_and_no_candidate_code():
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, H, n = 1, 2, 6
+    logits = torch.zeros((B, H, n), device=dev)
+    lse = torch.full((B, H), math.log(n), device=dev)        # alpha = 1/6 each
+    sc = torch.tensor([[[0.5, 0.2, 0.2, 0.9, 0.2, 0.0], [1, 1, 1, 1, 1, 1]]],
+                      dtype=torch.float32, device=dev)
+    pos = torch.tensor([[[3, 7, 5, 1, 20, 21], [0, 1, 2, 3, 4, 5]]], dtype=torch.int32,
+                       device=dev)
+    free = torch.full((2,), -9, dtype=torch.int32, device=dev)
+    t = torch.tensor([21], dtype=torch.int64, device=dev)
+    kvc.kvc_h2o_accumulate_evict(logits, lse, sc, pos, free, n_slots=n, t=t, L_local=2, budget=5)
+    assert kvc.kvc_device_status() == 0
+    assert int(free[0]) == 1               # tie at 0.2+1/6: larger position 7 is evicted
+    assert int(free[1]) == 5               # all tie: the largest candidate position (5 <= 19)
+    t.fill_(2)                             # row 0 now has no position <= t - L_local = 0
+    pos[0, 0] = torch.tensor([3, 7, 5, 9, 20, 21], dtype=torch.int32)
+    kvc.kvc_h2o_accumulate_evict(logits, lse, sc, pos, free, n_slots=n, t=t, L_local=2, budget=5)
+    assert kvc.kvc_device_status() == 6    # KVC_DEV_NO_CANDIDATE (row 0)
+    assert int(free[1]) == 0               # row 1: position 0 is the only candidate
