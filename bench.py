@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import math
@@ -85,7 +86,15 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def wait_first(self, timeout=3.0):
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout:
+            time.sleep(0.02)
+
+    def window(self, t_begin, t_end):
+        self.t_begin, self.t_end = t_begin, t_end
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -100,7 +109,10 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lo, hi = getattr(self, "t_begin", -1e30), getattr(self, "t_end", 1e30)
+        for ts, ln in self.lines:
+            if not (lo <= ts <= hi + 0.25):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -246,10 +258,13 @@ def run_gpu(args):
     build.build()
     kvc.load()
     w = I.WORKLOADS[args.workload]
+    if args.layers:
+        w = dataclasses.replace(w, layers=args.layers)
     R = WORKLOAD_CLASSES[args.workload](w, dev, kvc)
     stream = torch.cuda.current_stream()
 
-    total = args.warmup + args.steps
+    # distinct per-step inputs (reused cyclically past 64 steps)
+    total = min(args.warmup + args.steps, 64)
     inputs = [R.step_inputs(i, w.seed * 7 + 17) for i in range(total)]
     torch.cuda.synchronize()
 
@@ -274,7 +289,7 @@ def run_gpu(args):
             dist.barrier()
 
     for i in range(args.warmup):
-        R.load_inputs(*inputs[i])
+        R.load_inputs(*inputs[i % total])
         g_app.replay()
         g_dec.replay()
     bytes_per_launch = R.decode_bytes_per_launch()
@@ -289,15 +304,19 @@ def run_gpu(args):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        clocks.wait_first()
+        torch.cuda.synchronize()
+        t_host0 = time.perf_counter()
         ev_s.record(stream)
         for i in range(args.steps):
-            R.load_inputs(*inputs[args.warmup + i])
+            R.load_inputs(*inputs[(args.warmup + i) % len(inputs)])
             g_app.replay()
             marks[i][0].record(stream)
             g_dec.replay()
             marks[i][1].record(stream)
         ev_e.record(stream)
         torch.cuda.synchronize()
+        clocks.window(t_host0, time.perf_counter())
     barrier()
     elapsed_ms = ev_s.elapsed_time(ev_e)
     decode_ms = sum(a.elapsed_time(b) for a, b in marks) / args.steps / w.layers
@@ -306,7 +325,7 @@ def run_gpu(args):
         raise RuntimeError(f"device range check fired in the timed region: {code}")
 
     # --- end to end: host inputs -> C-ABI calls -> host outputs ------------------------------
-    host_in = [tuple(x.cpu().pin_memory() for x in inputs[i % total]) for i in range(args.steps)]
+    host_in = [tuple(x.cpu().pin_memory() for x in inputs[i]) for i in range(total)]
     host_out = torch.empty(R.out.shape, dtype=R.out.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host_in[0])
     d2h = host_out.numel() * host_out.element_size()
@@ -315,7 +334,7 @@ def run_gpu(args):
     barrier()
     e0.record(stream)
     for i in range(args.steps):
-        R.load_inputs(*host_in[i])
+        R.load_inputs(*host_in[i % total])
         R.appends()
         R.decodes()
         host_out.copy_(R.out, non_blocking=True)
@@ -403,8 +422,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (smaller case for profiling)")
     ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_CLASSES), default="streaming")
     ap.add_argument("--no-cpu-baseline", action="store_true")
