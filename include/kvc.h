@@ -218,6 +218,27 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
                            float scale, float *out, float *logits, int64_t logits_stride,
                            float *lse, void *ws, size_t ws_bytes, void *stream);
 
+/* Decode attention without a caller workspace.  No counterpart on the pages: this is a
+ * deployment convenience of this library.  Some callers cannot allocate device memory at the
+ * point where they decode -- an engine that fixes its whole memory plan at start-up, a plugin
+ * running inside another framework's stream capture (an allocation there would invalidate the
+ * capture), a process held to an external memory budget -- so they cannot hand
+ * kvc_decode_attn a workspace.  This entry point computes exactly what kvc_decode_attn
+ * computes (same arguments without ws / ws_bytes) using a scratch array of 8 MiB that the
+ * library keeps in its own device module: it allocates and frees nothing.
+ * Limits and rules:
+ *   - a problem whose workspace (kvc_decode_attn_workspace_bytes) exceeds 8 MiB is rejected
+ *     with KVC_ERR_WORKSPACE before anything is launched;
+ *   - the scratch is shared by every call in the process on that GPU and keeps the previous
+ *     call's contents; each call clears the part that must start at zero on its own stream,
+ *     but calls that may overlap on the GPU race on it -- order them on one stream;
+ *   - the scratch's device address is looked up once per device by the first call made with
+ *     that device current; make that first call before capturing a stream on that device. */
+kvc_status kvc_decode_attn_noalloc(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                                   const int32_t *len, int32_t n_valid, const kvc_rope *rope,
+                                   float scale, float *out, float *logits,
+                                   int64_t logits_stride, float *lse, void *stream);
+
 /* ---------------------------------------------------------------------------------------- */
 /* H2O score accumulation and eviction for one decode step.  [KVC] "Heavy-Hitter Oracle (H2O)
  * e a esparsidade de cauda pesada": s_j = sum_t alpha_{t,j}; when the cache is over its

@@ -115,6 +115,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 namespace kvc {
 
+void set_last_error(const char *msg) { g_last_error = msg; }
+
 DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm)
 {
     DecodePlan pl{};

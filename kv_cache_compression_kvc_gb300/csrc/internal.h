@@ -42,6 +42,8 @@ struct DecodePlan {
 };
 
 DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm);
+// Sets the calling thread's kvc_last_error() message.
+void set_last_error(const char *msg);
 cudaError_t launch_decode_attn_f32(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16(const DecodeParams &p, int D, int G, cudaStream_t stream);
 

@@ -70,6 +70,8 @@ SIGNATURES = {
     "kvc_decode_attn_workspace_bytes": (_SZ, [_I32] * 5),
     "kvc_decode_attn": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P, _I64, _P,
                                _P, _SZ, _P]),
+    "kvc_decode_attn_noalloc": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P,
+                                       _I64, _P, _P]),
     "kvc_h2o_accumulate_evict": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P,
                                         _I32, _I32, _P]),
     "kvc_h2o_prefill_workspace_bytes": (_SZ, [_I32] * 4),
@@ -225,6 +227,25 @@ def kvc_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
         _ptr(q), Hq, ctypes.byref(c), _ptr(len), -1 if n_valid is None else int(n_valid),
         ctypes.byref(rope) if rope is not None else None, float(scale), _ptr(out),
         _ptr(logits), lstride, _ptr(lse), wp, wb, _stream(stream)))
+    return out
+
+
+def kvc_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+                            scale: float, len: Optional[torch.Tensor] = None,
+                            n_valid: Optional[int] = None, rope: Optional[kvc_rope] = None,
+                            out: Optional[torch.Tensor] = None,
+                            logits: Optional[torch.Tensor] = None,
+                            lse: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """kvc_decode_attn without a workspace (the library's fixed 8 MiB scratch is used)."""
+    c = cache_view(k_cache, v_cache)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    lstride = logits.stride(-2) if logits is not None else 0
+    _check(load().kvc_decode_attn_noalloc(
+        _ptr(q), Hq, ctypes.byref(c), _ptr(len), -1 if n_valid is None else int(n_valid),
+        ctypes.byref(rope) if rope is not None else None, float(scale), _ptr(out),
+        _ptr(logits), lstride, _ptr(lse), _stream(stream)))
     return out
 
 
