@@ -59,7 +59,9 @@ enum {
     KVC_DEV_BAD_INDEX = 3,      /* gather index outside [0, src cap)                          */
     KVC_DEV_BAD_POSITION = 4,   /* negative text position                                     */
     KVC_DEV_BAD_LENGTH = 5,     /* len outside [0, cap]                                       */
-    KVC_DEV_NO_CANDIDATE = 6    /* H2O: cache over budget but no historical token to evict    */
+    KVC_DEV_NO_CANDIDATE = 6,   /* H2O: cache over budget but no historical token to evict    */
+    KVC_DEV_TIMEOUT = 7,        /* a bounded wait inside a kernel gave up (results invalid)   */
+    KVC_DEV_SCHEDULE = 8        /* internal schedule bound violated (results invalid)         */
 };
 
 /* A KV cache (or a prompt's keys/values) in device memory.
@@ -85,13 +87,15 @@ typedef struct {
  * a >= n_sink lives at slot n_sink + (a - n_sink) mod (window + 1).  When the token at text
  * position *t is decoded it attends to the sinks and to tokens max(n_sink, t-window) .. t;
  * each attended token's in-cache position is its rank in that set and the query's is
- * min(t, n_sink + window).  Keys are stored before rotation and rotated at those positions on
- * every call.  Pairing: dimension i with i + d_head/2, angle position * theta^(-2i/d_head).  */
+ * min(t, n_sink + window).  Keys are stored before rotation; the query and every key are
+ * rotated at those positions on every call (computed through their distance: the rotated dot
+ * product depends only on the query position minus the key position).  Pairing: dimension i
+ * with i + d_head/2, angle position * theta^(-2i/d_head).                                    */
 typedef struct {
     int32_t n_sink;         /* S  (4 in the pages' configuration)                            */
     int32_t window;         /* W                                                             */
     const int64_t *t;       /* device scalar: text position of the token being decoded       */
-    const float *cos_sin;   /* device [n_pos][d_head/2][2] = (cos, sin), see kvc_rope_table  */
+    const float *cos_sin;   /* device [n_pos][2][d_head/2]: cosines then sines (kvc_rope_table) */
     int32_t n_pos;          /* rows of cos_sin; must be >= n_sink + window + 1               */
     int32_t reserved;
 } kvc_rope;
@@ -123,9 +127,10 @@ uint64_t kvc_kv_bytes(uint64_t n_layers, uint64_t n_heads_kv, uint64_t d_head, u
 kvc_status kvc_pyramid_budgets(int32_t n_layers, int64_t b_target, int64_t ratio_num,
                                int64_t ratio_den, int64_t *out);
 
-/* RoPE table, host: out[p][i][0] = cos(p*theta^(-2i/d_head)), out[p][i][1] = sin(...) for
- * p < n_pos, i < d_head/2, computed in double and rounded to fp32.  out: host
- * float[n_pos * d_head]; the caller uploads it for kvc_rope.cos_sin. */
+/* RoPE table, host: out[p][0][i] = cos(p*theta^(-2i/d_head)), out[p][1][i] = sin(...) for
+ * p < n_pos, i < d_head/2 (each row: d_head/2 cosines, then d_head/2 sines), computed in double
+ * and rounded to fp32.  out: host float[n_pos * d_head]; the caller uploads it for
+ * kvc_rope.cos_sin. */
 kvc_status kvc_rope_table(int32_t n_pos, int32_t d_head, double theta, float *out);
 
 /* ---------------------------------------------------------------------------------------- */

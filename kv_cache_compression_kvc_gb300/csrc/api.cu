@@ -119,27 +119,21 @@ void set_last_error(const char *msg) { g_last_error = msg; }
 
 DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm)
 {
+    // The decode kernel divides the P = B*Hkv pairs' slot tiles evenly over at most C = 2*n_sm
+    // persistent blocks (two per SM).  A pair's tiles then meet at most floor(C / P) + 2
+    // blocks, which bounds the partial states kept per pair; the bound does not depend on the
+    // tile size (so not on the element type either).
+    (void)cap;
     DecodePlan pl{};
     const long long pairs = (long long)B * Hkv;
-    const long long target = 8LL * (n_sm > 0 ? n_sm : 152);
-    const int min_chunk = 64;
-    long long max_splits = cap > 0 ? (cap + min_chunk - 1) / min_chunk : 1;
-    long long n_splits = (target + pairs - 1) / pairs;
-    n_splits = std::max(1LL, std::min(n_splits, max_splits));
-    long long chunk = cap > 0 ? (cap + n_splits - 1) / n_splits : 0;
-    chunk = (chunk + 15) / 16 * 16;
-    if (chunk > 0) n_splits = (cap + chunk - 1) / chunk;
-    if (n_splits < 1) n_splits = 1;
-    pl.n_splits = (int)n_splits;
-    pl.chunk = (int)std::max(chunk, 16LL);
-    if (pl.n_splits == 1) {
-        pl.chunk = std::max(cap, 1);
-        return pl;   // no workspace: the single block writes the output
-    }
-    const size_t rows = (size_t)B * Hq;
+    const long long ctas = 2LL * (n_sm > 0 ? n_sm : 152);
+    long long max_seg = ctas / pairs + 2;
+    if (max_seg > ctas) max_seg = ctas;
+    pl.max_seg = (int)max_seg;
+    const size_t G = (size_t)(Hq / Hkv);
     pl.off_o = 0;
-    pl.off_ml = align256(pl.off_o + rows * n_splits * D * sizeof(float));
-    pl.off_cnt = align256(pl.off_ml + rows * n_splits * 2 * sizeof(float));
+    pl.off_ml = align256(pl.off_o + (size_t)pairs * max_seg * G * D * sizeof(float));
+    pl.off_cnt = align256(pl.off_ml + (size_t)pairs * max_seg * G * 2 * sizeof(float));
     pl.bytes = align256(pl.off_cnt + (size_t)pairs * sizeof(int32_t));
     return pl;
 }
@@ -214,8 +208,8 @@ kvc_status kvc_rope_table(int32_t n_pos, int32_t d_head, double theta, float *ou
     for (int32_t p = 0; p < n_pos; ++p)
         for (int i = 0; i < half; ++i) {
             const double a = (double)p * inv_freq[i];
-            out[((size_t)p * half + i) * 2] = (float)std::cos(a);
-            out[((size_t)p * half + i) * 2 + 1] = (float)std::sin(a);
+            out[(size_t)p * d_head + i] = (float)std::cos(a);
+            out[(size_t)p * d_head + half + i] = (float)std::sin(a);
         }
     return ok();
 }
@@ -272,12 +266,10 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
     if (st != KVC_OK) return st;
     const kvc::DecodePlan pl = kvc::decode_plan(cache->batch, n_heads_q, cache->n_heads_kv,
                                                 cache->d_head, cache->cap, n_sm);
-    if (pl.bytes > 0) {
-        if (ws == nullptr || ws_bytes < pl.bytes)
-            return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn: workspace needs %zu bytes, got %zu",
-                        pl.bytes, ws_bytes);
-        if (!aligned256(ws)) return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn: workspace alignment");
-    }
+    if (ws == nullptr || ws_bytes < pl.bytes)
+        return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn: workspace needs %zu bytes, got %zu",
+                    pl.bytes, ws_bytes);
+    if (!aligned256(ws)) return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn: workspace alignment");
     kvc::DecodeParams p{};
     p.q = q;
     p.k = cache->k;
@@ -293,16 +285,21 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = out; p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;
     char *wsb = static_cast<char *>(ws);
-    p.ws_o = pl.bytes ? reinterpret_cast<float *>(wsb + pl.off_o) : nullptr;
-    p.ws_ml = pl.bytes ? reinterpret_cast<float *>(wsb + pl.off_ml) : nullptr;
-    p.ws_cnt = pl.bytes ? reinterpret_cast<int32_t *>(wsb + pl.off_cnt) : nullptr;
-    p.n_splits = pl.n_splits;
-    p.chunk = pl.chunk;
+    p.ws_o = reinterpret_cast<float *>(wsb + pl.off_o);
+    p.ws_ml = reinterpret_cast<float *>(wsb + pl.off_ml);
+    p.ws_cnt = reinterpret_cast<int32_t *>(wsb + pl.off_cnt);
+    p.P = cache->batch * cache->n_heads_kv;
+    p.max_seg = pl.max_seg;
+    p.n_sm = n_sm > 0 ? n_sm : 152;
     p.dev_code = code;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cache->dtype == KVC_BF16
-                        ? kvc::launch_decode_attn_bf16(p, cache->d_head, G, s)
-                        : kvc::launch_decode_attn_f32(p, cache->d_head, G, s);
+    cudaError_t e;
+    if (cache->dtype == KVC_BF16)
+        e = p.rope ? kvc::launch_decode_attn_bf16_rope(p, cache->d_head, G, s)
+                   : kvc::launch_decode_attn_bf16(p, cache->d_head, G, s);
+    else
+        e = p.rope ? kvc::launch_decode_attn_f32_rope(p, cache->d_head, G, s)
+                   : kvc::launch_decode_attn_f32(p, cache->d_head, G, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     return ok();
 }

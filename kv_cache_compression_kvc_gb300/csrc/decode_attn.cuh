@@ -1,22 +1,39 @@
-// decode_attn.cuh -- decode attention over the retained slots of a KV cache.
+// decode_attn.cuh -- decode attention over the retained slots of a KV cache (sm_103a).
 //
 // What it computes ("O KV cache", llmdeepdive 7.2, "01 · Conceito"): the new token's query
-// attends to every cached key of its KV head and mixes the cached values -- exact causal
+// attends to every valid cached key of its KV head and mixes the cached values -- exact causal
 // attention.  Where the time goes ("Compressão e Poda Dinâmica de KV Cache", "O gargalo de
-// memória do KV Cache..."): every emitted token reads the whole cache from HBM in a GEMV at
-// 1-2 FLOP per byte, so this kernel is an HBM stream.  How it is parallelised ("Implementação
-// prática em vLLM e SGLang": FlashDecoding splits the work along the time axis): the slots of
-// each (batch, KV head) are cut into n_splits contiguous chunks, one thread block each; each
-// block keeps an online softmax state (max m, sum l, weighted values o) for all G query heads
-// of the group, and the last block to finish a KV head (atomic ticket, nobody waits) merges
-// the chunk states by log-sum-exp.
+// memória do KV Cache..."): every emitted token reads the whole retained cache from HBM in a
+// GEMV at 1-2 FLOP per byte, so this kernel is an HBM stream.  How the work is split
+// ("Implementação prática em vLLM e SGLang": FlashDecoding parallelises along the time axis):
+// the slots of every (batch, KV head) pair are cut into tiles, and the flattened sequence of
+// (pair, tile) work items is divided evenly among persistent thread blocks, so a pair's slots
+// may be shared by several blocks; each block keeps an online-softmax state (max m, sum l,
+// weighted values o) per query head of the group, and when a pair spans several blocks the last
+// block to finish it (atomic ticket, no waiting) merges the states by log-sum-exp.
 //
-// Lane layout.  A key row of D elements is read by LPK = D/(2*VW) lanes; lane lk holds the VW
-// elements starting at lk*VW in the first half of the row and the VW elements at the same
-// offset in the second half, so the two members of every RoPE pair (i, i + D/2) sit in one
-// lane and rotating keys needs no shuffle.  32/LPK keys are in flight per warp step, UNR steps
-// are loaded before any arithmetic (K and V together) to keep enough bytes in flight.
-// Arithmetic is fp32; q is pre-scaled by scale*log2(e) so the softmax uses exp2.
+// Data movement.  K and V tiles (TK slots x d_head; 16 KB of keys per tile) stream from HBM into
+// an NS-stage shared-memory ring with cp.async.bulk issued by one thread, completion tracked by
+// mbarriers (transaction bytes); the block's eight warps compute from shared memory and release
+// each stage through a second mbarrier, after which the issuing thread refills it NS tiles
+// ahead.  Bytes in flight per SM come from the ring depth and the blocks per SM, not registers.
+//
+// Arithmetic.  fp32 throughout, with Blackwell's packed fp32x2 FMA (two lanes of a float2 per
+// instruction) for the q.k dot products and the p*v accumulation.  A key row is read by
+// LPK = D/(2*VW) lanes; lane lk holds the VW elements at lk*VW of the first half of the row and
+// the VW elements at the same offset of the second half, so both members of every RoPE pair
+// (i, i + D/2) sit in one lane.  q is pre-scaled by scale*log2(e) so the softmax is base 2; the
+// running max only moves when a logit exceeds it by more than 2^8 (the weights stay below 256,
+// far from fp32 overflow), which spares most rescales of o.
+//
+// RoPE at in-cache positions ("attention sinks", "como funciona"): the logit of query position
+// p_q against key position p_k depends only on the distance p_q - p_k, since rotations compose:
+// (R(p_q) q).(R(p_k) k) = q.R(p_k - p_q) k.  So q is never rotated; every key is combined with q
+// through the rotation by its distance, whose cos and sin come from the distance-indexed table
+// (planar rows: d_head/2 cosines then d_head/2 sines).
+//
+// Waits on mbarriers are bounded: after kMbarSpinLimit failed polls the thread records
+// KVC_DEV_TIMEOUT and carries on (results are then garbage, but the kernel always finishes).
 #pragma once
 
 #include "common.cuh"
@@ -24,321 +41,553 @@
 
 namespace kvc {
 
-template <typename T, int D, int G, int VW, int NW, int UNR>
-__global__ void __launch_bounds__(NW * 32)
+constexpr int kDecodeWarps = 8;
+constexpr int kDecodeThreads = kDecodeWarps * 32;
+constexpr int kDecodeTileKeyBytes = 16384;   // bytes of keys per tile
+constexpr uint32_t kMbarSpinLimit = 1u << 22;
+constexpr int kDevCodeTimeout = 7;           // KVC_DEV_TIMEOUT
+constexpr int kDevCodeSchedule = 8;          // KVC_DEV_SCHEDULE
+constexpr float kLazyMaxSlack = 8.0f;        // log2 units
+
+// ---- PTX helpers -----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int32_t *code)
+{
+    for (uint32_t it = 0; it < kMbarSpinLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return;
+    record_code(code, kDevCodeTimeout);
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// VW elements of T at a shared address, widened to VW/2 float2 (consecutive elements paired).
+template <typename T, int VW>
+__device__ __forceinline__ void lds_pairs(uint32_t addr, float2 *f)
+{
+    if constexpr (sizeof(T) == 4) {
+        static_assert(VW == 4, "fp32 lane vector");
+        float4 x;
+        asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                     : "r"(addr));
+        f[0] = make_float2(x.x, x.y);
+        f[1] = make_float2(x.z, x.w);
+    } else if constexpr (VW == 8) {
+        uint32_t a, b, c, d;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                     : "r"(addr));
+        f[0] = make_float2(bf16_lo(a), bf16_hi(a));
+        f[1] = make_float2(bf16_lo(b), bf16_hi(b));
+        f[2] = make_float2(bf16_lo(c), bf16_hi(c));
+        f[3] = make_float2(bf16_lo(d), bf16_hi(d));
+    } else {
+        static_assert(VW == 4, "bf16 lane vector");
+        uint32_t a, b;
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+        f[0] = make_float2(bf16_lo(a), bf16_hi(a));
+        f[1] = make_float2(bf16_lo(b), bf16_hi(b));
+    }
+}
+
+// Persistent schedule: tile t (pair-major) belongs to block floor(((t+1)*C - 1) / T).
+__device__ __forceinline__ int cta_of_tile(long long t, long long T, int C)
+{
+    return (int)(((t + 1) * (long long)C - 1) / T);
+}
+
+// Shared-memory plan of one instantiation (host and device agree): two blocks per SM with a
+// three-stage ring where they fit (and the group is small enough for 128 registers a thread),
+// else one block with a deeper ring.
+template <typename T, int D, int G>
+struct DecodeSmem {
+    static constexpr int TK = kDecodeTileKeyBytes / (D * (int)sizeof(T));
+    static constexpr int kTileBytes = TK * D * (int)sizeof(T);
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kMergeBytes = kDecodeWarps * G * (D + 2) * 4 + 16;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kTwoBlockBytes = kBarBytes + 3 * kStageBytes + kMergeBytes;
+    static constexpr int CPS = (G <= 4 && 2 * (kTwoBlockBytes + 1024) <= 233472) ? 2 : 1;
+    static constexpr int NS_one = (220 * 1024 - kMergeBytes - kBarBytes) / kStageBytes;
+    static constexpr int NS = CPS == 2 ? 3 : (NS_one > 6 ? 6 : NS_one);
+    static_assert(NS >= 2, "decode pipeline needs at least two stages");
+    static constexpr int kBytes = kBarBytes + NS * kStageBytes + kMergeBytes;
+};
+
+template <typename T, int D, int G, int VW, int UNR, bool ROPE, int CPS>
+__global__ void __launch_bounds__(kDecodeThreads, CPS)
 decode_attn_kernel(const DecodeParams p)
 {
+    using SM = DecodeSmem<T, D, G>;
+    constexpr int TK = SM::TK;
+    constexpr int NS = SM::NS;
+    constexpr int NW = kDecodeWarps;
     constexpr int HALF = D / 2;
     constexpr int LPK = HALF / VW;
     static_assert(LPK >= 1 && LPK <= 32 && (32 % LPK) == 0, "lane layout");
+    static_assert(VW % 2 == 0, "pairs of elements");
     constexpr int KPW = 32 / LPK;
-    constexpr int E = 2 * VW;
+    constexpr int P2 = VW / 2;          // float2 per half-row per lane
+    constexpr int KEYS_PER_STEP = NW * KPW * UNR;
+    static_assert(TK % KEYS_PER_STEP == 0, "tile must be a whole number of steps");
+    constexpr int STEPS = TK / KEYS_PER_STEP;
+    constexpr int EB = (int)sizeof(T);
 
-    const int split = blockIdx.x;
-    const int kh = blockIdx.y;
-    const int b = blockIdx.z;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bar_full = sbase;                 // NS x 8 bytes
+    const uint32_t bar_empty = sbase + 8 * NS;       // NS x 8 bytes
+    const uint32_t stage0 = sbase + SM::kBarBytes;
+    float *sm_m = reinterpret_cast<float *>(smem + SM::kBarBytes + NS * SM::kStageBytes);
+    float *sm_l = sm_m + NW * G;
+    float *sm_o = sm_l + NW * G;                     // [NW][G][D]
+    int *sm_flag = reinterpret_cast<int *>(sm_o + NW * G * D);
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int C = gridDim.x;
+    const int cta = blockIdx.x;
+    const long long T_all = (long long)p.P * p.NT;
+    const long long t_begin = (long long)cta * T_all / C;
+    const long long t_end = (long long)(cta + 1) * T_all / C;
+    const int n_tiles = (int)(t_end - t_begin);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, NW);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // ---- decode position (StreamingLLM layout) --------------------------------------------
+    int64_t tpos = 0;
+    int qpos = 0, ring_base = 0;
+    if (ROPE) {
+        tpos = *p.t;
+        if (tpos < 0) {
+            if (threadIdx.x == 0) record_code(p.dev_code, 4 /* KVC_DEV_BAD_POSITION */);
+            tpos = 0;
+        }
+        const int64_t sw = (int64_t)p.S + p.W;
+        qpos = (int)(tpos < sw ? tpos : sw);
+        if (tpos >= p.S) ring_base = (int)((tpos - p.S) % (int64_t)(p.W + 1));
+    }
+    // slots of pair q that may hold valid keys
+    auto pair_slots = [&](int q) -> int {
+        if (ROPE) return min(p.S + p.W + 1, p.cap);
+        if (p.len != nullptr) {
+            const int n = p.len[q];
+            return n < 0 ? 0 : (n > p.cap ? p.cap : n);
+        }
+        return p.n_valid;
+    };
+    // in-cache distance qpos - pos of physical slot j, and whether the slot is attended
+    auto slot_dist = [&](int j, bool &ok) -> int {
+        if (j < p.S) {
+            ok = ok && (j <= tpos);
+            return qpos - j;
+        }
+        int dd = ring_base - (j - p.S);
+        if (dd < 0) dd += p.W + 1;
+        ok = ok && (tpos >= p.S) && ((int64_t)dd <= tpos - p.S);
+        return dd;
+    };
+
+    // ---- tile loader: thread 0 issues the bulk copies of tile i into stage i % NS ----------
+    const bool dense = (p.ss == D);
+    auto issue_tile = [&](int i) {
+        const long long t = t_begin + i;
+        const int s = i % NS;
+        const int q = (int)(t / p.NT);
+        const int j0 = (int)(t % p.NT) * TK;
+        const int rows = max(0, min(TK, pair_slots(q) - j0));
+        const uint32_t full = bar_full + 8 * s;
+        const uint32_t kdst = stage0 + s * SM::kStageBytes;
+        const uint32_t vdst = kdst + SM::kTileBytes;
+        const int b = q / p.Hkv, kh = q % p.Hkv;
+        const size_t base = (size_t)b * p.sb + (size_t)kh * p.sh;
+        const T *kb = static_cast<const T *>(p.k) + base;
+        const T *vb = static_cast<const T *>(p.v) + base;
+        if (rows == 0) {
+            mbar_arrive(full);
+            return;
+        }
+        mbar_arrive_expect_tx(full, (uint32_t)(2 * rows * D * EB));
+        if (dense) {
+            bulk_g2s(kdst, kb + (size_t)j0 * D, rows * D * EB, full);
+            bulk_g2s(vdst, vb + (size_t)j0 * D, rows * D * EB, full);
+        } else {
+            for (int r = 0; r < rows; ++r) {
+                bulk_g2s(kdst + r * D * EB, kb + (size_t)(j0 + r) * p.ss, D * EB, full);
+                bulk_g2s(vdst + r * D * EB, vb + (size_t)(j0 + r) * p.ss, D * EB, full);
+            }
+        }
+    };
+    if (threadIdx.x == 0)
+        for (int i = 0; i < NS && i < n_tiles; ++i) issue_tile(i);
+
+    // ================================= compute ===================================================
     const int lk = lane % LPK;
     const int ks = lane / LPK;
     const int d0 = lk * VW;
-    const int bkh = b * p.Hkv + kh;
 
-    // ---- valid slots ----------------------------------------------------------------------
-    int n_slots;
-    int64_t t = 0;
-    int qpos = 0, ring_base = 0;
-    if (p.rope) {
-        t = *p.t;
-        if (t < 0) {
-            record_code(p.dev_code, 4 /* KVC_DEV_BAD_POSITION */);
-            t = 0;
-        }
-        n_slots = p.S + p.W + 1;
-        const int64_t sw = (int64_t)p.S + p.W;
-        qpos = (int)(t < sw ? t : sw);
-        if (t >= p.S) ring_base = (int)((t - p.S) % (int64_t)(p.W + 1));
-    } else if (p.len != nullptr) {
-        n_slots = p.len[bkh];
-        if (n_slots < 0 || n_slots > p.cap) {
-            if (split == 0 && threadIdx.x == 0) record_code(p.dev_code, 5 /* BAD_LENGTH */);
-            n_slots = n_slots < 0 ? 0 : p.cap;
-        }
-    } else {
-        n_slots = p.n_valid;
-    }
-    const int s_begin = split * p.chunk;
-    const int s_end = min(s_begin + p.chunk, n_slots);
+    float2 q1[G][P2], q2[G][P2], q2n[G][P2];   // q halves (pre-scaled); q2n = -q2 (RoPE form)
+    float2 o1[G][P2], o2[G][P2];
+    float m[G], l[G];
+    int cur = -1;              // pair in progress
+    int cur_slots = 0;
 
-    // ---- query: G heads, this lane's 2*VW dims, rotated and pre-scaled --------------------
-    float qf[G][E];
-    {
+    auto start_pair = [&](int q) {
+        cur = q;
+        cur_slots = pair_slots(q);
+        const int b = q / p.Hkv, kh = q % p.Hkv;
         const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)kh * G) * D;
-        float cs[2 * VW];
-        if (p.rope) {
-            const float *row = p.cos_sin + ((size_t)qpos * HALF + d0) * 2;
-#pragma unroll
-            for (int i = 0; i < 2 * VW; ++i) cs[i] = row[i];
-        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            load_cached<T, VW>(qb + (size_t)g * D + d0, &qf[g][0]);
-            load_cached<T, VW>(qb + (size_t)g * D + HALF + d0, &qf[g][VW]);
-            if (p.rope) {
+            float a[VW], c[VW];
+            load_cached<T, VW>(qb + (size_t)g * D + d0, a);
+            load_cached<T, VW>(qb + (size_t)g * D + HALF + d0, c);
 #pragma unroll
-                for (int i = 0; i < VW; ++i) {
-                    const float x1 = qf[g][i], x2 = qf[g][VW + i];
-                    const float c = cs[2 * i], s = cs[2 * i + 1];
-                    qf[g][i] = x1 * c - x2 * s;
-                    qf[g][VW + i] = x1 * s + x2 * c;
+            for (int i = 0; i < P2; ++i) {
+                q1[g][i] = make_float2(a[2 * i] * p.scale_log2, a[2 * i + 1] * p.scale_log2);
+                q2[g][i] = make_float2(c[2 * i] * p.scale_log2, c[2 * i + 1] * p.scale_log2);
+                q2n[g][i] = make_float2(-q2[g][i].x, -q2[g][i].y);
+                o1[g][i] = make_float2(0.f, 0.f);
+                o2[g][i] = make_float2(0.f, 0.f);
+            }
+            m[g] = kNegBig;
+            l[g] = 0.f;
+        }
+    };
+
+    // Merge this block's state for pair `q` and write the output or a partial state; the last
+    // block of a shared pair merges every partial.
+    auto finish_pair = [&](int q) {
+#pragma unroll
+        for (int off = LPK; off < 32; off <<= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float m_o = __shfl_xor_sync(0xffffffffu, m[g], off);
+                const float l_o = __shfl_xor_sync(0xffffffffu, l[g], off);
+                const float m_n = fmaxf(m[g], m_o);
+                const float c1 = ex2(m[g] - m_n), c2 = ex2(m_o - m_n);
+                l[g] = l[g] * c1 + l_o * c2;
+#pragma unroll
+                for (int i = 0; i < P2; ++i) {
+                    const float2 x = o1[g][i], y = o2[g][i];
+                    o1[g][i].x = x.x * c1 + __shfl_xor_sync(0xffffffffu, x.x, off) * c2;
+                    o1[g][i].y = x.y * c1 + __shfl_xor_sync(0xffffffffu, x.y, off) * c2;
+                    o2[g][i].x = y.x * c1 + __shfl_xor_sync(0xffffffffu, y.x, off) * c2;
+                    o2[g][i].y = y.y * c1 + __shfl_xor_sync(0xffffffffu, y.y, off) * c2;
+                }
+                m[g] = m_n;
+            }
+        }
+        if (ks == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float *row = sm_o + (warp * G + g) * D;
+#pragma unroll
+                for (int i = 0; i < P2; ++i) {
+                    row[d0 + 2 * i] = o1[g][i].x;
+                    row[d0 + 2 * i + 1] = o1[g][i].y;
+                    row[HALF + d0 + 2 * i] = o2[g][i].x;
+                    row[HALF + d0 + 2 * i + 1] = o2[g][i].y;
+                }
+                if (lk == 0) {
+                    sm_m[warp * G + g] = m[g];
+                    sm_l[warp * G + g] = l[g];
                 }
             }
-#pragma unroll
-            for (int e = 0; e < E; ++e) qf[g][e] *= p.scale_log2;
         }
-    }
-
-    float m[G], l[G], o[G][E];
+        __syncthreads();
+        const long long t_first = (long long)q * p.NT;
+        const int c_lo = cta_of_tile(t_first, T_all, C);
+        const int c_hi = cta_of_tile(t_first + p.NT - 1, T_all, C);
+        const int nseg = c_hi - c_lo + 1;
+        const int seg = cta - c_lo;
+        const bool seg_ok = nseg <= p.max_seg;   // guaranteed by the host plan; checked anyway
+        if (!seg_ok && threadIdx.x == 0) record_code(p.dev_code, kDevCodeSchedule);
+        const int rows0 = (q / p.Hkv) * p.Hq + (q % p.Hkv) * G;
+        for (int i = threadIdx.x; i < G * D; i += kDecodeThreads) {
+            const int g = i / D, d = i % D;
+            float M = sm_m[g];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = kNegBig;
-        l[g] = 0.f;
+            for (int w = 1; w < NW; ++w) M = fmaxf(M, sm_m[w * G + g]);
+            float L = 0.f, O = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[g][e] = 0.f;
-    }
+            for (int w = 0; w < NW; ++w) {
+                const float c = ex2(sm_m[w * G + g] - M);
+                L += sm_l[w * G + g] * c;
+                O += sm_o[(w * G + g) * D + d] * c;
+            }
+            if (nseg == 1) {
+                p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
+                if (d == 0 && p.lse != nullptr)
+                    p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+            } else if (seg_ok) {
+                const size_t slot = ((size_t)q * p.max_seg + seg) * G + g;
+                p.ws_o[slot * D + d] = O;
+                if (d == 0) {
+                    p.ws_ml[slot * 2] = M;
+                    p.ws_ml[slot * 2 + 1] = L;
+                }
+            }
+        }
+        if (nseg > 1 && seg_ok) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) *sm_flag = (atomicAdd(&p.ws_cnt[q], 1) == nseg - 1);
+            __syncthreads();
+            if (*sm_flag) {
+                __threadfence();
+                for (int i = threadIdx.x; i < G * D; i += kDecodeThreads) {
+                    const int g = i / D, d = i % D;
+                    float M = kNegBig;
+                    for (int sg = 0; sg < nseg; ++sg)
+                        M = fmaxf(M, __ldcg(&p.ws_ml[(((size_t)q * p.max_seg + sg) * G + g) * 2]));
+                    float L = 0.f, O = 0.f;
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const size_t slot = ((size_t)q * p.max_seg + sg) * G + g;
+                        const float c = ex2(__ldcg(&p.ws_ml[slot * 2]) - M);
+                        L += __ldcg(&p.ws_ml[slot * 2 + 1]) * c;
+                        O += __ldcg(&p.ws_o[slot * D + d]) * c;
+                    }
+                    p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
+                    if (d == 0 && p.lse != nullptr)
+                        p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+                }
+                if (threadIdx.x == 0) p.ws_cnt[q] = 0;   // leave the ticket zeroed
+            }
+        }
+        __syncthreads();   // the merge area is reused by the next pair
+    };
 
-    const T *kb = static_cast<const T *>(p.k) + (size_t)b * p.sb + (size_t)kh * p.sh;
-    const T *vb = static_cast<const T *>(p.v) + (size_t)b * p.sb + (size_t)kh * p.sh;
-    float *lg_out = p.logits ? p.logits + (size_t)(b * p.Hq + kh * G) * p.logits_stride : nullptr;
-
-    constexpr int STEP = KPW * UNR;
-    for (int blk = s_begin + warp * STEP; blk < s_end; blk += NW * STEP) {
-        RawVec<T, VW> kr[UNR][2], vr[UNR][2];
-        bool valid[UNR];
-        int kpos[UNR];
+    for (int i = 0; i < n_tiles; ++i) {
+        const long long t = t_begin + i;
+        const int s = i % NS;
+        const int q = (int)(t / p.NT);
+        if (q != cur) {
+            if (cur >= 0) finish_pair(cur);
+            start_pair(q);
+        }
+        mbar_wait(bar_full + 8 * s, (i / NS) & 1, p.dev_code);
+        const int j0 = (int)(t % p.NT) * TK;
+        const uint32_t kst = stage0 + s * SM::kStageBytes;
+        const uint32_t vst = kst + SM::kTileBytes;
+        float *lg_out =
+            p.logits ? p.logits + (size_t)((q / p.Hkv) * p.Hq + (q % p.Hkv) * G) * p.logits_stride
+                     : nullptr;
+#pragma unroll 1
+        for (int st = 0; st < STEPS; ++st) {
+            const int kbase = st * KEYS_PER_STEP + warp * KPW * UNR + ks;
+            float lg[UNR][G];
+            bool valid[UNR];
 #pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int j = blk + u * KPW + ks;
-            bool ok = j < s_end;
-            int pj = j;
-            if (p.rope && ok) {
-                if (j < p.S) {
-                    ok = j <= t;
+            for (int u = 0; u < UNR; ++u) {
+                const int kk = kbase + u * KPW;
+                const int j = j0 + kk;
+                bool ok = j < cur_slots;
+                int dist = 0;
+                if (ROPE) dist = slot_dist(j, ok);
+                valid[u] = ok;
+                float2 k1[P2], k2[P2];
+                const uint32_t row = kst + (uint32_t)(kk * D * EB);
+                lds_pairs<T, VW>(row + d0 * EB, k1);
+                lds_pairs<T, VW>(row + (HALF + d0) * EB, k2);
+                if constexpr (ROPE) {
+                    // rotate q by the key's distance and dot with the stored key
+                    const float *cs = p.cos_sin + (size_t)(ok ? dist : 0) * D;
+                    float2 cd[P2], sd[P2];
+#pragma unroll
+                    for (int i2 = 0; i2 < P2; i2 += 2) {
+                        const float4 c4 = __ldg(reinterpret_cast<const float4 *>(cs + d0 + 2 * i2));
+                        const float4 s4 =
+                            __ldg(reinterpret_cast<const float4 *>(cs + HALF + d0 + 2 * i2));
+                        cd[i2] = make_float2(c4.x, c4.y);
+                        sd[i2] = make_float2(s4.x, s4.y);
+                        cd[i2 + 1] = make_float2(c4.z, c4.w);
+                        sd[i2 + 1] = make_float2(s4.z, s4.w);
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int i2 = 0; i2 < P2; ++i2) {
+                            // u = q1 c - q2 s, w = q2 c + q1 s; logit += k1 u + k2 w
+                            const float2 uu =
+                                __ffma2_rn(q2n[g][i2], sd[i2], __fmul2_rn(q1[g][i2], cd[i2]));
+                            const float2 ww =
+                                __ffma2_rn(q1[g][i2], sd[i2], __fmul2_rn(q2[g][i2], cd[i2]));
+                            acc = __ffma2_rn(k1[i2], uu, acc);
+                            acc = __ffma2_rn(k2[i2], ww, acc);
+                        }
+                        lg[u][g] = acc.x + acc.y;
+                    }
                 } else {
-                    int dd = ring_base - (j - p.S);
-                    if (dd < 0) dd += p.W + 1;
-                    ok = (t >= p.S) && ((int64_t)dd <= t - p.S);
-                    pj = qpos - dd;
-                }
-            }
-            valid[u] = ok;
-            kpos[u] = pj;
-            if (ok) {
-                const size_t row = (size_t)j * p.ss;
-                kr[u][0].load(kb + row + d0);
-                kr[u][1].load(kb + row + HALF + d0);
-                vr[u][0].load(vb + row + d0);
-                vr[u][1].load(vb + row + HALF + d0);
-            } else {
-                kr[u][0].zero(); kr[u][1].zero();
-                vr[u][0].zero(); vr[u][1].zero();
-            }
-        }
-
-        float lg[UNR][G];
 #pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            float kf[E];
-            kr[u][0].to_float(&kf[0]);
-            kr[u][1].to_float(&kf[VW]);
-            if (p.rope && valid[u]) {
-                const float *row = p.cos_sin + ((size_t)kpos[u] * HALF + d0) * 2;
+                    for (int g = 0; g < G; ++g) {
+                        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < VW; i += 2) {
-                    const float4 cs = *reinterpret_cast<const float4 *>(row + 2 * i);
-                    const float a0 = kf[i], b0 = kf[VW + i];
-                    const float a1 = kf[i + 1], b1 = kf[VW + i + 1];
-                    kf[i] = a0 * cs.x - b0 * cs.y;
-                    kf[VW + i] = a0 * cs.y + b0 * cs.x;
-                    kf[i + 1] = a1 * cs.z - b1 * cs.w;
-                    kf[VW + i + 1] = a1 * cs.w + b1 * cs.z;
+                        for (int i2 = 0; i2 < P2; ++i2) {
+                            acc = __ffma2_rn(k1[i2], q1[g][i2], acc);
+                            acc = __ffma2_rn(k2[i2], q2[g][i2], acc);
+                        }
+                        lg[u][g] = acc.x + acc.y;
+                    }
                 }
             }
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float acc = 0.f;
+            for (int off = LPK / 2; off > 0; off >>= 1)
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc = fmaf(qf[g][e], kf[e], acc);
-                lg[u][g] = acc;
+                for (int u = 0; u < UNR; ++u)
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        lg[u][g] += __shfl_xor_sync(0xffffffffu, lg[u][g], off);
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                if (!valid[u]) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) lg[u][g] = -INFINITY;
+                } else if (lg_out != nullptr && lk == 0) {
+                    const int j = j0 + kbase + u * KPW;
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        lg_out[(size_t)g * p.logits_stride + j] = lg[u][g] * kLn2;
+                }
             }
-        }
-#pragma unroll
-        for (int off = LPK / 2; off > 0; off >>= 1) {
-#pragma unroll
-            for (int u = 0; u < UNR; ++u)
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    lg[u][g] += __shfl_xor_sync(0xffffffffu, lg[u][g], off);
-        }
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            if (!valid[u]) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) lg[u][g] = -INFINITY;
-            } else if (lg_out != nullptr && lk == 0) {
-                const int j = blk + u * KPW + ks;
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    lg_out[(size_t)g * p.logits_stride + j] = lg[u][g] * kLn2;
-            }
-        }
-
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float mx = lg[0][g];
-#pragma unroll
-            for (int u = 1; u < UNR; ++u) mx = fmaxf(mx, lg[u][g]);
-            const float m_new = fmaxf(m[g], mx);
-            const float corr = exp2f(m[g] - m_new);
-            l[g] *= corr;
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[g][e] *= corr;
-            m[g] = m_new;
-        }
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            float vf[E];
-            vr[u][0].to_float(&vf[0]);
-            vr[u][1].to_float(&vf[VW]);
+            // lazy running max: move it only when a logit exceeds it by more than the slack
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float pu = exp2f(lg[u][g] - m[g]);
-                l[g] += pu;
+                float mx = lg[0][g];
 #pragma unroll
-                for (int e = 0; e < E; ++e) o[g][e] = fmaf(pu, vf[e], o[g][e]);
+                for (int u = 1; u < UNR; ++u) mx = fmaxf(mx, lg[u][g]);
+                if (mx > m[g] + kLazyMaxSlack) {
+                    const float corr = ex2(m[g] - mx);
+                    l[g] *= corr;
+                    const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+                    for (int i2 = 0; i2 < P2; ++i2) {
+                        o1[g][i2] = __fmul2_rn(o1[g][i2], c2);
+                        o2[g][i2] = __fmul2_rn(o2[g][i2], c2);
+                    }
+                    m[g] = mx;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                // masked keys are skipped outright: their shared-memory rows may hold stale
+                // bytes, and 0 * (NaN or Inf) would poison the sum
+                if (!valid[u]) continue;
+                const int kk = kbase + u * KPW;
+                float2 v1[P2], v2[P2];
+                const uint32_t row = vst + (uint32_t)(kk * D * EB);
+                lds_pairs<T, VW>(row + d0 * EB, v1);
+                lds_pairs<T, VW>(row + (HALF + d0) * EB, v2);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float pu = ex2(lg[u][g] - m[g]);
+                    l[g] += pu;
+                    const float2 p2 = make_float2(pu, pu);
+#pragma unroll
+                    for (int i2 = 0; i2 < P2; ++i2) {
+                        o1[g][i2] = __ffma2_rn(p2, v1[i2], o1[g][i2]);
+                        o2[g][i2] = __ffma2_rn(p2, v2[i2], o2[g][i2]);
+                    }
+                }
             }
         }
-    }
-
-    // ---- merge the KPW lane groups of the warp --------------------------------------------
-#pragma unroll
-    for (int off = LPK; off < 32; off <<= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float m_o = __shfl_xor_sync(0xffffffffu, m[g], off);
-            const float l_o = __shfl_xor_sync(0xffffffffu, l[g], off);
-            const float m_n = fmaxf(m[g], m_o);
-            const float c1 = exp2f(m[g] - m_n), c2 = exp2f(m_o - m_n);
-            l[g] = l[g] * c1 + l_o * c2;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float o_o = __shfl_xor_sync(0xffffffffu, o[g][e], off);
-                o[g][e] = o[g][e] * c1 + o_o * c2;
-            }
-            m[g] = m_n;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (threadIdx.x == 0 && i + NS < n_tiles) {
+            // every warp has released stage s: refill it with tile i + NS
+            mbar_wait(bar_empty + 8 * s, (i / NS) & 1, p.dev_code);
+            issue_tile(i + NS);
         }
     }
-
-    // ---- merge the warps of the block ------------------------------------------------------
-    __shared__ float sm_m[NW][G], sm_l[NW][G];
-    __shared__ float sm_o[NW][G][D];
-    __shared__ int sm_last;
-    if (ks == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-#pragma unroll
-            for (int i = 0; i < VW; ++i) {
-                sm_o[warp][g][d0 + i] = o[g][i];
-                sm_o[warp][g][HALF + d0 + i] = o[g][VW + i];
-            }
-            if (lk == 0) {
-                sm_m[warp][g] = m[g];
-                sm_l[warp][g] = l[g];
-            }
-        }
-    }
-    __syncthreads();
-
-    const int rows0 = b * p.Hq + kh * G;   // first query row of this KV head
-    for (int i = threadIdx.x; i < G * D; i += NW * 32) {
-        const int g = i / D, d = i % D;
-        float M = sm_m[0][g];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) M = fmaxf(M, sm_m[w][g]);
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float c = exp2f(sm_m[w][g] - M);
-            L += sm_l[w][g] * c;
-            O += sm_o[w][g][d] * c;
-        }
-        if (p.n_splits == 1) {
-            p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
-            if (d == 0 && p.lse != nullptr)
-                p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-        } else {
-            const size_t slot = (size_t)(rows0 + g) * p.n_splits + split;
-            p.ws_o[slot * D + d] = O;
-            if (d == 0) {
-                p.ws_ml[slot * 2] = M;
-                p.ws_ml[slot * 2 + 1] = L;
-            }
-        }
-    }
-    if (p.n_splits == 1) return;
-
-    // ---- last block of this KV head merges the n_splits partial states ---------------------
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) sm_last = (atomicAdd(&p.ws_cnt[bkh], 1) == p.n_splits - 1);
-    __syncthreads();
-    if (!sm_last) return;
-    __threadfence();
-
-    for (int i = threadIdx.x; i < G * D; i += NW * 32) {
-        const int g = i / D, d = i % D;
-        const size_t base = (size_t)(rows0 + g) * p.n_splits;
-        float M = kNegBig;
-        for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, __ldcg(&p.ws_ml[(base + s) * 2]));
-        float L = 0.f, O = 0.f;
-        for (int s = 0; s < p.n_splits; ++s) {
-            const float c = exp2f(__ldcg(&p.ws_ml[(base + s) * 2]) - M);
-            L += __ldcg(&p.ws_ml[(base + s) * 2 + 1]) * c;
-            O += __ldcg(&p.ws_o[(base + s) * D + d]) * c;
-        }
-        p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
-        if (d == 0 && p.lse != nullptr)
-            p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-    }
-    if (threadIdx.x == 0) p.ws_cnt[bkh] = 0;   // leave the ticket zeroed for the next call
+    if (cur >= 0) finish_pair(cur);
 }
 
-// Elements per lane-half by (type, group size): keeps q and o (2*G*2*VW floats) in registers.
+// Elements per lane-half by (type, group size): keeps q and o (4*G*VW floats) in registers.
 template <typename T, int G>
 constexpr int decode_vw()
 {
     if constexpr (sizeof(T) == 4) return 4;
     else return G <= 2 ? 8 : 4;
 }
+constexpr int kDecodeUnroll = 2;
 
-constexpr int kDecodeWarps = 4;
-constexpr int kDecodeUnroll = 4;
-
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool ROPE>
 cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
 {
     constexpr int VW = decode_vw<T, G>();
-    dim3 grid(p.n_splits, p.Hkv, p.B);
-    decode_attn_kernel<T, D, G, VW, kDecodeWarps, kDecodeUnroll>
-        <<<grid, kDecodeWarps * 32, 0, stream>>>(p);
+    using SM = DecodeSmem<T, D, G>;
+    auto kern = decode_attn_kernel<T, D, G, VW, kDecodeUnroll, ROPE, SM::CPS>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SM::kBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    DecodeParams q = p;
+    q.NT = p.cap > 0 ? (p.cap + SM::TK - 1) / SM::TK : 1;
+    if (q.NT < 1) q.NT = 1;
+    const long long T_all = (long long)q.P * q.NT;
+    const long long max_ctas = (long long)p.n_sm * SM::CPS;
+    const int C = (int)(T_all < max_ctas ? T_all : max_ctas);
+    kern<<<C, kDecodeThreads, SM::kBytes, stream>>>(q);
     return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_decode_dtype(const DecodeParams &p, int D, int G, cudaStream_t stream)
+template <typename T, bool ROPE>
+cudaError_t launch_decode_variant(const DecodeParams &p, int D, int G, cudaStream_t stream)
 {
 #define KVC_DECODE_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_decode_typed<T, DD, GG>(p, stream);
+    if (D == DD && G == GG) return launch_decode_typed<T, DD, GG, ROPE>(p, stream);
 #define KVC_DECODE_D(DD) \
     KVC_DECODE_CASE(DD, 1) KVC_DECODE_CASE(DD, 2) KVC_DECODE_CASE(DD, 4) \
     KVC_DECODE_CASE(DD, 6) KVC_DECODE_CASE(DD, 8)

@@ -27,17 +27,16 @@ struct DecodeParams {
     float *logits;               // nullable, [B*Hq][logits_stride]
     int64_t logits_stride;
     float *lse;                  // nullable, [B*Hq]
-    float *ws_o;                 // [B*Hq][n_splits][D]
-    float *ws_ml;                // [B*Hq][n_splits][2]
-    int32_t *ws_cnt;             // [B*Hkv], zero between calls
-    int32_t n_splits;
-    int32_t chunk;               // slots per split
+    // persistent schedule: P = B*Hkv pairs of NT tiles each, split evenly over the blocks
+    int32_t P, NT, max_seg, n_sm;
+    float *ws_o;                 // [P][max_seg][G][D] partial weighted values
+    float *ws_ml;                // [P][max_seg][G][2] partial (max, sum)
+    int32_t *ws_cnt;             // [P] tickets, zero between calls
     int32_t *dev_code;
 };
 
 struct DecodePlan {
-    int32_t n_splits;
-    int32_t chunk;
+    int32_t max_seg;             // blocks that can share one (batch, KV head) pair
     size_t off_o, off_ml, off_cnt, bytes;
 };
 
@@ -46,6 +45,9 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm);
 void set_last_error(const char *msg);
 cudaError_t launch_decode_attn_f32(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16(const DecodeParams &p, int D, int G, cudaStream_t stream);
+cudaError_t launch_decode_attn_f32_rope(const DecodeParams &p, int D, int G, cudaStream_t stream);
+cudaError_t launch_decode_attn_bf16_rope(const DecodeParams &p, int D, int G,
+                                         cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------
 // Append, gather, position advance.

@@ -167,8 +167,8 @@ def kvc_pyramid_budgets(n_layers: int, b_target: int, ratio_num: int = 4, ratio_
 
 
 def kvc_rope_table(n_pos: int, d_head: int, theta: float = 10000.0) -> torch.Tensor:
-    """Host fp32 table [n_pos, d_head/2, 2] of (cos, sin); upload it for kvc_decode_attn."""
-    out = torch.empty((n_pos, d_head // 2, 2), dtype=torch.float32)
+    """Host fp32 table [n_pos, 2, d_head/2] (cosines, then sines); upload it for decode."""
+    out = torch.empty((n_pos, 2, d_head // 2), dtype=torch.float32)
     _check(load().kvc_rope_table(n_pos, d_head, theta, _ptr(out)))
     return out
 

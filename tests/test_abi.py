@@ -62,7 +62,7 @@ def test_rope_table_matches_oracle_rotation(kvc):
     rng = np.random.default_rng(3)
     x = rng.standard_normal(D)
     for p in (0, 1, 17, 299):
-        c, s = tab[p, :, 0], tab[p, :, 1]
+        c, s = tab[p, 0], tab[p, 1]
         y = np.concatenate([x[:D // 2] * c - x[D // 2:] * s, x[:D // 2] * s + x[D // 2:] * c])
         assert np.max(np.abs(y - oracle.rope(x, p))) < 1e-5   # fp32 table entries
 
