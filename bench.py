@@ -49,6 +49,15 @@ def dist_env():
     return rank, world, local
 
 
+def measured_tensor_peak():
+    """Sustained dense bf16 TFLOP/s (the select kernels run inside a long step)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return 1700.0
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -147,35 +156,23 @@ def kernel_traffic(kernel_file: str, key: str):
 
 
 # ----------------------------------------------------------------------------- workloads
-class Streaming:
-    """StreamingLLM decode: per layer append into the ring + RoPE decode over 4 + W + 1 slots."""
+def elem_bytes(dtype) -> int:
+    return torch.tensor([], dtype=dtype).element_size()
+
+
+class DecodeWorkload:
+    """A decode step = per layer: append the new token, decode attention (+ workload extras)."""
 
     kernel_file = "decode_attn.cuh"
-    traffic_key = "decode_attn/streaming"
 
     def __init__(self, w: I.Workload, dev, kvc):
         self.w, self.dev, self.kvc = w, dev, kvc
-        L, B, H, D, S, W = w.layers, w.batch, w.n_heads_kv, w.d_head, w.n_sink, w.window
-        self.slots = S + W + 1
-        self.K = torch.empty((L, B, H, self.slots, D), dtype=w.dtype, device=dev)
-        self.V = torch.empty_like(self.K)
-        ring_slot = [a if a < S else S + (a - S) % (W + 1) for a in
-                     list(range(S)) + list(range(w.prompt - W, w.prompt))]
-        idx = torch.tensor(ring_slot, device=dev)
-        for l in range(L):
-            k, v, _ = I.streaming_prefill(w, l, dev)
-            self.K[l][:, :, idx] = k
-            self.V[l][:, :, idx] = v
-        self.table = kvc.kvc_rope_table(self.slots, D, w.theta).to(dev)
-        self.t = torch.tensor([w.prompt], dtype=torch.int64, device=dev)
+        L, B, D = w.layers, w.batch, w.d_head
         self.q_s = torch.empty((L, B, w.n_heads_q, D), dtype=w.dtype, device=dev)
-        self.k_s = torch.empty((L, B, H, D), dtype=w.dtype, device=dev)
+        self.k_s = torch.empty((L, B, w.n_heads_kv, D), dtype=w.dtype, device=dev)
         self.v_s = torch.empty_like(self.k_s)
         self.out = torch.empty((L, B, w.n_heads_q, D), dtype=torch.float32, device=dev)
-        self.caches = [kvc.cache_view(self.K[l], self.V[l]) for l in range(L)]
-        self.rope = kvc.make_rope(S, W, self.t, self.table)
-        self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.slots, dev)
-        self.launches_per_step = 2 * L + 1
+        self.extra = {}
 
     def step_inputs(self, step, seed_base):
         w = self.w
@@ -192,6 +189,46 @@ class Streaming:
         self.k_s.copy_(k, non_blocking=True)
         self.v_s.copy_(v, non_blocking=True)
 
+    def qo_bytes(self):
+        w = self.w
+        return w.batch * w.n_heads_q * w.d_head * (elem_bytes(w.dtype) + 4)
+
+    def kv_bytes(self, slots):
+        w = self.w
+        return 2 * w.batch * w.n_heads_kv * slots * w.d_head * elem_bytes(w.dtype)
+
+
+class Streaming(DecodeWorkload):
+    """StreamingLLM decode: per layer append into the ring + RoPE decode over 4 + W + 1 slots."""
+
+    traffic_key = "decode_attn/streaming"
+
+    def __init__(self, w: I.Workload, dev, kvc):
+        super().__init__(w, dev, kvc)
+        L, B, H, D, S, W = w.layers, w.batch, w.n_heads_kv, w.d_head, w.n_sink, w.window
+        self.slots = S + W + 1
+        self.K = torch.empty((L, B, H, self.slots, D), dtype=w.dtype, device=dev)
+        self.V = torch.empty_like(self.K)
+        ring_slot = [a if a < S else S + (a - S) % (W + 1) for a in
+                     list(range(S)) + list(range(w.prompt - W, w.prompt))]
+        idx = torch.tensor(ring_slot, device=dev)
+        for l in range(L):
+            k, v, _ = I.streaming_prefill(w, l, dev)
+            self.K[l][:, :, idx] = k
+            self.V[l][:, :, idx] = v
+        self.table = kvc.kvc_rope_table(self.slots, D, w.theta).to(dev)
+        self.t = torch.tensor([w.prompt], dtype=torch.int64, device=dev)
+        self.caches = [kvc.cache_view(self.K[l], self.V[l]) for l in range(L)]
+        self.rope = kvc.make_rope(S, W, self.t, self.table)
+        self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.slots, dev)
+        self.launches_per_step = 2 * L + 1
+
+    def save_state(self):
+        return self.t.clone()
+
+    def restore_state(self, st):
+        self.t.copy_(st)
+
     def appends(self):
         kvc, w = self.kvc, self.w
         for l in range(w.layers):
@@ -206,13 +243,11 @@ class Streaming:
                                 out=self.out[l], ws=self.ws, cache=self.caches[l])
         kvc.kvc_position_advance(self.t, 1)
 
-    def decode_bytes_per_launch(self):
+    def decode_bytes(self, first_step, n_steps):
         """Algorithmic bytes of one decode launch: the attended K and V rows once, q and out."""
         w = self.w
-        n = min(int(self.t.item()) + 1, self.slots)
-        eb = torch.tensor([], dtype=w.dtype).element_size()
-        kv = 2 * w.batch * w.n_heads_kv * n * w.d_head * eb
-        return kv + w.batch * w.n_heads_q * w.d_head * (eb + 4)
+        n = min(w.prompt + first_step + 1, self.slots)
+        return self.kv_bytes(n) + self.qo_bytes()
 
     def describe(self):
         w = self.w
@@ -242,8 +277,245 @@ class Streaming:
         per = (time.perf_counter() - t0) / n
         return per, w.batch * w.n_heads_q * w.layers, n
 
+    def sample_description(self, n, slices):
+        return (f"{n} oracle StreamingLLM decodes of one (batch, head, layer) slice at the "
+                f"workload's shape, extrapolated to {slices} slices per step (extrapolated)")
 
-WORKLOAD_CLASSES = {"streaming": Streaming}
+
+class SelectDecode(DecodeWorkload):
+    """SnapKV selection per layer at the prompt, compaction, then TAIL-append decode steps.
+    The per-layer budget is the workload's (or the PyramidKV ramp)."""
+
+    traffic_key = "decode_attn/snapkv"
+
+    def __init__(self, w: I.Workload, dev, kvc, max_steps, pyramid=False):
+        super().__init__(w, dev, kvc)
+        L, B, Hkv, D = w.layers, w.batch, w.n_heads_kv, w.d_head
+        self.pyramid = pyramid
+        if pyramid:
+            self.budgets = kvc.kvc_pyramid_budgets(L, w.budget, w.pyramid_ratio, 1)
+        else:
+            self.budgets = [w.budget] * L
+        self.pre = max_steps
+        self.caps = [b + max_steps for b in self.budgets]
+        self.K, self.V, self.caches = [], [], []
+        self.lens = torch.zeros((L, B * Hkv), dtype=torch.int32, device=dev)
+        sel_ms, gat_ms = [], []
+        ws = torch.zeros(kvc.kvc_snapkv_select_workspace_bytes(
+            B, w.n_heads_q, Hkv, D, w.prompt, w.L_obs) + 256, dtype=torch.uint8, device=dev)
+        gen = I.pyramid_layer if pyramid else I.snapkv_layer
+        for l in range(L):
+            q_obs, k, v = gen(w, l, dev)
+            idx = torch.empty((B, Hkv, self.budgets[l]), dtype=torch.int32, device=dev)
+            Kc = torch.empty((B, Hkv, self.caps[l], D), dtype=w.dtype, device=dev)
+            Vc = torch.empty_like(Kc)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            torch.cuda.synchronize()
+            e[0].record()
+            kvc.kvc_snapkv_select(q_obs, k, seq_len=w.prompt, L_obs=w.L_obs,
+                                  budget=self.budgets[l], scale=w.scale, pool_k=w.pool_k,
+                                  idx_out=idx, ws=ws)
+            e[1].record()
+            kvc.kvc_compact_gather(k, v, idx, self.budgets[l], Kc, Vc, len_dst=self.lens[l])
+            e[2].record()
+            torch.cuda.synchronize()
+            sel_ms.append(e[0].elapsed_time(e[1]))
+            gat_ms.append(e[1].elapsed_time(e[2]))
+            self.K.append(Kc)
+            self.V.append(Vc)
+            self.caches.append(kvc.cache_view(Kc, Vc))
+            del q_obs, k, v
+        eb = elem_bytes(w.dtype)
+        sel_bytes = L * (B * Hkv * w.prompt * D * eb + B * w.n_heads_q * w.L_obs * D * eb)
+        sel_flop = L * 2.0 * B * w.n_heads_q * w.L_obs * w.prompt * D
+        gat_bytes = sum(2 * 2 * B * Hkv * b * D * eb + B * Hkv * b * 4 for b in self.budgets)
+        peak, _ = measured_peak()
+        tflops = measured_tensor_peak()
+        sel_roof = max(sel_bytes / (peak * 1e9), sel_flop / (tflops * 1e12)) * 1e3
+        gat_roof = gat_bytes / (peak * 1e9) * 1e3
+        self.extra["snapkv_select"] = {
+            "layers": L, "select_ms": round(sum(sel_ms), 3),
+            "compact_ms": round(sum(gat_ms), 3),
+            "select_roofline_ms": round(sel_roof, 3),
+            "select_frac": round(sel_roof / sum(sel_ms), 4),
+            "compact_roofline_ms": round(gat_roof, 3),
+            "compact_frac": round(gat_roof / sum(gat_ms), 4),
+            "algorithmic_select_bytes": sel_bytes, "select_flop": sel_flop,
+            "bound": "hbm" if sel_bytes / (peak * 1e9) >= sel_flop / (tflops * 1e12) else "tensor"}
+        self.ws = kvc.decode_workspace(B, w.n_heads_q, Hkv, D, max(self.caps), dev)
+        self.launches_per_step = 2 * L
+        self.appended = 0
+
+    def save_state(self):
+        return self.lens.clone()
+
+    def restore_state(self, st):
+        self.lens.copy_(st)
+
+    def appends(self):
+        kvc = self.kvc
+        for l in range(self.w.layers):
+            kvc.kvc_stream_append(None, None, kvc.KVC_APPEND_TAIL, self.k_s[l], self.v_s[l],
+                                  len=self.lens[l], cache=self.caches[l])
+
+    def decodes(self):
+        kvc, w = self.kvc, self.w
+        for l in range(w.layers):
+            kvc.kvc_decode_attn(self.q_s[l], None, None, scale=w.scale, len=self.lens[l],
+                                out=self.out[l], ws=self.ws, cache=self.caches[l])
+
+    def decode_bytes(self, first_step, n_steps):
+        tot = 0
+        for i in range(n_steps):
+            for b in self.budgets:
+                tot += self.kv_bytes(b + first_step + i + 1) + self.qo_bytes()
+        return tot / (n_steps * len(self.budgets))
+
+    def describe(self):
+        w = self.w
+        d = {"workload": ("PyramidKV long-context decode" if self.pyramid else
+                          "SnapKV prefill compression then decode"),
+             "layers": w.layers, "batch": w.batch, "n_heads_q": w.n_heads_q,
+             "n_heads_kv": w.n_heads_kv, "d_head": w.d_head, "prompt": w.prompt,
+             "L_obs": w.L_obs, "pool_k": w.pool_k, "kv_dtype": "bf16",
+             "budgets": (f"{self.budgets[0]}..{self.budgets[-1]} (ramp ratio {w.pyramid_ratio})"
+                         if self.pyramid else self.budgets[0]),
+             "l2": "inputs larger than L2",
+             "graph": "appends and decodes captured as two CUDA graphs per step"}
+        return d
+
+    def oracle_sample(self, budget_s=12.0):
+        import oracle
+        w = self.w
+        rng = np.random.default_rng(0)
+        n = int(np.mean(self.budgets)) + w.steps // 2
+        K, V = rng.standard_normal((n, w.d_head)), rng.standard_normal((n, w.d_head))
+        q = rng.standard_normal(w.d_head)
+        oracle.attend(q, K, V, w.scale)
+        cnt, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.attend(q, K, V, w.scale)
+            cnt += 1
+        return (time.perf_counter() - t0) / cnt, w.batch * w.n_heads_q * w.layers, cnt
+
+    def sample_description(self, n, slices):
+        return (f"{n} oracle decodes of one (batch, head, layer) slice over the mean retained "
+                f"length, extrapolated to {slices} slices per step (extrapolated)")
+
+
+class H2O(DecodeWorkload):
+    """H2O: prompt scores + one-shot compression per layer, then per step: append into the freed
+    slot, decode with logits, accumulate scores and evict one token per (batch, head)."""
+
+    traffic_key = "decode_attn/h2o"
+
+    def __init__(self, w: I.Workload, dev, kvc):
+        super().__init__(w, dev, kvc)
+        L, B, H, D = w.layers, w.batch, w.n_heads_kv, w.d_head
+        K_hh = w.budget - w.L_local
+        self.cap = w.budget + 1
+        self.K = torch.empty((L, B, H, self.cap, D), dtype=w.dtype, device=dev)
+        self.V = torch.empty_like(self.K)
+        self.pos = torch.full((L, B, H, self.cap), -1, dtype=torch.int32, device=dev)
+        self.score = torch.zeros((L, B, H, self.cap), dtype=torch.float32, device=dev)
+        self.free = torch.full((L, B * H), w.budget, dtype=torch.int32, device=dev)
+        self.logits = torch.empty((L, B, H, self.cap), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((L, B, H), dtype=torch.float32, device=dev)
+        ws = torch.zeros(kvc.kvc_h2o_prefill_workspace_bytes(B, H, D, w.prompt) + 256,
+                         dtype=torch.uint8, device=dev)
+        init_ms = []
+        for l in range(L):
+            q, k, v = I.h2o_layer(w, l, dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            idx, sc = kvc.kvc_h2o_prefill_select(q, k, seq_len=w.prompt, L_local=w.L_local,
+                                                 K_hh=K_hh, scale=w.scale, ws=ws)
+            e1.record()
+            kvc.kvc_compact_gather(k, v, idx, w.budget, self.K[l], self.V[l],
+                                   pos_dst=self.pos[l])
+            self.score[l, :, :, :w.budget] = sc
+            torch.cuda.synchronize()
+            init_ms.append(e0.elapsed_time(e1))
+            del q, k, v
+        self.extra["h2o_prompt_select_ms"] = round(sum(init_ms), 3)
+        self.t = torch.tensor([w.prompt], dtype=torch.int64, device=dev)
+        self.caches = [kvc.cache_view(self.K[l], self.V[l]) for l in range(L)]
+        self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.cap, dev)
+        self.launches_per_step = 3 * L + 1
+
+    def save_state(self):
+        return (self.t.clone(), self.free.clone(), self.pos.clone(), self.score.clone(),
+                self.K.clone(), self.V.clone())
+
+    def restore_state(self, st):
+        for dst, src in zip((self.t, self.free, self.pos, self.score, self.K, self.V), st):
+            dst.copy_(src)
+
+    def appends(self):
+        kvc = self.kvc
+        for l in range(self.w.layers):
+            kvc.kvc_stream_append(None, None, kvc.KVC_APPEND_FREE_SLOT, self.k_s[l],
+                                  self.v_s[l], t=self.t, free_slot=self.free[l],
+                                  pos=self.pos[l], score=self.score[l], cache=self.caches[l])
+
+    def decodes(self):
+        kvc, w = self.kvc, self.w
+        for l in range(w.layers):
+            kvc.kvc_decode_attn(self.q_s[l], None, None, scale=w.scale, n_valid=self.cap,
+                                out=self.out[l], logits=self.logits[l], lse=self.lse[l],
+                                ws=self.ws, cache=self.caches[l])
+            kvc.kvc_h2o_accumulate_evict(self.logits[l], self.lse[l], self.score[l],
+                                         self.pos[l], self.free[l], n_slots=self.cap, t=self.t,
+                                         L_local=w.L_local, budget=w.budget)
+        kvc.kvc_position_advance(self.t, 1)
+
+    def decode_bytes(self, first_step, n_steps):
+        w = self.w
+        return (self.kv_bytes(self.cap) + self.qo_bytes() +
+                w.batch * w.n_heads_q * (self.cap + 1) * 4)
+
+    def describe(self):
+        w = self.w
+        return {"workload": "H2O eviction during decode", "layers": w.layers,
+                "batch": w.batch, "n_heads": w.n_heads_q, "d_head": w.d_head,
+                "prompt": w.prompt, "budget": w.budget, "L_local": w.L_local,
+                "K_hh": w.budget - w.L_local, "kv_dtype": "bf16", "l2": "inputs larger than L2",
+                "graph": "appends, then decode + accumulate/evict per layer, as two CUDA graphs"}
+
+    def oracle_sample(self, budget_s=12.0):
+        import oracle
+        w = self.w
+        rng = np.random.default_rng(0)
+        n = self.cap
+        K, V = rng.standard_normal((n, w.d_head)), rng.standard_normal((n, w.d_head))
+        q = rng.standard_normal(w.d_head)
+        pos = np.arange(n)
+        s = rng.random(n)
+        oracle.h2o_step(q, K, V, pos, s, n, w.L_local, w.budget, w.scale)
+        cnt, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.h2o_step(q, K, V, pos, s, n, w.L_local, w.budget, w.scale)
+            cnt += 1
+        return (time.perf_counter() - t0) / cnt, w.batch * w.n_heads_q * w.layers, cnt
+
+    def sample_description(self, n, slices):
+        return (f"{n} oracle H2O steps (attend, accumulate, evict) of one (batch, head, layer) "
+                f"slice, extrapolated to {slices} slices per step (extrapolated)")
+
+
+def make_workload(name, w, dev, kvc, max_steps):
+    if name == "streaming":
+        return Streaming(w, dev, kvc)
+    if name == "snapkv":
+        return SelectDecode(w, dev, kvc, max_steps)
+    if name == "pyramid":
+        return SelectDecode(w, dev, kvc, max_steps, pyramid=True)
+    if name == "h2o":
+        return H2O(w, dev, kvc)
+    raise ValueError(name)
+
+
+WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid"]
 
 
 # ----------------------------------------------------------------------------- main arms
@@ -260,7 +532,7 @@ def run_gpu(args):
     w = I.WORKLOADS[args.workload]
     if args.layers:
         w = dataclasses.replace(w, layers=args.layers)
-    R = WORKLOAD_CLASSES[args.workload](w, dev, kvc)
+    R = make_workload(args.workload, w, dev, kvc, args.warmup + 2 * args.steps + 2)
     stream = torch.cuda.current_stream()
 
     # distinct per-step inputs (reused cyclically past 64 steps)
@@ -270,17 +542,18 @@ def run_gpu(args):
 
     # --- capture the step as two graphs (appends; decodes + position advance) ---------------
     R.load_inputs(*inputs[0])
-    t_save = R.t.clone()
+    state = R.save_state()
     R.appends()                             # one eager pass: per-device library set-up happens
-    R.decodes()                             # outside capture (it rewrites the same ring slot)
+    R.decodes()                             # outside capture; its effects are then undone
     torch.cuda.synchronize()
-    R.t.copy_(t_save)
+    R.restore_state(state)
     g_app, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_app):
         R.appends()
     with torch.cuda.graph(g_dec):
         R.decodes()
-    R.t.copy_(t_save)
+    R.restore_state(state)
+    del state
     torch.cuda.synchronize()
 
     def barrier():
@@ -292,7 +565,7 @@ def run_gpu(args):
         R.load_inputs(*inputs[i % total])
         g_app.replay()
         g_dec.replay()
-    bytes_per_launch = R.decode_bytes_per_launch()
+    bytes_per_launch = R.decode_bytes(args.warmup, args.steps)
     code = kvc.kvc_device_status()
     if code != 0:
         raise RuntimeError(f"device range check fired during warm-up: {code}")
@@ -320,6 +593,7 @@ def run_gpu(args):
     barrier()
     elapsed_ms = ev_s.elapsed_time(ev_e)
     decode_ms = sum(a.elapsed_time(b) for a, b in marks) / args.steps / w.layers
+    dec_share = sum(a.elapsed_time(b) for a, b in marks) / elapsed_ms
     code = kvc.kvc_device_status()
     if code != 0:
         raise RuntimeError(f"device range check fired in the timed region: {code}")
@@ -358,10 +632,7 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         per, slices, n = R.oracle_sample()
         cpu = {"value": w.batch / (per * slices), "unit": "tokens/s", "cores": 1,
-               "kind": "oracle",
-               "sample": f"{n} oracle StreamingLLM decodes of one (batch, head, layer) slice at "
-                         f"the workload's shape, extrapolated to {slices} slices per step "
-                         f"(extrapolated)"}
+               "kind": "oracle", "sample": R.sample_description(n, slices)}
     line = {
         "metric": "compressed-KV decode attention tokens/s (HBM GB/s and % of roofline in "
                   "'roofline')",
@@ -371,6 +642,8 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,1) keys/values/queries, sink-boosted keys; no model)",
         "config": R.describe(),
         "roofline": {"bound": "hbm", "kernel": "decode_attn_kernel",
+                     "note": "decode graph (all layers) average per layer; the graph also holds "
+                             "the per-layer H2O update where the workload has one",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": bytes_per_launch,
@@ -382,6 +655,8 @@ def run_gpu(args):
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
     }
+    line.update(R.extra)
+    line["decode_share_of_step"] = round(dec_share, 4)
     print(json.dumps(line), flush=True)
 
 
@@ -393,8 +668,13 @@ def run_reference(args):
     w = I.WORKLOADS[args.workload]
     import oracle
     oracle.build()
-    R = WORKLOAD_CLASSES[args.workload].__new__(WORKLOAD_CLASSES[args.workload])
+    cls = {"streaming": Streaming, "snapkv": SelectDecode, "pyramid": SelectDecode,
+           "h2o": H2O}[args.workload]
+    R = cls.__new__(cls)
     R.w = w
+    R.budgets = ([w.budget] * w.layers if args.workload != "pyramid" else
+                 [int(x) for x in oracle.pyramid_budgets(w.layers, w.budget, w.pyramid_ratio, 1)])
+    R.cap = w.budget + 1
     per_step = []
     budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup + args.steps):
@@ -427,7 +707,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (smaller case for profiling)")
     ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
-    ap.add_argument("--workload", choices=sorted(WORKLOAD_CLASSES), default="streaming")
+    ap.add_argument("--workload", choices=WORKLOAD_NAMES, default="streaming")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
