@@ -397,6 +397,19 @@ kvc_status kvc_compact_gather(const kvc_cache *src, const int32_t *idx, int64_t 
 }
 
 // ------------------------------------------------------------------------------------------
+// Observation-window scores: bf16 inputs of supported shapes run on the tensor cores, the rest
+// (fp32, short windows with several heads) on the CUDA-core kernels.
+static cudaError_t run_scores(const kvc::ScoreParams &sp, int dtype, float scale, int32_t *code,
+                              cudaStream_t s)
+{
+    if (dtype == KVC_BF16 && scale > 0.f) {
+        bool used = false;
+        cudaError_t e = kvc::launch_obs_scores_tc(sp, code, s, &used);
+        if (e != cudaSuccess || used) return e;
+    }
+    return kvc::launch_obs_scores(sp, dtype, s);
+}
+
 // SnapKV workspace: [s (G heads, prefix columns)] [pooled score] [row states] [row lse].
 static void snapkv_layout(int B, int Hq, int Hkv, int N, int L_obs, int n_sm, size_t *off_s,
                           size_t *off_score, kvc::ScorePlan *pl)
@@ -476,7 +489,7 @@ kvc_status kvc_snapkv_select(const void *q_obs, const kvc_cache *prompt, int32_t
     sp.row_lse2 = reinterpret_cast<float *>(wsb + pl.off_lse);
     sp.n_chunks = pl.n_chunks;
     sp.chunk = pl.chunk;
-    cudaError_t e = kvc::launch_obs_scores(sp, prompt->dtype, s);
+    cudaError_t e = run_scores(sp, prompt->dtype, scale, code, s);
     if (e != cudaSuccess) return cuda_fail(e, "observation scores launch");
     if (budget >= seq_len) {
         e = kvc::launch_iota_rows(idx_out, n_keep, B * Hkv, n_keep, s);
@@ -573,7 +586,7 @@ kvc_status kvc_h2o_prefill_select(const void *q, const kvc_cache *prompt, int32_
     sp.n_chunks = pl.n_chunks;
     sp.chunk = pl.chunk;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = kvc::launch_obs_scores(sp, prompt->dtype, s);
+    cudaError_t e = run_scores(sp, prompt->dtype, scale, code, s);
     if (e != cudaSuccess) return cuda_fail(e, "prompt scores launch");
     const long long keep_ll = (long long)K_hh + L_local;
     const int n_keep = (int)std::min<long long>(N, keep_ll);

@@ -115,6 +115,11 @@ struct ScorePlan {
 };
 ScorePlan score_plan(int B, int Hkv, int G, int N, int L_obs, int n_sm, size_t base_off);
 cudaError_t launch_obs_scores(const ScoreParams &p, int dtype, cudaStream_t stream);
+// Tensor-core (tcgen05) scoring for bf16 inputs.  Sets *used = false, launching nothing, when
+// the shape is not supported (then the CUDA-core kernels are used).
+bool obs_scores_tc_supported(const ScoreParams &p);
+cudaError_t launch_obs_scores_tc(const ScoreParams &p, int32_t *dev_code, cudaStream_t stream,
+                                 bool *used);
 
 // Pool (kernel pool_k, zero padding, divisor pool_k, sum left to right) + max over the G heads.
 cudaError_t launch_pool_groupmax(const float *s, int64_t s_row_stride, float *score, int BH,

@@ -253,21 +253,26 @@ __global__ void pool_groupmax_kernel(const float *s, int64_t s_row_stride, float
 
 ScorePlan score_plan(int B, int Hkv, int G, int N, int L_obs, int n_sm, size_t base_off)
 {
+    // Pass 1 splits the keys into n_chunks chunks of whole 128-key tiles so that about four
+    // blocks per SM are in flight (counted in 128-row tiles, the tensor-core kernel's unit;
+    // the CUDA-core kernel, which uses smaller row tiles, then simply has more blocks).
+    constexpr int KTILE = 128;
     ScorePlan pl;
     const int R = G * L_obs;
-    const long long row_blocks = (long long)G * ((L_obs + RT - 1) / RT);
+    const long long mtiles = (R + KTILE - 1) / KTILE;
     const long long pairs = (long long)B * Hkv;
-    const long long base = pairs * row_blocks;
+    const long long base = pairs * mtiles;
     const long long want = 4LL * (n_sm > 0 ? n_sm : 152);
+    const long long key_tiles = (N + KTILE - 1) / KTILE;
     long long n_chunks = (want + base - 1) / base;
-    const long long max_chunks = (N + KT - 1) / KT;
-    if (n_chunks > max_chunks) n_chunks = max_chunks;
+    if (n_chunks > key_tiles) n_chunks = key_tiles;
     if (n_chunks < 1) n_chunks = 1;
-    long long chunk = (N + n_chunks - 1) / n_chunks;
-    chunk = ((chunk + KT - 1) / KT) * KT;
-    n_chunks = (N + chunk - 1) / chunk;
+    long long chunk_tiles = (key_tiles + n_chunks - 1) / n_chunks;
+    if (chunk_tiles < 1) chunk_tiles = 1;
+    n_chunks = (key_tiles + chunk_tiles - 1) / chunk_tiles;
+    if (n_chunks < 1) n_chunks = 1;
     pl.n_chunks = (int)n_chunks;
-    pl.chunk = (int)chunk;
+    pl.chunk = (int)(chunk_tiles * KTILE);
     auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
     pl.off_ml = align(base_off);
     pl.off_lse = align(pl.off_ml + (size_t)pairs * n_chunks * R * 2 * sizeof(float));

@@ -1,0 +1,528 @@
+// obs_scores_tc.cu -- observation-window attention scores on the 5th-generation tensor cores.
+//
+// SnapKV steps 1-2 ("Compressão e Poda Dinâmica de KV Cache", "SnapKV e a seleção de contexto
+// no prefill") and H2O's prompt column sums (section "Heavy-Hitter Oracle (H2O)..."), for bf16
+// inputs.  The product of the window queries with the prompt keys is a genuine dense
+// contraction (rows x keys x d_head), so it runs on tcgen05.mma (bf16 operands, fp32
+// accumulators in tensor memory); softmax and the reductions run in the epilogue warps.
+//
+// Same two passes as the CUDA-core kernels (obs_scores.cu):
+//   pass 1 (ROWSTATS): A = a 128-row tile of window queries, B = 128-key tiles streamed along
+//     the prompt; the accumulator has one row per TMEM lane, so each epilogue thread folds its
+//     own row's logits into a running (max, sum of exp2) with no cross-thread reduction;
+//   pass 2 (COLSUM): the transposed product, A = a 128-key tile, B = 128-row blocks of the
+//     window queries; the accumulator has one key per TMEM lane, so each epilogue thread sums
+//     its key's probabilities exp2(l - lse) over the rows of each query head, again without
+//     cross-thread reduction, and writes each column sum once (deterministic).
+//
+// Block roles (192 threads): warp 0 issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle,
+// K-major tiles of 128 rows x 64 elements), warp 1 owns the tensor-memory allocation and one
+// of its threads issues the MMAs (M = N = 128, K = 16 per instruction) and the commits, warps
+// 2-5 are the epilogue (tcgen05.ld of their 32 TMEM lanes).  Operand stages and the two
+// accumulator buffers are handed over with mbarriers; every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvc {
+
+namespace {
+
+constexpr int TC_ROWS = 128;         // MMA M and N
+constexpr int TC_THREADS = 192;
+constexpr int TC_SUB_BYTES = TC_ROWS * 128;   // one 128-row x 64-element bf16 sub-tile
+constexpr uint32_t TC_TMEM_COLS = 256;        // two fp32 accumulators of 128 columns
+
+// ---- tcgen05 / TMA helpers ---------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;               // leading-dimension offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;     // stride between 8-row groups
+    d |= (uint64_t)1 << 46;               // descriptor version
+    d |= (uint64_t)2 << 61;               // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M = N = 128.
+constexpr uint32_t kIdescBf16M128N128 =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdescBf16M128N128), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
+                     "r"(bar)
+                 : "memory");
+}
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one value per thread and column).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void epilogue_sync()
+{
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+struct TcParams {
+    ScoreParams sp;       // shapes, scale, outputs, workspace (see internal.h)
+    int32_t n_mtiles;     // row tiles of 128 per (batch, KV head)    (pass 1)
+    int32_t chunk_tiles;  // key tiles of 128 per pass-1 block
+    int32_t n_col_tiles;  // key tiles of 128 covering the n_cols written columns (pass 2)
+    int32_t *dev_code;
+};
+
+// Window row r of the group -> (head g, text position) with rows ordered g*L_obs + w.
+__device__ __forceinline__ int row_pos(const ScoreParams &p, int r)
+{
+    return p.N - p.L_obs + (r % p.L_obs);
+}
+
+template <int D, int MODE>   // MODE 0: row statistics, 1: column sums
+__global__ void __launch_bounds__(TC_THREADS, 1)
+tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                 const TcParams tp)
+{
+    constexpr int SUBS = D / 64;                 // 64-element sub-tiles per operand tile
+    constexpr int TILE_BYTES = SUBS * TC_SUB_BYTES;
+    constexpr int KSTEPS = D / 16;
+    constexpr int NS = (200 * 1024 - TILE_BYTES) / TILE_BYTES > 4
+                           ? 4
+                           : (200 * 1024 - TILE_BYTES) / TILE_BYTES;
+    static_assert(NS >= 2, "tensor-core scoring needs two operand stages");
+    const ScoreParams &p = tp.sp;
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte aligned operand area (the swizzle pattern is anchored to 1024-byte lines)
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t fixed = base;                          // one operand tile, loaded once
+    const uint32_t stage0 = base + TILE_BYTES;            // NS streamed operand tiles
+    const uint32_t bars = stage0 + NS * TILE_BYTES;       // mbarriers
+    const uint32_t bar_fixed = bars;
+    const uint32_t bar_full = bars + 8;                   // NS
+    const uint32_t bar_empty = bar_full + 8 * NS;         // NS
+    const uint32_t bar_acc_full = bar_empty + 8 * NS;     // 2
+    const uint32_t bar_acc_empty = bar_acc_full + 16;     // 2
+    const uint32_t tmem_slot = bar_acc_empty + 16;        // u32 written by tcgen05.alloc
+    float *sm_lse = reinterpret_cast<float *>(smem_raw + (tmem_slot + 16 - raw));   // [2][128]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int R = p.G * p.L_obs;
+    const int first_pos = p.N - p.L_obs;
+
+    // ---- work item of this block --------------------------------------------------------------
+    int pair, fixed_row0 = 0, t_begin = 0, n_items = 0, mtile = 0, ktile = 0, chunk = 0;
+    if (MODE == 0) {
+        const int per_pair = tp.n_mtiles * p.n_chunks;
+        pair = blockIdx.x / per_pair;
+        mtile = (blockIdx.x % per_pair) / p.n_chunks;
+        chunk = blockIdx.x % p.n_chunks;
+        // keys a row tile can see: up to the largest position among its rows
+        const int r_lo = mtile * TC_ROWS;
+        const int r_hi = min(r_lo + TC_ROWS, R) - 1;
+        const int w_hi = (r_lo / p.L_obs != r_hi / p.L_obs) ? p.L_obs - 1 : r_hi % p.L_obs;
+        const int kt_needed = (first_pos + w_hi) / TC_ROWS + 1;
+        t_begin = chunk * tp.chunk_tiles;
+        n_items = max(0, min(t_begin + tp.chunk_tiles, kt_needed) - t_begin);
+        fixed_row0 = r_lo;
+    } else {
+        pair = blockIdx.x / tp.n_col_tiles;
+        ktile = blockIdx.x % tp.n_col_tiles;
+        // row blocks whose rows can see this key tile: positions >= its first key
+        const int k0 = ktile * TC_ROWS;
+        int rb0 = 0;
+        if (k0 > first_pos) rb0 = (k0 - first_pos) / TC_ROWS;   // rows sorted by position when G = 1
+        if (p.G > 1) rb0 = 0;
+        t_begin = rb0;
+        n_items = max(0, (R + TC_ROWS - 1) / TC_ROWS - rb0);
+    }
+    const int b = pair / p.Hkv, kh = pair % p.Hkv;
+    const int qrow_group = (b * p.Hq + kh * p.G) * p.L_obs;   // first q row of this group
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_fixed, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_acc_full + 8 * a, 1);
+            mbar_init(bar_acc_empty + 8 * a, 4);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         tmem_slot),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    uint32_t tmem_base;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot));
+
+    if (n_items > 0) {
+        if (warp == 0 && lane == 0) {
+            // ============================== TMA producer ==========================================
+            mbar_arrive_expect_tx(bar_fixed, TILE_BYTES);
+            for (int a = 0; a < SUBS; ++a) {
+                if (MODE == 0)
+                    tma_load_2d(fixed + a * TC_SUB_BYTES, &qmap, a * 64, qrow_group + fixed_row0,
+                                bar_fixed);
+                else
+                    tma_load_4d(fixed + a * TC_SUB_BYTES, &kmap, a * 64, ktile * TC_ROWS, kh, b,
+                                bar_fixed);
+            }
+            for (int i = 0; i < n_items; ++i) {
+                const int s = i % NS;
+                if (i >= NS) mbar_wait(bar_empty + 8 * s, ((i / NS) - 1) & 1, tp.dev_code);
+                const uint32_t dst = stage0 + s * TILE_BYTES;
+                mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
+                for (int a = 0; a < SUBS; ++a) {
+                    if (MODE == 0)
+                        tma_load_4d(dst + a * TC_SUB_BYTES, &kmap, a * 64,
+                                    (t_begin + i) * TC_ROWS, kh, b, bar_full + 8 * s);
+                    else
+                        tma_load_2d(dst + a * TC_SUB_BYTES, &qmap, a * 64,
+                                    qrow_group + (t_begin + i) * TC_ROWS, bar_full + 8 * s);
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ============================== MMA issuer ============================================
+            mbar_wait(bar_fixed, 0, tp.dev_code);
+            for (int i = 0; i < n_items; ++i) {
+                const int s = i % NS, ab = i & 1;
+                mbar_wait(bar_full + 8 * s, (i / NS) & 1, tp.dev_code);
+                if (i >= 2) mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) - 1) & 1, tp.dev_code);
+                tc_fence_after();
+                const uint32_t a_base = fixed;                        // fixed operand = A
+                const uint32_t b_base = stage0 + s * TILE_BYTES;      // streamed operand = B
+#pragma unroll
+                for (int k = 0; k < KSTEPS; ++k) {
+                    const uint32_t off = (k >> 2) * TC_SUB_BYTES + (k & 3) * 32;
+                    umma_bf16(tmem_base + ab * 128, sw128_desc(a_base + off),
+                              sw128_desc(b_base + off), k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar_empty + 8 * s);       // operand stage free once the MMAs finish
+                umma_commit(bar_acc_full + 8 * ab);   // accumulator ready for the epilogue
+            }
+        } else if (warp >= 2) {
+            // ============================== epilogue ==============================================
+            const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
+            const int et = q4 * 32 + lane;            // this thread's lane (row or key)
+            const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+            if (MODE == 0) {
+                const int r = fixed_row0 + et;        // window row of the group
+                const bool row_ok = r < R;
+                const int pos = row_ok ? row_pos(p, r) : -1;
+                float m_run = kNegBig, z_run = 0.f;
+                for (int i = 0; i < n_items; ++i) {
+                    const int ab = i & 1;
+                    mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, tp.dev_code);
+                    tc_fence_after();
+                    const int k0 = (t_begin + i) * TC_ROWS;
+                    const bool need_mask = k0 + TC_ROWS - 1 > first_pos || k0 + TC_ROWS > p.N;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float v[32];
+                        tmem_ld32(tmem_base + ab * 128 + lane_off + c * 32, v);
+                        if (need_mask) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int key = k0 + c * 32 + j;
+                                if (key > pos || key >= p.N) v[j] = -INFINITY;
+                            }
+                        }
+                        float mx = v[0];
+#pragma unroll
+                        for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
+                        const float m_new = fmaxf(m_run, mx * p.scale_log2);
+                        float z = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) z += ex2(fmaf(v[j], p.scale_log2, -m_new));
+                        z_run = z_run * ex2(m_run - m_new) + z;
+                        m_run = m_new;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
+                }
+                if (row_ok) {
+                    float *dst = p.row_ml + (((size_t)pair * p.n_chunks + chunk) * R + r) * 2;
+                    dst[0] = m_run;
+                    dst[1] = z_run;
+                }
+            } else {
+                const int key = ktile * TC_ROWS + et;
+                const float *lse_g = p.row_lse2 + (size_t)pair * R;
+                const bool mask_tile = ktile * TC_ROWS + TC_ROWS - 1 > first_pos;
+                float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
+                int g_cur = t_begin * TC_ROWS / p.L_obs;   // head of the first row handled
+                float acc_g = 0.f;
+                for (int i = 0; i < n_items; ++i) {
+                    const int ab = i & 1;
+                    const int r0 = (t_begin + i) * TC_ROWS;   // first row of this block
+                    // stage the block's row log2-sum-exp values (double buffered)
+                    float *lse_buf = sm_lse + (i & 1) * TC_ROWS;
+                    lse_buf[et] = (r0 + et < R) ? lse_g[r0 + et] : 0.f;
+                    epilogue_sync();
+                    mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, tp.dev_code);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        const int rc = r0 + c * 32;         // first row of this chunk
+                        if (rc >= R) break;
+                        float v[32];
+                        tmem_ld32(tmem_base + ab * 128 + lane_off + c * 32, v);
+                        // the chunk's rows span heads g_a .. g_b (at most two when L_obs >= 32)
+                        const int g_a = rc / p.L_obs;
+                        const int rows_here = min(32, R - rc);
+                        const int split = min(rows_here, (g_a + 1) * p.L_obs - rc);   // rows in g_a
+                        if (g_a != g_cur) {                 // flush the finished head
+                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                            acc_g = 0.f;
+                            g_cur = g_a;
+                        }
+                        float s_a = 0.f, s_b = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float lse = lse_buf[c * 32 + j];
+                            float pr = ex2(fmaf(v[j], p.scale_log2, -lse));
+                            if (mask_tile) {
+                                // position of row rc + j inside its head (g_a, or g_a + 1 past
+                                // the split)
+                                const int hb = (j < split ? g_a : g_a + 1) * p.L_obs;
+                                if (key > first_pos + (rc + j - hb)) pr = 0.f;
+                            }
+                            if (j < split) s_a += pr;
+                            else if (j < rows_here) s_b += pr;
+                        }
+                        acc_g += s_a;
+                        if (split < rows_here) {            // the chunk crosses into head g_a + 1
+                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                            g_cur = g_a + 1;
+                            acc_g = s_b;
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
+                }
+                if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+            }
+        }
+    } else if (MODE == 0 && warp >= 2) {
+        // no key tile reaches this block's rows: an empty state for every row
+        const int r = fixed_row0 + (warp & 3) * 32 + lane;
+        if (r < R) {
+            float *dst = p.row_ml + (((size_t)pair * p.n_chunks + chunk) * R + r) * 2;
+            dst[0] = kNegBig;
+            dst[1] = 0.f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+}
+
+template <int D>
+constexpr int tc_smem_bytes()
+{
+    constexpr int TILE_BYTES = (D / 64) * TC_SUB_BYTES;
+    constexpr int NS = (200 * 1024 - TILE_BYTES) / TILE_BYTES > 4
+                           ? 4
+                           : (200 * 1024 - TILE_BYTES) / TILE_BYTES;
+    return 1024 + (1 + NS) * TILE_BYTES + 8 * (1 + 2 * NS + 4) + 16 + 2 * TC_ROWS * 4 + 64;
+}
+
+// ---- host: tensor maps through the driver entry point ------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode != nullptr;
+}
+
+bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t row_bytes)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, TC_ROWS};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_4d(CUtensorMap *m, const void *ptr, uint64_t d, uint64_t n, uint64_t h, uint64_t bsz,
+               uint64_t s_slot, uint64_t s_h, uint64_t s_b)
+{
+    cuuint64_t dims[4] = {d, n, h, bsz};
+    cuuint64_t strides[3] = {s_slot, s_h, s_b};
+    cuuint32_t box[4] = {64, TC_ROWS, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+__global__ void rowlse_tc_kernel(const ScoreParams p)
+{
+    const int R = p.G * p.L_obs;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)p.B * p.Hkv * R) return;
+    const long long bkh = i / R;
+    const int r = (int)(i % R);
+    float M = kNegBig;
+    for (int c = 0; c < p.n_chunks; ++c)
+        M = fmaxf(M, p.row_ml[((bkh * p.n_chunks + c) * R + r) * 2]);
+    float Z = 0.f;
+    for (int c = 0; c < p.n_chunks; ++c) {
+        const float *s = p.row_ml + ((bkh * p.n_chunks + c) * R + r) * 2;
+        Z += s[1] * exp2f(s[0] - M);
+    }
+    p.row_lse2[bkh * R + r] = M + log2f(Z);
+}
+
+template <int D>
+cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const CUtensorMap &km,
+                            int32_t *dev_code, cudaStream_t stream)
+{
+    constexpr int SMEM = tc_smem_bytes<D>();
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_scores_kernel<D, 0>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc_scores_kernel<D, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const int R = sp.G * sp.L_obs;
+    TcParams tp;
+    tp.sp = sp;
+    tp.n_mtiles = (R + TC_ROWS - 1) / TC_ROWS;
+    tp.chunk_tiles = sp.chunk / TC_ROWS;
+    tp.n_col_tiles = (sp.n_cols + TC_ROWS - 1) / TC_ROWS;
+    tp.dev_code = dev_code;
+    const long long pairs = (long long)sp.B * sp.Hkv;
+    tc_scores_kernel<D, 0><<<(unsigned)(pairs * tp.n_mtiles * sp.n_chunks), TC_THREADS, SMEM,
+                             stream>>>(qm, km, tp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long rows = pairs * R;
+    rowlse_tc_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(sp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || tp.n_col_tiles == 0) return e;
+    tc_scores_kernel<D, 1><<<(unsigned)(pairs * tp.n_col_tiles), TC_THREADS, SMEM, stream>>>(
+        qm, km, tp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool obs_scores_tc_supported(const ScoreParams &p)
+{
+    return (p.D == 64 || p.D == 128 || p.D == 256) && (p.L_obs >= 32 || p.G == 1) &&
+           p.chunk % TC_ROWS == 0;
+}
+
+cudaError_t launch_obs_scores_tc(const ScoreParams &p, int32_t *dev_code, cudaStream_t stream,
+                                 bool *used)
+{
+    *used = false;
+    if (!obs_scores_tc_supported(p) || !get_encoder()) return cudaSuccess;
+    CUtensorMap qm, km;
+    const uint64_t eb = 2;
+    if (!encode_2d(&qm, p.q, (uint64_t)p.D, (uint64_t)p.B * p.Hq * p.L_obs, (uint64_t)p.D * eb))
+        return cudaSuccess;
+    if (!encode_4d(&km, p.k, (uint64_t)p.D, (uint64_t)p.N, (uint64_t)p.Hkv, (uint64_t)p.B,
+                   (uint64_t)p.ss * eb, (uint64_t)p.sh * eb, (uint64_t)p.sb * eb))
+        return cudaSuccess;
+    *used = true;
+    switch (p.D) {
+    case 64: return launch_tc_typed<64>(p, qm, km, dev_code, stream);
+    case 128: return launch_tc_typed<128>(p, qm, km, dev_code, stream);
+    default: return launch_tc_typed<256>(p, qm, km, dev_code, stream);
+    }
+}
+
+}  // namespace kvc

@@ -80,6 +80,29 @@ def test_snapkv_select_ragged(dtype, B, Hq, Hkv, D, N, L_obs, budget):
     _check_snapkv(q, K, N, L_obs, budget, 5, 1 / math.sqrt(D), kvc)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,D,N,L_obs,budget", [
+    (2, 8, 2, 128, 1100, 32, 400),      # the SnapKV workload's group shape, ragged prompt
+    (1, 12, 2, 256, 900, 64, 333),      # the long-context group shape (G = 6, D = 256)
+    (1, 4, 1, 64, 513, 48, 100),        # heads straddle 32-row chunks of the accumulator
+    (1, 2, 1, 128, 4200, 96, 700),      # several pass-1 chunks per row tile
+])
+def test_snapkv_select_tensor_core_shapes(B, Hq, Hkv, D, N, L_obs, budget):
+    """bf16 shapes that take the tcgen05 scoring path (window of at least 32 queries)."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    q = I.randn((B, Hq, L_obs, D), 170 + N, dev, torch.bfloat16)
+    K = I.randn((B, Hkv, N, D), 171 + N, dev, torch.bfloat16)
+    _check_snapkv(q, K, N, L_obs, budget, 5, 1 / math.sqrt(D), kvc)
+
+
+def test_snapkv_tiny_workload_bf16():
+    dev = cuda_or_skip()
+    kvc = lib()
+    w = I.WORKLOADS["tiny"]
+    q, k, v = I.prompt_qkv(1, 8, 2, 512, 64, w.seed, dev, torch.bfloat16)
+    _check_snapkv(q[:, :, -32:].contiguous(), k, 512, 32, 128, 5, w.scale, kvc)
+
+
 def test_snapkv_exact_ties_keep_lowest_index():
     """Identical keys give identical scores: the lower index must win every tie."""
     dev = cuda_or_skip()
@@ -223,6 +246,13 @@ def test_h2o_bf16_ragged():
     dev = cuda_or_skip()
     kvc = lib()
     _h2o_run(2, 3, 333, 128, 70, 35, 40, torch.bfloat16, 4321, kvc, dev, check_every=3)
+
+
+def test_h2o_bf16_multi_tile_prompt():
+    """A prompt of several 128-row tiles: causal row and column tiles on the tensor cores."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    _h2o_run(1, 2, 700, 128, 200, 100, 6, torch.bfloat16, 987, kvc, dev, check_every=2)
 
 
 def test_h2o_evict_candidates_and_no_candidate_code():
