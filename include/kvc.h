@@ -138,7 +138,7 @@ kvc_status kvc_rope_table(int32_t n_pos, int32_t d_head, double theta, float *ou
  *   1. the last L_obs prompt queries (observation window) attend causally to all seq_len
  *      prompt keys (scale * q.k, softmax per query);
  *   2. s_h[i] = (1/L_obs) * sum over the window of the attention to key i, per query head;
- *   3. average pooling of s_h over the prefix i < seq_len-L_obs, kernel pool_k (odd), stride 1,
+ *   3. average pooling of s_h over the prefix i < seq_len-L_obs, kernel pool_k (odd, <= 15), stride 1,
  *      zero padding, divisor pool_k; then max over the query heads of each KV head;
  *   4. the budget-L_obs prefix positions with the largest pooled score are kept (equal scores
  *      keep the lower index), in ascending order, followed by the window

@@ -449,8 +449,9 @@ kvc_status kvc_snapkv_select(const void *q_obs, const kvc_cache *prompt, int32_t
                     prompt->n_heads_kv);
     if (L_obs <= 0 || seq_len < L_obs || seq_len > prompt->cap)
         return fail(KVC_ERR_SHAPE, "kvc_snapkv_select: need 0 < L_obs <= seq_len <= cap");
-    if (pool_k <= 0 || pool_k % 2 == 0)
-        return fail(KVC_ERR_INVALID_ARG, "kvc_snapkv_select: pool_k %d must be odd", pool_k);
+    if (pool_k <= 0 || pool_k % 2 == 0 || pool_k > 15)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_snapkv_select: pool_k %d must be odd, 1..15",
+                    pool_k);
     if (budget < L_obs)
         return fail(KVC_ERR_CAPACITY, "kvc_snapkv_select: budget %d < L_obs %d", budget, L_obs);
     if (!std::isfinite(scale)) return fail(KVC_ERR_INVALID_ARG, "kvc_snapkv_select: scale");

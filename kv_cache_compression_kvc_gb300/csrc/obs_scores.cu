@@ -228,25 +228,46 @@ __global__ void __launch_bounds__(NT) colsum_kernel(const ScoreParams p)
 }
 
 // Pool (kernel pool_k, stride 1, zero padding, divisor pool_k) then max over the G heads.
-// The pooled sum adds s[i-r] .. s[i+r] left to right in fp32 and divides by pool_k with an
-// IEEE division: a fixed arithmetic order, so a reader can replay it exactly.
+// Every pooled sum adds s[i-r] .. s[i+r] left to right in fp32 (terms outside the prefix are
+// zeros, and adding +0 leaves a non-negative sum unchanged) and divides by pool_k with an IEEE
+// division: a fixed arithmetic order, so a reader can replay it exactly.  Each thread produces
+// POOL_RUN consecutive outputs from one window of loads (a sliding window over the row).
+constexpr int POOL_RUN = 8;
+constexpr int POOL_MAXK = 15;
+
+template <int PK>
 __global__ void pool_groupmax_kernel(const float *s, int64_t s_row_stride, float *score, int BH,
-                                     int G, int n, int pool_k)
+                                     int G, int n)
 {
-    const long long i_g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i_g >= (long long)BH * n) return;
-    const int bh = (int)(i_g / n);
-    const int i = (int)(i_g % n);
-    const int r = (pool_k - 1) / 2;
-    float best = -INFINITY;
+    constexpr int r = (PK - 1) / 2;
+    constexpr int WIN = POOL_RUN + PK - 1;
+    const int runs = (n + POOL_RUN - 1) / POOL_RUN;
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (long long)BH * runs) return;
+    const int bh = (int)(t / runs);
+    const int i0 = (int)(t % runs) * POOL_RUN;
+    float best[POOL_RUN];
+#pragma unroll
+    for (int u = 0; u < POOL_RUN; ++u) best[u] = -INFINITY;
     for (int g = 0; g < G; ++g) {
         const float *sg = s + (size_t)(bh * G + g) * s_row_stride;
-        float acc = 0.f;
-        for (int j = i - r; j <= i + r; ++j)
-            if (j >= 0 && j < n) acc = __fadd_rn(acc, sg[j]);
-        best = fmaxf(best, __fdiv_rn(acc, (float)pool_k));
+        float win[WIN];
+#pragma unroll
+        for (int j = 0; j < WIN; ++j) {
+            const int idx = i0 - r + j;
+            win[j] = (idx >= 0 && idx < n) ? sg[idx] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < POOL_RUN; ++u) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < PK; ++j) acc = __fadd_rn(acc, win[u + j]);
+            best[u] = fmaxf(best[u], __fdiv_rn(acc, (float)PK));
+        }
     }
-    score[(size_t)bh * n + i] = best;
+#pragma unroll
+    for (int u = 0; u < POOL_RUN; ++u)
+        if (i0 + u < n) score[(size_t)bh * n + i0 + u] = best[u];
 }
 
 }  // namespace
@@ -302,10 +323,17 @@ cudaError_t launch_obs_scores(const ScoreParams &p, int dtype, cudaStream_t stre
 cudaError_t launch_pool_groupmax(const float *s, int64_t s_row_stride, float *score, int BH,
                                  int G, int n, int pool_k, cudaStream_t stream)
 {
-    const long long total = (long long)BH * n;
+    const long long total = (long long)BH * ((n + POOL_RUN - 1) / POOL_RUN);
     if (total == 0) return cudaSuccess;
-    pool_groupmax_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(
-        s, s_row_stride, score, BH, G, n, pool_k);
+    const unsigned blocks = (unsigned)((total + 255) / 256);
+    switch (pool_k) {
+#define KVC_POOL_CASE(PK) \
+    case PK: pool_groupmax_kernel<PK><<<blocks, 256, 0, stream>>>(s, s_row_stride, score, BH, G, n); break;
+    KVC_POOL_CASE(1) KVC_POOL_CASE(3) KVC_POOL_CASE(5) KVC_POOL_CASE(7)
+    KVC_POOL_CASE(9) KVC_POOL_CASE(11) KVC_POOL_CASE(13) KVC_POOL_CASE(15)
+#undef KVC_POOL_CASE
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

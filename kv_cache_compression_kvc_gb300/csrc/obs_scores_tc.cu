@@ -10,10 +10,14 @@
 //   pass 1 (ROWSTATS): A = a 128-row tile of window queries, B = 128-key tiles streamed along
 //     the prompt; the accumulator has one row per TMEM lane, so each epilogue thread folds its
 //     own row's logits into a running (max, sum of exp2) with no cross-thread reduction;
-//   pass 2 (COLSUM): the transposed product, A = a 128-key tile, B = 128-row blocks of the
+//   pass 2 (COLSUM): the transposed product, A = 128-key tiles, B = 128-row blocks of the
 //     window queries; the accumulator has one key per TMEM lane, so each epilogue thread sums
 //     its key's probabilities exp2(l - lse) over the rows of each query head, again without
-//     cross-thread reduction, and writes each column sum once (deterministic).
+//     cross-thread reduction, and writes each column sum once (deterministic).  When every head
+//     lies inside one 128-row block (SnapKV windows of 32, 64 or 128 queries), a block keeps one
+//     row block resident and streams a chunk of key tiles; otherwise (H2O's whole-prompt
+//     window, one head of many row blocks) a block keeps one key tile and streams the row
+//     blocks that can see it.
 //
 // Block roles (192 threads): warp 0 issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle,
 // K-major tiles of 128 rows x 64 elements), warp 1 owns the tensor-memory allocation and one
@@ -121,6 +125,8 @@ struct TcParams {
     int32_t n_mtiles;     // row tiles of 128 per (batch, KV head)    (pass 1)
     int32_t chunk_tiles;  // key tiles of 128 per pass-1 block
     int32_t n_col_tiles;  // key tiles of 128 covering the n_cols written columns (pass 2)
+    int32_t col_chunks;   // pass 2 with a resident row block: key-tile chunks per row block
+    int32_t col_chunk_tiles;
     int32_t *dev_code;
 };
 
@@ -130,7 +136,8 @@ __device__ __forceinline__ int row_pos(const ScoreParams &p, int r)
     return p.N - p.L_obs + (r % p.L_obs);
 }
 
-template <int D, int MODE>   // MODE 0: row statistics, 1: column sums
+// MODE 0: row statistics; 1: column sums, key tile resident; 2: column sums, row block resident
+template <int D, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  const TcParams tp)
@@ -179,6 +186,15 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         t_begin = chunk * tp.chunk_tiles;
         n_items = max(0, min(t_begin + tp.chunk_tiles, kt_needed) - t_begin);
         fixed_row0 = r_lo;
+    } else if (MODE == 2) {
+        const int n_rb = (R + TC_ROWS - 1) / TC_ROWS;
+        const int per_pair = n_rb * tp.col_chunks;
+        pair = blockIdx.x / per_pair;
+        mtile = (blockIdx.x % per_pair) / tp.col_chunks;      // resident row block
+        chunk = blockIdx.x % tp.col_chunks;
+        t_begin = chunk * tp.col_chunk_tiles;                  // first key tile
+        n_items = max(0, min(t_begin + tp.col_chunk_tiles, tp.n_col_tiles) - t_begin);
+        fixed_row0 = mtile * TC_ROWS;
     } else {
         pair = blockIdx.x / tp.n_col_tiles;
         ktile = blockIdx.x % tp.n_col_tiles;
@@ -223,7 +239,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             // ============================== TMA producer ==========================================
             mbar_arrive_expect_tx(bar_fixed, TILE_BYTES);
             for (int a = 0; a < SUBS; ++a) {
-                if (MODE == 0)
+                if (MODE != 1)
                     tma_load_2d(fixed + a * TC_SUB_BYTES, &qmap, a * 64, qrow_group + fixed_row0,
                                 bar_fixed);
                 else
@@ -236,7 +252,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 const uint32_t dst = stage0 + s * TILE_BYTES;
                 mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
                 for (int a = 0; a < SUBS; ++a) {
-                    if (MODE == 0)
+                    if (MODE != 1)
                         tma_load_4d(dst + a * TC_SUB_BYTES, &kmap, a * 64,
                                     (t_begin + i) * TC_ROWS, kh, b, bar_full + 8 * s);
                     else
@@ -252,8 +268,10 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 mbar_wait(bar_full + 8 * s, (i / NS) & 1, tp.dev_code);
                 if (i >= 2) mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) - 1) & 1, tp.dev_code);
                 tc_fence_after();
-                const uint32_t a_base = fixed;                        // fixed operand = A
-                const uint32_t b_base = stage0 + s * TILE_BYTES;      // streamed operand = B
+                // MODE 0/1: A = resident tile, B = streamed tile; MODE 2: A = streamed keys,
+                // B = resident rows (the accumulator then has one key per lane)
+                const uint32_t a_base = MODE == 2 ? stage0 + s * TILE_BYTES : fixed;
+                const uint32_t b_base = MODE == 2 ? fixed : stage0 + s * TILE_BYTES;
 #pragma unroll
                 for (int k = 0; k < KSTEPS; ++k) {
                     const uint32_t off = (k >> 2) * TC_SUB_BYTES + (k & 3) * 32;
@@ -309,6 +327,70 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     dst[0] = m_run;
                     dst[1] = z_run;
                 }
+            } else if (MODE == 2) {
+                // resident rows fixed_row0 .. +127 hold whole heads: per key tile, each thread
+                // sums its key's column over each head and writes it
+                const float *lse_g = p.row_lse2 + (size_t)pair * R;
+                float *lse_buf = sm_lse;
+                lse_buf[et] = (fixed_row0 + et < R) ? lse_g[fixed_row0 + et] : 0.f;
+                epilogue_sync();
+                float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
+                const int rows_blk = min(TC_ROWS, R - fixed_row0);
+                for (int i = 0; i < n_items; ++i) {
+                    const int ab = i & 1;
+                    const int key = (t_begin + i) * TC_ROWS + et;
+                    const bool mask_tile = (t_begin + i) * TC_ROWS + TC_ROWS - 1 > first_pos;
+                    mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, tp.dev_code);
+                    tc_fence_after();
+                    int g_cur = fixed_row0 / p.L_obs;
+                    float acc_g = 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        const int rc = fixed_row0 + c * 32;
+                        if (c * 32 >= rows_blk) break;
+                        float v[32];
+                        tmem_ld32(tmem_base + ab * 128 + lane_off + c * 32, v);
+                        const int g_a = rc / p.L_obs;
+                        const int rows_here = min(32, rows_blk - c * 32);
+                        const int split = min(rows_here, (g_a + 1) * p.L_obs - rc);
+                        if (g_a != g_cur) {
+                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                            acc_g = 0.f;
+                            g_cur = g_a;
+                        }
+                        if (split == 32 && !mask_tile) {
+                            // the whole chunk is one head and every key is visible
+                            float s_a = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                s_a += ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
+                            acc_g += s_a;
+                            continue;
+                        }
+                        float s_a = 0.f, s_b = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float lse = lse_buf[c * 32 + j];
+                            float pr = ex2(fmaf(v[j], p.scale_log2, -lse));
+                            if (mask_tile) {
+                                const int hb = (j < split ? g_a : g_a + 1) * p.L_obs;
+                                if (key > first_pos + (rc + j - hb)) pr = 0.f;
+                            }
+                            if (j < split) s_a += pr;
+                            else if (j < rows_here) s_b += pr;
+                        }
+                        acc_g += s_a;
+                        if (split < rows_here) {
+                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                            g_cur = g_a + 1;
+                            acc_g = s_b;
+                        }
+                    }
+                    if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
+                }
             } else {
                 const int key = ktile * TC_ROWS + et;
                 const float *lse_g = p.row_lse2 + (size_t)pair * R;
@@ -339,6 +421,15 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                             if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
                             acc_g = 0.f;
                             g_cur = g_a;
+                        }
+                        if (split == 32 && !mask_tile) {
+                            // the whole chunk is one head and every key is visible
+                            float s_a = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                s_a += ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
+                            acc_g += s_a;
+                            continue;
                         }
                         float s_a = 0.f, s_b = 0.f;
 #pragma unroll
@@ -474,6 +565,9 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
         e = cudaFuncSetAttribute(tc_scores_kernel<D, 1>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc_scores_kernel<D, 2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     const int R = sp.G * sp.L_obs;
@@ -482,6 +576,8 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     tp.n_mtiles = (R + TC_ROWS - 1) / TC_ROWS;
     tp.chunk_tiles = sp.chunk / TC_ROWS;
     tp.n_col_tiles = (sp.n_cols + TC_ROWS - 1) / TC_ROWS;
+    tp.col_chunks = 1;
+    tp.col_chunk_tiles = tp.n_col_tiles;
     tp.dev_code = dev_code;
     const long long pairs = (long long)sp.B * sp.Hkv;
     tc_scores_kernel<D, 0><<<(unsigned)(pairs * tp.n_mtiles * sp.n_chunks), TC_THREADS, SMEM,
@@ -492,8 +588,22 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     rowlse_tc_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(sp);
     e = cudaGetLastError();
     if (e != cudaSuccess || tp.n_col_tiles == 0) return e;
-    tc_scores_kernel<D, 1><<<(unsigned)(pairs * tp.n_col_tiles), TC_THREADS, SMEM, stream>>>(
-        qm, km, tp);
+    const int n_rb = (R + TC_ROWS - 1) / TC_ROWS;
+    if (R <= TC_ROWS || (sp.G > 1 && TC_ROWS % sp.L_obs == 0)) {
+        // every head inside one row block: keep the row block, stream the key tiles
+        int n_sm = 152;
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        const long long base = pairs * n_rb;
+        long long chunks = (4LL * n_sm + base - 1) / base;
+        if (chunks > tp.n_col_tiles) chunks = tp.n_col_tiles;
+        tp.col_chunk_tiles = (int)((tp.n_col_tiles + chunks - 1) / chunks);
+        tp.col_chunks = (tp.n_col_tiles + tp.col_chunk_tiles - 1) / tp.col_chunk_tiles;
+        tc_scores_kernel<D, 2><<<(unsigned)(base * tp.col_chunks), TC_THREADS, SMEM, stream>>>(
+            qm, km, tp);
+    } else {
+        tc_scores_kernel<D, 1><<<(unsigned)(pairs * tp.n_col_tiles), TC_THREADS, SMEM, stream>>>(
+            qm, km, tp);
+    }
     return cudaGetLastError();
 }
 

@@ -6,11 +6,14 @@
 // kept indices keep their original order, followed by `tail` always-kept indices n .. n+tail-1
 // (the SnapKV observation window, or H2O's recent quota).
 //
-// One 1024-thread block per row.  Scores are mapped to order-preserving 32-bit keys; four
-// 8-bit radix passes (shared-memory histograms) find the exact key T of the k-th largest and
-// how many keys equal to T are still to be taken.  A last pair of passes emits, in index order,
-// every key > T plus the first `need` keys == T: each warp owns a contiguous segment, counts
-// its keeps with ballots, a block scan gives each warp its output offset.
+// One 1024-thread block per row.  Scores are mapped to order-preserving 32-bit keys (staged in
+// shared memory when the row fits).  A min/max pass finds the highest bit in which the row's
+// keys differ, so the radix passes skip the bits every key shares (scores of one row sit in a
+// few octaves); then 8-bit radix passes with one private shared-memory histogram per warp find
+// the exact key T of the k-th largest and how many keys equal to T are still to be taken.  A
+// last pair of passes emits, in index order, every key > T plus the first `need` keys == T:
+// each warp owns a contiguous segment, counts its keeps with ballots, a block scan gives each
+// warp its output offset.
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,14 +30,18 @@ __device__ __forceinline__ uint32_t order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+constexpr int TK_SMEM_KEYS = 40 * 1024;   // rows up to this many keys are staged in smem
+
 __global__ void __launch_bounds__(TK_THREADS)
 topk_rows_kernel(const float *score, int64_t score_stride, int n, int k, int tail, int32_t *idx,
                  int64_t idx_stride)
 {
+    __shared__ uint32_t whist[TK_WARPS][256];
     __shared__ uint32_t hist[256];
-    __shared__ uint32_t sh_bin, sh_above;
+    __shared__ uint32_t sh_bin, sh_above, sh_lo, sh_hi;
     __shared__ uint32_t w_gt[TK_WARPS], w_eq[TK_WARPS];
     __shared__ uint32_t w_keep_before[TK_WARPS], w_eq_before[TK_WARPS];
+    extern __shared__ uint32_t skeys[];
 
     const float *s = score + (size_t)blockIdx.x * score_stride;
     int32_t *out = idx + (size_t)blockIdx.x * idx_stride;
@@ -46,16 +53,53 @@ topk_rows_kernel(const float *score, int64_t score_stride, int n, int k, int tai
         for (int j = tid; j < n; j += TK_THREADS) out[j] = j;
         return;
     }
+    const bool staged = n <= TK_SMEM_KEYS;
+    auto key_at = [&](int i) -> uint32_t { return staged ? skeys[i] : order_key(s[i]); };
 
-    // ---- radix select of the k-th largest key ----------------------------------------------
-    uint32_t prefix = 0, mask = 0;
+    // ---- stage the keys, find their range ---------------------------------------------------
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int i = tid; i < n; i += TK_THREADS) {
+        const uint32_t u = order_key(s[i]);
+        if (staged) skeys[i] = u;
+        lo = min(lo, u);
+        hi = max(hi, u);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (tid == 0) { sh_lo = 0xffffffffu; sh_hi = 0u; }
+    __syncthreads();
+    if (lane == 0) { atomicMin(&sh_lo, lo); atomicMax(&sh_hi, hi); }
+    __syncthreads();
+    lo = sh_lo;
+    hi = sh_hi;
+    const uint32_t diff = lo ^ hi;
+    const int top = diff ? 31 - __clz(diff) : -1;   // highest bit where keys differ
+
+    // ---- radix select of the k-th largest key over the differing bits ------------------------
+    // bits every key shares (all 32 when the keys are all equal, top = -1)
+    const uint32_t shared_mask = top < 0 ? 0xffffffffu : (top >= 31 ? 0u : ~((2u << top) - 1u));
+    uint32_t prefix = hi & shared_mask;
+    uint32_t mask = shared_mask;
     uint32_t need = (uint32_t)k;   // still to take among keys matching the prefix
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int j = tid; j < 256; j += TK_THREADS) hist[j] = 0;
+    for (int t = top; t >= 0; t -= 8) {
+        const int shift = t >= 7 ? t - 7 : 0;
+        const uint32_t dmask = (2u << (t - shift)) - 1u;   // digit of bits shift .. t
+        for (int j = tid; j < TK_WARPS * 256; j += TK_THREADS) (&whist[0][0])[j] = 0;
         __syncthreads();
+        uint32_t *mine = whist[warp];
         for (int i = tid; i < n; i += TK_THREADS) {
-            const uint32_t u = order_key(s[i]);
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+            const uint32_t u = key_at(i);
+            if ((u & mask) == prefix) atomicAdd(&mine[(u >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        for (int j = tid; j < 256; j += TK_THREADS) {
+            uint32_t c = 0;
+#pragma unroll 8
+            for (int w = 0; w < TK_WARPS; ++w) c += whist[w][j];
+            hist[j] = c;
         }
         __syncthreads();
         if (warp == 0) {
@@ -81,11 +125,11 @@ topk_rows_kernel(const float *score, int64_t score_stride, int n, int k, int tai
         }
         __syncthreads();
         prefix |= sh_bin << shift;
-        mask |= 255u << shift;
+        mask |= dmask << shift;
         need -= sh_above;
         __syncthreads();
     }
-    const uint32_t T = prefix;
+    const uint32_t T = prefix;   // every bit fixed: the exact k-th largest key
 
     // ---- counts per warp segment ------------------------------------------------------------
     const int seg = ((n + TK_WARPS - 1) / TK_WARPS + 31) & ~31;
@@ -94,7 +138,7 @@ topk_rows_kernel(const float *score, int64_t score_stride, int n, int k, int tai
     uint32_t gt = 0, eq = 0;
     for (int i0 = beg; i0 < end; i0 += 32) {
         const int i = i0 + lane;
-        const uint32_t u = i < end ? order_key(s[i]) : 0u;
+        const uint32_t u = i < end ? key_at(i) : 0u;
         gt += __popc(__ballot_sync(0xffffffffu, i < end && u > T));
         eq += __popc(__ballot_sync(0xffffffffu, i < end && u == T));
     }
@@ -119,7 +163,7 @@ topk_rows_kernel(const float *score, int64_t score_stride, int n, int k, int tai
     const uint32_t lt_mask = (1u << lane) - 1u;
     for (int i0 = beg; i0 < end; i0 += 32) {
         const int i = i0 + lane;
-        const uint32_t u = i < end ? order_key(s[i]) : 0u;
+        const uint32_t u = i < end ? key_at(i) : 0u;
         const bool is_eq = i < end && u == T;
         const uint32_t eq_ballot = __ballot_sync(0xffffffffu, is_eq);
         const uint32_t eq_rank = eq_seen + __popc(eq_ballot & lt_mask);
@@ -144,8 +188,19 @@ cudaError_t launch_topk_rows(const float *score, int64_t score_stride, int rows,
                              int tail, int32_t *idx, int64_t idx_stride, cudaStream_t stream)
 {
     if (rows == 0) return cudaSuccess;
-    topk_rows_kernel<<<rows, TK_THREADS, 0, stream>>>(score, score_stride, n, k, tail, idx,
-                                                       idx_stride);
+    const int dyn = n <= TK_SMEM_KEYS ? n * (int)sizeof(uint32_t) : 0;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             TK_SMEM_KEYS * (int)sizeof(uint32_t));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    topk_rows_kernel<<<rows, TK_THREADS, dyn, stream>>>(score, score_stride, n, k, tail, idx,
+                                                         idx_stride);
     return cudaGetLastError();
 }
 
