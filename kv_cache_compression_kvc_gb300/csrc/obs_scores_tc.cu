@@ -115,6 +115,52 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// All 128 columns of a tile (four 32-column loads, one wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[4][32])
+{
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t *r = reinterpret_cast<uint32_t *>(v[c]);
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+            "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+              "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+              "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+              "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+              "=r"(r[31])
+            : "r"(taddr + c * 32));
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Sum of 32 values with four independent chains (short dependency chains for one warp per
+// scheduler).
+__device__ __forceinline__ float sum32(const float *x)
+{
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        a0 += x[j];
+        a1 += x[j + 1];
+        a2 += x[j + 2];
+        a3 += x[j + 3];
+    }
+    return (a0 + a1) + (a2 + a3);
+}
+__device__ __forceinline__ float max32(const float *x)
+{
+    float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
+#pragma unroll
+    for (int j = 4; j < 32; j += 4) {
+        a0 = fmaxf(a0, x[j]);
+        a1 = fmaxf(a1, x[j + 1]);
+        a2 = fmaxf(a2, x[j + 2]);
+        a3 = fmaxf(a3, x[j + 3]);
+    }
+    return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+}
+
 __device__ __forceinline__ void epilogue_sync()
 {
     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -297,27 +343,27 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     tc_fence_after();
                     const int k0 = (t_begin + i) * TC_ROWS;
                     const bool need_mask = k0 + TC_ROWS - 1 > first_pos || k0 + TC_ROWS > p.N;
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        float v[32];
-                        tmem_ld32(tmem_base + ab * 128 + lane_off + c * 32, v);
-                        if (need_mask) {
+                    float v[4][32];
+                    tmem_ld128(tmem_base + ab * 128 + lane_off, v);
+                    if (need_mask) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
                                 const int key = k0 + c * 32 + j;
-                                if (key > pos || key >= p.N) v[j] = -INFINITY;
+                                if (key > pos || key >= p.N) v[c][j] = -INFINITY;
                             }
-                        }
-                        float mx = v[0];
-#pragma unroll
-                        for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
-                        const float m_new = fmaxf(m_run, mx * p.scale_log2);
-                        float z = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) z += ex2(fmaf(v[j], p.scale_log2, -m_new));
-                        z_run = z_run * ex2(m_run - m_new) + z;
-                        m_run = m_new;
                     }
+                    const float mx = fmaxf(fmaxf(max32(v[0]), max32(v[1])),
+                                           fmaxf(max32(v[2]), max32(v[3])));
+                    const float m_new = fmaxf(m_run, mx * p.scale_log2);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[c][j] = ex2(fmaf(v[c][j], p.scale_log2, -m_new));
+                    const float z = (sum32(v[0]) + sum32(v[1])) + (sum32(v[2]) + sum32(v[3]));
+                    z_run = z_run * ex2(m_run - m_new) + z;
+                    m_run = m_new;
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
@@ -344,12 +390,13 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     tc_fence_after();
                     int g_cur = fixed_row0 / p.L_obs;
                     float acc_g = 0.f;
-#pragma unroll 1
+                    float vt[4][32];
+                    tmem_ld128(tmem_base + ab * 128 + lane_off, vt);
+#pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int rc = fixed_row0 + c * 32;
                         if (c * 32 >= rows_blk) break;
-                        float v[32];
-                        tmem_ld32(tmem_base + ab * 128 + lane_off + c * 32, v);
+                        float *v = vt[c];
                         const int g_a = rc / p.L_obs;
                         const int rows_here = min(32, rows_blk - c * 32);
                         const int split = min(rows_here, (g_a + 1) * p.L_obs - rc);
@@ -360,11 +407,10 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                         }
                         if (split == 32 && !mask_tile) {
                             // the whole chunk is one head and every key is visible
-                            float s_a = 0.f;
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
-                                s_a += ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
-                            acc_g += s_a;
+                                v[j] = ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
+                            acc_g += sum32(v);
                             continue;
                         }
                         float s_a = 0.f, s_b = 0.f;
@@ -424,11 +470,10 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                         }
                         if (split == 32 && !mask_tile) {
                             // the whole chunk is one head and every key is visible
-                            float s_a = 0.f;
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
-                                s_a += ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
-                            acc_g += s_a;
+                                v[j] = ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
+                            acc_g += sum32(v);
                             continue;
                         }
                         float s_a = 0.f, s_b = 0.f;
