@@ -294,6 +294,13 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
     p.dev_code = code;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    bool used = false;
+    if (cache->dtype == KVC_BF16 && !p.rope && G > 1) {
+        // query groups: the two matrix products of the group run on the tensor cores
+        e = kvc::launch_decode_attn_mma(p, cache->d_head, G, s, &used);
+        if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+        if (used) return ok();
+    }
     if (cache->dtype == KVC_BF16)
         e = p.rope ? kvc::launch_decode_attn_bf16_rope(p, cache->d_head, G, s)
                    : kvc::launch_decode_attn_bf16(p, cache->d_head, G, s);

@@ -1,0 +1,458 @@
+// decode_mma.cu -- grouped-query decode attention on the tensor cores (bf16 caches, no RoPE).
+//
+// Same result and same schedule as decode_attn.cuh (persistent blocks over the flattened
+// (pair, tile) space, a shared-memory ring, last-block log-sum-exp merge), but the arithmetic of
+// a query group runs as matrix products.  With G query heads sharing every K/V row, the logits
+// of a tile are the [G x D] x [D x keys] product and the output update the [G x keys] x
+// [keys x D] product -- a dense contraction of G rows.  On CUDA cores the bf16 widening, the
+// FMAs and the cross-lane reductions per key exceed what the SMs can issue while HBM delivers
+// the cache at full rate once G >= 4, so these two products use mma.sync (m16n8k16, bf16 in,
+// fp32 accumulate) with the G heads as rows 0..G-1 of the 16-row tile.
+//
+// Data movement.  K and V tiles (TK slots x D) arrive by TMA (cp.async.bulk.tensor, 4-D tensor
+// map over [batch][head][slot][dim], 128-byte swizzle) into an NS-stage ring; ldmatrix reads
+// the swizzled tiles without bank conflicts (.trans for V, whose rows are keys).
+//
+// Warp layout.  Each warp owns 16 keys of the tile: it computes their logits for all heads,
+// updates its online-softmax state (lazy running max, base-2 exponentials), converts the
+// probabilities in place into the A operand of the P.V product (the accumulator layout of
+// m16n8 is the operand layout of m16k16) and accumulates o.  For D = 256 two warps share the
+// same 16 keys and split the head dimension of o.  P is rounded to bf16 for the P.V product;
+// the sums l are kept in fp32.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvc {
+
+namespace {
+
+constexpr int MW = 8;                        // warps per block
+constexpr int M_THREADS = MW * 32;
+constexpr float kSlack = 8.0f;               // lazy running max, log2 units
+constexpr int kCodeSchedule = 8;             // KVC_DEV_SCHEDULE
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D(16x8 fp32) += A(16x16 bf16, rows 8..15 zero) * B(16x8 bf16)
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Byte offset of (row, 8-element chunk) inside a tile stored as D/64 sub-tiles of rows x 128 B
+// with the 128-byte swizzle (16-byte chunk c of row r at c ^ (r mod 8)).
+__device__ __forceinline__ uint32_t sw_off(int row, int chunk, int rows_per_sub)
+{
+    const int sub = chunk >> 3, c = chunk & 7;
+    return (uint32_t)(sub * rows_per_sub * 128 + row * 128 + ((c ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ int cta_of(long long t, long long T, int C)
+{
+    return (int)(((t + 1) * (long long)C - 1) / T);
+}
+
+template <int D, int G>
+struct MmaPlan {
+    static constexpr int TK = D == 256 ? 64 : 128;             // slots per tile
+    static constexpr int PAIRS = D == 256 ? 2 : 1;             // warps sharing 16 keys
+    static constexpr int KGROUPS = MW / PAIRS;                  // 16-key groups per tile
+    static_assert(KGROUPS * 16 == TK, "tile = 16 keys per key group");
+    static constexpr int DW = D / PAIRS;                        // output dims per warp
+    static constexpr int TILE_BYTES = TK * D * 2;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int MERGE_BYTES = KGROUPS * G * (D + 2) * 4 + 16;
+    static constexpr int BAR_BYTES = 128;
+    static constexpr int NS_fit = (220 * 1024 - 1024 - MERGE_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int NS = NS_fit > 4 ? 4 : NS_fit;
+    static_assert(NS >= 2, "two stages at least");
+    static constexpr int SMEM = 1024 + NS * STAGE_BYTES + BAR_BYTES + MERGE_BYTES;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(M_THREADS, 1)
+decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const DecodeParams p)
+{
+    using PL = MmaPlan<D, G>;
+    constexpr int TK = PL::TK, NS = PL::NS, DW = PL::DW;
+    constexpr int KSTEPS = D / 16;
+    constexpr int NB = DW / 8;                 // 8-dim output blocks per warp
+    static_assert(G <= 8, "group fits rows 0..7 of the 16-row tile");
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t stage0 = base;
+    const uint32_t bars = stage0 + NS * PL::STAGE_BYTES;
+    const uint32_t bar_full = bars, bar_empty = bars + 8 * NS;
+    float *sm_m = reinterpret_cast<float *>(smem_raw + (bars + PL::BAR_BYTES - raw));
+    float *sm_l = sm_m + PL::KGROUPS * G;
+    float *sm_o = sm_l + PL::KGROUPS * G;      // [KGROUPS][G][D]
+    int *sm_flag = reinterpret_cast<int *>(sm_o + PL::KGROUPS * G * D);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kg = warp / PL::PAIRS;           // key group (16 keys of the tile)
+    const int half = warp % PL::PAIRS;         // output-dim half (D = 256)
+    const int gr = lane >> 2, tq = lane & 3;   // mma fragment row / column pair
+    const int C = gridDim.x, cta = blockIdx.x;
+    const long long T_all = (long long)p.P * p.NT;
+    const long long t_begin = (long long)cta * T_all / C;
+    const long long t_end = (long long)(cta + 1) * T_all / C;
+    const int n_tiles = (int)(t_end - t_begin);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, MW);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto pair_slots = [&](int q) -> int {
+        if (p.len != nullptr) {
+            const int n = p.len[q];
+            return n < 0 ? 0 : (n > p.cap ? p.cap : n);
+        }
+        return p.n_valid;
+    };
+    auto issue_tile = [&](int i) {
+        const long long t = t_begin + i;
+        const int s = i % NS;
+        const int q = (int)(t / p.NT);
+        const int j0 = (int)(t % p.NT) * TK;
+        const uint32_t full = bar_full + 8 * s;
+        if (j0 >= pair_slots(q)) {
+            mbar_arrive(full);
+            return;
+        }
+        const int b = q / p.Hkv, kh = q % p.Hkv;
+        const uint32_t kdst = stage0 + s * PL::STAGE_BYTES, vdst = kdst + PL::TILE_BYTES;
+        mbar_arrive_expect_tx(full, (uint32_t)PL::STAGE_BYTES);
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub) {
+            tma_load_4d(kdst + sub * TK * 128, &kmap, sub * 64, j0, kh, b, full);
+            tma_load_4d(vdst + sub * TK * 128, &vmap, sub * 64, j0, kh, b, full);
+        }
+    };
+    if (threadIdx.x == 0)
+        for (int i = 0; i < NS && i < n_tiles; ++i) issue_tile(i);
+
+    // ---- per-pair state ---------------------------------------------------------------------
+    uint32_t qa0[KSTEPS], qa2[KSTEPS];         // q rows as A fragments (rows >= G are zero)
+    float o[NB][4];
+    float m_row = kNegBig, l_part = 0.f;       // row gr (head gr); l summed over the 4 lanes later
+    int cur = -1, cur_slots = 0;
+    float *lg_row = nullptr;
+
+    auto start_pair = [&](int q) {
+        cur = q;
+        cur_slots = pair_slots(q);
+        const int b = q / p.Hkv, kh = q % p.Hkv;
+        const __nv_bfloat16 *qb =
+            static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)b * p.Hq + (size_t)kh * G) * D;
+#pragma unroll
+        for (int s = 0; s < KSTEPS; ++s) {
+            if (gr < G) {
+                qa0[s] = *reinterpret_cast<const uint32_t *>(qb + (size_t)gr * D + 16 * s + 2 * tq);
+                qa2[s] = *reinterpret_cast<const uint32_t *>(qb + (size_t)gr * D + 16 * s + 2 * tq + 8);
+            } else {
+                qa0[s] = 0u;
+                qa2[s] = 0u;
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NB; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        m_row = kNegBig;
+        l_part = 0.f;
+        lg_row = (p.logits != nullptr && gr < G)
+                     ? p.logits + (size_t)((q / p.Hkv) * p.Hq + (q % p.Hkv) * G + gr) * p.logits_stride
+                     : nullptr;
+    };
+
+    auto finish_pair = [&](int q) {
+        float l_row = l_part;
+        l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+        l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+        if (gr < G) {
+#pragma unroll
+            for (int n = 0; n < NB; ++n) {
+                const int d = half * DW + 8 * n + 2 * tq;
+                sm_o[(kg * G + gr) * D + d] = o[n][0];
+                sm_o[(kg * G + gr) * D + d + 1] = o[n][1];
+            }
+            if (tq == 0 && half == 0) {
+                sm_m[kg * G + gr] = m_row;
+                sm_l[kg * G + gr] = l_row;
+            }
+        }
+        __syncthreads();
+        const long long t_first = (long long)q * p.NT;
+        const int c_lo = cta_of(t_first, T_all, C);
+        const int c_hi = cta_of(t_first + p.NT - 1, T_all, C);
+        const int nseg = c_hi - c_lo + 1, seg = cta - c_lo;
+        const bool seg_ok = nseg <= p.max_seg;
+        if (!seg_ok && threadIdx.x == 0) record_code(p.dev_code, kCodeSchedule);
+        const int rows0 = (q / p.Hkv) * p.Hq + (q % p.Hkv) * G;
+        for (int i = threadIdx.x; i < G * D; i += M_THREADS) {
+            const int g = i / D, d = i % D;
+            float M = sm_m[g];
+#pragma unroll
+            for (int w = 1; w < PL::KGROUPS; ++w) M = fmaxf(M, sm_m[w * G + g]);
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < PL::KGROUPS; ++w) {
+                const float c = ex2(sm_m[w * G + g] - M);
+                L += sm_l[w * G + g] * c;
+                O += sm_o[(w * G + g) * D + d] * c;
+            }
+            if (nseg == 1) {
+                p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
+                if (d == 0 && p.lse != nullptr)
+                    p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+            } else if (seg_ok) {
+                const size_t slot = ((size_t)q * p.max_seg + seg) * G + g;
+                p.ws_o[slot * D + d] = O;
+                if (d == 0) {
+                    p.ws_ml[slot * 2] = M;
+                    p.ws_ml[slot * 2 + 1] = L;
+                }
+            }
+        }
+        if (nseg > 1 && seg_ok) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) *sm_flag = (atomicAdd(&p.ws_cnt[q], 1) == nseg - 1);
+            __syncthreads();
+            if (*sm_flag) {
+                __threadfence();
+                for (int i = threadIdx.x; i < G * D; i += M_THREADS) {
+                    const int g = i / D, d = i % D;
+                    float M = kNegBig;
+                    for (int sg = 0; sg < nseg; ++sg)
+                        M = fmaxf(M, __ldcg(&p.ws_ml[(((size_t)q * p.max_seg + sg) * G + g) * 2]));
+                    float L = 0.f, O = 0.f;
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const size_t slot = ((size_t)q * p.max_seg + sg) * G + g;
+                        const float c = ex2(__ldcg(&p.ws_ml[slot * 2]) - M);
+                        L += __ldcg(&p.ws_ml[slot * 2 + 1]) * c;
+                        O += __ldcg(&p.ws_o[slot * D + d]) * c;
+                    }
+                    p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
+                    if (d == 0 && p.lse != nullptr)
+                        p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+                }
+                if (threadIdx.x == 0) p.ws_cnt[q] = 0;
+            }
+        }
+        __syncthreads();
+    };
+
+    for (int i = 0; i < n_tiles; ++i) {
+        const long long t = t_begin + i;
+        const int s = i % NS;
+        const int q = (int)(t / p.NT);
+        if (q != cur) {
+            if (cur >= 0) finish_pair(cur);
+            start_pair(q);
+        }
+        mbar_wait(bar_full + 8 * s, (i / NS) & 1, p.dev_code);
+        const int j0 = (int)(t % p.NT) * TK;
+        const int key0 = kg * 16;                          // this warp's 16 keys in the tile
+        if (j0 + key0 < cur_slots) {
+            const uint32_t kst = stage0 + s * PL::STAGE_BYTES, vst = kst + PL::TILE_BYTES;
+            // ---- logits: S[16 x 16 keys] = Q . K^T over D -------------------------------------
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const int mrow = lane & 7, mi = lane >> 3;    // ldmatrix: matrix mi, row mrow
+#pragma unroll
+            for (int sp = 0; sp < KSTEPS / 2; ++sp) {
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kst + sw_off(key0 + 8 * nb + mrow, 4 * sp + mi, TK), b0, b1, b2, b3);
+                    mma16816(sc[nb], qa0[2 * sp], qa2[2 * sp], b0, b1);
+                    mma16816(sc[nb], qa0[2 * sp + 1], qa2[2 * sp + 1], b2, b3);
+                }
+            }
+            // ---- online softmax on row gr (keys key0 + 8nb + 2tq + e) ---------------------------
+            float lg[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = j0 + key0 + 8 * nb + 2 * tq + e;
+                    const float v = sc[nb][e] * p.scale_log2;
+                    lg[nb][e] = j < cur_slots ? v : -INFINITY;
+                    mx = fmaxf(mx, lg[nb][e]);
+                    if (lg_row != nullptr && j < cur_slots) lg_row[j] = v * kLn2;
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            if (mx > m_row + kSlack) {
+                const float corr = ex2(m_row - mx);
+                l_part *= corr;
+#pragma unroll
+                for (int n = 0; n < NB; ++n) {
+                    o[n][0] *= corr;
+                    o[n][1] *= corr;
+                }
+                m_row = mx;
+            }
+            float pr[2][2];
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    pr[nb][e] = ex2(lg[nb][e] - m_row);
+                    l_part += pr[nb][e];
+                }
+            const uint32_t pa0 = pack_bf16(pr[0][0], pr[0][1]);   // keys 2tq, 2tq+1
+            const uint32_t pa2 = pack_bf16(pr[1][0], pr[1][1]);   // keys 8+2tq, 9+2tq
+            // ---- o[16 x DW] += P[16 x 16 keys] . V[16 keys x DW] --------------------------------
+            // Slots past the pair's length are still in the tile (the cache may hold any bytes
+            // there); their probabilities are 0, but 0 * NaN would poison the product, so the
+            // warp zeroes those rows of its dim range first.
+            const int valid_here = cur_slots - (j0 + key0);
+            if (valid_here < 16) {
+                constexpr int CH = DW / 8;                 // 16-byte chunks per row in my range
+                for (int x = lane; x < (16 - valid_here) * CH; x += 32) {
+                    const int rr = key0 + valid_here + x / CH;
+                    const int chunk = (half * DW) / 8 + x % CH;
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                                     vst + sw_off(rr, chunk, TK)),
+                                 "r"(0u)
+                                 : "memory");
+                }
+                __syncwarp();
+                // order these generic-proxy writes before the next TMA write into the stage
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            const int vrow = key0 + (mi & 1) * 8 + mrow;
+#pragma unroll
+            for (int n = 0; n < NB; n += 2) {
+                uint32_t b0, b1, b2, b3;
+                const int chunk = (half * DW) / 8 + n + (mi >> 1);
+                ldsm_x4_t(vst + sw_off(vrow, chunk, TK), b0, b1, b2, b3);
+                mma16816(o[n], pa0, pa2, b0, b1);
+                mma16816(o[n + 1], pa0, pa2, b2, b3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (threadIdx.x == 0 && i + NS < n_tiles) {
+            mbar_wait(bar_empty + 8 * s, (i / NS) & 1, p.dev_code);
+            issue_tile(i + NS);
+        }
+    }
+    if (cur >= 0) finish_pair(cur);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+std::once_flag g_enc_once;
+
+bool encoder()
+{
+    std::call_once(g_enc_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            g_enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_enc != nullptr;
+}
+
+bool encode_cache(CUtensorMap *m, const void *ptr, const DecodeParams &p, int D, int TK)
+{
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.cap, (cuuint64_t)p.Hkv, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)p.ss * 2, (cuuint64_t)p.sh * 2, (cuuint64_t)p.sb * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)TK, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream, bool *used)
+{
+    using PL = MmaPlan<D, G>;
+    CUtensorMap km, vm;
+    if (!encode_cache(&km, p.k, p, D, PL::TK) || !encode_cache(&vm, p.v, p, D, PL::TK))
+        return cudaSuccess;   // not encodable (unusual strides): the caller falls back
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, PL::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    DecodeParams q = p;
+    q.NT = p.cap > 0 ? (p.cap + PL::TK - 1) / PL::TK : 1;
+    const long long T_all = (long long)q.P * q.NT;
+    const int C = (int)(T_all < p.n_sm ? T_all : p.n_sm);
+    *used = true;
+    decode_mma_kernel<D, G><<<C, M_THREADS, PL::SMEM, stream>>>(km, vm, q);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_attn_mma(const DecodeParams &p, int D, int G, cudaStream_t stream,
+                                   bool *used)
+{
+    *used = false;
+    if (p.rope || !encoder()) return cudaSuccess;
+#define KVC_MMA_CASE(DD, GG) \
+    if (D == DD && G == GG) return launch_typed<DD, GG>(p, stream, used);
+    KVC_MMA_CASE(64, 2) KVC_MMA_CASE(64, 4) KVC_MMA_CASE(64, 6) KVC_MMA_CASE(64, 8)
+    KVC_MMA_CASE(128, 2) KVC_MMA_CASE(128, 4) KVC_MMA_CASE(128, 6) KVC_MMA_CASE(128, 8)
+    KVC_MMA_CASE(256, 2) KVC_MMA_CASE(256, 4) KVC_MMA_CASE(256, 6) KVC_MMA_CASE(256, 8)
+#undef KVC_MMA_CASE
+    return cudaSuccess;
+}
+
+}  // namespace kvc

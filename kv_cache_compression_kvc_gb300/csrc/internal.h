@@ -45,6 +45,10 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm);
 void set_last_error(const char *msg);
 cudaError_t launch_decode_attn_f32(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16(const DecodeParams &p, int D, int G, cudaStream_t stream);
+// Tensor-core grouped-query decode (bf16, no RoPE, group 2..8).  Sets *used = false, launching
+// nothing, when the case is not covered (the CUDA-core kernel then runs).
+cudaError_t launch_decode_attn_mma(const DecodeParams &p, int D, int G, cudaStream_t stream,
+                                   bool *used);
 cudaError_t launch_decode_attn_f32_rope(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16_rope(const DecodeParams &p, int D, int G,
                                          cudaStream_t stream);
