@@ -162,4 +162,77 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+
+// ---- split-slot decode: merge of the partial softmax states of one (batch, KV head) pair -------
+// Called by all NT threads of the last block to finish pair q.  Partial state s of head g is
+// (m, l) at ws_ml[((q*max_seg + s)*G + g)*2] and o[0..D) at ws_o[((q*max_seg + s)*G + g)*D]
+// (m in log2 units, o not yet divided by l).  One warp per head reduces the (m, l) pairs with
+// shuffles and leaves the weights 2^(m_s - M) / L in `scratch`; then every output sums its
+// nseg partial values with independent loads instead of a dependent chain of L2 round trips.
+// scratch: n_scratch floats; pairs with nseg * G > n_scratch take the serial loop.
+template <int G, int D, int NT>
+__device__ __forceinline__ void merge_pair_partials(const float *ws_o, const float *ws_ml,
+                                                    int max_seg, int q, int nseg, float *out,
+                                                    float *lse, int rows0, float *scratch,
+                                                    int n_scratch)
+{
+    constexpr int NWARP = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t base = (size_t)q * max_seg * G;   // partial state (s, g) is base + s*G + g
+    if (nseg * G > n_scratch) {
+        for (int i = threadIdx.x; i < G * D; i += NT) {
+            const int g = i / D, d = i % D;
+            float M = kNegBig;
+            for (int s = 0; s < nseg; ++s) M = fmaxf(M, __ldcg(&ws_ml[(base + s * G + g) * 2]));
+            float L = 0.f, O = 0.f;
+            for (int s = 0; s < nseg; ++s) {
+                const size_t slot = base + s * G + g;
+                const float c = ex2(__ldcg(&ws_ml[slot * 2]) - M);
+                L += __ldcg(&ws_ml[slot * 2 + 1]) * c;
+                O += __ldcg(&ws_o[slot * D + d]) * c;
+            }
+            out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
+            if (d == 0 && lse != nullptr)
+                lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+        return;
+    }
+    for (int g = warp; g < G; g += NWARP) {
+        float M = kNegBig;
+        for (int s = lane; s < nseg; s += 32) M = fmaxf(M, __ldcg(&ws_ml[(base + s * G + g) * 2]));
+        M = warp_max(M);
+        float L = 0.f;
+        for (int s = lane; s < nseg; s += 32) {
+            const size_t slot = base + s * G + g;
+            const float c = ex2(__ldcg(&ws_ml[slot * 2]) - M);
+            scratch[s * G + g] = c;
+            L += __ldcg(&ws_ml[slot * 2 + 1]) * c;
+        }
+        L = warp_sum(L);
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int s = lane; s < nseg; s += 32) scratch[s * G + g] *= inv;
+        if (lane == 0 && lse != nullptr)
+            lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * D; i += NT) {
+        const int g = i / D, d = i % D;
+        const float *src = ws_o + (base + g) * D + d;
+        const float *w = scratch + g;
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        int s = 0;
+        for (; s + 4 <= nseg; s += 4) {
+            const float v0 = __ldcg(src + (size_t)(s + 0) * G * D);
+            const float v1 = __ldcg(src + (size_t)(s + 1) * G * D);
+            const float v2 = __ldcg(src + (size_t)(s + 2) * G * D);
+            const float v3 = __ldcg(src + (size_t)(s + 3) * G * D);
+            acc0 = fmaf(w[(s + 0) * G], v0, acc0);
+            acc1 = fmaf(w[(s + 1) * G], v1, acc1);
+            acc2 = fmaf(w[(s + 2) * G], v2, acc2);
+            acc3 = fmaf(w[(s + 3) * G], v3, acc3);
+        }
+        for (; s < nseg; ++s) acc0 = fmaf(w[s * G], __ldcg(src + (size_t)s * G * D), acc0);
+        out[(size_t)(rows0 + g) * D + d] = (acc0 + acc1) + (acc2 + acc3);
+    }
+}
 }  // namespace kvc

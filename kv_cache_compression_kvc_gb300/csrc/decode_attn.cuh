@@ -184,12 +184,19 @@ decode_attn_kernel(const DecodeParams p)
 
     // ---- tile loader: thread 0 issues the bulk copies of tile i into stage i % NS ----------
     const bool dense = (p.ss == D);
+    // The issuing thread keeps the slot count of the pair it is loading: one global read per
+    // pair, not one per tile on the critical path of every copy.
+    int iss_q = -1, iss_slots = 0;
     auto issue_tile = [&](int i) {
         const long long t = t_begin + i;
         const int s = i % NS;
         const int q = (int)(t / p.NT);
         const int j0 = (int)(t % p.NT) * TK;
-        const int rows = max(0, min(TK, pair_slots(q) - j0));
+        if (q != iss_q) {
+            iss_q = q;
+            iss_slots = pair_slots(q);
+        }
+        const int rows = max(0, min(TK, iss_slots - j0));
         const uint32_t full = bar_full + 8 * s;
         const uint32_t kdst = stage0 + s * SM::kStageBytes;
         const uint32_t vdst = kdst + SM::kTileBytes;
@@ -330,22 +337,8 @@ decode_attn_kernel(const DecodeParams p)
             __syncthreads();
             if (*sm_flag) {
                 __threadfence();
-                for (int i = threadIdx.x; i < G * D; i += kDecodeThreads) {
-                    const int g = i / D, d = i % D;
-                    float M = kNegBig;
-                    for (int sg = 0; sg < nseg; ++sg)
-                        M = fmaxf(M, __ldcg(&p.ws_ml[(((size_t)q * p.max_seg + sg) * G + g) * 2]));
-                    float L = 0.f, O = 0.f;
-                    for (int sg = 0; sg < nseg; ++sg) {
-                        const size_t slot = ((size_t)q * p.max_seg + sg) * G + g;
-                        const float c = ex2(__ldcg(&p.ws_ml[slot * 2]) - M);
-                        L += __ldcg(&p.ws_ml[slot * 2 + 1]) * c;
-                        O += __ldcg(&p.ws_o[slot * D + d]) * c;
-                    }
-                    p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
-                    if (d == 0 && p.lse != nullptr)
-                        p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-                }
+                merge_pair_partials<G, D, kDecodeThreads>(p.ws_o, p.ws_ml, p.max_seg, q, nseg, p.out,
+                                                    p.lse, rows0, sm_o, NW * G * D);
                 if (threadIdx.x == 0) p.ws_cnt[q] = 0;   // leave the ticket zeroed
             }
         }

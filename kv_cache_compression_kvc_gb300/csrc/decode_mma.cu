@@ -152,13 +152,20 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         return p.n_valid;
     };
+    // The issuing thread keeps the slot count of the pair it is loading: one global read per
+    // pair, not one per tile on the critical path of every copy.
+    int iss_q = -1, iss_slots = 0;
     auto issue_tile = [&](int i) {
         const long long t = t_begin + i;
         const int s = i % NS;
         const int q = (int)(t / p.NT);
         const int j0 = (int)(t % p.NT) * TK;
         const uint32_t full = bar_full + 8 * s;
-        if (j0 >= pair_slots(q)) {
+        if (q != iss_q) {
+            iss_q = q;
+            iss_slots = pair_slots(q);
+        }
+        if (j0 >= iss_slots) {
             mbar_arrive(full);
             return;
         }
@@ -262,22 +269,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             __syncthreads();
             if (*sm_flag) {
                 __threadfence();
-                for (int i = threadIdx.x; i < G * D; i += M_THREADS) {
-                    const int g = i / D, d = i % D;
-                    float M = kNegBig;
-                    for (int sg = 0; sg < nseg; ++sg)
-                        M = fmaxf(M, __ldcg(&p.ws_ml[(((size_t)q * p.max_seg + sg) * G + g) * 2]));
-                    float L = 0.f, O = 0.f;
-                    for (int sg = 0; sg < nseg; ++sg) {
-                        const size_t slot = ((size_t)q * p.max_seg + sg) * G + g;
-                        const float c = ex2(__ldcg(&p.ws_ml[slot * 2]) - M);
-                        L += __ldcg(&p.ws_ml[slot * 2 + 1]) * c;
-                        O += __ldcg(&p.ws_o[slot * D + d]) * c;
-                    }
-                    p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
-                    if (d == 0 && p.lse != nullptr)
-                        p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-                }
+                merge_pair_partials<G, D, M_THREADS>(p.ws_o, p.ws_ml, p.max_seg, q, nseg, p.out,
+                                                    p.lse, rows0, sm_o, PL::KGROUPS * G * D);
                 if (threadIdx.x == 0) p.ws_cnt[q] = 0;
             }
         }
