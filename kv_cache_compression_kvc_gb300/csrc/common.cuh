@@ -166,20 +166,29 @@ __device__ __forceinline__ float ex2(float x)
 // ---- split-slot decode: merge of the partial softmax states of one (batch, KV head) pair -------
 // Called by all NT threads of the last block to finish pair q.  Partial state s of head g is
 // (m, l) at ws_ml[((q*max_seg + s)*G + g)*2] and o[0..D) at ws_o[((q*max_seg + s)*G + g)*D]
-// (m in log2 units, o not yet divided by l).  One warp per head reduces the (m, l) pairs with
-// shuffles and leaves the weights 2^(m_s - M) / L in `scratch`; then every output sums its
-// nseg partial values with independent loads instead of a dependent chain of L2 round trips.
-// scratch: n_scratch floats; pairs with nseg * G > n_scratch take the serial loop.
+// (m in log2 units, o not yet divided by l).  The merge reads nseg * G * (D + 2) floats that sit
+// in L2, so its cost is latency: one warp per head reduces the (m, l) pairs with shuffles and
+// leaves the weights 2^(m_s - M) / L in `scratch`; then each thread owns 16-byte chunks of the
+// output and sums them over the segments with UNR independent loads in flight.  When the
+// output has fewer chunks than threads, H thread subsets split the segments and add their
+// sums through shared memory.  scratch: n_scratch floats; a pair that needs more than that
+// takes the plain loop.
 template <int G, int D, int NT>
-__device__ __forceinline__ void merge_pair_partials(const float *ws_o, const float *ws_ml,
+__device__ __noinline__ void merge_pair_partials(const float *ws_o, const float *ws_ml,
                                                     int max_seg, int q, int nseg, float *out,
                                                     float *lse, int rows0, float *scratch,
                                                     int n_scratch)
 {
+    static_assert(D % 4 == 0, "16-byte output chunks");
     constexpr int NWARP = NT / 32;
+    constexpr int NCH = G * D / 4;                        // 16-byte chunks of the output
+    constexpr int H_RAW = NT / NCH;
+    constexpr int H = H_RAW < 1 ? 1 : (H_RAW > 8 ? 8 : H_RAW);   // segment subsets
+    constexpr int CPT = (NCH + NT - 1) / NT;              // chunks per thread (H == 1)
+    constexpr int UNR = CPT >= 8 ? 1 : 8 / CPT;           // segments per batch of loads
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const size_t base = (size_t)q * max_seg * G;   // partial state (s, g) is base + s*G + g
-    if (nseg * G > n_scratch) {
+    const size_t base = (size_t)q * max_seg * G;          // state (s, g) is base + s*G + g
+    if (nseg * G + (H - 1) * G * D > n_scratch) {
         for (int i = threadIdx.x; i < G * D; i += NT) {
             const int g = i / D, d = i % D;
             float M = kNegBig;
@@ -197,42 +206,104 @@ __device__ __forceinline__ void merge_pair_partials(const float *ws_o, const flo
         }
         return;
     }
+    float *w = scratch;                                   // [nseg][G] weights
+    float *part = scratch + nseg * G;                     // [H-1][NCH][4] subset sums
     for (int g = warp; g < G; g += NWARP) {
-        float M = kNegBig;
-        for (int s = lane; s < nseg; s += 32) M = fmaxf(M, __ldcg(&ws_ml[(base + s * G + g) * 2]));
+        const float *ml = ws_ml + (base + g) * 2;         // segment s at ml[s * 2G]
+        float m0 = kNegBig, l0 = 0.f;
+        if (lane < nseg) {
+            m0 = __ldcg(ml + (size_t)lane * 2 * G);
+            l0 = __ldcg(ml + (size_t)lane * 2 * G + 1);
+        }
+        float M = m0;
+        for (int s = lane + 32; s < nseg; s += 32) M = fmaxf(M, __ldcg(ml + (size_t)s * 2 * G));
         M = warp_max(M);
         float L = 0.f;
-        for (int s = lane; s < nseg; s += 32) {
-            const size_t slot = base + s * G + g;
-            const float c = ex2(__ldcg(&ws_ml[slot * 2]) - M);
-            scratch[s * G + g] = c;
-            L += __ldcg(&ws_ml[slot * 2 + 1]) * c;
+        if (lane < nseg) {
+            const float c = ex2(m0 - M);
+            w[lane * G + g] = c;
+            L = l0 * c;
+        }
+        for (int s = lane + 32; s < nseg; s += 32) {
+            const float c = ex2(__ldcg(ml + (size_t)s * 2 * G) - M);
+            w[s * G + g] = c;
+            L += __ldcg(ml + (size_t)s * 2 * G + 1) * c;
         }
         L = warp_sum(L);
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        for (int s = lane; s < nseg; s += 32) scratch[s * G + g] *= inv;
+        for (int s = lane; s < nseg; s += 32) w[s * G + g] *= inv;
         if (lane == 0 && lse != nullptr)
             lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += NT) {
-        const int g = i / D, d = i % D;
-        const float *src = ws_o + (base + g) * D + d;
-        const float *w = scratch + g;
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-        int s = 0;
-        for (; s + 4 <= nseg; s += 4) {
-            const float v0 = __ldcg(src + (size_t)(s + 0) * G * D);
-            const float v1 = __ldcg(src + (size_t)(s + 1) * G * D);
-            const float v2 = __ldcg(src + (size_t)(s + 2) * G * D);
-            const float v3 = __ldcg(src + (size_t)(s + 3) * G * D);
-            acc0 = fmaf(w[(s + 0) * G], v0, acc0);
-            acc1 = fmaf(w[(s + 1) * G], v1, acc1);
-            acc2 = fmaf(w[(s + 2) * G], v2, acc2);
-            acc3 = fmaf(w[(s + 3) * G], v3, acc3);
+    const int h = H > 1 ? (int)threadIdx.x / NCH : 0;     // segment subset of this thread
+    float4 acc[CPT];
+    int chunk[CPT];
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        chunk[k] = H > 1 ? (int)threadIdx.x % NCH : (int)threadIdx.x + k * NT;
+    }
+    const bool active = h < H;
+    const size_t seg_stride = (size_t)G * D / 4;          // float4 units between segments
+    const float4 *src = reinterpret_cast<const float4 *>(ws_o) + base * (D / 4);
+    if (active) {
+        for (int s0 = h; s0 < nseg; s0 += H * UNR) {
+            float4 v[CPT][UNR];
+#pragma unroll
+            for (int k = 0; k < CPT; ++k)
+#pragma unroll
+                for (int u = 0; u < UNR; ++u) {
+                    const int s = s0 + u * H;
+                    v[k][u] = (chunk[k] < NCH && s < nseg)
+                                  ? __ldcg(src + (size_t)s * seg_stride + chunk[k])
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int g = chunk[k] * 4 / D;
+#pragma unroll
+                for (int u = 0; u < UNR; ++u) {
+                    const int s = s0 + u * H;
+                    const float c = s < nseg ? w[s * G + g] : 0.f;
+                    acc[k].x = fmaf(c, v[k][u].x, acc[k].x);
+                    acc[k].y = fmaf(c, v[k][u].y, acc[k].y);
+                    acc[k].z = fmaf(c, v[k][u].z, acc[k].z);
+                    acc[k].w = fmaf(c, v[k][u].w, acc[k].w);
+                }
+            }
         }
-        for (; s < nseg; ++s) acc0 = fmaf(w[s * G], __ldcg(src + (size_t)s * G * D), acc0);
-        out[(size_t)(rows0 + g) * D + d] = (acc0 + acc1) + (acc2 + acc3);
+    }
+    if (H > 1) {
+        if (active && h > 0) {
+            float *dst = part + ((size_t)(h - 1) * NCH + chunk[0]) * 4;
+            dst[0] = acc[0].x;
+            dst[1] = acc[0].y;
+            dst[2] = acc[0].z;
+            dst[3] = acc[0].w;
+        }
+        __syncthreads();
+        if (h == 0) {
+#pragma unroll
+            for (int j = 1; j < H; ++j) {
+                const float *pj = part + ((size_t)(j - 1) * NCH + chunk[0]) * 4;
+                acc[0].x += pj[0];
+                acc[0].y += pj[1];
+                acc[0].z += pj[2];
+                acc[0].w += pj[3];
+            }
+        }
+    }
+    if (h == 0) {
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            if (chunk[k] >= NCH) continue;
+            float *o = out + (size_t)rows0 * D + (size_t)chunk[k] * 4;
+            o[0] = acc[k].x;
+            o[1] = acc[k].y;
+            o[2] = acc[k].z;
+            o[3] = acc[k].w;
+        }
     }
 }
 }  // namespace kvc
