@@ -90,7 +90,11 @@ typedef struct {
  * min(t, n_sink + window).  Keys are stored before rotation; the query and every key are
  * rotated at those positions on every call (computed through their distance: the rotated dot
  * product depends only on the query position minus the key position).  Pairing: dimension i
- * with i + d_head/2, angle position * theta^(-2i/d_head).                                    */
+ * with i + d_head/2, angle position * theta^(-2i/d_head).  Row p of cos_sin holds the cosines
+ * and sines of p times the pair frequencies; since those angles are linear in p, the kernel may
+ * also compose a distance from two rows (cos(a+b) = cos a cos b - sin a sin b, and likewise for
+ * the sine), which it does for one query head per KV head when n_pos covers one tile of slots
+ * (16 KB of keys: 64 rows for bf16 with d_head 128).                                          */
 typedef struct {
     int32_t n_sink;         /* S  (4 in the pages' configuration)                            */
     int32_t window;         /* W                                                             */

@@ -281,6 +281,7 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
     if (rope != nullptr) {
         p.rope = 1; p.S = rope->n_sink; p.W = rope->window; p.t = rope->t;
         p.cos_sin = rope->cos_sin;
+        p.n_pos = rope->n_pos;
     }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = out; p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;

@@ -30,7 +30,21 @@
 // p_q against key position p_k depends only on the distance p_q - p_k, since rotations compose:
 // (R(p_q) q).(R(p_k) k) = q.R(p_k - p_q) k.  So q is never rotated; every key is combined with q
 // through the rotation by its distance, whose cos and sin come from the distance-indexed table
-// (planar rows: d_head/2 cosines then d_head/2 sines).
+// (planar rows: d_head/2 cosines then d_head/2 sines).  The attended keys are visited in rank
+// order -- the sinks, then the ring from its oldest token to the newest -- which is their
+// in-cache position r, so the distance of key r is simply qpos - r.  A tile of TK ranks maps to
+// at most three contiguous runs of physical slots (sinks; ring up to its last slot; ring from its
+// first slot), copied separately into consecutive rows of the stage.
+//
+// Factored rotation (one query head per KV head, table of at least TK rows).  Reading a table
+// row per key puts an L2 round trip in front of every logit.  Instead, each lane always holds
+// the same key offsets kk of a tile, and within the tile starting at rank r0
+//     dist = base + (TK - 1 - kk),   base = qpos - r0 - (TK - 1).
+// With pair i of the head dimension written as a complex number, the logit term is
+// Re(conj(q_i) k_i e^{-i dist th_i}) = Re([conj(q_i) e^{-i (TK-1-kk) th_i}] e^{-i base th_i} k_i).
+// The bracket is a per-lane constant formed once per pair from table row TK-1-kk; the issuing
+// thread copies row |base| into the stage with the keys, so the per-key work reads only shared
+// memory.  A negative base (the newest tile) uses row |base| with the sine negated.
 //
 // Waits on mbarriers are bounded: after kMbarSpinLimit failed polls the thread records
 // KVC_DEV_TIMEOUT and carries on (results are then garbage, but the kernel always finishes).
@@ -86,11 +100,12 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long T, int C)
 // Shared-memory plan of one instantiation (host and device agree): two blocks per SM with a
 // three-stage ring where they fit (and the group is small enough for 128 registers a thread),
 // else one block with a deeper ring.
-template <typename T, int D, int G>
+template <typename T, int D, int G, int RM = 0>
 struct DecodeSmem {
     static constexpr int TK = kDecodeTileKeyBytes / (D * (int)sizeof(T));
     static constexpr int kTileBytes = TK * D * (int)sizeof(T);
-    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRotBytes = RM == 2 ? D * 4 : 0;   // staged base row (factored RoPE)
+    static constexpr int kStageBytes = 2 * kTileBytes + kRotBytes;
     static constexpr int kMergeBytes = kDecodeWarps * G * (D + 2) * 4 + 16;
     static constexpr int kBarBytes = 256;
     static constexpr int kTwoBlockBytes = kBarBytes + 3 * kStageBytes + kMergeBytes;
@@ -101,11 +116,14 @@ struct DecodeSmem {
     static constexpr int kBytes = kBarBytes + NS * kStageBytes + kMergeBytes;
 };
 
-template <typename T, int D, int G, int VW, int UNR, bool ROPE, int CPS>
+// RM: 0 no RoPE, 1 RoPE with one table row per key, 2 factored RoPE (G == 1, n_pos >= TK).
+template <typename T, int D, int G, int VW, int UNR, int RM, int CPS>
 __global__ void __launch_bounds__(kDecodeThreads, CPS)
 decode_attn_kernel(const DecodeParams p)
 {
-    using SM = DecodeSmem<T, D, G>;
+    using SM = DecodeSmem<T, D, G, RM>;
+    constexpr bool ROPE = RM != 0;
+    constexpr bool FACT = RM == 2;
     constexpr int TK = SM::TK;
     constexpr int NS = SM::NS;
     constexpr int NW = kDecodeWarps;
@@ -119,6 +137,7 @@ decode_attn_kernel(const DecodeParams p)
     static_assert(TK % KEYS_PER_STEP == 0, "tile must be a whole number of steps");
     constexpr int STEPS = TK / KEYS_PER_STEP;
     constexpr int EB = (int)sizeof(T);
+    static_assert(!FACT || (G == 1 && STEPS == 1), "factored RoPE: fixed key offsets per lane");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
@@ -149,37 +168,36 @@ decode_attn_kernel(const DecodeParams p)
     __syncthreads();
 
     // ---- decode position (StreamingLLM layout) --------------------------------------------
-    int64_t tpos = 0;
-    int qpos = 0, ring_base = 0;
+    // With RoPE the tiles run over ranks: rank r < S is sink slot r; rank r >= S is ring token
+    // a_old + (r - S), at slot S + (ring_off + r - S) mod (W + 1), a_old = max(S, t - W) being the
+    // oldest ring token still attended.  n_att = min(t + 1, S + W + 1) ranks are attended.
+    int qpos = 0, n_att = 0, ring_off = 0;
     if (ROPE) {
-        tpos = *p.t;
+        int64_t tpos = *p.t;
         if (tpos < 0) {
             if (threadIdx.x == 0) record_code(p.dev_code, 4 /* KVC_DEV_BAD_POSITION */);
             tpos = 0;
         }
         const int64_t sw = (int64_t)p.S + p.W;
         qpos = (int)(tpos < sw ? tpos : sw);
-        if (tpos >= p.S) ring_base = (int)((tpos - p.S) % (int64_t)(p.W + 1));
+        n_att = qpos + 1;
+        const int64_t a_old = tpos - p.W > (int64_t)p.S ? tpos - p.W : (int64_t)p.S;
+        ring_off = (int)((a_old - p.S) % (int64_t)(p.W + 1));
     }
-    // slots of pair q that may hold valid keys
+    auto rank_slot = [&](int r) -> int {
+        if (r < p.S) return r;
+        int x = ring_off + (r - p.S);
+        if (x > p.W) x -= p.W + 1;
+        return p.S + x;
+    };
+    // number of work items (slots without RoPE, ranks with it) of pair q
     auto pair_slots = [&](int q) -> int {
-        if (ROPE) return min(p.S + p.W + 1, p.cap);
+        if (ROPE) return n_att;
         if (p.len != nullptr) {
             const int n = p.len[q];
             return n < 0 ? 0 : (n > p.cap ? p.cap : n);
         }
         return p.n_valid;
-    };
-    // in-cache distance qpos - pos of physical slot j, and whether the slot is attended
-    auto slot_dist = [&](int j, bool &ok) -> int {
-        if (j < p.S) {
-            ok = ok && (j <= tpos);
-            return qpos - j;
-        }
-        int dd = ring_base - (j - p.S);
-        if (dd < 0) dd += p.W + 1;
-        ok = ok && (tpos >= p.S) && ((int64_t)dd <= tpos - p.S);
-        return dd;
     };
 
     // ---- tile loader: thread 0 issues the bulk copies of tile i into stage i % NS ----------
@@ -208,14 +226,37 @@ decode_attn_kernel(const DecodeParams p)
             mbar_arrive(full);
             return;
         }
-        mbar_arrive_expect_tx(full, (uint32_t)(2 * rows * D * EB));
-        if (dense) {
-            bulk_g2s(kdst, kb + (size_t)j0 * D, rows * D * EB, full);
-            bulk_g2s(vdst, vb + (size_t)j0 * D, rows * D * EB, full);
+        mbar_arrive_expect_tx(full, (uint32_t)(2 * rows * D * EB + SM::kRotBytes));
+        if constexpr (FACT) {
+            // |base| <= max(TK - 1, qpos) < n_pos (checked on the host)
+            const int row = min(abs(qpos - j0 - (TK - 1)), p.n_pos - 1);
+            bulk_g2s(vdst + SM::kTileBytes, p.cos_sin + (size_t)row * D, D * 4, full);
+        }
+        // copy rows [r_a, r_b) of the tile's work items, physically contiguous from slot j_a
+        auto copy_run = [&](int r_a, int r_b, int j_a) {
+            if (r_b <= r_a) return;
+            const uint32_t off = (uint32_t)((r_a - j0) * D * EB);
+            if (dense) {
+                bulk_g2s(kdst + off, kb + (size_t)j_a * D, (r_b - r_a) * D * EB, full);
+                bulk_g2s(vdst + off, vb + (size_t)j_a * D, (r_b - r_a) * D * EB, full);
+            } else {
+                for (int r = 0; r < r_b - r_a; ++r) {
+                    bulk_g2s(kdst + off + r * D * EB, kb + (size_t)(j_a + r) * p.ss, D * EB, full);
+                    bulk_g2s(vdst + off + r * D * EB, vb + (size_t)(j_a + r) * p.ss, D * EB, full);
+                }
+            }
+        };
+        const int j1 = j0 + rows;
+        if (!ROPE) {
+            copy_run(j0, j1, j0);
         } else {
-            for (int r = 0; r < rows; ++r) {
-                bulk_g2s(kdst + r * D * EB, kb + (size_t)(j0 + r) * p.ss, D * EB, full);
-                bulk_g2s(vdst + r * D * EB, vb + (size_t)(j0 + r) * p.ss, D * EB, full);
+            copy_run(j0, min(j1, p.S), j0);                          // sinks
+            const int ra = max(j0, p.S);
+            if (ra < j1) {
+                const int sa = rank_slot(ra);                        // ring, up to its last slot
+                const int rb = min(j1, ra + (p.S + p.W + 1 - sa));
+                copy_run(ra, rb, sa);
+                copy_run(rb, j1, p.S);                               // ring, from its first slot
             }
         }
     };
@@ -228,6 +269,7 @@ decode_attn_kernel(const DecodeParams p)
     const int d0 = lk * VW;
 
     float2 q1[G][P2], q2[G][P2], q2n[G][P2];   // q halves (pre-scaled); q2n = -q2 (RoPE form)
+    float2 pr[UNR][P2], pi[UNR][P2];            // factored RoPE: conj(q) e^{-i (TK-1-kk) th}
     float2 o1[G][P2], o2[G][P2];
     float m[G], l[G];
     int cur = -1;              // pair in progress
@@ -253,6 +295,29 @@ decode_attn_kernel(const DecodeParams p)
             }
             m[g] = kNegBig;
             l[g] = 0.f;
+        }
+        if constexpr (FACT) {
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int rk = TK - 1 - (warp * KPW * UNR + ks + u * KPW);
+                const float *row = p.cos_sin + (size_t)rk * D;
+#pragma unroll
+                for (int i2 = 0; i2 < P2; i2 += 2) {
+                    const float4 c4 = __ldg(reinterpret_cast<const float4 *>(row + d0 + 2 * i2));
+                    const float4 s4 =
+                        __ldg(reinterpret_cast<const float4 *>(row + HALF + d0 + 2 * i2));
+                    const float2 cc[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
+                    const float2 ss[2] = {make_float2(s4.x, s4.y), make_float2(s4.z, s4.w)};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // (q1 - i q2)(c - i s) = (q1 c - q2 s) - i (q1 s + q2 c)
+                        const float2 a = q1[0][i2 + h], b = q2[0][i2 + h];
+                        pr[u][i2 + h] = __ffma2_rn(q2n[0][i2 + h], ss[h], __fmul2_rn(a, cc[h]));
+                        const float2 t = __ffma2_rn(a, ss[h], __fmul2_rn(b, cc[h]));
+                        pi[u][i2 + h] = make_float2(-t.x, -t.y);
+                    }
+                }
+            }
         }
     };
 
@@ -360,6 +425,24 @@ decode_attn_kernel(const DecodeParams p)
         float *lg_out =
             p.logits ? p.logits + (size_t)((q / p.Hkv) * p.Hq + (q % p.Hkv) * G) * p.logits_stride
                      : nullptr;
+        // factored RoPE: the tile's base row e^{-i base th} (cosines, sines signed by base)
+        float2 cb[P2], ncb[P2], sb[P2];
+        if constexpr (FACT) {
+            const float *row =
+                reinterpret_cast<const float *>(smem + (vst - sbase) + SM::kTileBytes);
+            const float sg = (qpos - j0 - (TK - 1)) < 0 ? -1.f : 1.f;
+#pragma unroll
+            for (int x = 0; x < VW; x += 4) {
+                const float4 c4 = *reinterpret_cast<const float4 *>(row + d0 + x);
+                const float4 s4 = *reinterpret_cast<const float4 *>(row + HALF + d0 + x);
+                cb[x / 2] = make_float2(c4.x, c4.y);
+                cb[x / 2 + 1] = make_float2(c4.z, c4.w);
+                sb[x / 2] = make_float2(sg * s4.x, sg * s4.y);
+                sb[x / 2 + 1] = make_float2(sg * s4.z, sg * s4.w);
+            }
+#pragma unroll
+            for (int i2 = 0; i2 < P2; ++i2) ncb[i2] = make_float2(-cb[i2].x, -cb[i2].y);
+        }
 #pragma unroll 1
         for (int st = 0; st < STEPS; ++st) {
             const int kbase = st * KEYS_PER_STEP + warp * KPW * UNR + ks;
@@ -369,17 +452,27 @@ decode_attn_kernel(const DecodeParams p)
             for (int u = 0; u < UNR; ++u) {
                 const int kk = kbase + u * KPW;
                 const int j = j0 + kk;
-                bool ok = j < cur_slots;
-                int dist = 0;
-                if (ROPE) dist = slot_dist(j, ok);
+                const bool ok = j < cur_slots;
                 valid[u] = ok;
                 float2 k1[P2], k2[P2];
                 const uint32_t row = kst + (uint32_t)(kk * D * EB);
                 lds_pairs<T, VW>(row + d0 * EB, k1);
                 lds_pairs<T, VW>(row + (HALF + d0) * EB, k2);
-                if constexpr (ROPE) {
-                    // rotate q by the key's distance and dot with the stored key
-                    const float *cs = p.cos_sin + (size_t)(ok ? dist : 0) * D;
+                if constexpr (FACT) {
+                    // q' = (pr + i pi) e^{-i base th};  logit = Re(q' (k1 + i k2))
+                    //    = k1 (pr c + pi s) + k2 (pr s - pi c)
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int i2 = 0; i2 < P2; ++i2) {
+                        const float2 re = __ffma2_rn(pi[u][i2], sb[i2], __fmul2_rn(pr[u][i2], cb[i2]));
+                        const float2 w2 = __ffma2_rn(pr[u][i2], sb[i2], __fmul2_rn(pi[u][i2], ncb[i2]));
+                        acc = __ffma2_rn(k1[i2], re, acc);
+                        acc = __ffma2_rn(k2[i2], w2, acc);
+                    }
+                    lg[u][0] = acc.x + acc.y;
+                } else if constexpr (ROPE) {
+                    // rotate q by the key's distance (rank j: qpos - j) and dot with the key
+                    const float *cs = p.cos_sin + (size_t)(ok ? qpos - j : 0) * D;
                     float2 cd[P2], sd[P2];
 #pragma unroll
                     for (int i2 = 0; i2 < P2; i2 += 2) {
@@ -432,7 +525,7 @@ decode_attn_kernel(const DecodeParams p)
 #pragma unroll
                     for (int g = 0; g < G; ++g) lg[u][g] = -INFINITY;
                 } else if (lg_out != nullptr && lk == 0) {
-                    const int j = j0 + kbase + u * KPW;
+                    const int j = ROPE ? rank_slot(j0 + kbase + u * KPW) : j0 + kbase + u * KPW;
 #pragma unroll
                     for (int g = 0; g < G; ++g)
                         lg_out[(size_t)g * p.logits_stride + j] = lg[u][g] * kLn2;
@@ -499,12 +592,12 @@ constexpr int decode_vw()
 }
 constexpr int kDecodeUnroll = 2;
 
-template <typename T, int D, int G, bool ROPE>
-cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
+template <typename T, int D, int G, int RM>
+cudaError_t launch_decode_rm(const DecodeParams &p, cudaStream_t stream)
 {
     constexpr int VW = decode_vw<T, G>();
-    using SM = DecodeSmem<T, D, G>;
-    auto kern = decode_attn_kernel<T, D, G, VW, kDecodeUnroll, ROPE, SM::CPS>;
+    using SM = DecodeSmem<T, D, G, RM>;
+    auto kern = decode_attn_kernel<T, D, G, VW, kDecodeUnroll, RM, SM::CPS>;
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -522,6 +615,21 @@ cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
     const int C = (int)(T_all < max_ctas ? T_all : max_ctas);
     kern<<<C, kDecodeThreads, SM::kBytes, stream>>>(q);
     return cudaGetLastError();
+}
+
+// RoPE with one query head per KV head takes the factored rotation when the table covers the
+// per-lane offsets 0 .. TK-1; otherwise each key reads its table row.
+template <typename T, int D, int G, bool ROPE>
+cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
+{
+    if constexpr (!ROPE) {
+        return launch_decode_rm<T, D, G, 0>(p, stream);
+    } else if constexpr (G == 1) {
+        if (p.n_pos >= DecodeSmem<T, D, G, 2>::TK) return launch_decode_rm<T, D, G, 2>(p, stream);
+        return launch_decode_rm<T, D, G, 1>(p, stream);
+    } else {
+        return launch_decode_rm<T, D, G, 1>(p, stream);
+    }
 }
 
 template <typename T, bool ROPE>

@@ -21,7 +21,8 @@ struct DecodeParams {
     // RoPE / StreamingLLM layout (rope != 0)
     int32_t rope, S, W;
     const int64_t *t;
-    const float *cos_sin;        // [n_pos][D/2][2]
+    const float *cos_sin;        // [n_pos][2][D/2]: cosines then sines per distance
+    int32_t n_pos;               // rows of cos_sin
     float scale_log2;            // scale * log2(e)
     float *out;                  // [B][Hq][D]
     float *logits;               // nullable, [B*Hq][logits_stride]

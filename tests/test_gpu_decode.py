@@ -119,23 +119,34 @@ def test_append_tail_and_free_slot_layout():
         assert int(pos[b, h, s]) == 77
 
 
-@pytest.mark.parametrize("dtype,D,G,S,W", [(torch.float32, 64, 1, 4, 20),
-                                           (torch.bfloat16, 128, 2, 4, 37),
-                                           (torch.bfloat16, 64, 1, 0, 9),
-                                           (torch.float32, 256, 4, 2, 130)])
-def test_streaming_ring_rope_matches_oracle_every_step(dtype, D, G, S, W):
+# (dtype, D, G, S, W, extra table rows, wraps of the ring).  With one query head per KV head and
+# a table of at least one tile of rows, the kernel factors the rotation into a per-lane constant
+# and per-tile base rows; the cases with extra rows exercise that form: rings spanning several
+# tiles (wrap point inside a tile), sinks spanning two tiles, no sinks, a partial last tile.
+@pytest.mark.parametrize("dtype,D,G,S,W,extra,wraps", [
+    (torch.float32, 64, 1, 4, 20, 0, 3),
+    (torch.bfloat16, 128, 2, 4, 37, 0, 3),
+    (torch.bfloat16, 64, 1, 0, 9, 0, 3),
+    (torch.float32, 256, 4, 2, 130, 0, 3),
+    (torch.bfloat16, 128, 1, 4, 150, 64, 2),
+    (torch.bfloat16, 64, 1, 0, 200, 0, 2),
+    (torch.float32, 64, 1, 70, 20, 0, 2),
+    (torch.bfloat16, 256, 1, 3, 40, 30, 3),
+    (torch.float32, 128, 1, 1, 45, 5, 3),
+])
+def test_streaming_ring_rope_matches_oracle_every_step(dtype, D, G, S, W, extra, wraps):
     """Token by token from an empty cache: ring append then decode with RoPE at in-cache
     positions; every step against the oracle's StreamingLLM decode from the full history."""
     dev = cuda_or_skip()
     kvc = lib()
     B, Hkv = 2, 2
     Hq = Hkv * G
-    T = S + 3 * (W + 1) + 5
+    T = S + wraps * (W + 1) + 5
     cap = S + W + 1 + 3                        # extra slots past the ring are never used
     K = torch.zeros((B, Hkv, cap, D), device=dev, dtype=dtype)
     V = torch.zeros_like(K)
     qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, T, 50 + D + W, dev, dtype)
-    table = kvc.kvc_rope_table(S + W + 1, D, 10000.0).to(dev)
+    table = kvc.kvc_rope_table(S + W + 1 + extra, D, 10000.0).to(dev)
     t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
     rope = kvc.make_rope(S, W, t_dev, table)
     scale = 1 / math.sqrt(D)
@@ -156,10 +167,12 @@ def test_streaming_ring_rope_matches_oracle_every_step(dtype, D, G, S, W):
         assert torch.equal(K[:, :, a], ks[a]), "sink slot overwritten"
 
 
-def test_streaming_worked_example_positions():
+@pytest.mark.parametrize("table_rows", [8, 200])
+def test_streaming_worked_example_positions(table_rows):
     """The pages' example: cache [0,1,2,3,6,7,8] decoding the next token uses positions 0..7.
     With values one-hot per token, the output mixes exactly the tokens 0,1,2,3,6,7,8,9, and the
-    logits (rotated at cache positions) equal the oracle's."""
+    logits (rotated at cache positions) equal the oracle's.  With 200 table rows the kernel
+    takes the factored rotation (table rows >= one tile of slots)."""
     dev = cuda_or_skip()
     kvc = lib()
     S, W, D = 4, 3, 64
@@ -170,7 +183,7 @@ def test_streaming_worked_example_positions():
     for a in range(10):
         vs[a, 0, 0, a] = 1.0
     q = I.randn((1, 1, D), 62, dev)
-    table = kvc.kvc_rope_table(S + W + 1, D).to(dev)
+    table = kvc.kvc_rope_table(table_rows, D).to(dev)
     t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
     for t in range(10):
         t_dev.fill_(t)
@@ -183,3 +196,10 @@ def test_streaming_worked_example_positions():
     assert list(cpos) == list(range(8)) and qpos == 7
     ref = oracle.stream_decode(9, S, W, f64(q[0, 0]), f64(ks[:, 0, 0]), f64(vs[:, 0, 0]), 0.125)
     assert_close(out, ref, 1e-5, "worked example")
+    # logit of each cached token: scale * R(qpos) q . R(cache position) k, at the token's slot
+    lg = logits[0, 0].cpu().numpy()
+    qr = oracle.rope(f64(q[0, 0]), qpos)
+    for a, pos in zip(tok, cpos):
+        want = 0.125 * float(np.dot(qr, oracle.rope(f64(ks[a, 0, 0]), int(pos))))
+        got = float(lg[oracle.stream_slot(int(a), S, W)])
+        assert abs(got - want) <= 1e-5 * max(1.0, abs(want)), f"logit of token {a}"
