@@ -505,6 +505,11 @@ kvc_status kvc_snapkv_select(const void *q_obs, const kvc_cache *prompt, int32_t
         if (e != cudaSuccess) return cuda_fail(e, "iota launch");
         return ok();
     }
+    bool fused = false;
+    e = kvc::launch_pool_topk(s_cols, n, B * Hkv, G, n, budget - L_obs, L_obs, pool_k, idx_out,
+                              budget, s, &fused);
+    if (e != cudaSuccess) return cuda_fail(e, "pool + top-k launch");
+    if (fused) return ok();
     e = kvc::launch_pool_groupmax(s_cols, n, pooled, B * Hkv, G, n, pool_k, s);
     if (e != cudaSuccess) return cuda_fail(e, "pool launch");
     e = kvc::launch_topk_rows(pooled, n, B * Hkv, n, budget - L_obs, L_obs, idx_out, budget, s);

@@ -132,6 +132,11 @@ cudaError_t launch_pool_groupmax(const float *s, int64_t s_row_stride, float *sc
 
 // Exact top-k per row (ties: lower index), ascending emission, then `tail` indices
 // n .. n+tail-1 appended.  idx row stride = k + tail.
+// SnapKV steps 3-4 fused (pool + group max + top-k) with one thread-block cluster per row; sets
+// *used = false, launching nothing, when the row is too long for the cluster's shared memory.
+cudaError_t launch_pool_topk(const float *s, int64_t s_row_stride, int rows, int G, int n, int k,
+                             int tail, int pool_k, int32_t *idx, int64_t idx_stride,
+                             cudaStream_t stream, bool *used);
 cudaError_t launch_topk_rows(const float *score, int64_t score_stride, int rows, int n, int k,
                              int tail, int32_t *idx, int64_t idx_stride, cudaStream_t stream);
 cudaError_t launch_iota_rows(int32_t *idx, int64_t idx_stride, int rows, int n,

@@ -19,11 +19,14 @@
 //     window, one head of many row blocks) a block keeps one key tile and streams the row
 //     blocks that can see it.
 //
-// Block roles (192 threads): warp 0 issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle,
+// Block roles (320 threads): warp 0 issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle,
 // K-major tiles of 128 rows x 64 elements), warp 1 owns the tensor-memory allocation and one
 // of its threads issues the MMAs (M = N = 128, K = 16 per instruction) and the commits, warps
-// 2-5 are the epilogue (tcgen05.ld of their 32 TMEM lanes).  Operand stages and the two
-// accumulator buffers are handed over with mbarriers; every wait is bounded.
+// 2-9 are the epilogue in two sets of four (each warp reads its 32 TMEM lanes with tcgen05.ld).
+// The epilogue (exp2 and sums of 16K logits per tile) is the long stage, so the two sets take
+// alternate tiles: with four accumulators in tensor memory the MMAs run up to four tiles ahead
+// and two epilogue warps share each scheduler.  Operand stages and accumulators are handed over
+// with mbarriers; every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,9 +40,10 @@ namespace kvc {
 namespace {
 
 constexpr int TC_ROWS = 128;         // MMA M and N
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 320;      // TMA warp, MMA warp, two epilogue sets of four warps
 constexpr int TC_SUB_BYTES = TC_ROWS * 128;   // one 128-row x 64-element bf16 sub-tile
-constexpr uint32_t TC_TMEM_COLS = 256;        // two fp32 accumulators of 128 columns
+constexpr int TC_NACC = 4;                    // fp32 accumulators of 128 columns
+constexpr uint32_t TC_TMEM_COLS = 128 * TC_NACC;
 
 // ---- tcgen05 / TMA helpers ---------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -134,6 +138,25 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[4][32])
     }
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 64 columns (two 32-column loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[2][32])
+{
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        uint32_t *r = reinterpret_cast<uint32_t *>(v[c]);
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+            "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+              "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+              "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+              "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+              "=r"(r[31])
+            : "r"(taddr + c * 32));
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 // Sum of 32 values with four independent chains (short dependency chains for one warp per
 // scheduler).
 __device__ __forceinline__ float sum32(const float *x)
@@ -161,9 +184,10 @@ __device__ __forceinline__ float max32(const float *x)
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
 
-__device__ __forceinline__ void epilogue_sync()
+// Named barrier over the epilogue warps that take part (128 threads per set).
+__device__ __forceinline__ void epilogue_sync(int nsets)
 {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(128 * nsets) : "memory");
 }
 
 struct TcParams {
@@ -207,10 +231,14 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const uint32_t bar_fixed = bars;
     const uint32_t bar_full = bars + 8;                   // NS
     const uint32_t bar_empty = bar_full + 8 * NS;         // NS
-    const uint32_t bar_acc_full = bar_empty + 8 * NS;     // 2
-    const uint32_t bar_acc_empty = bar_acc_full + 16;     // 2
-    const uint32_t tmem_slot = bar_acc_empty + 16;        // u32 written by tcgen05.alloc
+    const uint32_t bar_acc_full = bar_empty + 8 * NS;     // TC_NACC
+    const uint32_t bar_acc_empty = bar_acc_full + 8 * TC_NACC;   // TC_NACC
+    const uint32_t tmem_slot = bar_acc_empty + 8 * TC_NACC;      // u32 written by tcgen05.alloc
     float *sm_lse = reinterpret_cast<float *>(smem_raw + (tmem_slot + 16 - raw));   // [2][128]
+    float *sm_mz = sm_lse + 2 * TC_ROWS;                  // [128][2] second set's row states
+    // epilogue sets: column sums with a resident key tile carry sums across row blocks, so
+    // one set takes every item there
+    constexpr int NSETS = MODE == 1 ? 1 : 2;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -261,9 +289,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < TC_NACC; ++a) {
             mbar_init(bar_acc_full + 8 * a, 1);
-            mbar_init(bar_acc_empty + 8 * a, 4);
+            mbar_init(bar_acc_empty + 8 * a, 4);   // the four warps of the set owning it
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -310,9 +338,10 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             // ============================== MMA issuer ============================================
             mbar_wait(bar_fixed, 0, tp.dev_code);
             for (int i = 0; i < n_items; ++i) {
-                const int s = i % NS, ab = i & 1;
+                const int s = i % NS, ab = i % TC_NACC;
                 mbar_wait(bar_full + 8 * s, (i / NS) & 1, tp.dev_code);
-                if (i >= 2) mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) - 1) & 1, tp.dev_code);
+                if (i >= TC_NACC)
+                    mbar_wait(bar_acc_empty + 8 * ab, ((i / TC_NACC) - 1) & 1, tp.dev_code);
                 tc_fence_after();
                 // MODE 0/1: A = resident tile, B = streamed tile; MODE 2: A = streamed keys,
                 // B = resident rows (the accumulator then has one key per lane)
@@ -327,8 +356,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 umma_commit(bar_empty + 8 * s);       // operand stage free once the MMAs finish
                 umma_commit(bar_acc_full + 8 * ab);   // accumulator ready for the epilogue
             }
-        } else if (warp >= 2) {
+        } else if (warp >= 2 && (warp - 2) / 4 < NSETS) {
             // ============================== epilogue ==============================================
+            const int set = (warp - 2) / 4;           // items set, set + NSETS, ...
             const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
             const int et = q4 * 32 + lane;            // this thread's lane (row or key)
             const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -337,9 +367,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 const bool row_ok = r < R;
                 const int pos = row_ok ? row_pos(p, r) : -1;
                 float m_run = kNegBig, z_run = 0.f;
-                for (int i = 0; i < n_items; ++i) {
-                    const int ab = i & 1;
-                    mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, tp.dev_code);
+                for (int i = set; i < n_items; i += NSETS) {
+                    const int ab = i % TC_NACC;
+                    mbar_wait(bar_acc_full + 8 * ab, (i / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
                     const int k0 = (t_begin + i) * TC_ROWS;
                     const bool need_mask = k0 + TC_ROWS - 1 > first_pos || k0 + TC_ROWS > p.N;
@@ -368,35 +398,44 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
                 }
-                if (row_ok) {
+                // the second set hands its row states to the first, which merges and writes
+                if (set == 1) {
+                    sm_mz[2 * et] = m_run;
+                    sm_mz[2 * et + 1] = z_run;
+                }
+                epilogue_sync(NSETS);
+                if (set == 0 && row_ok) {
+                    const float m1 = sm_mz[2 * et], z1 = sm_mz[2 * et + 1];
+                    const float M = fmaxf(m_run, m1);
                     float *dst = p.row_ml + (((size_t)pair * p.n_chunks + chunk) * R + r) * 2;
-                    dst[0] = m_run;
-                    dst[1] = z_run;
+                    dst[0] = M;
+                    dst[1] = z_run * ex2(m_run - M) + z1 * ex2(m1 - M);
                 }
             } else if (MODE == 2) {
                 // resident rows fixed_row0 .. +127 hold whole heads: per key tile, each thread
                 // sums its key's column over each head and writes it
                 const float *lse_g = p.row_lse2 + (size_t)pair * R;
                 float *lse_buf = sm_lse;
-                lse_buf[et] = (fixed_row0 + et < R) ? lse_g[fixed_row0 + et] : 0.f;
-                epilogue_sync();
+                if (set == 0) lse_buf[et] = (fixed_row0 + et < R) ? lse_g[fixed_row0 + et] : 0.f;
+                epilogue_sync(NSETS);
                 float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
                 const int rows_blk = min(TC_ROWS, R - fixed_row0);
-                for (int i = 0; i < n_items; ++i) {
-                    const int ab = i & 1;
+                for (int i = set; i < n_items; i += NSETS) {
+                    const int ab = i % TC_NACC;
                     const int key = (t_begin + i) * TC_ROWS + et;
                     const bool mask_tile = (t_begin + i) * TC_ROWS + TC_ROWS - 1 > first_pos;
-                    mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, tp.dev_code);
+                    mbar_wait(bar_acc_full + 8 * ab, (i / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
                     int g_cur = fixed_row0 / p.L_obs;
                     float acc_g = 0.f;
-                    float vt[4][32];
-                    tmem_ld128(tmem_base + ab * 128 + lane_off, vt);
+                    float vt[2][32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int rc = fixed_row0 + c * 32;
                         if (c * 32 >= rows_blk) break;
-                        float *v = vt[c];
+                        // 64 columns per tensor-memory read keep the registers for two sets
+                        if ((c & 1) == 0) tmem_ld64(tmem_base + ab * 128 + lane_off + c * 32, vt);
+                        float *v = vt[c & 1];
                         const int g_a = rc / p.L_obs;
                         const int rows_here = min(32, rows_blk - c * 32);
                         const int split = min(rows_here, (g_a + 1) * p.L_obs - rc);
@@ -445,13 +484,13 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 int g_cur = t_begin * TC_ROWS / p.L_obs;   // head of the first row handled
                 float acc_g = 0.f;
                 for (int i = 0; i < n_items; ++i) {
-                    const int ab = i & 1;
+                    const int ab = i % TC_NACC;
                     const int r0 = (t_begin + i) * TC_ROWS;   // first row of this block
                     // stage the block's row log2-sum-exp values (double buffered)
                     float *lse_buf = sm_lse + (i & 1) * TC_ROWS;
                     lse_buf[et] = (r0 + et < R) ? lse_g[r0 + et] : 0.f;
-                    epilogue_sync();
-                    mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, tp.dev_code);
+                    epilogue_sync(NSETS);
+                    mbar_wait(bar_acc_full + 8 * ab, (i / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -504,7 +543,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
             }
         }
-    } else if (MODE == 0 && warp >= 2) {
+    } else if (MODE == 0 && warp >= 2 && warp < 6) {
         // no key tile reaches this block's rows: an empty state for every row
         const int r = fixed_row0 + (warp & 3) * 32 + lane;
         if (r < R) {
@@ -530,7 +569,8 @@ constexpr int tc_smem_bytes()
     constexpr int NS = (200 * 1024 - TILE_BYTES) / TILE_BYTES > 4
                            ? 4
                            : (200 * 1024 - TILE_BYTES) / TILE_BYTES;
-    return 1024 + (1 + NS) * TILE_BYTES + 8 * (1 + 2 * NS + 4) + 16 + 2 * TC_ROWS * 4 + 64;
+    return 1024 + (1 + NS) * TILE_BYTES + 8 * (1 + 2 * NS + 2 * TC_NACC) + 16 +
+           4 * TC_ROWS * 4 + 64;
 }
 
 // ---- host: tensor maps through the driver entry point ------------------------------------------

@@ -175,6 +175,312 @@ topk_rows_kernel(const float *score, int64_t score_stride, int n, int k, int tai
     }
 }
 
+// ---- SnapKV: pooling, group max and top-k in one cluster per row ------------------------------
+// Steps 3-4 of SnapKV for one (batch, KV head) row: the G per-query-head column sums are
+// average-pooled (window PK, zeros outside the row, left-to-right fp32 sum then one division,
+// the same arithmetic as pool_groupmax_kernel), the max over the group is taken, and the k
+// largest are selected as above.  The division comes after the max over the group: a correctly
+// rounded division by a positive constant is monotonic, so max_g(sum_g / PK) and
+// max_g(sum_g) / PK are the same float.  Radix digits are 10 bits wide (three passes cover the
+// bits in which pooled scores of one row differ), with one histogram per four warps.  A cluster of TKC_CL blocks shares the row.  Block c copies
+// the G column-sum rows of its slice into shared memory (cp.async, one round trip per
+// sub-chunk), pools them into order-preserving keys, and keeps the keys in shared memory.  Every
+// cross-block quantity -- the key range, each radix histogram, the per-block counts -- is pushed
+// with remote reductions into the shared memory of every block of the cluster, so after each
+// cluster barrier all blocks read the same totals locally and take the same decisions; a final
+// exchange of per-block counts gives each block the output offset of its slice, so indices still
+// come out ascending.
+constexpr int TKC_THREADS = 512;
+constexpr int TKC_WARPS = TKC_THREADS / 32;
+constexpr int TKC_CL = 8;              // blocks per row (portable cluster size)
+constexpr int TKC_MAX_G = 8;           // query heads per KV head handled by the fused kernel
+constexpr int TKC_SMEM = 180 * 1024;   // dynamic shared memory budget (keys + pooling rows)
+constexpr int TKC_BITS = 10;           // radix digit width
+constexpr int TKC_BINS = 1 << TKC_BITS;
+constexpr int TKC_HGROUPS = 4;         // histogram copies (warps 4h .. 4h+3 share copy h)
+
+__device__ __forceinline__ uint32_t cl_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cl_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of this variable in the shared memory of cluster block `rank`
+__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ void cl_red_add(uint32_t a, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cl_red_min(uint32_t a, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.min.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cl_red_max(uint32_t a, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.max.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cl_st(uint32_t a, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// dynamic shared memory: seg keys, then two buffers of G rows of sub + PK - 1 pooling inputs
+template <int PK>
+__global__ void __launch_bounds__(TKC_THREADS)
+pool_topk_cluster_kernel(const float *s, int64_t s_row_stride, int G, int n, int k, int tail,
+                         int32_t *idx, int64_t idx_stride, int seg, int sub)
+{
+    __shared__ uint32_t whist[TKC_HGROUPS][TKC_BINS];
+    __shared__ uint32_t cl_hist[4][TKC_BINS];   // summed histogram of each pass (every block)
+    __shared__ uint32_t cl_lohi[2];             // key range of the row (every block)
+    __shared__ uint32_t cl_cnt[TKC_CL][2];      // (keys > T, keys == T) per block (every block)
+    __shared__ uint32_t sh_bin, sh_above, sh_lo, sh_hi;
+    __shared__ uint32_t w_gt[TKC_WARPS], w_eq[TKC_WARPS];
+    __shared__ uint32_t w_keep_before[TKC_WARPS], w_eq_before[TKC_WARPS];
+    extern __shared__ uint32_t skeys[];
+
+    constexpr int r = (PK - 1) / 2;
+    const int row = blockIdx.x / TKC_CL;
+    const uint32_t rank = cl_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t *out = idx + (size_t)row * idx_stride;
+    float *pin = reinterpret_cast<float *>(skeys + seg);   // [2][G][sub + PK - 1]
+    const int wlen = sub + PK - 1;
+
+    if (rank == 0)
+        for (int j = tid; j < tail; j += TKC_THREADS) out[k + j] = n + j;
+    const int beg = (int)rank * seg;
+    const int end = min(beg + seg, n);
+    const int cnt = max(0, end - beg);
+    if (k <= 0) return;                         // same branch in every block of the cluster
+    if (k >= n) {
+        for (int j = beg + tid; j < end; j += TKC_THREADS) out[j] = j;
+        return;
+    }
+    for (int j = tid; j < 4 * TKC_BINS; j += TKC_THREADS) (&cl_hist[0][0])[j] = 0u;
+    if (tid == 0) {
+        cl_lohi[0] = 0xffffffffu;
+        cl_lohi[1] = 0u;
+        sh_lo = 0xffffffffu;
+        sh_hi = 0u;
+    }
+    __syncthreads();
+
+    // ---- stage the pooled, group-max keys of this block's slice --------------------------------
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    const float *srow = s + (size_t)row * G * s_row_stride;
+    // inputs c0 - r .. c0 + sub + r - 1 of every head into buffer `buf` (zeros outside the row);
+    // the next sub-chunk's copies are in flight while this one is pooled
+    auto issue = [&](int c0, int buf) {
+        float *dst0 = pin + (size_t)buf * G * wlen;
+        for (int g = 0; g < G; ++g) {
+            const float *src = srow + (size_t)g * s_row_stride;
+            float *dst = dst0 + g * wlen;
+            for (int x = tid; x < wlen; x += TKC_THREADS) {
+                const int ix = c0 - r + x;
+                if (ix >= 0 && ix < n)
+                    cp_async4(smem_addr(dst + x), src + ix);
+                else
+                    dst[x] = 0.f;
+            }
+        }
+        cp_async_commit();
+    };
+    if (beg < end) issue(beg, 0);
+    for (int c0 = beg, it = 0; c0 < end; c0 += sub, ++it) {
+        if (c0 + sub < end) {
+            issue(c0 + sub, (it + 1) & 1);
+            cp_async_wait_group<1>();
+        } else {
+            cp_async_wait_group<0>();
+        }
+        __syncthreads();
+        const float *pbuf = pin + (size_t)(it & 1) * G * wlen;
+        const int c1 = min(c0 + sub, end);
+        for (int i = c0 + tid; i < c1; i += TKC_THREADS) {
+            float best = -INFINITY;
+            for (int g = 0; g < G; ++g) {
+                const float *w = pbuf + g * wlen + (i - c0);   // inputs i - r .. i + r
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < PK; ++j) acc = __fadd_rn(acc, w[j]);
+                best = fmaxf(best, acc);
+            }
+            const uint32_t key = order_key(__fdiv_rn(best, (float)PK));
+            skeys[i - beg] = key;
+            lo = min(lo, key);
+            hi = max(hi, key);
+        }
+        __syncthreads();                        // this buffer is refilled two sub-chunks on
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        atomicMin(&sh_lo, lo);
+        atomicMax(&sh_hi, hi);
+    }
+    __syncthreads();
+    cl_sync();                                  // every block's buffers are cleared
+    if (tid < TKC_CL) {
+        cl_red_min(cl_map(&cl_lohi[0], tid), sh_lo);
+        cl_red_max(cl_map(&cl_lohi[1], tid), sh_hi);
+    }
+    cl_sync();
+    lo = cl_lohi[0];
+    hi = cl_lohi[1];
+    const uint32_t diff = lo ^ hi;
+    const int top = diff ? 31 - __clz(diff) : -1;
+
+    // ---- radix select over the differing bits, histograms summed across the cluster ----------
+    const uint32_t shared_mask = top < 0 ? 0xffffffffu : (top >= 31 ? 0u : ~((2u << top) - 1u));
+    uint32_t prefix = hi & shared_mask;
+    uint32_t mask = shared_mask;
+    uint32_t need = (uint32_t)k;
+    int pass = 0;
+    for (int t = top; t >= 0; t -= TKC_BITS, ++pass) {
+        const int shift = t >= TKC_BITS - 1 ? t - (TKC_BITS - 1) : 0;
+        const uint32_t dmask = (2u << (t - shift)) - 1u;
+        for (int j = tid; j < TKC_HGROUPS * TKC_BINS; j += TKC_THREADS) (&whist[0][0])[j] = 0u;
+        __syncthreads();
+        uint32_t *mine = whist[warp / (TKC_WARPS / TKC_HGROUPS)];
+        for (int i = tid; i < cnt; i += TKC_THREADS) {
+            const uint32_t u = skeys[i];
+            if ((u & mask) == prefix) atomicAdd(&mine[(u >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        // this block's bin b goes to every block of the cluster
+        for (int bin = tid; bin < TKC_BINS; bin += TKC_THREADS) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int h = 0; h < TKC_HGROUPS; ++h) c += whist[h][bin];
+            if (c)
+#pragma unroll
+                for (int dst = 0; dst < TKC_CL; ++dst)
+                    cl_red_add(cl_map(&cl_hist[pass][bin], (uint32_t)dst), c);
+        }
+        cl_sync();
+        if (warp == 0) {
+            // lane L owns bins 32L .. 32L+31; keys in bins above lane L's range
+            constexpr int PER = TKC_BINS / 32;
+            uint32_t c[PER], tot = 0;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                c[j] = cl_hist[pass][lane * PER + j];
+                tot += c[j];
+            }
+            uint32_t incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += x;
+            }
+            uint32_t cum = incl - tot;
+#pragma unroll
+            for (int j = PER - 1; j >= 0; --j) {
+                if (cum < need && cum + c[j] >= need) {
+                    sh_bin = (uint32_t)(lane * PER + j);
+                    sh_above = cum;
+                }
+                cum += c[j];
+            }
+        }
+        __syncthreads();
+        prefix |= sh_bin << shift;
+        mask |= dmask << shift;
+        need -= sh_above;
+    }
+    const uint32_t T = prefix;
+
+    // ---- counts per warp segment, then per block across the cluster -----------------------------
+    const int wseg = ((cnt + TKC_WARPS - 1) / TKC_WARPS + 31) & ~31;
+    const int wb = warp * wseg;
+    const int we = min(wb + wseg, cnt);
+    uint32_t gt = 0, eq = 0;
+    for (int i0 = wb; i0 < we; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t u = i < we ? skeys[i] : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, i < we && u > T));
+        eq += __popc(__ballot_sync(0xffffffffu, i < we && u == T));
+    }
+    if (lane == 0) {
+        w_gt[warp] = gt;
+        w_eq[warp] = eq;
+    }
+    __syncthreads();
+    if (tid < TKC_CL) {
+        uint32_t g_all = 0, e_all = 0;
+        for (int w = 0; w < TKC_WARPS; ++w) {
+            g_all += w_gt[w];
+            e_all += w_eq[w];
+        }
+        cl_st(cl_map(&cl_cnt[rank][0], (uint32_t)tid), g_all);
+        cl_st(cl_map(&cl_cnt[rank][1], (uint32_t)tid), e_all);
+    }
+    cl_sync();                                  // last access to another block's shared memory
+    if (tid == 0) {
+        // keys kept by the blocks before this one (index order), and their keys equal to T
+        uint32_t eq_run = 0, keep_run = 0;
+        for (uint32_t c = 0; c < rank; ++c) {
+            const uint32_t g_c = cl_cnt[c][0], e_c = cl_cnt[c][1];
+            const uint32_t take = eq_run >= need ? 0u : (e_c < need - eq_run ? e_c : need - eq_run);
+            keep_run += g_c + take;
+            eq_run += e_c;
+        }
+        for (int w = 0; w < TKC_WARPS; ++w) {
+            w_eq_before[w] = eq_run;
+            w_keep_before[w] = keep_run;
+            const uint32_t take =
+                eq_run >= need ? 0u : (w_eq[w] < need - eq_run ? w_eq[w] : need - eq_run);
+            keep_run += w_gt[w] + take;
+            eq_run += w_eq[w];
+        }
+    }
+    __syncthreads();
+
+    // ---- emit in index order ---------------------------------------------------------------------
+    uint32_t eq_seen = w_eq_before[warp];
+    uint32_t written = w_keep_before[warp];
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int i0 = wb; i0 < we; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t u = i < we ? skeys[i] : 0u;
+        const bool is_eq = i < we && u == T;
+        const uint32_t eq_ballot = __ballot_sync(0xffffffffu, is_eq);
+        const uint32_t eq_rank = eq_seen + __popc(eq_ballot & lt_mask);
+        const bool keep = (i < we) && (u > T || (is_eq && eq_rank < need));
+        const uint32_t keep_ballot = __ballot_sync(0xffffffffu, keep);
+        if (keep) out[written + __popc(keep_ballot & lt_mask)] = beg + i;
+        written += __popc(keep_ballot);
+        eq_seen += __popc(eq_ballot);
+    }
+}
+
 __global__ void iota_rows_kernel(int32_t *idx, int64_t idx_stride, int rows, int n)
 {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -182,7 +488,60 @@ __global__ void iota_rows_kernel(int32_t *idx, int64_t idx_stride, int rows, int
     idx[(size_t)(i / n) * idx_stride + (size_t)(i % n)] = (int32_t)(i % n);
 }
 
+template <int PK>
+cudaError_t launch_pool_topk_typed(const float *s, int64_t s_row_stride, int rows, int G, int n,
+                                   int k, int tail, int32_t *idx, int64_t idx_stride,
+                                   cudaStream_t stream, bool *used)
+{
+    const int seg = (n + TKC_CL - 1) / TKC_CL;
+    const int sub = 2 * TKC_THREADS;            // pooled keys per sub-chunk (two per thread)
+    const size_t dyn = (size_t)seg * 4 + 2 * (size_t)G * (sub + PK - 1) * 4;
+    if (dyn > (size_t)TKC_SMEM) return cudaSuccess;   // too long: the two-kernel path runs
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(pool_topk_cluster_kernel<PK>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TKC_SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * TKC_CL));
+    cfg.blockDim = dim3(TKC_THREADS);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = TKC_CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, pool_topk_cluster_kernel<PK>, s, s_row_stride, G, n, k,
+                                       tail, idx, idx_stride, seg, sub);
+    if (e == cudaSuccess) *used = true;
+    return e;
+}
+
 }  // namespace
+
+cudaError_t launch_pool_topk(const float *s, int64_t s_row_stride, int rows, int G, int n, int k,
+                             int tail, int pool_k, int32_t *idx, int64_t idx_stride,
+                             cudaStream_t stream, bool *used)
+{
+    *used = false;
+    if (rows == 0 || n <= 0 || G < 1 || G > TKC_MAX_G) return cudaSuccess;
+    switch (pool_k) {
+#define KVC_PT_CASE(PK) \
+    case PK: return launch_pool_topk_typed<PK>(s, s_row_stride, rows, G, n, k, tail, idx, \
+                                               idx_stride, stream, used);
+    KVC_PT_CASE(1) KVC_PT_CASE(3) KVC_PT_CASE(5) KVC_PT_CASE(7)
+    KVC_PT_CASE(9) KVC_PT_CASE(11) KVC_PT_CASE(13) KVC_PT_CASE(15)
+#undef KVC_PT_CASE
+    default: return cudaSuccess;
+    }
+}
 
 cudaError_t launch_topk_rows(const float *score, int64_t score_stride, int rows, int n, int k,
                              int tail, int32_t *idx, int64_t idx_stride, cudaStream_t stream)

@@ -103,6 +103,32 @@ def test_snapkv_tiny_workload_bf16():
     _check_snapkv(q[:, :, -32:].contiguous(), k, 512, 32, 128, 5, w.scale, kvc)
 
 
+@pytest.mark.parametrize("pool_k", [1, 3, 7, 15])
+@pytest.mark.parametrize("dtype,budget", [(torch.bfloat16, 333), (torch.float32, 48)])
+def test_snapkv_select_pool_widths(pool_k, dtype, budget):
+    """Other pooling widths (zero padding at both ends), and a budget equal to the window
+    (nothing kept from the prefix)."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hq, Hkv, D, N, L_obs = 1, 8, 2, 128, 2300, 48
+    q = I.randn((B, Hq, L_obs, D), 300 + pool_k, dev, dtype)
+    K = I.randn((B, Hkv, N, D), 301 + pool_k, dev, dtype)
+    _check_snapkv(q, K, N, L_obs, budget, pool_k, 1 / math.sqrt(D), kvc)
+
+
+def test_snapkv_ties_across_the_row():
+    """All prefix keys identical and a budget that takes ties from several eighths of the row:
+    the lowest indices still win."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    D, N, L_obs = 64, 400, 16
+    K = I.randn((1, 1, N, D), 91, dev)
+    K[0, 0, :N - L_obs] = K[0, 0, 5]
+    q = I.randn((1, 2, L_obs, D), 92, dev)
+    idx = _check_snapkv(q, K, N, L_obs, 16 + 200, 5, 0.125, kvc)
+    assert list(idx[0, 0, :200]) == list(range(2, 202))
+
+
 def test_snapkv_exact_ties_keep_lowest_index():
     """Identical keys give identical scores: the lower index must win every tie."""
     dev = cuda_or_skip()
