@@ -5,8 +5,11 @@
 // from the decode kernel's logits; then, if the cache holds more than the budget, the token
 // with the smallest s among those outside the recent quota (pos <= t - L_local) is evicted --
 // equal scores evict the larger position -- and its slot becomes the next token's slot
-// (in-place compaction by slot reuse: no row moves).  One warp per row; the argmin is a warp
-// reduction over (s, pos, slot).
+// (in-place compaction by slot reuse: no row moves).  One block of H2O_THREADS per row: each
+// thread updates a strided set of slots with its loads batched (H2O_BATCH in flight), keeps its
+// own best candidate, and the block reduces (s, pos, slot) with shuffles and one shared-memory
+// step.  The order (lower s first, then larger pos) is total since positions are distinct, so
+// the result does not depend on how the reduction is split.
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,27 +23,55 @@ __device__ __forceinline__ bool evict_before(float sa, int pa, float sb, int pb)
     return sa < sb || (sa == sb && pa > pb);
 }
 
-__global__ void h2o_accumulate_evict_kernel(const H2OParams p)
+constexpr int H2O_THREADS = 128;
+constexpr int H2O_BATCH = 4;
+
+// folds candidate (os, op, oj) into (bs, bp, bj); oj < 0 is "no candidate"
+__device__ __forceinline__ void h2o_fold(float &bs, int &bp, int &bj, float os, int op, int oj)
 {
-    const int row = (int)((blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= p.rows) return;
+    if (oj >= 0 && (bj < 0 || evict_before(os, op, bs, bp))) {
+        bs = os;
+        bp = op;
+        bj = oj;
+    }
+}
+
+__global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const H2OParams p)
+{
+    __shared__ float w_s[H2O_THREADS / 32];
+    __shared__ int w_p[H2O_THREADS / 32], w_j[H2O_THREADS / 32];
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t t = *p.t;
-    const float *lg = p.logits + (size_t)row * p.logits_stride;
-    float *s = p.score + (size_t)row * p.stride;
-    const int32_t *pos = p.pos + (size_t)row * p.stride;
+    const float *__restrict__ lg = p.logits + (size_t)row * p.logits_stride;
+    float *__restrict__ s = p.score + (size_t)row * p.stride;
+    const int32_t *__restrict__ pos = p.pos + (size_t)row * p.stride;
     const float lse = p.lse[row];
     const int64_t limit = t - p.L_local;
+    const int n = p.n_slots;
 
     float best_s = INFINITY;
     int best_p = -1, best_j = -1;
-    for (int j = lane; j < p.n_slots; j += 32) {
-        const float sj = s[j] + expf(lg[j] - lse);
-        s[j] = sj;
-        const int pj = pos[j];
-        if ((int64_t)pj <= limit &&
-            (best_j < 0 || evict_before(sj, pj, best_s, best_p))) {
-            best_s = sj; best_p = pj; best_j = j;
+    for (int j0 = tid; j0 < n; j0 += H2O_THREADS * H2O_BATCH) {
+        float sv[H2O_BATCH], lv[H2O_BATCH];
+        int pv[H2O_BATCH];
+#pragma unroll
+        for (int u = 0; u < H2O_BATCH; ++u) {
+            const int j = j0 + u * H2O_THREADS;
+            if (j < n) {
+                sv[u] = s[j];
+                lv[u] = __ldg(lg + j);
+                pv[u] = __ldg(pos + j);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < H2O_BATCH; ++u) {
+            const int j = j0 + u * H2O_THREADS;
+            if (j < n) {
+                const float sj = sv[u] + expf(lv[u] - lse);
+                s[j] = sj;
+                if ((int64_t)pv[u] <= limit) h2o_fold(best_s, best_p, best_j, sj, pv[u], j);
+            }
         }
     }
 #pragma unroll
@@ -48,11 +79,16 @@ __global__ void h2o_accumulate_evict_kernel(const H2OParams p)
         const float os = __shfl_xor_sync(0xffffffffu, best_s, o);
         const int op = __shfl_xor_sync(0xffffffffu, best_p, o);
         const int oj = __shfl_xor_sync(0xffffffffu, best_j, o);
-        if (oj >= 0 && (best_j < 0 || evict_before(os, op, best_s, best_p))) {
-            best_s = os; best_p = op; best_j = oj;
-        }
+        h2o_fold(best_s, best_p, best_j, os, op, oj);
     }
-    if (lane == 0 && p.n_slots > p.budget) {
+    if (lane == 0) {
+        w_s[warp] = best_s;
+        w_p[warp] = best_p;
+        w_j[warp] = best_j;
+    }
+    __syncthreads();
+    if (tid == 0 && n > p.budget) {
+        for (int w = 1; w < H2O_THREADS / 32; ++w) h2o_fold(best_s, best_p, best_j, w_s[w], w_p[w], w_j[w]);
         if (best_j < 0) record_code(p.dev_code, 6 /* KVC_DEV_NO_CANDIDATE */);
         else p.free_slot[row] = best_j;
     }
@@ -72,9 +108,7 @@ __global__ void gather_scores_kernel(const float *s_full, int64_t s_stride, cons
 cudaError_t launch_h2o_accumulate_evict(const H2OParams &p, cudaStream_t stream)
 {
     if (p.rows == 0) return cudaSuccess;
-    const int threads = 128;
-    const long long blocks = ((long long)p.rows * 32 + threads - 1) / threads;
-    h2o_accumulate_evict_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
+    h2o_accumulate_evict_kernel<<<(unsigned)p.rows, H2O_THREADS, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
