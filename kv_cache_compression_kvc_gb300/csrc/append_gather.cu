@@ -41,6 +41,8 @@ __global__ void append_kernel(const AppendParams p, int row_bytes)
     const int li = lane % rm.lpr;
     const bool active = row < p.B * p.H;
     const int b = active ? row / p.H : 0, h = active ? row % p.H : 0;
+    pdl_trigger();
+    pdl_wait();                                 // lengths, slots and t may come from the previous kernel
 
     int64_t t = p.t != nullptr ? *p.t : 0;
     int slot = -1;
@@ -130,6 +132,8 @@ __global__ void gather_kernel(const GatherParams p, int row_bytes)
 
 __global__ void position_advance_kernel(int64_t *t, int64_t delta)
 {
+    pdl_trigger();
+    pdl_wait();
     *t += delta;
 }
 
@@ -143,8 +147,7 @@ cudaError_t launch_append(const AppendParams &p, int elem_bytes, cudaStream_t st
     const int warps = (rows + rm.rpw - 1) / rm.rpw;
     const int threads = 256;
     const int blocks = (warps * 32 + threads - 1) / threads;
-    append_kernel<<<blocks, threads, 0, stream>>>(p, row_bytes);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, p, row_bytes);
 }
 
 cudaError_t launch_gather(const GatherParams &p, int elem_bytes, cudaStream_t stream)
@@ -162,8 +165,7 @@ cudaError_t launch_gather(const GatherParams &p, int elem_bytes, cudaStream_t st
 
 cudaError_t launch_position_advance(int64_t *t, int64_t delta, cudaStream_t stream)
 {
-    position_advance_kernel<<<1, 1, 0, stream>>>(t, delta);
-    return cudaGetLastError();
+    return launch_pdl(position_advance_kernel, dim3(1), dim3(1), 0, stream, t, delta);
 }
 
 }  // namespace kvc

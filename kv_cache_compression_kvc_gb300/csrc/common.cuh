@@ -155,6 +155,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// ---- programmatic dependent launch -----------------------------------------------------------
+// A kernel launched with programmatic stream serialization may start while the previous kernel
+// in the stream is still finishing.  It must call pdl_wait() before it reads anything that kernel
+// may have written; pdl_trigger() lets the next kernel in the stream start its own prologue.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2(float x)
 {
     float y;

@@ -166,6 +166,8 @@ decode_attn_kernel(const DecodeParams p)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    pdl_trigger();
+    pdl_wait();                                      // inputs may come from the previous kernel
 
     // ---- decode position (StreamingLLM layout) --------------------------------------------
     // With RoPE the tiles run over ranks: rank r < S is sink slot r; rank r >= S is ring token
@@ -613,8 +615,7 @@ cudaError_t launch_decode_rm(const DecodeParams &p, cudaStream_t stream)
     const long long T_all = (long long)q.P * q.NT;
     const long long max_ctas = (long long)p.n_sm * SM::CPS;
     const int C = (int)(T_all < max_ctas ? T_all : max_ctas);
-    kern<<<C, kDecodeThreads, SM::kBytes, stream>>>(q);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)C), dim3(kDecodeThreads), (size_t)SM::kBytes, stream, q);
 }
 
 // RoPE with one query head per KV head takes the factored rotation when the table covers the

@@ -144,6 +144,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    pdl_trigger();
+    pdl_wait();                                // inputs may come from the previous kernel
 
     auto pair_slots = [&](int q) -> int {
         if (p.len != nullptr) {
@@ -428,8 +430,8 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream, bool *used)
     const long long T_all = (long long)q.P * q.NT;
     const int C = (int)(T_all < p.n_sm ? T_all : p.n_sm);
     *used = true;
-    decode_mma_kernel<D, G><<<C, M_THREADS, PL::SMEM, stream>>>(km, vm, q);
-    return cudaGetLastError();
+    return launch_pdl(decode_mma_kernel<D, G>, dim3((unsigned)C), dim3(M_THREADS), (size_t)PL::SMEM,
+                      stream, km, vm, q);
 }
 
 }  // namespace

@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const
     __shared__ int w_p[H2O_THREADS / 32], w_j[H2O_THREADS / 32];
     const int row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
+    pdl_wait();                                 // logits and lse come from the decode kernel
     const int64_t t = *p.t;
     const float *__restrict__ lg = p.logits + (size_t)row * p.logits_stride;
     float *__restrict__ s = p.score + (size_t)row * p.stride;
@@ -108,8 +110,8 @@ __global__ void gather_scores_kernel(const float *s_full, int64_t s_stride, cons
 cudaError_t launch_h2o_accumulate_evict(const H2OParams &p, cudaStream_t stream)
 {
     if (p.rows == 0) return cudaSuccess;
-    h2o_accumulate_evict_kernel<<<(unsigned)p.rows, H2O_THREADS, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(h2o_accumulate_evict_kernel, dim3((unsigned)p.rows), dim3(H2O_THREADS), 0,
+                      stream, p);
 }
 
 cudaError_t launch_gather_scores(const float *s_full, int64_t s_stride, const int32_t *idx,

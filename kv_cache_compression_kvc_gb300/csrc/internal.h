@@ -6,10 +6,31 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace kvc {
 
 // ------------------------------------------------------------------------------------------
 // Decode attention (split over slots, log-sum-exp merge by the last block of each KV head).
+// Launches `kernel` with programmatic stream serialization: its prologue may overlap the end of
+// the previous kernel in the stream; the kernel calls pdl_wait() before reading its inputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 struct DecodeParams {
     const void *q;
     const void *k;
