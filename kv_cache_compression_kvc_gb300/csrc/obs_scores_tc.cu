@@ -184,10 +184,15 @@ __device__ __forceinline__ float max32(const float *x)
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
 
-// Named barrier over the epilogue warps that take part (128 threads per set).
+// Named barriers: 1 over every epilogue warp that takes part (128 threads per set), 2 + set
+// over the four warps of one set.
 __device__ __forceinline__ void epilogue_sync(int nsets)
 {
     asm volatile("bar.sync 1, %0;" ::"r"(128 * nsets) : "memory");
+}
+__device__ __forceinline__ void set_sync(int set)
+{
+    asm volatile("bar.sync %0, 128;" ::"r"(2 + set) : "memory");
 }
 
 struct TcParams {
@@ -197,6 +202,7 @@ struct TcParams {
     int32_t n_col_tiles;  // key tiles of 128 covering the n_cols written columns (pass 2)
     int32_t col_chunks;   // pass 2 with a resident row block: key-tile chunks per row block
     int32_t col_chunk_tiles;
+    int32_t n_work;       // work items of the launch (blocks take them round-robin)
     int32_t *dev_code;
 };
 
@@ -206,85 +212,119 @@ __device__ __forceinline__ int row_pos(const ScoreParams &p, int r)
     return p.N - p.L_obs + (r % p.L_obs);
 }
 
+// One work item: a resident ("fixed") operand tile and a run of streamed tiles.
+//   MODE 0: fixed = a 128-row tile of window queries, streamed = key tiles of one chunk;
+//   MODE 1: fixed = one key tile, streamed = the row blocks that can see it;
+//   MODE 2: fixed = a 128-row block holding whole heads, streamed = key tiles of one chunk.
+struct TcItem {
+    int pair, fixed_row0, t_begin, n_tiles, chunk, ktile;
+};
+
+template <int MODE>
+__device__ __forceinline__ TcItem tc_item(const TcParams &tp, int u)
+{
+    const ScoreParams &p = tp.sp;
+    const int R = p.G * p.L_obs;
+    const int first_pos = p.N - p.L_obs;
+    TcItem it{};
+    if (MODE == 0) {
+        const int per_pair = tp.n_mtiles * p.n_chunks;
+        it.pair = u / per_pair;
+        const int mtile = (u % per_pair) / p.n_chunks;
+        it.chunk = u % p.n_chunks;
+        // keys a row tile can see: up to the largest position among its rows
+        const int r_lo = mtile * TC_ROWS;
+        const int r_hi = min(r_lo + TC_ROWS, R) - 1;
+        const int w_hi = (r_lo / p.L_obs != r_hi / p.L_obs) ? p.L_obs - 1 : r_hi % p.L_obs;
+        const int kt_needed = (first_pos + w_hi) / TC_ROWS + 1;
+        it.t_begin = it.chunk * tp.chunk_tiles;
+        it.n_tiles = max(0, min(it.t_begin + tp.chunk_tiles, kt_needed) - it.t_begin);
+        it.fixed_row0 = r_lo;
+    } else if (MODE == 2) {
+        const int n_rb = (R + TC_ROWS - 1) / TC_ROWS;
+        const int per_pair = n_rb * tp.col_chunks;
+        it.pair = u / per_pair;
+        const int mtile = (u % per_pair) / tp.col_chunks;      // resident row block
+        it.chunk = u % tp.col_chunks;
+        it.t_begin = it.chunk * tp.col_chunk_tiles;              // first key tile
+        it.n_tiles = max(0, min(it.t_begin + tp.col_chunk_tiles, tp.n_col_tiles) - it.t_begin);
+        it.fixed_row0 = mtile * TC_ROWS;
+    } else {
+        it.pair = u / tp.n_col_tiles;
+        it.ktile = u % tp.n_col_tiles;
+        // row blocks whose rows can see this key tile: positions >= its first key
+        const int k0 = it.ktile * TC_ROWS;
+        int rb0 = 0;
+        if (k0 > first_pos) rb0 = (k0 - first_pos) / TC_ROWS;   // rows sorted by position when G = 1
+        if (p.G > 1) rb0 = 0;
+        it.t_begin = rb0;
+        it.n_tiles = max(0, (R + TC_ROWS - 1) / TC_ROWS - rb0);
+    }
+    return it;
+}
+
+template <int D>
+struct TcPlan {
+    static constexpr int SUBS = D / 64;                       // 64-element sub-tiles per tile
+    static constexpr int TILE_BYTES = SUBS * TC_SUB_BYTES;
+    static constexpr int NFIX = D >= 256 ? 1 : 2;             // resident tiles (double-buffered)
+    static constexpr int NS_RAW = (200 * 1024 - NFIX * TILE_BYTES) / TILE_BYTES;
+    static constexpr int NS = NS_RAW > 4 ? 4 : NS_RAW;        // streamed tiles in flight
+    static_assert(NS >= 2, "tensor-core scoring needs two operand stages");
+    static constexpr int BAR_BYTES = 8 * (2 * NFIX + 2 * NS + 2 * TC_NACC) + 16;
+    static constexpr int SMEM_USED = 1024 + (NFIX + NS) * TILE_BYTES + BAR_BYTES +
+                                     4 * TC_ROWS * 4 + 2 * TC_ROWS * 2 * 4 + 64;
+    // every block allocates all of tensor memory: one block per SM, so at least half the SM's
+    // shared memory is requested
+    static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
+};
+
+// Persistent blocks: block c takes the work items c, c + gridDim.x, ...  The roles walk the same
+// item sequence; stage, accumulator and epilogue-set indices follow block-global tile counters,
+// the resident tile alternates between NFIX buffers per item.
 // MODE 0: row statistics; 1: column sums, key tile resident; 2: column sums, row block resident
 template <int D, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  const TcParams tp)
 {
-    constexpr int SUBS = D / 64;                 // 64-element sub-tiles per operand tile
-    constexpr int TILE_BYTES = SUBS * TC_SUB_BYTES;
+    using PL = TcPlan<D>;
+    constexpr int SUBS = PL::SUBS, TILE_BYTES = PL::TILE_BYTES, NFIX = PL::NFIX, NS = PL::NS;
     constexpr int KSTEPS = D / 16;
-    constexpr int NS = (200 * 1024 - TILE_BYTES) / TILE_BYTES > 4
-                           ? 4
-                           : (200 * 1024 - TILE_BYTES) / TILE_BYTES;
-    static_assert(NS >= 2, "tensor-core scoring needs two operand stages");
     const ScoreParams &p = tp.sp;
+    // epilogue sets: with a resident key tile the column sums carry across row blocks; two sets
+    // (alternate row blocks, partial sums merged per item) when every row is one head, one set
+    // when a key's column crosses heads
+    const int NSETS = (MODE == 1 && p.G > 1) ? 1 : 2;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned operand area (the swizzle pattern is anchored to 1024-byte lines)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t fixed = base;                          // one operand tile, loaded once
-    const uint32_t stage0 = base + TILE_BYTES;            // NS streamed operand tiles
+    const uint32_t fixed0 = base;                         // NFIX resident tiles
+    const uint32_t stage0 = base + NFIX * TILE_BYTES;     // NS streamed tiles
     const uint32_t bars = stage0 + NS * TILE_BYTES;       // mbarriers
-    const uint32_t bar_fixed = bars;
-    const uint32_t bar_full = bars + 8;                   // NS
+    const uint32_t bar_fix_full = bars;                   // NFIX
+    const uint32_t bar_fix_empty = bar_fix_full + 8 * NFIX;   // NFIX
+    const uint32_t bar_full = bar_fix_empty + 8 * NFIX;   // NS
     const uint32_t bar_empty = bar_full + 8 * NS;         // NS
     const uint32_t bar_acc_full = bar_empty + 8 * NS;     // TC_NACC
     const uint32_t bar_acc_empty = bar_acc_full + 8 * TC_NACC;   // TC_NACC
     const uint32_t tmem_slot = bar_acc_empty + 8 * TC_NACC;      // u32 written by tcgen05.alloc
-    float *sm_lse = reinterpret_cast<float *>(smem_raw + (tmem_slot + 16 - raw));   // [2][128]
-    float *sm_mz = sm_lse + 2 * TC_ROWS;                  // [128][2] second set's row states
-    // epilogue sets: column sums with a resident key tile carry sums across row blocks, so
-    // one set takes every item there
-    constexpr int NSETS = MODE == 1 ? 1 : 2;
+    float *sm_lse = reinterpret_cast<float *>(smem_raw + (tmem_slot + 16 - raw));   // [4][128]
+    float *sm_mz = sm_lse + 4 * TC_ROWS;                  // [2][128][2] second set's states
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int R = p.G * p.L_obs;
     const int first_pos = p.N - p.L_obs;
-
-    // ---- work item of this block --------------------------------------------------------------
-    int pair, fixed_row0 = 0, t_begin = 0, n_items = 0, mtile = 0, ktile = 0, chunk = 0;
-    if (MODE == 0) {
-        const int per_pair = tp.n_mtiles * p.n_chunks;
-        pair = blockIdx.x / per_pair;
-        mtile = (blockIdx.x % per_pair) / p.n_chunks;
-        chunk = blockIdx.x % p.n_chunks;
-        // keys a row tile can see: up to the largest position among its rows
-        const int r_lo = mtile * TC_ROWS;
-        const int r_hi = min(r_lo + TC_ROWS, R) - 1;
-        const int w_hi = (r_lo / p.L_obs != r_hi / p.L_obs) ? p.L_obs - 1 : r_hi % p.L_obs;
-        const int kt_needed = (first_pos + w_hi) / TC_ROWS + 1;
-        t_begin = chunk * tp.chunk_tiles;
-        n_items = max(0, min(t_begin + tp.chunk_tiles, kt_needed) - t_begin);
-        fixed_row0 = r_lo;
-    } else if (MODE == 2) {
-        const int n_rb = (R + TC_ROWS - 1) / TC_ROWS;
-        const int per_pair = n_rb * tp.col_chunks;
-        pair = blockIdx.x / per_pair;
-        mtile = (blockIdx.x % per_pair) / tp.col_chunks;      // resident row block
-        chunk = blockIdx.x % tp.col_chunks;
-        t_begin = chunk * tp.col_chunk_tiles;                  // first key tile
-        n_items = max(0, min(t_begin + tp.col_chunk_tiles, tp.n_col_tiles) - t_begin);
-        fixed_row0 = mtile * TC_ROWS;
-    } else {
-        pair = blockIdx.x / tp.n_col_tiles;
-        ktile = blockIdx.x % tp.n_col_tiles;
-        // row blocks whose rows can see this key tile: positions >= its first key
-        const int k0 = ktile * TC_ROWS;
-        int rb0 = 0;
-        if (k0 > first_pos) rb0 = (k0 - first_pos) / TC_ROWS;   // rows sorted by position when G = 1
-        if (p.G > 1) rb0 = 0;
-        t_begin = rb0;
-        n_items = max(0, (R + TC_ROWS - 1) / TC_ROWS - rb0);
-    }
-    const int b = pair / p.Hkv, kh = pair % p.Hkv;
-    const int qrow_group = (b * p.Hq + kh * p.G) * p.L_obs;   // first q row of this group
+    const int C = gridDim.x;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar_fixed, 1);
+        for (int f = 0; f < NFIX; ++f) {
+            mbar_init(bar_fix_full + 8 * f, 1);
+            mbar_init(bar_fix_empty + 8 * f, 1);
+        }
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
@@ -308,71 +348,110 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     uint32_t tmem_base;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot));
 
-    if (n_items > 0) {
-        if (warp == 0 && lane == 0) {
-            // ============================== TMA producer ==========================================
-            mbar_arrive_expect_tx(bar_fixed, TILE_BYTES);
+    if (warp == 0 && lane == 0) {
+        // ================================ TMA producer ============================================
+        long long g = 0;                            // streamed tiles so far
+        int k = 0;                                  // items with tiles so far
+        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+            const TcItem it = tc_item<MODE>(tp, u);
+            if (it.n_tiles == 0) continue;
+            const int b = it.pair / p.Hkv, kh = it.pair % p.Hkv;
+            const int qrow_group = (b * p.Hq + kh * p.G) * p.L_obs;
+            const int f = k % NFIX;
+            if (k >= NFIX) mbar_wait(bar_fix_empty + 8 * f, ((k / NFIX) - 1) & 1, tp.dev_code);
+            const uint32_t fx = fixed0 + f * TILE_BYTES;
+            mbar_arrive_expect_tx(bar_fix_full + 8 * f, TILE_BYTES);
             for (int a = 0; a < SUBS; ++a) {
                 if (MODE != 1)
-                    tma_load_2d(fixed + a * TC_SUB_BYTES, &qmap, a * 64, qrow_group + fixed_row0,
-                                bar_fixed);
+                    tma_load_2d(fx + a * TC_SUB_BYTES, &qmap, a * 64, qrow_group + it.fixed_row0,
+                                bar_fix_full + 8 * f);
                 else
-                    tma_load_4d(fixed + a * TC_SUB_BYTES, &kmap, a * 64, ktile * TC_ROWS, kh, b,
-                                bar_fixed);
+                    tma_load_4d(fx + a * TC_SUB_BYTES, &kmap, a * 64, it.ktile * TC_ROWS, kh, b,
+                                bar_fix_full + 8 * f);
             }
-            for (int i = 0; i < n_items; ++i) {
-                const int s = i % NS;
-                if (i >= NS) mbar_wait(bar_empty + 8 * s, ((i / NS) - 1) & 1, tp.dev_code);
+            for (int i = 0; i < it.n_tiles; ++i, ++g) {
+                const int s = (int)(g % NS);
+                if (g >= NS) mbar_wait(bar_empty + 8 * s, (int)((g / NS) - 1) & 1, tp.dev_code);
                 const uint32_t dst = stage0 + s * TILE_BYTES;
                 mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
                 for (int a = 0; a < SUBS; ++a) {
                     if (MODE != 1)
                         tma_load_4d(dst + a * TC_SUB_BYTES, &kmap, a * 64,
-                                    (t_begin + i) * TC_ROWS, kh, b, bar_full + 8 * s);
+                                    (it.t_begin + i) * TC_ROWS, kh, b, bar_full + 8 * s);
                     else
                         tma_load_2d(dst + a * TC_SUB_BYTES, &qmap, a * 64,
-                                    qrow_group + (t_begin + i) * TC_ROWS, bar_full + 8 * s);
+                                    qrow_group + (it.t_begin + i) * TC_ROWS, bar_full + 8 * s);
                 }
             }
-        } else if (warp == 1 && lane == 0) {
-            // ============================== MMA issuer ============================================
-            mbar_wait(bar_fixed, 0, tp.dev_code);
-            for (int i = 0; i < n_items; ++i) {
-                const int s = i % NS, ab = i % TC_NACC;
-                mbar_wait(bar_full + 8 * s, (i / NS) & 1, tp.dev_code);
-                if (i >= TC_NACC)
-                    mbar_wait(bar_acc_empty + 8 * ab, ((i / TC_NACC) - 1) & 1, tp.dev_code);
+            ++k;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ================================ MMA issuer ==============================================
+        long long g = 0;
+        int k = 0;
+        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+            const TcItem it = tc_item<MODE>(tp, u);
+            if (it.n_tiles == 0) continue;
+            const int f = k % NFIX;
+            mbar_wait(bar_fix_full + 8 * f, (k / NFIX) & 1, tp.dev_code);
+            const uint32_t fx = fixed0 + f * TILE_BYTES;
+            for (int i = 0; i < it.n_tiles; ++i, ++g) {
+                const int s = (int)(g % NS), ab = (int)(g % TC_NACC);
+                mbar_wait(bar_full + 8 * s, (int)(g / NS) & 1, tp.dev_code);
+                if (g >= TC_NACC)
+                    mbar_wait(bar_acc_empty + 8 * ab, (int)((g / TC_NACC) - 1) & 1, tp.dev_code);
                 tc_fence_after();
                 // MODE 0/1: A = resident tile, B = streamed tile; MODE 2: A = streamed keys,
                 // B = resident rows (the accumulator then has one key per lane)
-                const uint32_t a_base = MODE == 2 ? stage0 + s * TILE_BYTES : fixed;
-                const uint32_t b_base = MODE == 2 ? fixed : stage0 + s * TILE_BYTES;
+                const uint32_t a_base = MODE == 2 ? stage0 + s * TILE_BYTES : fx;
+                const uint32_t b_base = MODE == 2 ? fx : stage0 + s * TILE_BYTES;
 #pragma unroll
-                for (int k = 0; k < KSTEPS; ++k) {
-                    const uint32_t off = (k >> 2) * TC_SUB_BYTES + (k & 3) * 32;
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const uint32_t off = (kk >> 2) * TC_SUB_BYTES + (kk & 3) * 32;
                     umma_bf16(tmem_base + ab * 128, sw128_desc(a_base + off),
-                              sw128_desc(b_base + off), k > 0 ? 1u : 0u);
+                              sw128_desc(b_base + off), kk > 0 ? 1u : 0u);
                 }
                 umma_commit(bar_empty + 8 * s);       // operand stage free once the MMAs finish
                 umma_commit(bar_acc_full + 8 * ab);   // accumulator ready for the epilogue
             }
-        } else if (warp >= 2 && (warp - 2) / 4 < NSETS) {
-            // ============================== epilogue ==============================================
-            const int set = (warp - 2) / 4;           // items set, set + NSETS, ...
-            const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
-            const int et = q4 * 32 + lane;            // this thread's lane (row or key)
-            const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+            umma_commit(bar_fix_empty + 8 * f);       // resident tile free after the item's MMAs
+            ++k;
+        }
+    } else if (warp >= 2 && (warp - 2) / 4 < NSETS) {
+        // ================================ epilogue ================================================
+        const int set = (warp - 2) / 4;           // global tiles g with g % NSETS == set
+        const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
+        const int et = q4 * 32 + lane;            // this thread's lane (row or key)
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        long long g = 0;
+        int k = 0;
+        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+            const TcItem it = tc_item<MODE>(tp, u);
+            const int b = it.pair / p.Hkv, kh = it.pair % p.Hkv;
             if (MODE == 0) {
-                const int r = fixed_row0 + et;        // window row of the group
+                const int r = it.fixed_row0 + et;     // window row of the group
                 const bool row_ok = r < R;
+                float *dst = p.row_ml + (((size_t)it.pair * p.n_chunks + it.chunk) * R + r) * 2;
+                if (it.n_tiles == 0) {
+                    // no key tile reaches these rows: an empty state for every row
+                    if (set == 0 && row_ok) {
+                        dst[0] = kNegBig;
+                        dst[1] = 0.f;
+                    }
+                    continue;
+                }
                 const int pos = row_ok ? row_pos(p, r) : -1;
                 float m_run = kNegBig, z_run = 0.f;
-                for (int i = set; i < n_items; i += NSETS) {
-                    const int ab = i % TC_NACC;
-                    mbar_wait(bar_acc_full + 8 * ab, (i / TC_NACC) & 1, tp.dev_code);
+                for (int i = 0; i < it.n_tiles; ++i) {
+                    const long long gg = g + i;
+                    if ((int)(gg % NSETS) != set) continue;
+                    const int ab = (int)(gg % TC_NACC);
+                    mbar_wait(bar_acc_full + 8 * ab, (int)(gg / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
-                    const int k0 = (t_begin + i) * TC_ROWS;
-                    const bool need_mask = k0 + TC_ROWS - 1 > first_pos || k0 + TC_ROWS > p.N;
+                    const int k0 = (it.t_begin + i) * TC_ROWS;
+                    // this row sees keys up to its own position: mask only where the tile
+                    // reaches past it (or past the prompt)
+                    const bool need_mask = k0 + TC_ROWS - 1 > pos || k0 + TC_ROWS > p.N;
                     float v[4][32];
                     tmem_ld128(tmem_base + ab * 128 + lane_off, v);
                     if (need_mask) {
@@ -399,39 +478,43 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
                 }
                 // the second set hands its row states to the first, which merges and writes
+                float *mz = sm_mz + (k & 1) * 2 * TC_ROWS;
                 if (set == 1) {
-                    sm_mz[2 * et] = m_run;
-                    sm_mz[2 * et + 1] = z_run;
+                    mz[2 * et] = m_run;
+                    mz[2 * et + 1] = z_run;
                 }
                 epilogue_sync(NSETS);
                 if (set == 0 && row_ok) {
-                    const float m1 = sm_mz[2 * et], z1 = sm_mz[2 * et + 1];
+                    const float m1 = mz[2 * et], z1 = mz[2 * et + 1];
                     const float M = fmaxf(m_run, m1);
-                    float *dst = p.row_ml + (((size_t)pair * p.n_chunks + chunk) * R + r) * 2;
                     dst[0] = M;
                     dst[1] = z_run * ex2(m_run - M) + z1 * ex2(m1 - M);
                 }
             } else if (MODE == 2) {
+                if (it.n_tiles == 0) continue;
                 // resident rows fixed_row0 .. +127 hold whole heads: per key tile, each thread
                 // sums its key's column over each head and writes it
-                const float *lse_g = p.row_lse2 + (size_t)pair * R;
-                float *lse_buf = sm_lse;
-                if (set == 0) lse_buf[et] = (fixed_row0 + et < R) ? lse_g[fixed_row0 + et] : 0.f;
+                const float *lse_g = p.row_lse2 + (size_t)it.pair * R;
+                float *lse_buf = sm_lse + (k & 1) * TC_ROWS;
+                if (set == 0)
+                    lse_buf[et] = (it.fixed_row0 + et < R) ? lse_g[it.fixed_row0 + et] : 0.f;
                 epilogue_sync(NSETS);
                 float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
-                const int rows_blk = min(TC_ROWS, R - fixed_row0);
-                for (int i = set; i < n_items; i += NSETS) {
-                    const int ab = i % TC_NACC;
-                    const int key = (t_begin + i) * TC_ROWS + et;
-                    const bool mask_tile = (t_begin + i) * TC_ROWS + TC_ROWS - 1 > first_pos;
-                    mbar_wait(bar_acc_full + 8 * ab, (i / TC_NACC) & 1, tp.dev_code);
+                const int rows_blk = min(TC_ROWS, R - it.fixed_row0);
+                for (int i = 0; i < it.n_tiles; ++i) {
+                    const long long gg = g + i;
+                    if ((int)(gg % NSETS) != set) continue;
+                    const int ab = (int)(gg % TC_NACC);
+                    const int key = (it.t_begin + i) * TC_ROWS + et;
+                    const bool mask_tile = (it.t_begin + i) * TC_ROWS + TC_ROWS - 1 > first_pos;
+                    mbar_wait(bar_acc_full + 8 * ab, (int)(gg / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
-                    int g_cur = fixed_row0 / p.L_obs;
+                    int g_cur = it.fixed_row0 / p.L_obs;
                     float acc_g = 0.f;
                     float vt[2][32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const int rc = fixed_row0 + c * 32;
+                        const int rc = it.fixed_row0 + c * 32;
                         if (c * 32 >= rows_blk) break;
                         // 64 columns per tensor-memory read keep the registers for two sets
                         if ((c & 1) == 0) tmem_ld64(tmem_base + ab * 128 + lane_off + c * 32, vt);
@@ -444,7 +527,11 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                             acc_g = 0.f;
                             g_cur = g_a;
                         }
-                        if (split == 32 && !mask_tile) {
+                        // rows of the chunk see keys up to their positions; the smallest is
+                        // the chunk's first row, or 0 past a head boundary
+                        const bool mask_c =
+                            mask_tile && key > first_pos + (split < rows_here ? 0 : rc - g_a * p.L_obs);
+                        if (split == 32 && !mask_c) {
                             // the whole chunk is one head and every key is visible
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
@@ -457,7 +544,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                         for (int j = 0; j < 32; ++j) {
                             const float lse = lse_buf[c * 32 + j];
                             float pr = ex2(fmaf(v[j], p.scale_log2, -lse));
-                            if (mask_tile) {
+                            if (mask_c) {
                                 const int hb = (j < split ? g_a : g_a + 1) * p.L_obs;
                                 if (key > first_pos + (rc + j - hb)) pr = 0.f;
                             }
@@ -477,21 +564,26 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
                 }
             } else {
-                const int key = ktile * TC_ROWS + et;
-                const float *lse_g = p.row_lse2 + (size_t)pair * R;
-                const bool mask_tile = ktile * TC_ROWS + TC_ROWS - 1 > first_pos;
+                if (it.n_tiles == 0) continue;
+                const int key = it.ktile * TC_ROWS + et;
+                const float *lse_g = p.row_lse2 + (size_t)it.pair * R;
+                const bool mask_tile = it.ktile * TC_ROWS + TC_ROWS - 1 > first_pos;
                 float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
-                int g_cur = t_begin * TC_ROWS / p.L_obs;   // head of the first row handled
+                int g_cur = it.t_begin * TC_ROWS / p.L_obs;   // head of the first row handled
                 float acc_g = 0.f;
-                for (int i = 0; i < n_items; ++i) {
-                    const int ab = i % TC_NACC;
-                    const int r0 = (t_begin + i) * TC_ROWS;   // first row of this block
-                    // stage the block's row log2-sum-exp values (double buffered)
-                    float *lse_buf = sm_lse + (i & 1) * TC_ROWS;
+                int n_mine = 0;                               // this set's row blocks so far
+                for (int i = 0; i < it.n_tiles; ++i) {
+                    const long long gg = g + i;
+                    if ((int)(gg % NSETS) != set) continue;
+                    const int ab = (int)(gg % TC_NACC);
+                    const int r0 = (it.t_begin + i) * TC_ROWS;   // first row of this block
+                    // stage the block's row log2-sum-exp values (per set, double buffered)
+                    float *lse_buf = sm_lse + (set * 2 + ((int)(gg / NSETS) & 1)) * TC_ROWS;
                     lse_buf[et] = (r0 + et < R) ? lse_g[r0 + et] : 0.f;
-                    epilogue_sync(NSETS);
-                    mbar_wait(bar_acc_full + 8 * ab, (i / TC_NACC) & 1, tp.dev_code);
+                    set_sync(set);
+                    mbar_wait(bar_acc_full + 8 * ab, (int)(gg / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
+                    ++n_mine;
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         const int rc = r0 + c * 32;         // first row of this chunk
@@ -507,7 +599,11 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                             acc_g = 0.f;
                             g_cur = g_a;
                         }
-                        if (split == 32 && !mask_tile) {
+                        // rows of the chunk see keys up to their positions; the smallest is
+                        // the chunk's first row, or 0 past a head boundary
+                        const bool mask_c =
+                            mask_tile && key > first_pos + (split < rows_here ? 0 : rc - g_a * p.L_obs);
+                        if (split == 32 && !mask_c) {
                             // the whole chunk is one head and every key is visible
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
@@ -520,7 +616,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                         for (int j = 0; j < 32; ++j) {
                             const float lse = lse_buf[c * 32 + j];
                             float pr = ex2(fmaf(v[j], p.scale_log2, -lse));
-                            if (mask_tile) {
+                            if (mask_c) {
                                 // position of row rc + j inside its head (g_a, or g_a + 1 past
                                 // the split)
                                 const int hb = (j < split ? g_a : g_a + 1) * p.L_obs;
@@ -540,16 +636,20 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
                 }
-                if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                (void)n_mine;
+                if (NSETS == 1) {
+                    if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                } else {
+                    // one head (G == 1): the second set hands its partial sum to the first
+                    float *part = sm_mz + (k & 1) * 2 * TC_ROWS;
+                    if (set == 1) part[et] = acc_g;
+                    epilogue_sync(NSETS);
+                    if (set == 0 && key < p.n_cols)
+                        s_base[key] = (acc_g + part[et]) * p.col_mult;
+                }
             }
-        }
-    } else if (MODE == 0 && warp >= 2 && warp < 6) {
-        // no key tile reaches this block's rows: an empty state for every row
-        const int r = fixed_row0 + (warp & 3) * 32 + lane;
-        if (r < R) {
-            float *dst = p.row_ml + (((size_t)pair * p.n_chunks + chunk) * R + r) * 2;
-            dst[0] = kNegBig;
-            dst[1] = 0.f;
+            g += it.n_tiles;
+            if (it.n_tiles > 0) ++k;
         }
     }
 
@@ -565,12 +665,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 template <int D>
 constexpr int tc_smem_bytes()
 {
-    constexpr int TILE_BYTES = (D / 64) * TC_SUB_BYTES;
-    constexpr int NS = (200 * 1024 - TILE_BYTES) / TILE_BYTES > 4
-                           ? 4
-                           : (200 * 1024 - TILE_BYTES) / TILE_BYTES;
-    return 1024 + (1 + NS) * TILE_BYTES + 8 * (1 + 2 * NS + 2 * TC_NACC) + 16 +
-           4 * TC_ROWS * 4 + 64;
+    return TcPlan<D>::SMEM;
 }
 
 // ---- host: tensor maps through the driver entry point ------------------------------------------
@@ -655,6 +750,9 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
+    int n_sm = 152;
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (n_sm <= 0) n_sm = 152;
     const int R = sp.G * sp.L_obs;
     TcParams tp;
     tp.sp = sp;
@@ -664,9 +762,16 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     tp.col_chunks = 1;
     tp.col_chunk_tiles = tp.n_col_tiles;
     tp.dev_code = dev_code;
+    // one persistent block per SM (at most one per work item); with a single resident tile the
+    // item boundaries would stall the pipeline, so every item gets its own block there
+    auto grid = [&](long long work) {
+        return (unsigned)(TcPlan<D>::NFIX == 1 || work < n_sm ? work : n_sm);
+    };
     const long long pairs = (long long)sp.B * sp.Hkv;
-    tc_scores_kernel<D, 0><<<(unsigned)(pairs * tp.n_mtiles * sp.n_chunks), TC_THREADS, SMEM,
-                             stream>>>(qm, km, tp);
+    const long long work0 = pairs * tp.n_mtiles * sp.n_chunks;
+    if (work0 > 0x7fffffffLL) return cudaErrorInvalidValue;
+    tp.n_work = (int)work0;
+    tc_scores_kernel<D, 0><<<grid(work0), TC_THREADS, SMEM, stream>>>(qm, km, tp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long rows = pairs * R;
@@ -676,18 +781,20 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     const int n_rb = (R + TC_ROWS - 1) / TC_ROWS;
     if (R <= TC_ROWS || (sp.G > 1 && TC_ROWS % sp.L_obs == 0)) {
         // every head inside one row block: keep the row block, stream the key tiles
-        int n_sm = 152;
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
         const long long base = pairs * n_rb;
         long long chunks = (4LL * n_sm + base - 1) / base;
         if (chunks > tp.n_col_tiles) chunks = tp.n_col_tiles;
         tp.col_chunk_tiles = (int)((tp.n_col_tiles + chunks - 1) / chunks);
         tp.col_chunks = (tp.n_col_tiles + tp.col_chunk_tiles - 1) / tp.col_chunk_tiles;
-        tc_scores_kernel<D, 2><<<(unsigned)(base * tp.col_chunks), TC_THREADS, SMEM, stream>>>(
-            qm, km, tp);
+        const long long work2 = base * tp.col_chunks;
+        if (work2 > 0x7fffffffLL) return cudaErrorInvalidValue;
+        tp.n_work = (int)work2;
+        tc_scores_kernel<D, 2><<<grid(work2), TC_THREADS, SMEM, stream>>>(qm, km, tp);
     } else {
-        tc_scores_kernel<D, 1><<<(unsigned)(pairs * tp.n_col_tiles), TC_THREADS, SMEM, stream>>>(
-            qm, km, tp);
+        const long long work1 = pairs * tp.n_col_tiles;
+        if (work1 > 0x7fffffffLL) return cudaErrorInvalidValue;
+        tp.n_work = (int)work1;
+        tc_scores_kernel<D, 1><<<grid(work1), TC_THREADS, SMEM, stream>>>(qm, km, tp);
     }
     return cudaGetLastError();
 }
