@@ -101,24 +101,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
                      "r"(bar)
                  : "memory");
 }
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one value per thread and column).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
-{
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 // All 128 columns of a tile (four 32-column loads, one wait).
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[4][32])
 {
@@ -157,19 +139,28 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[2][32])
     }
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-// Sum of 32 values with four independent chains (short dependency chains for one warp per
-// scheduler).
-__device__ __forceinline__ float sum32(const float *x)
+// sum_j exp2(v[j] * scale + off[j]) over 32 values with packed fp32x2 FMA and adds (two
+// independent chains); `off` is one value for all (off_u) or per element (off_v, 8-byte aligned).
+__device__ __forceinline__ float exp2_sum32(const float *v, float scale, float off_u,
+                                            const float *off_v)
 {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    const float2 s2 = make_float2(scale, scale);
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
-        a0 += x[j];
-        a1 += x[j + 1];
-        a2 += x[j + 2];
-        a3 += x[j + 3];
+        const float2 o0 = off_v ? *reinterpret_cast<const float2 *>(off_v + j) : make_float2(off_u, off_u);
+        const float2 o1 = off_v ? *reinterpret_cast<const float2 *>(off_v + j + 2) : make_float2(off_u, off_u);
+        float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), s2, o0);
+        float2 y = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), s2, o1);
+        x.x = ex2(x.x);
+        x.y = ex2(x.y);
+        y.x = ex2(y.x);
+        y.y = ex2(y.y);
+        a0 = __fadd2_rn(a0, x);
+        a1 = __fadd2_rn(a1, y);
     }
-    return (a0 + a1) + (a2 + a3);
+    const float2 a = __fadd2_rn(a0, a1);
+    return a.x + a.y;
 }
 __device__ __forceinline__ float max32(const float *x)
 {
@@ -423,6 +414,60 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
         const int et = q4 * 32 + lane;            // this thread's lane (row or key)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        // Column sums over one block of rows r0 .. r0 + rows_blk - 1 (tensor-memory columns from
+        // tcol) for this thread's key.  (g_cur, acc_g) carry the sum of the head in progress; a
+        // finished head's sum is written.  nlse: the rows' negated log2-sum-exp.  The head g_a
+        // and row-in-head rem of each 32-row chunk advance incrementally (heads have at least
+        // 32 rows, or there is one head).
+        auto colsum_rows = [&](uint32_t tcol, int r0, int rows_blk, int key, bool mask_tile,
+                               const float *nlse, float *s_base, int &g_cur, float &acc_g) {
+            int g_a = r0 / p.L_obs;
+            int rem = r0 - g_a * p.L_obs;
+            float vt[2][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c * 32 >= rows_blk) break;
+                // 64 columns per tensor-memory read (one wait for two chunks)
+                if ((c & 1) == 0) tmem_ld64(tcol + c * 32, vt);
+                const float *v = vt[c & 1];
+                const int rows_here = min(32, rows_blk - c * 32);
+                const int split = min(rows_here, p.L_obs - rem);      // rows in head g_a
+                if (g_a != g_cur) {                                   // flush the finished head
+                    if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                    acc_g = 0.f;
+                    g_cur = g_a;
+                }
+                // rows see keys up to their positions; the smallest in the chunk is its first
+                // row, or the next head's first window row past a head boundary
+                const bool mask_c = mask_tile && key > first_pos + (split < rows_here ? 0 : rem);
+                if (split == 32 && !mask_c) {
+                    acc_g += exp2_sum32(v, p.scale_log2, 0.f, nlse + c * 32);
+                } else {
+                    float s_a = 0.f, s_b = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        float pr = ex2(fmaf(v[j], p.scale_log2, nlse[c * 32 + j]));
+                        if (mask_c) {
+                            const int w = j < split ? rem + j : j - split;   // row inside its head
+                            if (key > first_pos + w) pr = 0.f;
+                        }
+                        if (j < split) s_a += pr;
+                        else if (j < rows_here) s_b += pr;
+                    }
+                    acc_g += s_a;
+                    if (split < rows_here) {                          // into head g_a + 1
+                        if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
+                        g_cur = g_a + 1;
+                        acc_g = s_b;
+                    }
+                }
+                rem += 32;
+                if (rem >= p.L_obs) {
+                    rem -= p.L_obs;
+                    ++g_a;
+                }
+            }
+        };
         long long g = 0;
         int k = 0;
         for (int u = blockIdx.x; u < tp.n_work; u += C) {
@@ -466,11 +511,10 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     const float mx = fmaxf(fmaxf(max32(v[0]), max32(v[1])),
                                            fmaxf(max32(v[2]), max32(v[3])));
                     const float m_new = fmaxf(m_run, mx * p.scale_log2);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[c][j] = ex2(fmaf(v[c][j], p.scale_log2, -m_new));
-                    const float z = (sum32(v[0]) + sum32(v[1])) + (sum32(v[2]) + sum32(v[3]));
+                    const float z = (exp2_sum32(v[0], p.scale_log2, -m_new, nullptr) +
+                                     exp2_sum32(v[1], p.scale_log2, -m_new, nullptr)) +
+                                    (exp2_sum32(v[2], p.scale_log2, -m_new, nullptr) +
+                                     exp2_sum32(v[3], p.scale_log2, -m_new, nullptr));
                     z_run = z_run * ex2(m_run - m_new) + z;
                     m_run = m_new;
                     tc_fence_before();
@@ -493,11 +537,11 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             } else if (MODE == 2) {
                 if (it.n_tiles == 0) continue;
                 // resident rows fixed_row0 .. +127 hold whole heads: per key tile, each thread
-                // sums its key's column over each head and writes it
+                // sums its key's column over each head and writes it (lse_buf holds -lse)
                 const float *lse_g = p.row_lse2 + (size_t)it.pair * R;
                 float *lse_buf = sm_lse + (k & 1) * TC_ROWS;
                 if (set == 0)
-                    lse_buf[et] = (it.fixed_row0 + et < R) ? lse_g[it.fixed_row0 + et] : 0.f;
+                    lse_buf[et] = (it.fixed_row0 + et < R) ? -lse_g[it.fixed_row0 + et] : 0.f;
                 epilogue_sync(NSETS);
                 float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
                 const int rows_blk = min(TC_ROWS, R - it.fixed_row0);
@@ -511,53 +555,8 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     tc_fence_after();
                     int g_cur = it.fixed_row0 / p.L_obs;
                     float acc_g = 0.f;
-                    float vt[2][32];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int rc = it.fixed_row0 + c * 32;
-                        if (c * 32 >= rows_blk) break;
-                        // 64 columns per tensor-memory read keep the registers for two sets
-                        if ((c & 1) == 0) tmem_ld64(tmem_base + ab * 128 + lane_off + c * 32, vt);
-                        float *v = vt[c & 1];
-                        const int g_a = rc / p.L_obs;
-                        const int rows_here = min(32, rows_blk - c * 32);
-                        const int split = min(rows_here, (g_a + 1) * p.L_obs - rc);
-                        if (g_a != g_cur) {
-                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
-                            acc_g = 0.f;
-                            g_cur = g_a;
-                        }
-                        // rows of the chunk see keys up to their positions; the smallest is
-                        // the chunk's first row, or 0 past a head boundary
-                        const bool mask_c =
-                            mask_tile && key > first_pos + (split < rows_here ? 0 : rc - g_a * p.L_obs);
-                        if (split == 32 && !mask_c) {
-                            // the whole chunk is one head and every key is visible
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                v[j] = ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
-                            acc_g += sum32(v);
-                            continue;
-                        }
-                        float s_a = 0.f, s_b = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float lse = lse_buf[c * 32 + j];
-                            float pr = ex2(fmaf(v[j], p.scale_log2, -lse));
-                            if (mask_c) {
-                                const int hb = (j < split ? g_a : g_a + 1) * p.L_obs;
-                                if (key > first_pos + (rc + j - hb)) pr = 0.f;
-                            }
-                            if (j < split) s_a += pr;
-                            else if (j < rows_here) s_b += pr;
-                        }
-                        acc_g += s_a;
-                        if (split < rows_here) {
-                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
-                            g_cur = g_a + 1;
-                            acc_g = s_b;
-                        }
-                    }
+                    colsum_rows(tmem_base + ab * 128 + lane_off, it.fixed_row0, rows_blk, key,
+                                mask_tile, lse_buf, s_base, g_cur, acc_g);
                     if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
                     tc_fence_before();
                     __syncwarp();
@@ -572,66 +571,29 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 int g_cur = it.t_begin * TC_ROWS / p.L_obs;   // head of the first row handled
                 float acc_g = 0.f;
                 int n_mine = 0;                               // this set's row blocks so far
+                // this thread's row of the set's next row block, loaded one block ahead
+                auto lse_of = [&](int i) -> float {
+                    const int r = (it.t_begin + i) * TC_ROWS + et;
+                    return (i < it.n_tiles && r < R) ? -lse_g[r] : 0.f;
+                };
+                const int i_first = (int)(((set - g) % NSETS + NSETS) % NSETS);
+                float lse_next = lse_of(i_first);
                 for (int i = 0; i < it.n_tiles; ++i) {
                     const long long gg = g + i;
                     if ((int)(gg % NSETS) != set) continue;
                     const int ab = (int)(gg % TC_NACC);
                     const int r0 = (it.t_begin + i) * TC_ROWS;   // first row of this block
-                    // stage the block's row log2-sum-exp values (per set, double buffered)
+                    // stage the block's negated row log2-sum-exp values (per set, double
+                    // buffered)
                     float *lse_buf = sm_lse + (set * 2 + ((int)(gg / NSETS) & 1)) * TC_ROWS;
-                    lse_buf[et] = (r0 + et < R) ? lse_g[r0 + et] : 0.f;
+                    lse_buf[et] = lse_next;
+                    lse_next = lse_of(i + NSETS);
                     set_sync(set);
                     mbar_wait(bar_acc_full + 8 * ab, (int)(gg / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
                     ++n_mine;
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        const int rc = r0 + c * 32;         // first row of this chunk
-                        if (rc >= R) break;
-                        float v[32];
-                        tmem_ld32(tmem_base + ab * 128 + lane_off + c * 32, v);
-                        // the chunk's rows span heads g_a .. g_b (at most two when L_obs >= 32)
-                        const int g_a = rc / p.L_obs;
-                        const int rows_here = min(32, R - rc);
-                        const int split = min(rows_here, (g_a + 1) * p.L_obs - rc);   // rows in g_a
-                        if (g_a != g_cur) {                 // flush the finished head
-                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
-                            acc_g = 0.f;
-                            g_cur = g_a;
-                        }
-                        // rows of the chunk see keys up to their positions; the smallest is
-                        // the chunk's first row, or 0 past a head boundary
-                        const bool mask_c =
-                            mask_tile && key > first_pos + (split < rows_here ? 0 : rc - g_a * p.L_obs);
-                        if (split == 32 && !mask_c) {
-                            // the whole chunk is one head and every key is visible
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                v[j] = ex2(fmaf(v[j], p.scale_log2, -lse_buf[c * 32 + j]));
-                            acc_g += sum32(v);
-                            continue;
-                        }
-                        float s_a = 0.f, s_b = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float lse = lse_buf[c * 32 + j];
-                            float pr = ex2(fmaf(v[j], p.scale_log2, -lse));
-                            if (mask_c) {
-                                // position of row rc + j inside its head (g_a, or g_a + 1 past
-                                // the split)
-                                const int hb = (j < split ? g_a : g_a + 1) * p.L_obs;
-                                if (key > first_pos + (rc + j - hb)) pr = 0.f;
-                            }
-                            if (j < split) s_a += pr;
-                            else if (j < rows_here) s_b += pr;
-                        }
-                        acc_g += s_a;
-                        if (split < rows_here) {            // the chunk crosses into head g_a + 1
-                            if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
-                            g_cur = g_a + 1;
-                            acc_g = s_b;
-                        }
-                    }
+                    colsum_rows(tmem_base + ab * 128 + lane_off, r0, min(TC_ROWS, R - r0), key,
+                                mask_tile, lse_buf, s_base, g_cur, acc_g);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
