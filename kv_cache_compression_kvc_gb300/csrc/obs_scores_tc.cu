@@ -254,13 +254,18 @@ __device__ __forceinline__ TcItem tc_item(const TcParams &tp, int u)
     return it;
 }
 
-template <int D>
+// CONTIG: blocks take contiguous item ranges whose items mostly share the resident tile (the key
+// chunks of one pair), which is then reloaded only when it changes, from one buffer; the room
+// goes to more streamed stages.  Otherwise items are taken round-robin and every item reloads
+// (double-buffered where it fits).
+template <int D, bool CONTIG>
 struct TcPlan {
     static constexpr int SUBS = D / 64;                       // 64-element sub-tiles per tile
     static constexpr int TILE_BYTES = SUBS * TC_SUB_BYTES;
-    static constexpr int NFIX = D >= 256 ? 1 : 2;             // resident tiles (double-buffered)
+    static constexpr int NFIX = (CONTIG || D >= 256) ? 1 : 2;  // resident tile buffers
     static constexpr int NS_RAW = (200 * 1024 - NFIX * TILE_BYTES) / TILE_BYTES;
-    static constexpr int NS = NS_RAW > 4 ? 4 : NS_RAW;        // streamed tiles in flight
+    static constexpr int NS_CAP = CONTIG ? 8 : 4;
+    static constexpr int NS = NS_RAW > NS_CAP ? NS_CAP : NS_RAW;   // streamed tiles in flight
     static_assert(NS >= 2, "tensor-core scoring needs two operand stages");
     static constexpr int BAR_BYTES = 8 * (2 * NFIX + 2 * NS + 2 * TC_NACC) + 16;
     static constexpr int SMEM_USED = 1024 + (NFIX + NS) * TILE_BYTES + BAR_BYTES +
@@ -270,16 +275,18 @@ struct TcPlan {
     static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
 };
 
-// Persistent blocks: block c takes the work items c, c + gridDim.x, ...  The roles walk the same
-// item sequence; stage, accumulator and epilogue-set indices follow block-global tile counters,
-// the resident tile alternates between NFIX buffers per item.
+// Persistent blocks: block c takes a contiguous range of work items (CONTIG) or the items
+// c, c + gridDim.x, ...  The roles walk the same item sequence; stage, accumulator and
+// epilogue-set indices follow block-global tile counters; the resident tile is loaded into the
+// next of NFIX buffers whenever an item's resident tile differs from the previous item's, and the
+// MMA thread releases a buffer after the last item that uses it.
 // MODE 0: row statistics; 1: column sums, key tile resident; 2: column sums, row block resident
-template <int D, int MODE>
+template <int D, int MODE, bool CONTIG>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  const TcParams tp)
 {
-    using PL = TcPlan<D>;
+    using PL = TcPlan<D, CONTIG>;
     constexpr int SUBS = PL::SUBS, TILE_BYTES = PL::TILE_BYTES, NFIX = PL::NFIX, NS = PL::NS;
     constexpr int KSTEPS = D / 16;
     const ScoreParams &p = tp.sp;
@@ -310,6 +317,14 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const int R = p.G * p.L_obs;
     const int first_pos = p.N - p.L_obs;
     const int C = gridDim.x;
+    // this block's item sequence
+    const int u_first = CONTIG ? (int)((long long)blockIdx.x * tp.n_work / C) : (int)blockIdx.x;
+    const int u_end = CONTIG ? (int)((long long)(blockIdx.x + 1) * tp.n_work / C) : tp.n_work;
+    const int u_step = CONTIG ? 1 : C;
+    // identity of an item's resident tile
+    auto fixed_id = [&](const TcItem &it) -> long long {
+        return (long long)it.pair * (1LL << 32) + (MODE == 1 ? it.ktile : it.fixed_row0);
+    };
 
     if (threadIdx.x == 0) {
         for (int f = 0; f < NFIX; ++f) {
@@ -342,23 +357,30 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (warp == 0 && lane == 0) {
         // ================================ TMA producer ============================================
         long long g = 0;                            // streamed tiles so far
-        int k = 0;                                  // items with tiles so far
-        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+        int nrl = 0;                                // resident-tile loads so far
+        long long prev_id = -1;
+        for (int u = u_first; u < u_end; u += u_step) {
             const TcItem it = tc_item<MODE>(tp, u);
             if (it.n_tiles == 0) continue;
             const int b = it.pair / p.Hkv, kh = it.pair % p.Hkv;
             const int qrow_group = (b * p.Hq + kh * p.G) * p.L_obs;
-            const int f = k % NFIX;
-            if (k >= NFIX) mbar_wait(bar_fix_empty + 8 * f, ((k / NFIX) - 1) & 1, tp.dev_code);
-            const uint32_t fx = fixed0 + f * TILE_BYTES;
-            mbar_arrive_expect_tx(bar_fix_full + 8 * f, TILE_BYTES);
-            for (int a = 0; a < SUBS; ++a) {
-                if (MODE != 1)
-                    tma_load_2d(fx + a * TC_SUB_BYTES, &qmap, a * 64, qrow_group + it.fixed_row0,
-                                bar_fix_full + 8 * f);
-                else
-                    tma_load_4d(fx + a * TC_SUB_BYTES, &kmap, a * 64, it.ktile * TC_ROWS, kh, b,
-                                bar_fix_full + 8 * f);
+            const long long id = fixed_id(it);
+            if (id != prev_id) {
+                prev_id = id;
+                const int f = nrl % NFIX;
+                if (nrl >= NFIX)
+                    mbar_wait(bar_fix_empty + 8 * f, ((nrl / NFIX) - 1) & 1, tp.dev_code);
+                const uint32_t fx = fixed0 + f * TILE_BYTES;
+                mbar_arrive_expect_tx(bar_fix_full + 8 * f, TILE_BYTES);
+                for (int a = 0; a < SUBS; ++a) {
+                    if (MODE != 1)
+                        tma_load_2d(fx + a * TC_SUB_BYTES, &qmap, a * 64,
+                                    qrow_group + it.fixed_row0, bar_fix_full + 8 * f);
+                    else
+                        tma_load_4d(fx + a * TC_SUB_BYTES, &kmap, a * 64, it.ktile * TC_ROWS, kh,
+                                    b, bar_fix_full + 8 * f);
+                }
+                ++nrl;
             }
             for (int i = 0; i < it.n_tiles; ++i, ++g) {
                 const int s = (int)(g % NS);
@@ -374,17 +396,22 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                                     qrow_group + (it.t_begin + i) * TC_ROWS, bar_full + 8 * s);
                 }
             }
-            ++k;
         }
     } else if (warp == 1 && lane == 0) {
         // ================================ MMA issuer ==============================================
         long long g = 0;
-        int k = 0;
-        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+        int nrl = 0, f = 0;
+        long long prev_id = -1;
+        for (int u = u_first; u < u_end; u += u_step) {
             const TcItem it = tc_item<MODE>(tp, u);
             if (it.n_tiles == 0) continue;
-            const int f = k % NFIX;
-            mbar_wait(bar_fix_full + 8 * f, (k / NFIX) & 1, tp.dev_code);
+            const long long id = fixed_id(it);
+            if (id != prev_id) {
+                prev_id = id;
+                f = nrl % NFIX;
+                mbar_wait(bar_fix_full + 8 * f, (nrl / NFIX) & 1, tp.dev_code);
+                ++nrl;
+            }
             const uint32_t fx = fixed0 + f * TILE_BYTES;
             for (int i = 0; i < it.n_tiles; ++i, ++g) {
                 const int s = (int)(g % NS), ab = (int)(g % TC_NACC);
@@ -405,8 +432,17 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 umma_commit(bar_empty + 8 * s);       // operand stage free once the MMAs finish
                 umma_commit(bar_acc_full + 8 * ab);   // accumulator ready for the epilogue
             }
-            umma_commit(bar_fix_empty + 8 * f);       // resident tile free after the item's MMAs
-            ++k;
+            // release the resident buffer after its last item: the next item with tiles loads
+            // a different resident tile (or there is none)
+            long long next_id = -1;
+            for (int v = u + u_step; v < u_end; v += u_step) {
+                const TcItem nx = tc_item<MODE>(tp, v);
+                if (nx.n_tiles > 0) {
+                    next_id = fixed_id(nx);
+                    break;
+                }
+            }
+            if (next_id != -1 && next_id != id) umma_commit(bar_fix_empty + 8 * f);
         }
     } else if (warp >= 2 && (warp - 2) / 4 < NSETS) {
         // ================================ epilogue ================================================
@@ -470,7 +506,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         };
         long long g = 0;
         int k = 0;
-        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+        for (int u = u_first; u < u_end; u += u_step) {
             const TcItem it = tc_item<MODE>(tp, u);
             const int b = it.pair / p.Hkv, kh = it.pair % p.Hkv;
             if (MODE == 0) {
@@ -627,7 +663,8 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 template <int D>
 constexpr int tc_smem_bytes()
 {
-    return TcPlan<D>::SMEM;
+    return TcPlan<D, false>::SMEM > TcPlan<D, true>::SMEM ? TcPlan<D, false>::SMEM
+                                                          : TcPlan<D, true>::SMEM;
 }
 
 // ---- host: tensor maps through the driver entry point ------------------------------------------
@@ -701,15 +738,15 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_scores_kernel<D, 0>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(tc_scores_kernel<D, 1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(tc_scores_kernel<D, 2>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
+        void (*kerns[5])(const CUtensorMap, const CUtensorMap, const TcParams) = {
+            tc_scores_kernel<D, 0, false>, tc_scores_kernel<D, 0, true>,
+            tc_scores_kernel<D, 1, false>, tc_scores_kernel<D, 2, false>,
+            tc_scores_kernel<D, 2, true>};
+        for (auto kf : kerns) {
+            cudaError_t e =
+                cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+            if (e != cudaSuccess) return e;
+        }
         configured[dev] = true;
     }
     int n_sm = 152;
@@ -724,16 +761,22 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     tp.col_chunks = 1;
     tp.col_chunk_tiles = tp.n_col_tiles;
     tp.dev_code = dev_code;
-    // one persistent block per SM (at most one per work item); with a single resident tile the
-    // item boundaries would stall the pipeline, so every item gets its own block there
-    auto grid = [&](long long work) {
-        return (unsigned)(TcPlan<D>::NFIX == 1 || work < n_sm ? work : n_sm);
+    // one persistent block per SM (at most one per work item); round-robin items with a single
+    // resident buffer would stall the pipeline at every item, so each gets its own block there
+    auto grid = [&](long long work, bool contig) {
+        return (unsigned)((!contig && TcPlan<D, false>::NFIX == 1) || work < n_sm ? work : n_sm);
     };
     const long long pairs = (long long)sp.B * sp.Hkv;
     const long long work0 = pairs * tp.n_mtiles * sp.n_chunks;
     if (work0 > 0x7fffffffLL) return cudaErrorInvalidValue;
     tp.n_work = (int)work0;
-    tc_scores_kernel<D, 0><<<grid(work0), TC_THREADS, SMEM, stream>>>(qm, km, tp);
+    // several key chunks per row tile: contiguous items share the resident tile (where that buys
+    // streamed stages: with d_head 256 two stages is all that fits either way)
+    constexpr bool kContigPays = TcPlan<D, true>::NS > TcPlan<D, false>::NS;
+    if (kContigPays && sp.n_chunks >= 2)
+        tc_scores_kernel<D, 0, true><<<grid(work0, true), TC_THREADS, SMEM, stream>>>(qm, km, tp);
+    else
+        tc_scores_kernel<D, 0, false><<<grid(work0, false), TC_THREADS, SMEM, stream>>>(qm, km, tp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long rows = pairs * R;
@@ -751,12 +794,18 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
         const long long work2 = base * tp.col_chunks;
         if (work2 > 0x7fffffffLL) return cudaErrorInvalidValue;
         tp.n_work = (int)work2;
-        tc_scores_kernel<D, 2><<<grid(work2), TC_THREADS, SMEM, stream>>>(qm, km, tp);
+        if (kContigPays && tp.col_chunks >= 2)
+            tc_scores_kernel<D, 2, true><<<grid(work2, true), TC_THREADS, SMEM, stream>>>(qm, km,
+                                                                                         tp);
+        else
+            tc_scores_kernel<D, 2, false><<<grid(work2, false), TC_THREADS, SMEM, stream>>>(qm, km,
+                                                                                           tp);
     } else {
         const long long work1 = pairs * tp.n_col_tiles;
         if (work1 > 0x7fffffffLL) return cudaErrorInvalidValue;
         tp.n_work = (int)work1;
-        tc_scores_kernel<D, 1><<<grid(work1), TC_THREADS, SMEM, stream>>>(qm, km, tp);
+        tc_scores_kernel<D, 1, false><<<grid(work1, false), TC_THREADS, SMEM, stream>>>(qm, km,
+                                                                                       tp);
     }
     return cudaGetLastError();
 }
