@@ -49,6 +49,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the job (the slowest rank sets the job's time).
+    Without an initialised process group the values are returned as they are."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(batch: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank decodes its own batch of independent sequences (weak
+    scaling), so the job emits batch * steps * world tokens in the slowest rank's time."""
+    return batch * steps * world / (elapsed_ms / 1e3)
+
+
 def measured_tensor_peak():
     """Sustained dense bf16 TFLOP/s (the select kernels run inside a long step)."""
     try:
@@ -631,15 +647,10 @@ def run_gpu(args):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
 
-    times = torch.tensor([elapsed_ms, e2e_ms, decode_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms, decode_ms = times.tolist()
+    elapsed_ms, e2e_ms, decode_ms = max_over_ranks([elapsed_ms, e2e_ms, decode_ms], dev)
     if rank != 0:
         return
-    tokens = w.batch * args.steps * world
-    value = tokens / (elapsed_ms / 1e3)
+    value = job_tokens_per_s(w.batch, args.steps, world, elapsed_ms)
     peak, peak_kind = measured_peak()
     achieved = bytes_per_launch / (decode_ms / 1e3) / 1e9
     cpu = None
@@ -663,7 +674,8 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "avg_launch_ms": round(decode_ms, 5),
                      "traffic": kernel_traffic(R.kernel_file, R.traffic_key)},
-        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(w.batch, args.steps, world, e2e_ms), 2),
+                "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": R.launches_per_step * args.steps,
         "clocks": clocks.summary(),
