@@ -506,6 +506,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         };
         long long g = 0;
         int k = 0;
+        // MODE 2: this thread's resident row, its negated log2-sum-exp, and whose it is
+        long long nlse_id = -1;
+        float my_nlse = 0.f;
         for (int u = u_first; u < u_end; u += u_step) {
             const TcItem it = tc_item<MODE>(tp, u);
             const int b = it.pair / p.Hkv, kh = it.pair % p.Hkv;
@@ -574,10 +577,28 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 if (it.n_tiles == 0) continue;
                 // resident rows fixed_row0 .. +127 hold whole heads: per key tile, each thread
                 // sums its key's column over each head and writes it (lse_buf holds -lse)
-                const float *lse_g = p.row_lse2 + (size_t)it.pair * R;
                 float *lse_buf = sm_lse + (k & 1) * TC_ROWS;
-                if (set == 0)
-                    lse_buf[et] = (it.fixed_row0 + et < R) ? -lse_g[it.fixed_row0 + et] : 0.f;
+                if (set == 0) {
+                    // the row's log2-sum-exp from pass 1's per-chunk (max, sum) states, when
+                    // the resident row block changes (same arithmetic as rowlse_tc_kernel)
+                    const long long id = fixed_id(it);
+                    if (id != nlse_id) {
+                        nlse_id = id;
+                        const int r = it.fixed_row0 + et;
+                        my_nlse = 0.f;
+                        if (r < R) {
+                            const float *st = p.row_ml + ((size_t)it.pair * p.n_chunks * R + r) * 2;
+                            const size_t cstep = (size_t)R * 2;
+                            float M = kNegBig;
+                            for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, st[c * cstep]);
+                            float Z = 0.f;
+                            for (int c = 0; c < p.n_chunks; ++c)
+                                Z += st[c * cstep + 1] * exp2f(st[c * cstep] - M);
+                            my_nlse = -(M + log2f(Z));
+                        }
+                    }
+                    lse_buf[et] = my_nlse;
+                }
                 epilogue_sync(NSETS);
                 float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
                 const int rows_blk = min(TC_ROWS, R - it.fixed_row0);
@@ -779,12 +800,17 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
         tc_scores_kernel<D, 0, false><<<grid(work0, false), TC_THREADS, SMEM, stream>>>(qm, km, tp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long long rows = pairs * R;
-    rowlse_tc_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(sp);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || tp.n_col_tiles == 0) return e;
     const int n_rb = (R + TC_ROWS - 1) / TC_ROWS;
-    if (R <= TC_ROWS || (sp.G > 1 && TC_ROWS % sp.L_obs == 0)) {
+    const bool rows_resident = R <= TC_ROWS || (sp.G > 1 && TC_ROWS % sp.L_obs == 0);
+    // the column pass with resident rows folds each row's chunk states itself; with streamed
+    // rows (or no column pass) the row log-sum-exp values are written first
+    if (!rows_resident || tp.n_col_tiles == 0) {
+        const long long rows = pairs * R;
+        rowlse_tc_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(sp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess || tp.n_col_tiles == 0) return e;
+    }
+    if (rows_resident) {
         // every head inside one row block: keep the row block, stream the key tiles
         const long long base = pairs * n_rb;
         long long chunks = (4LL * n_sm + base - 1) / base;
