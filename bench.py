@@ -313,6 +313,8 @@ class SelectDecode(DecodeWorkload):
         L, B, Hkv, D = w.layers, w.batch, w.n_heads_kv, w.d_head
         self.pyramid = pyramid
         if pyramid:
+            self.traffic_key = "decode_mma/pyramid"
+        if pyramid:
             self.budgets = kvc.kvc_pyramid_budgets(L, w.budget, w.pyramid_ratio, 1)
         else:
             self.budgets = [w.budget] * L
@@ -337,6 +339,7 @@ class SelectDecode(DecodeWorkload):
                 kvc.kvc_snapkv_select(q_obs, k, seq_len=w.prompt, L_obs=w.L_obs,
                                       budget=self.budgets[l], scale=w.scale, pool_k=w.pool_k,
                                       idx_out=idx, ws=ws)
+                kvc.kvc_compact_gather(k, v, idx, self.budgets[l], Kc, Vc, len_dst=self.lens[l])
                 warm = False
             flush.fill_(l & 0xff)
             torch.cuda.synchronize()
@@ -366,6 +369,7 @@ class SelectDecode(DecodeWorkload):
         self.extra["snapkv_select"] = {
             "layers": L, "select_ms": round(sum(sel_ms), 3),
             "compact_ms": round(sum(gat_ms), 3),
+            "compact_ms_max_layer": round(max(gat_ms), 3),
             "select_roofline_ms": round(sel_roof, 3),
             "select_frac": round(sel_roof / sum(sel_ms), 4),
             "compact_roofline_ms": round(gat_roof, 3),
