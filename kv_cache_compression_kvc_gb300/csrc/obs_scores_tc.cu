@@ -64,6 +64,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
+// The same load with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap *map, int c0,
+                                                 int c1, int c2, int c3, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+        "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 __device__ __forceinline__ void tc_fence_before()
 {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -359,6 +377,10 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         long long g = 0;                            // streamed tiles so far
         int nrl = 0;                                // resident-tile loads so far
         long long prev_id = -1;
+        // keys streamed once per pass (one row tile per pair) are marked evict-first, so that
+        // what the pass writes (and the next kernel reads) is not pushed out of L2 by them
+        const bool once = MODE != 1 && tp.n_mtiles == 1;
+        const uint64_t pol = l2_evict_first_policy();
         for (int u = u_first; u < u_end; u += u_step) {
             const TcItem it = tc_item<MODE>(tp, u);
             if (it.n_tiles == 0) continue;
@@ -388,7 +410,10 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 const uint32_t dst = stage0 + s * TILE_BYTES;
                 mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
                 for (int a = 0; a < SUBS; ++a) {
-                    if (MODE != 1)
+                    if (MODE != 1 && once)
+                        tma_load_4d_hint(dst + a * TC_SUB_BYTES, &kmap, a * 64,
+                                         (it.t_begin + i) * TC_ROWS, kh, b, bar_full + 8 * s, pol);
+                    else if (MODE != 1)
                         tma_load_4d(dst + a * TC_SUB_BYTES, &kmap, a * 64,
                                     (it.t_begin + i) * TC_ROWS, kh, b, bar_full + 8 * s);
                     else
