@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import ctypes
 import dataclasses
+import datetime
 import hashlib
 import json
 import math
@@ -87,7 +88,7 @@ def measured_peak():
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -110,8 +111,14 @@ class ClockSampler:
         return self
 
     def _read(self):
+        # nvidia-smi's own timestamp dates each sample: its output reaches the pipe in bursts
         for line in self.proc.stdout:
-            self.lines.append((time.perf_counter(), line.strip()))
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except (ValueError, IndexError):
+                continue
+            self.lines.append((ts, parts[1:]))
 
     def wait_first(self, timeout=3.0):
         t0 = time.perf_counter()
@@ -119,6 +126,7 @@ class ClockSampler:
             time.sleep(0.02)
 
     def window(self, t_begin, t_end):
+        """Timed region in time.time() seconds."""
         self.t_begin, self.t_end = t_begin, t_end
 
     def __exit__(self, *exc):
@@ -135,10 +143,12 @@ class ClockSampler:
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         lo, hi = getattr(self, "t_begin", -1e30), getattr(self, "t_end", 1e30)
-        for ts, ln in self.lines:
-            if not (lo <= ts <= hi + 0.25):
-                continue
-            parts = [p.strip() for p in ln.split(",")]
+        inside = [x for x in self.lines if lo <= x[0] <= hi]
+        if not inside:
+            # a region shorter than the 200 ms period: the samples next to it
+            near = sorted(self.lines, key=lambda x: min(abs(x[0] - lo), abs(x[0] - hi)))
+            inside = [x for x in near[:2] if min(abs(x[0] - lo), abs(x[0] - hi)) < 0.3]
+        for ts, parts in inside:
             if len(parts) < 7:
                 continue
             try:
@@ -254,11 +264,12 @@ class Streaming(DecodeWorkload):
                                   t=self.t, n_sink=w.n_sink, window=w.window,
                                   cache=self.caches[l])
 
-    def decodes(self):
+    def decodes(self, flags=0):
         kvc, w = self.kvc, self.w
         for l in range(w.layers):
-            kvc.kvc_decode_attn(self.q_s[l], None, None, scale=w.scale, rope=self.rope,
-                                out=self.out[l], ws=self.ws, cache=self.caches[l])
+            kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
+                                   rope=self.rope, out=self.out[l], ws=self.ws,
+                                   cache=self.caches[l])
         kvc.kvc_position_advance(self.t, 1)
 
     def decode_bytes(self, first_step, n_steps):
@@ -392,11 +403,12 @@ class SelectDecode(DecodeWorkload):
             kvc.kvc_stream_append(None, None, kvc.KVC_APPEND_TAIL, self.k_s[l], self.v_s[l],
                                   len=self.lens[l], cache=self.caches[l])
 
-    def decodes(self):
+    def decodes(self, flags=0):
         kvc, w = self.kvc, self.w
         for l in range(w.layers):
-            kvc.kvc_decode_attn(self.q_s[l], None, None, scale=w.scale, len=self.lens[l],
-                                out=self.out[l], ws=self.ws, cache=self.caches[l])
+            kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
+                                   len=self.lens[l], out=self.out[l], ws=self.ws,
+                                   cache=self.caches[l])
 
     def decode_bytes(self, first_step, n_steps):
         tot = 0
@@ -492,12 +504,12 @@ class H2O(DecodeWorkload):
                                   self.v_s[l], t=self.t, free_slot=self.free[l],
                                   pos=self.pos[l], score=self.score[l], cache=self.caches[l])
 
-    def decodes(self):
+    def decodes(self, flags=0):
         kvc, w = self.kvc, self.w
         for l in range(w.layers):
-            kvc.kvc_decode_attn(self.q_s[l], None, None, scale=w.scale, n_valid=self.cap,
-                                out=self.out[l], logits=self.logits[l], lse=self.lse[l],
-                                ws=self.ws, cache=self.caches[l])
+            kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
+                                   n_valid=self.cap, out=self.out[l], logits=self.logits[l],
+                                   lse=self.lse[l], ws=self.ws, cache=self.caches[l])
             kvc.kvc_h2o_accumulate_evict(self.logits[l], self.lse[l], self.score[l],
                                          self.pos[l], self.free[l], n_slots=self.cap, t=self.t,
                                          L_local=w.L_local, budget=w.budget)
@@ -585,7 +597,9 @@ def run_gpu(args):
     with torch.cuda.graph(g_app):
         R.appends()
     with torch.cuda.graph(g_dec):
-        R.decodes()
+        # the appends graph has finished before this one starts, so every cache slot and length
+        # a decode reads is settled (kvc.h, KVC_DECODE_KV_SETTLED)
+        R.decodes(kvc.KVC_DECODE_KV_SETTLED)
     R.restore_state(state)
     del state
     torch.cuda.synchronize()
@@ -613,7 +627,7 @@ def run_gpu(args):
     with ClockSampler(local) as clocks:
         clocks.wait_first()
         torch.cuda.synchronize()
-        t_host0 = time.perf_counter()
+        t_host0 = time.time()
         ev_s.record(stream)
         for i in range(args.steps):
             R.load_inputs(*inputs[(args.warmup + i) % len(inputs)])
@@ -623,7 +637,7 @@ def run_gpu(args):
             marks[i][1].record(stream)
         ev_e.record(stream)
         torch.cuda.synchronize()
-        clocks.window(t_host0, time.perf_counter())
+        clocks.window(t_host0, time.time())
     barrier()
     elapsed_ms = ev_s.elapsed_time(ev_e)
     decode_ms = sum(a.elapsed_time(b) for a, b in marks) / args.steps / w.layers

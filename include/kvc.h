@@ -227,6 +227,33 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
                            float scale, float *out, float *logits, int64_t logits_stride,
                            float *lse, void *ws, size_t ws_bytes, void *stream);
 
+/* kvc_decode_attn with flags (kvc_decode_attn is this call with flags 0).  No counterpart on
+ * the pages: it lets the decode kernel overlap the kernel launched before it.
+ * KVC_DECODE_KV_SETTLED: the caller guarantees that the cache slots and the lengths (len) this
+ * call reads were last written before an ordering point that this call follows on the stream
+ * -- the start of the CUDA graph holding the call, an event the stream waited for, or a kernel
+ * launched without programmatic dependent launch (it begins only once all earlier work has
+ * finished) -- and that nothing launched between that point and this call writes them.  The
+ * kernel may then read the lengths and start loading cache tiles before it waits for the
+ * kernel launched just before it, so those loads overlap that kernel's end.  q, out, logits,
+ * lse and the workspace are always accessed only after that wait.  The flag is a permission:
+ * kernels that cannot use it ignore it.  A call that sets it when the guarantee does not hold
+ * may read stale slots or lengths.
+ * KVC_DECODE_BALANCE: with len, divide the work among thread blocks by the lengths rather than
+ * by the capacity.  By default every (batch, KV head) pair is given cap slots' worth of blocks
+ * and the slots past its length are skipped, which costs nothing when the lengths are close to
+ * cap; when they differ widely (a ragged batch) the pairs' blocks finish at very different
+ * times, and this flag balances them at the price of a scan of the lengths at the start of
+ * every block.  Same results either way (the log-sum-exp merge order may differ).
+ * Other bits must be 0 (KVC_ERR_INVALID_ARG). */
+#define KVC_DECODE_KV_SETTLED 1u
+#define KVC_DECODE_BALANCE 2u
+kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                              const int32_t *len, int32_t n_valid, const kvc_rope *rope,
+                              float scale, float *out, float *logits, int64_t logits_stride,
+                              float *lse, void *ws, size_t ws_bytes, uint32_t flags,
+                              void *stream);
+
 /* Decode attention without a caller workspace.  No counterpart on the pages: this is a
  * deployment convenience of this library.  Some callers cannot allocate device memory at the
  * point where they decode -- an engine that fixes its whole memory plan at start-up, a plugin

@@ -228,6 +228,17 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
                            float scale, float *out, float *logits, int64_t logits_stride,
                            float *lse, void *ws, size_t ws_bytes, void *stream)
 {
+    return kvc_decode_attn_ex(q, n_heads_q, cache, len, n_valid, rope, scale, out, logits,
+                              logits_stride, lse, ws, ws_bytes, 0u, stream);
+}
+
+kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                              const int32_t *len, int32_t n_valid, const kvc_rope *rope,
+                              float scale, float *out, float *logits, int64_t logits_stride,
+                              float *lse, void *ws, size_t ws_bytes, uint32_t flags, void *stream)
+{
+    if (flags & ~(uint32_t)(KVC_DECODE_KV_SETTLED | KVC_DECODE_BALANCE))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: unknown flags 0x%x", flags);
     kvc_status st = check_cache(cache, "kvc_decode_attn", true);
     if (st != KVC_OK) return st;
     if (q == nullptr || out == nullptr) return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: null q/out");
@@ -292,6 +303,8 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
     p.P = cache->batch * cache->n_heads_kv;
     p.max_seg = pl.max_seg;
     p.n_sm = n_sm > 0 ? n_sm : 152;
+    p.kv_settled = (flags & KVC_DECODE_KV_SETTLED) ? 1 : 0;
+    p.balance = (flags & KVC_DECODE_BALANCE) ? 1 : 0;
     p.dev_code = code;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;

@@ -34,7 +34,6 @@ namespace {
 constexpr int MW = 8;                        // warps per block
 constexpr int M_THREADS = MW * 32;
 constexpr float kSlack = 8.0f;               // lazy running max, log2 units
-constexpr int kCodeSchedule = 8;             // KVC_DEV_SCHEDULE
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, int c3, uint32_t bar)
@@ -87,6 +86,8 @@ __device__ __forceinline__ int cta_of(long long t, long long T, int C)
     return (int)(((t + 1) * (long long)C - 1) / T);
 }
 
+constexpr int kPrefMax = 1024;               // pairs whose tile offsets a block scans into smem
+
 template <int D, int G>
 struct MmaPlan {
     static constexpr int TK = D == 256 ? 64 : 128;             // slots per tile
@@ -98,12 +99,117 @@ struct MmaPlan {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int MERGE_BYTES = KGROUPS * G * (D + 2) * 4 + 16;
     static constexpr int BAR_BYTES = 128;
-    static constexpr int NS_fit = (220 * 1024 - 1024 - MERGE_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int PREF_BYTES = ((kPrefMax + 1) * 4 + 15) / 16 * 16;
+    static constexpr int SMEM_MAX = 227 * 1024;                 // dynamic shared memory per block
+    static constexpr int NS_fit =
+        (SMEM_MAX - 1024 - MERGE_BYTES - BAR_BYTES - PREF_BYTES) / STAGE_BYTES;
     static constexpr int NS = NS_fit > 4 ? 4 : NS_fit;
     static_assert(NS >= 2, "two stages at least");
-    static constexpr int SMEM = 1024 + NS * STAGE_BYTES + BAR_BYTES + MERGE_BYTES;
+    static constexpr int SMEM = 1024 + NS * STAGE_BYTES + BAR_BYTES + MERGE_BYTES + PREF_BYTES;
 };
 
+// Release / acquire ticket on a pair's counter (one thread, after a block barrier): the block's
+// partial state is visible to whichever block takes the last ticket.
+__device__ __forceinline__ int ticket_acq_rel(int *p)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
+// Bulk copy global -> shared memory, completion counted in bytes on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Log-sum-exp merge of the nseg partial states of one pair, segment s held in workspace slot
+// slot_of(s).  Every load of a batch of segments is issued before any is used: the merge costs
+// one L2 round trip per eight segments.
+template <int G, int D>
+__device__ __forceinline__ void merge_segments(const float *ws_o, const float *ws_ml, int slot0,
+                                               int c_lo, int nseg, float *out, float *lse,
+                                               int rows0)
+{
+    constexpr int NCH = G * D / 4;                         // 16-byte chunks of the G output rows
+    constexpr int CPT = (NCH + M_THREADS - 1) / M_THREADS; // chunks per thread
+    constexpr int UNR = 8;                                 // segments per batch of loads
+    float M[CPT], L[CPT];
+    float4 O[CPT];
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        M[k] = kNegBig;
+        L[k] = 0.f;
+        O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int s0 = 0; s0 < nseg; s0 += UNR) {
+        float4 o[CPT][UNR];
+        float m[CPT][UNR], l[CPT][UNR];
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int ch = threadIdx.x + k * M_THREADS;
+            const int g = ch * 4 / D, d = ch * 4 % D;
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int s = s0 + u;
+                if (ch < NCH && s < nseg) {
+                    const size_t st = (size_t)(s == 0 ? slot0 : 2 * (c_lo + s)) * G + g;
+                    o[k][u] = __ldcg(reinterpret_cast<const float4 *>(ws_o + st * D + d));
+                    m[k][u] = __ldcg(ws_ml + st * 2);
+                    l[k][u] = __ldcg(ws_ml + st * 2 + 1);
+                } else {
+                    o[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    m[k][u] = kNegBig;
+                    l[k][u] = 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            float mb = M[k];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) mb = fmaxf(mb, m[k][u]);
+            const float cm = ex2(M[k] - mb);
+            L[k] *= cm;
+            O[k].x *= cm; O[k].y *= cm; O[k].z *= cm; O[k].w *= cm;
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const float c = ex2(m[k][u] - mb);
+                L[k] += l[k][u] * c;
+                O[k].x += o[k][u].x * c; O[k].y += o[k][u].y * c;
+                O[k].z += o[k][u].z * c; O[k].w += o[k][u].w * c;
+            }
+            M[k] = mb;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        const int ch = threadIdx.x + k * M_THREADS;
+        if (ch >= NCH) continue;
+        const int g = ch * 4 / D, d = ch * 4 % D;
+        const bool any = L[k] > 0.f;
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (any) r = make_float4(O[k].x / L[k], O[k].y / L[k], O[k].z / L[k], O[k].w / L[k]);
+        *reinterpret_cast<float4 *>(out + (size_t)(rows0 + g) * D + d) = r;
+        if (d == 0 && lse != nullptr)
+            lse[rows0 + g] = any ? (M[k] + log2f(L[k])) * kLn2 : -INFINITY;
+    }
+}
+
+// Schedule.  The tiles of all pairs form one sequence (pair by pair, TK slots per tile) that
+// the blocks split into equal contiguous ranges.  Pair q holds tiles [pref(q), pref(q + 1)):
+//   len == nullptr:         ceil(n_valid / TK) tiles for every pair;
+//   balance, P <= kPrefMax: ceil(len[q] / TK) tiles, offsets from a block-wide scan of the
+//                           lengths (every tile holds slots, so the ranges balance the bytes
+//                           read however the lengths differ; the scan delays each block's first
+//                           load by a read of the lengths and two block barriers);
+//   otherwise:              ceil(cap / TK) tiles; tiles past the length are skipped.
+// A pair split over several blocks leaves one partial state per block: block c keeps the state
+// of the first pair of its range in workspace slot 2c and that of its last pair in slot 2c + 1
+// (a block's other pairs are complete inside its range).  The block that takes a pair's last
+// ticket merges them.
 template <int D, int G>
 __global__ void __launch_bounds__(M_THREADS, 1)
 decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -120,48 +226,125 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t stage0 = base;
     const uint32_t bars = stage0 + NS * PL::STAGE_BYTES;
-    const uint32_t bar_full = bars, bar_empty = bars + 8 * NS;
+    const uint32_t bar_full = bars, bar_empty = bars + 8 * NS, bar_merge = bars + 16 * NS;
     float *sm_m = reinterpret_cast<float *>(smem_raw + (bars + PL::BAR_BYTES - raw));
     float *sm_l = sm_m + PL::KGROUPS * G;
     float *sm_o = sm_l + PL::KGROUPS * G;      // [KGROUPS][G][D]
     int *sm_flag = reinterpret_cast<int *>(sm_o + PL::KGROUPS * G * D);
+    int *sm_pref = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(sm_m) + PL::MERGE_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kg = warp / PL::PAIRS;           // key group (16 keys of the tile)
     const int half = warp % PL::PAIRS;         // output-dim half (D = 256)
     const int gr = lane >> 2, tq = lane & 3;   // mma fragment row / column pair
     const int C = gridDim.x, cta = blockIdx.x;
-    const long long T_all = (long long)p.P * p.NT;
-    const long long t_begin = (long long)cta * T_all / C;
-    const long long t_end = (long long)(cta + 1) * T_all / C;
-    const int n_tiles = (int)(t_end - t_begin);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, MW);
         }
+        mbar_init(bar_merge, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    pdl_trigger();
-    pdl_wait();                                // inputs may come from the previous kernel
+    // Lengths and cache slots written before the previous kernel began may be read before
+    // waiting for it; everything else (q, outputs, workspace) only after.
+    if (!p.kv_settled) {
+        pdl_trigger();
+        pdl_wait();                            // inputs may come from the previous kernel
+    }
 
     auto pair_slots = [&](int q) -> int {
         if (p.len != nullptr) {
             const int n = p.len[q];
             return n < 0 ? 0 : (n > p.cap ? p.cap : n);
         }
-        return p.n_valid;
+        return p.n_valid < 0 ? 0 : (p.n_valid > p.cap ? p.cap : p.n_valid);
     };
+    const int mode = p.len == nullptr ? 0 : (p.balance && p.P <= kPrefMax ? 1 : 2);
+    const int ntq = mode == 0 ? (pair_slots(0) + TK - 1) / TK : p.NT;
+    if (mode == 1) {
+        // exclusive scan of the pairs' tile counts into sm_pref[0..P]
+        constexpr int PER = (kPrefMax + M_THREADS - 1) / M_THREADS;
+        int cnt[PER], sum = 0;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int q = threadIdx.x * PER + k;
+            cnt[k] = q < p.P ? (pair_slots(q) + TK - 1) / TK : 0;
+            sum += cnt[k];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int *wsum = reinterpret_cast<int *>(sm_m);   // MW warp totals (merge area, free now)
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int run = incl - sum;
+        for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int q = threadIdx.x * PER + k;
+            if (q < p.P) sm_pref[q] = run;
+            run += cnt[k];
+        }
+        if (threadIdx.x == M_THREADS - 1) sm_pref[p.P] = run;
+        __syncthreads();
+    }
+    auto pref = [&](int q) -> long long {
+        return mode == 1 ? (long long)sm_pref[q] : (long long)q * ntq;
+    };
+    const long long T = pref(p.P);
+    // the first Ce blocks split the tiles, each at least one (a pair's segments are then the
+    // blocks c_lo..c_hi, every one of which takes a ticket)
+    const int Ce = T < C ? (int)T : C;
+    const long long t_begin = cta < Ce ? (long long)cta * T / Ce : 0;
+    const long long t_end = cta < Ce ? (long long)(cta + 1) * T / Ce : 0;
+    const int n_tiles = (int)(t_end - t_begin);
+    // pair holding tile t < T: the last q with pref(q) <= t
+    auto pair_of = [&](long long t) -> int {
+        if (mode != 1) return (int)(t / ntq);
+        int lo = 0, hi = p.P - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm_pref[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    // tile cursors (pair q covers tiles [q_lo, q_hi)), advanced monotonically
+    struct Cursor {
+        int q;
+        long long lo, hi;
+    };
+    auto cursor_at = [&](long long t) -> Cursor {
+        Cursor c;
+        c.q = pair_of(t);
+        c.lo = pref(c.q);
+        c.hi = pref(c.q + 1);
+        return c;
+    };
+    auto advance = [&](Cursor &c, long long t) {
+        while (t >= c.hi) {
+            ++c.q;
+            c.lo = c.hi;
+            c.hi = pref(c.q + 1);
+        }
+    };
+
     // The issuing thread keeps the slot count of the pair it is loading: one global read per
     // pair, not one per tile on the critical path of every copy.
+    Cursor ic{};
     int iss_q = -1, iss_slots = 0;
     auto issue_tile = [&](int i) {
         const long long t = t_begin + i;
         const int s = i % NS;
-        const int q = (int)(t / p.NT);
-        const int j0 = (int)(t % p.NT) * TK;
+        advance(ic, t);
+        const int q = ic.q;
+        const int j0 = (int)(t - ic.lo) * TK;
         const uint32_t full = bar_full + 8 * s;
         if (q != iss_q) {
             iss_q = q;
@@ -180,18 +363,35 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             tma_load_4d(vdst + sub * TK * 128, &vmap, sub * 64, j0, kh, b, full);
         }
     };
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && n_tiles > 0) {
+        ic = cursor_at(t_begin);
         for (int i = 0; i < NS && i < n_tiles; ++i) issue_tile(i);
+    }
+    if (p.kv_settled) {
+        pdl_trigger();
+        pdl_wait();                            // q, outputs and workspace follow the previous kernel
+    }
+
+    // pairs without a tile (no valid slot) still get their rows: out = 0, lse = -inf
+    if (mode != 2) {
+        for (int q = cta; q < p.P; q += C) {
+            if (pref(q + 1) != pref(q)) continue;
+            const int rows0 = (q / p.Hkv) * p.Hq + (q % p.Hkv) * G;
+            for (int i = threadIdx.x; i < G * D; i += M_THREADS) {
+                p.out[(size_t)rows0 * D + i] = 0.f;
+                if (i % D == 0 && p.lse != nullptr) p.lse[rows0 + i / D] = -INFINITY;
+            }
+        }
+    }
 
     // ---- per-pair state ---------------------------------------------------------------------
     uint32_t qa0[KSTEPS], qa2[KSTEPS];         // q rows as A fragments (rows >= G are zero)
     float o[NB][4];
     float m_row = kNegBig, l_part = 0.f;       // row gr (head gr); l summed over the 4 lanes later
-    int cur = -1, cur_slots = 0;
+    int cur_slots = 0;
     float *lg_row = nullptr;
 
     auto start_pair = [&](int q) {
-        cur = q;
         cur_slots = pair_slots(q);
         const int b = q / p.Hkv, kh = q % p.Hkv;
         const __nv_bfloat16 *qb =
@@ -215,7 +415,79 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                      : nullptr;
     };
 
-    auto finish_pair = [&](int q) {
+    // Merge of the pair this block finishes last, its ring of stages idle by then: every partial
+    // state comes into shared memory by bulk copies issued at once (one round trip to L2 for up
+    // to GS segments), then each thread combines its 16-byte chunks of the G output rows.
+    auto merge_staged = [&](int slot0, int c_lo, int nseg, int rows0) {
+        constexpr int O_BYTES = G * D * 4, ML_BYTES = G * 8;
+        constexpr int GS = NS * PL::STAGE_BYTES / (O_BYTES + ML_BYTES);
+        static_assert(GS >= 1, "one partial state fits the ring");
+        constexpr int NCH = G * D / 4;
+        constexpr int CPT = (NCH + M_THREADS - 1) / M_THREADS;
+        const float *so = reinterpret_cast<const float *>(smem_raw + (stage0 - raw));
+        const float *sml = reinterpret_cast<const float *>(smem_raw + (stage0 - raw) + GS * O_BYTES);
+        float M[CPT], L[CPT];
+        float4 O[CPT];
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            M[k] = kNegBig;
+            L[k] = 0.f;
+            O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        uint32_t phase = 0;
+        for (int s0 = 0; s0 < nseg; s0 += GS) {
+            const int ng = min(GS, nseg - s0);
+            if (threadIdx.x == 0) {
+                // the partial states were written by other blocks through the generic proxy
+                // (made visible by the acquire); the ring was last read by this block's warps
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(bar_merge, (uint32_t)(ng * (O_BYTES + ML_BYTES)));
+                for (int u = 0; u < ng; ++u) {
+                    const int s = s0 + u;
+                    const size_t slot = (size_t)(s == 0 ? slot0 : 2 * (c_lo + s));
+                    bulk_g2s(stage0 + u * O_BYTES, p.ws_o + slot * G * D, O_BYTES, bar_merge);
+                    bulk_g2s(stage0 + GS * O_BYTES + u * ML_BYTES, p.ws_ml + slot * G * 2,
+                             ML_BYTES, bar_merge);
+                }
+            }
+            mbar_wait(bar_merge, phase & 1u, p.dev_code);
+            ++phase;
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int ch = threadIdx.x + k * M_THREADS;
+                if (ch >= NCH) continue;
+                const int g = ch * 4 / D, d = ch * 4 % D;
+                float mb = M[k];
+                for (int u = 0; u < ng; ++u) mb = fmaxf(mb, sml[u * 2 * G + 2 * g]);
+                const float cm = ex2(M[k] - mb);
+                L[k] *= cm;
+                O[k].x *= cm; O[k].y *= cm; O[k].z *= cm; O[k].w *= cm;
+                for (int u = 0; u < ng; ++u) {
+                    const float c = ex2(sml[u * 2 * G + 2 * g] - mb);
+                    const float4 v = *reinterpret_cast<const float4 *>(so + u * G * D + g * D + d);
+                    L[k] += sml[u * 2 * G + 2 * g + 1] * c;
+                    O[k].x += v.x * c; O[k].y += v.y * c; O[k].z += v.z * c; O[k].w += v.w * c;
+                }
+                M[k] = mb;
+            }
+            __syncthreads();                   // the next group's copies reuse the ring
+        }
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int ch = threadIdx.x + k * M_THREADS;
+            if (ch >= NCH) continue;
+            const int g = ch * 4 / D, d = ch * 4 % D;
+            const bool any = L[k] > 0.f;
+            float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (any) r = make_float4(O[k].x / L[k], O[k].y / L[k], O[k].z / L[k], O[k].w / L[k]);
+            *reinterpret_cast<float4 *>(p.out + (size_t)(rows0 + g) * D + d) = r;
+            if (d == 0 && p.lse != nullptr)
+                p.lse[rows0 + g] = any ? (M[k] + log2f(L[k])) * kLn2 : -INFINITY;
+        }
+    };
+
+    auto finish_pair = [&](int q, long long q_lo, long long q_hi, bool ring_idle) {
         float l_row = l_part;
         l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
         l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
@@ -232,12 +504,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
         }
         __syncthreads();
-        const long long t_first = (long long)q * p.NT;
-        const int c_lo = cta_of(t_first, T_all, C);
-        const int c_hi = cta_of(t_first + p.NT - 1, T_all, C);
-        const int nseg = c_hi - c_lo + 1, seg = cta - c_lo;
-        const bool seg_ok = nseg <= p.max_seg;
-        if (!seg_ok && threadIdx.x == 0) record_code(p.dev_code, kCodeSchedule);
+        const int c_lo = cta_of(q_lo, T, Ce);
+        const int c_hi = cta_of(q_hi - 1, T, Ce);
+        const int nseg = c_hi - c_lo + 1;
+        const int slot = 2 * cta + (t_begin < q_lo ? 1 : 0);
         const int rows0 = (q / p.Hkv) * p.Hq + (q % p.Hkv) * G;
         for (int i = threadIdx.x; i < G * D; i += M_THREADS) {
             const int g = i / D, d = i % D;
@@ -255,40 +525,49 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 p.out[(size_t)(rows0 + g) * D + d] = L > 0.f ? O / L : 0.f;
                 if (d == 0 && p.lse != nullptr)
                     p.lse[rows0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-            } else if (seg_ok) {
-                const size_t slot = ((size_t)q * p.max_seg + seg) * G + g;
-                p.ws_o[slot * D + d] = O;
+            } else {
+                const size_t st = (size_t)slot * G + g;
+                p.ws_o[st * D + d] = O;
                 if (d == 0) {
-                    p.ws_ml[slot * 2] = M;
-                    p.ws_ml[slot * 2 + 1] = L;
+                    p.ws_ml[st * 2] = M;
+                    p.ws_ml[st * 2 + 1] = L;
                 }
             }
         }
-        if (nseg > 1 && seg_ok) {
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) *sm_flag = (atomicAdd(&p.ws_cnt[q], 1) == nseg - 1);
+        __syncthreads();
+        if (nseg > 1) {
+            if (threadIdx.x == 0) *sm_flag = (ticket_acq_rel(&p.ws_cnt[q]) == nseg - 1);
             __syncthreads();
             if (*sm_flag) {
-                __threadfence();
-                merge_pair_partials<G, D, M_THREADS>(p.ws_o, p.ws_ml, p.max_seg, q, nseg, p.out,
-                                                    p.lse, rows0, sm_o, PL::KGROUPS * G * D);
+                const long long tb_lo = (long long)c_lo * T / Ce;  // first tile of block c_lo
+                const int slot0 = 2 * c_lo + (tb_lo < q_lo ? 1 : 0);
+                if (ring_idle && nseg > 8)         // one batch of register loads covers <= 8
+                    merge_staged(slot0, c_lo, nseg, rows0);
+                else
+                    merge_segments<G, D>(p.ws_o, p.ws_ml, slot0, c_lo, nseg, p.out, p.lse, rows0);
                 if (threadIdx.x == 0) p.ws_cnt[q] = 0;
             }
+            __syncthreads();
         }
-        __syncthreads();
     };
 
+    Cursor mc{};
+    if (n_tiles > 0) mc = cursor_at(t_begin);
+    int cur = -1;
+    long long cur_lo = 0, cur_hi = 0;
     for (int i = 0; i < n_tiles; ++i) {
         const long long t = t_begin + i;
         const int s = i % NS;
-        const int q = (int)(t / p.NT);
-        if (q != cur) {
-            if (cur >= 0) finish_pair(cur);
-            start_pair(q);
+        advance(mc, t);
+        if (mc.q != cur) {
+            if (cur >= 0) finish_pair(cur, cur_lo, cur_hi, false);
+            cur = mc.q;
+            cur_lo = mc.lo;
+            cur_hi = mc.hi;
+            start_pair(cur);
         }
         mbar_wait(bar_full + 8 * s, (i / NS) & 1, p.dev_code);
-        const int j0 = (int)(t % p.NT) * TK;
+        const int j0 = (int)(t - cur_lo) * TK;
         const int key0 = kg * 16;                          // this warp's 16 keys in the tile
         if (j0 + key0 < cur_slots) {
             const uint32_t kst = stage0 + s * PL::STAGE_BYTES, vst = kst + PL::TILE_BYTES;
@@ -376,7 +655,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             issue_tile(i + NS);
         }
     }
-    if (cur >= 0) finish_pair(cur);
+    if (cur >= 0) finish_pair(cur, cur_lo, cur_hi, true);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
@@ -428,7 +707,11 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream, bool *used)
     DecodeParams q = p;
     q.NT = p.cap > 0 ? (p.cap + PL::TK - 1) / PL::TK : 1;
     const long long T_all = (long long)q.P * q.NT;
-    const int C = (int)(T_all < p.n_sm ? T_all : p.n_sm);
+    long long C = T_all < p.n_sm ? T_all : p.n_sm;
+    // two partial-state slots per block in the workspace
+    const long long slots = (long long)q.P * q.max_seg;
+    if (2 * C > slots) C = slots / 2;
+    if (C < 1) C = 1;
     *used = true;
     return launch_pdl(decode_mma_kernel<D, G>, dim3((unsigned)C), dim3(M_THREADS), (size_t)PL::SMEM,
                       stream, km, vm, q);

@@ -44,6 +44,8 @@ struct DecodeParams {
     const int64_t *t;
     const float *cos_sin;        // [n_pos][2][D/2]: cosines then sines per distance
     int32_t n_pos;               // rows of cos_sin
+    int32_t kv_settled;          // cache slots and lengths final before the previous launch began
+    int32_t balance;             // split the tiles by the lengths (not by capacity)
     float scale_log2;            // scale * log2(e)
     float *out;                  // [B][Hq][D]
     float *logits;               // nullable, [B*Hq][logits_stride]

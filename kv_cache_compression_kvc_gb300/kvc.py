@@ -19,6 +19,8 @@ from . import build as _build
 KVC_OK = 0
 KVC_F32, KVC_BF16 = 0, 1
 KVC_APPEND_TAIL, KVC_APPEND_RING, KVC_APPEND_FREE_SLOT = 0, 1, 2
+KVC_DECODE_KV_SETTLED = 1
+KVC_DECODE_BALANCE = 2
 STATUS_NAMES = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_SHAPE", 3: "KVC_ERR_ALIGN",
                 4: "KVC_ERR_CAPACITY", 5: "KVC_ERR_CUDA", 6: "KVC_ERR_WORKSPACE",
                 7: "KVC_ERR_DEVICE"}
@@ -49,6 +51,7 @@ _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _U64 = ctypes.c_uint64
 _SZ = ctypes.c_size_t
+_U32 = ctypes.c_uint32
 _F32 = ctypes.c_float
 _CACHE_P = ctypes.POINTER(kvc_cache)
 _ROPE_P = ctypes.POINTER(kvc_rope)
@@ -70,6 +73,8 @@ SIGNATURES = {
     "kvc_decode_attn_workspace_bytes": (_SZ, [_I32] * 5),
     "kvc_decode_attn": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P, _I64, _P,
                                _P, _SZ, _P]),
+    "kvc_decode_attn_ex": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P, _I64,
+                                  _P, _P, _SZ, _U32, _P]),
     "kvc_decode_attn_noalloc": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P,
                                        _I64, _P, _P]),
     "kvc_h2o_accumulate_evict": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P,
@@ -227,6 +232,28 @@ def kvc_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
         _ptr(q), Hq, ctypes.byref(c), _ptr(len), -1 if n_valid is None else int(n_valid),
         ctypes.byref(rope) if rope is not None else None, float(scale), _ptr(out),
         _ptr(logits), lstride, _ptr(lse), wp, wb, _stream(stream)))
+    return out
+
+
+def kvc_decode_attn_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+                       scale: float, flags: int = 0, len: Optional[torch.Tensor] = None,
+                       n_valid: Optional[int] = None, rope: Optional[kvc_rope] = None,
+                       out: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                       stream=None, cache: Optional[kvc_cache] = None) -> torch.Tensor:
+    """kvc_decode_attn with flags (KVC_DECODE_KV_SETTLED: see kvc.h for the caller's promise)."""
+    c = cache if cache is not None else cache_view(k_cache, v_cache)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(B, Hq, c.n_heads_kv, D, c.cap, q.device)
+    wp, wb = _ws_ptr(ws)
+    lstride = logits.stride(-2) if logits is not None else 0
+    _check(load().kvc_decode_attn_ex(
+        _ptr(q), Hq, ctypes.byref(c), _ptr(len), -1 if n_valid is None else int(n_valid),
+        ctypes.byref(rope) if rope is not None else None, float(scale), _ptr(out),
+        _ptr(logits), lstride, _ptr(lse), wp, wb, int(flags), _stream(stream)))
     return out
 
 

@@ -88,6 +88,9 @@ def test_validation_rejects_bad_calls_before_launch(kvc):
     st = lib.kvc_decode_attn(4096, 1, ctypes.byref(c), None, 17, None, 1.0, 4096, None, 0, None,
                              None, 0, None)
     assert st == 4                                                 # n_valid > cap
+    st = lib.kvc_decode_attn_ex(4096, 1, ctypes.byref(c), None, 4, None, 1.0, 4096, None, 0,
+                                None, None, 0, 4, None)
+    assert st == 1 and "flags" in kvc.kvc_last_error()            # unknown flag bit
     st = lib.kvc_stream_append(ctypes.byref(c), 7, 4096, 4096, None, None, 0, 0, None, None, 0,
                                None, 0, None)
     assert st == 1                                                 # bad policy

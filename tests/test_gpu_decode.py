@@ -68,6 +68,66 @@ def test_decode_host_n_valid_and_empty(dtype):
             assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
 
 
+@pytest.mark.parametrize("D,G", [(128, 4), (256, 6), (64, 8)])
+@pytest.mark.parametrize("case", ["ragged", "one_pair", "many_pairs"])
+def test_gqa_decode_schedules(D, G, case):
+    """Tensor-core group decode under both schedules -- blocks split by capacity (default) and
+    by the lengths (KVC_DECODE_BALANCE; capacity again past 1024 pairs) -- on ragged pairs with
+    empty and full ones, one pair split over every block, and many pairs.  Both orderings of
+    the first loads (KVC_DECODE_KV_SETTLED or not) give the same bits."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    dtype = torch.bfloat16
+    if case == "ragged":
+        B, Hkv, cap = 5, 4, 2000
+    elif case == "one_pair":
+        B, Hkv, cap = 1, 1, 20000
+    else:
+        B, Hkv, cap = 65, 16, 200
+    Hq = Hkv * G
+    seed = 100 + D + G + len(case)
+    K = I.randn((B, Hkv, cap, D), seed, dev, dtype)
+    V = I.randn((B, Hkv, cap, D), seed + 1, dev, dtype)
+    q = I.randn((B, Hq, D), seed + 2, dev, dtype)
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, cap + 1, size=(B, Hkv))
+    if case == "ragged":
+        lens.flat[:4] = [0, cap, 1, 129]
+    elif case == "one_pair":
+        lens[:] = cap
+    else:
+        lens.flat[:3] = [0, cap, 1]
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev).flatten()
+    scale = 1 / math.sqrt(D)
+    S, BAL = kvc.KVC_DECODE_KV_SETTLED, kvc.KVC_DECODE_BALANCE
+    outs = {}
+    for flags in (0, S, BAL, S | BAL):
+        lse = torch.empty((B, Hq), device=dev)
+        out = kvc.kvc_decode_attn_ex(q, K, V, scale=scale, flags=flags, len=lens_t, lse=lse)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status() == 0
+        outs[flags] = (out.cpu(), lse.cpu())
+    for a, b in ((0, S), (BAL, S | BAL)):
+        assert torch.equal(outs[a][0], outs[b][0]) and torch.equal(outs[a][1], outs[b][1])
+    if case == "many_pairs":                 # a sample of the heads
+        heads = [(b, h) for b in range(B) for h in range(Hq)]
+        pick = rng.choice(len(heads), size=300, replace=False)
+        heads = [heads[i] for i in pick] + [(0, g) for g in range(G)]
+    else:
+        heads = [(b, h) for b in range(B) for h in range(Hq)]
+    Kc, Vc, qh = K.cpu(), V.cpu(), f64(q)
+    for b, h in heads:
+        n = int(lens[b, h // G])
+        o, _, ls = oracle.attend(qh[b, h], f64(Kc[b, h // G, :n]), f64(Vc[b, h // G, :n]), scale)
+        for flags in (0, BAL):
+            out, lse = outs[flags]
+            assert_close(out[b, h].numpy(), o, TOL[dtype], f"out ({b},{h}) n={n} flags={flags}")
+            if n == 0:
+                assert torch.all(out[b, h] == 0) and math.isinf(float(lse[b, h]))
+            else:
+                assert abs(float(lse[b, h]) - ls) <= 1e-3, (b, h, flags, float(lse[b, h]), ls)
+
+
 def test_decode_strided_cache_view():
     """A cache that is a slice of a larger buffer (slot stride > d_head, capacity padding)."""
     dev = cuda_or_skip()

@@ -75,3 +75,28 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     with contextlib.redirect_stdout(out):
         assert bench.run_reference(args) is None
     assert out.getvalue() == "", "a non-zero rank prints nothing and does no work"
+
+
+def test_clock_samples_are_dated_by_their_own_timestamps():
+    """Samples inside the timed region count; a region shorter than the sampling period takes
+    the samples next to it; hardware slowdowns are reported."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import datetime
+    c = bench.ClockSampler(0)
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+
+    def line(dt_s, sm, slow="Not Active"):
+        ts = (base + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, {sm}, 2070, 900.0, {slow}, Not Active, Not Active, Not Active\n"
+
+    c.proc = types.SimpleNamespace(stdout=io.StringIO(
+        line(0.0, 1500) + line(0.2, 2070) + line(0.4, 2070, "Active") + line(0.6, 1980)))
+    c._read()
+    t0 = base.timestamp()
+    c.window(t0 + 0.1, t0 + 0.5)
+    got = c.summary()
+    assert got["samples"] == 2 and got["sm_mhz"] == 2070.0 and got["reasons"] == ["hw_slowdown"]
+    c.window(t0 + 0.62, t0 + 0.7)            # no sample inside: the nearest ones
+    got = c.summary()
+    assert got["samples"] >= 1 and 1980.0 <= got["sm_mhz"] <= 2070.0
