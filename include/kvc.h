@@ -229,16 +229,16 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
 
 /* kvc_decode_attn with flags (kvc_decode_attn is this call with flags 0).  No counterpart on
  * the pages: it lets the decode kernel overlap the kernel launched before it.
- * KVC_DECODE_KV_SETTLED: the caller guarantees that the cache slots and the lengths (len) this
- * call reads were last written before an ordering point that this call follows on the stream
- * -- the start of the CUDA graph holding the call, an event the stream waited for, or a kernel
- * launched without programmatic dependent launch (it begins only once all earlier work has
- * finished) -- and that nothing launched between that point and this call writes them.  The
- * kernel may then read the lengths and start loading cache tiles before it waits for the
- * kernel launched just before it, so those loads overlap that kernel's end.  q, out, logits,
- * lse and the workspace are always accessed only after that wait.  The flag is a permission:
- * kernels that cannot use it ignore it.  A call that sets it when the guarantee does not hold
- * may read stale slots or lengths.
+ * KVC_DECODE_KV_SETTLED: the caller guarantees that the cache slots, the lengths (len) and,
+ * with rope, the decode position *rope->t that this call reads were last written before an
+ * ordering point that this call follows on the stream -- the start of the CUDA graph holding
+ * the call, an event the stream waited for, or a kernel launched without programmatic
+ * dependent launch (it begins only once all earlier work has finished) -- and that nothing
+ * launched between that point and this call writes them.  The kernel may then read them and
+ * start loading cache tiles before it waits for the kernel launched just before it, so those
+ * loads overlap that kernel's end.  q, out, logits, lse and the workspace are always accessed
+ * only after that wait.  The flag is a permission: kernels that cannot use it ignore it.  A
+ * call that sets it when the guarantee does not hold may read stale slots or lengths.
  * KVC_DECODE_BALANCE: with len, divide the work among thread blocks by the lengths rather than
  * by the capacity.  By default every (batch, KV head) pair is given cap slots' worth of blocks
  * and the slots past its length are skipped, which costs nothing when the lengths are close to

@@ -166,8 +166,12 @@ decode_attn_kernel(const DecodeParams p)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    pdl_trigger();
-    pdl_wait();                                      // inputs may come from the previous kernel
+    // With a settled cache the position, the lengths and the first tiles are read before
+    // waiting for the previous kernel; q, the outputs and the workspace always after.
+    if (!p.kv_settled) {
+        pdl_trigger();
+        pdl_wait();                                  // inputs may come from the previous kernel
+    }
 
     // ---- decode position (StreamingLLM layout) --------------------------------------------
     // With RoPE the tiles run over ranks: rank r < S is sink slot r; rank r >= S is ring token
@@ -264,6 +268,10 @@ decode_attn_kernel(const DecodeParams p)
     };
     if (threadIdx.x == 0)
         for (int i = 0; i < NS && i < n_tiles; ++i) issue_tile(i);
+    if (p.kv_settled) {
+        pdl_trigger();
+        pdl_wait();
+    }
 
     // ================================= compute ===================================================
     const int lk = lane % LPK;

@@ -42,6 +42,13 @@ def test_decode_matches_oracle_ragged(dtype, D, G):
     lse = torch.empty((B, Hq), device=dev)
     out = kvc.kvc_decode_attn(q, K, V, scale=scale, len=lens.flatten(), logits=logits, lse=lse)
     assert kvc.kvc_device_status() == 0
+    # the settled-cache load order gives the same bits
+    lg2, lse2 = torch.full_like(logits, float("nan")), torch.empty_like(lse)
+    out2 = kvc.kvc_decode_attn_ex(q, K, V, scale=scale, flags=kvc.KVC_DECODE_KV_SETTLED,
+                                  len=lens.flatten(), logits=lg2, lse=lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert torch.equal(torch.nan_to_num(logits, 7.0), torch.nan_to_num(lg2, 7.0))
     ref, ref_lg, ref_lse = _oracle_decode(q, K, V, lens.cpu().numpy(), scale, G)
     assert_close(out.cpu(), ref, TOL[dtype], "decode out")
     assert_close(lse.cpu(), ref_lse, 1e-4, "lse")
@@ -215,7 +222,12 @@ def test_streaming_ring_rope_matches_oracle_every_step(dtype, D, G, S, W, extra,
         t_dev.fill_(t)
         kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_RING, ks[t], vs[t], t=t_dev, n_sink=S,
                               window=W)
-        out = kvc.kvc_decode_attn(qs[t], K, V, scale=scale, rope=rope).cpu().numpy()
+        out_t = kvc.kvc_decode_attn(qs[t], K, V, scale=scale, rope=rope)
+        t_dev.add_(0)        # a plain kernel: an ordering point after the append (kvc.h)
+        out_s = kvc.kvc_decode_attn_ex(qs[t], K, V, scale=scale, rope=rope,
+                                       flags=kvc.KVC_DECODE_KV_SETTLED)
+        assert torch.equal(out_t, out_s), "settled-cache load order changed the result"
+        out = out_t.cpu().numpy()
         for b in range(B):
             for h in range(Hq):
                 ref = oracle.stream_decode(t, S, W, f64(qs[t, b, h]), hk[:t + 1, b, h // G],
