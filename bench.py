@@ -488,6 +488,9 @@ class H2O(DecodeWorkload):
         self.caches = [kvc.cache_view(self.K[l], self.V[l]) for l in range(L)]
         self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.cap, dev)
         self.launches_per_step = 3 * L + 1
+        # the score update of layer l runs on a second stream beside the decode of layer l + 1
+        self.side = torch.cuda.Stream(device=dev)
+        self.done = [torch.cuda.Event() for _ in range(L)]
 
     def save_state(self):
         return (self.t.clone(), self.free.clone(), self.pos.clone(), self.score.clone(),
@@ -505,14 +508,22 @@ class H2O(DecodeWorkload):
                                   pos=self.pos[l], score=self.score[l], cache=self.caches[l])
 
     def decodes(self, flags=0):
+        # Nothing in the decode of layer l + 1 reads layer l's scores or freed slot (only the
+        # next step's append into layer l does), so each layer's accumulate/evict runs on a
+        # second stream once that layer's logits are out; the streams join before the
+        # position advance that ends the step.
         kvc, w = self.kvc, self.w
+        main = torch.cuda.current_stream()
         for l in range(w.layers):
             kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
                                    n_valid=self.cap, out=self.out[l], logits=self.logits[l],
                                    lse=self.lse[l], ws=self.ws, cache=self.caches[l])
+            self.done[l].record(main)
+            self.side.wait_event(self.done[l])
             kvc.kvc_h2o_accumulate_evict(self.logits[l], self.lse[l], self.score[l],
                                          self.pos[l], self.free[l], n_slots=self.cap, t=self.t,
-                                         L_local=w.L_local, budget=w.budget)
+                                         L_local=w.L_local, budget=w.budget, stream=self.side)
+        main.wait_stream(self.side)
         kvc.kvc_position_advance(self.t, 1)
 
     def decode_bytes(self, first_step, n_steps):
@@ -526,7 +537,9 @@ class H2O(DecodeWorkload):
                 "batch": w.batch, "n_heads": w.n_heads_q, "d_head": w.d_head,
                 "prompt": w.prompt, "budget": w.budget, "L_local": w.L_local,
                 "K_hh": w.budget - w.L_local, "kv_dtype": "bf16", "l2": "inputs larger than L2",
-                "graph": "appends, then decode + accumulate/evict per layer, as two CUDA graphs"}
+                "graph": "appends, then decode + accumulate/evict per layer (the update of "
+                         "layer l on a second stream beside the decode of layer l + 1), as two "
+                         "CUDA graphs"}
 
     def oracle_sample(self, budget_s=12.0):
         import oracle
