@@ -437,13 +437,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         uint32_t phase = 0;
         for (int s0 = 0; s0 < nseg; s0 += GS) {
             const int ng = min(GS, nseg - s0);
-            if (threadIdx.x == 0) {
+            if (warp == 0) {
                 // the partial states were written by other blocks through the generic proxy
                 // (made visible by the acquire); the ring was last read by this block's warps
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(bar_merge, (uint32_t)(ng * (O_BYTES + ML_BYTES)));
-                for (int u = 0; u < ng; ++u) {
+                if (lane == 0)
+                    mbar_arrive_expect_tx(bar_merge, (uint32_t)(ng * (O_BYTES + ML_BYTES)));
+                __syncwarp();
+                for (int u = lane; u < ng; u += 32) {       // the copies issued by 32 lanes
                     const int s = s0 + u;
                     const size_t slot = (size_t)(s == 0 ? slot0 : 2 * (c_lo + s));
                     bulk_g2s(stage0 + u * O_BYTES, p.ws_o + slot * G * D, O_BYTES, bar_merge);
