@@ -212,6 +212,31 @@ class DecodeWorkload:
         v = torch.randn(shp_k, generator=g, device=self.dev).to(w.dtype)
         return q, k, v
 
+    def append_layer(self, l):
+        raise NotImplementedError
+
+    def decode_layer(self, l, flags=0):
+        raise NotImplementedError
+
+    def end_step(self):
+        pass
+
+    def appends(self):
+        for l in range(self.w.layers):
+            self.append_layer(l)
+
+    def decodes(self, flags=0):
+        for l in range(self.w.layers):
+            self.decode_layer(l, flags)
+        self.end_step()
+
+    def step_interleaved(self):
+        """One step as a model runs it: per layer, append the new token, then attend."""
+        for l in range(self.w.layers):
+            self.append_layer(l)
+            self.decode_layer(l)
+        self.end_step()
+
     def load_inputs(self, q, k, v):
         self.q_s.copy_(q, non_blocking=True)
         self.k_s.copy_(k, non_blocking=True)
@@ -257,20 +282,20 @@ class Streaming(DecodeWorkload):
     def restore_state(self, st):
         self.t.copy_(st)
 
-    def appends(self):
-        kvc, w = self.kvc, self.w
-        for l in range(w.layers):
-            kvc.kvc_stream_append(None, None, kvc.KVC_APPEND_RING, self.k_s[l], self.v_s[l],
-                                  t=self.t, n_sink=w.n_sink, window=w.window,
-                                  cache=self.caches[l])
-
-    def decodes(self, flags=0):
-        kvc, w = self.kvc, self.w
-        for l in range(w.layers):
-            kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
-                                   rope=self.rope, out=self.out[l], ws=self.ws,
+    def append_layer(self, l):
+        w = self.w
+        self.kvc.kvc_stream_append(None, None, self.kvc.KVC_APPEND_RING, self.k_s[l],
+                                   self.v_s[l], t=self.t, n_sink=w.n_sink, window=w.window,
                                    cache=self.caches[l])
-        kvc.kvc_position_advance(self.t, 1)
+
+    def decode_layer(self, l, flags=0):
+        w = self.w
+        self.kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
+                                    rope=self.rope, out=self.out[l], ws=self.ws,
+                                    cache=self.caches[l])
+
+    def end_step(self):
+        self.kvc.kvc_position_advance(self.t, 1)
 
     def decode_bytes(self, first_step, n_steps):
         """Algorithmic bytes of one decode launch: the attended K and V rows once, q and out."""
@@ -397,18 +422,14 @@ class SelectDecode(DecodeWorkload):
     def restore_state(self, st):
         self.lens.copy_(st)
 
-    def appends(self):
-        kvc = self.kvc
-        for l in range(self.w.layers):
-            kvc.kvc_stream_append(None, None, kvc.KVC_APPEND_TAIL, self.k_s[l], self.v_s[l],
-                                  len=self.lens[l], cache=self.caches[l])
+    def append_layer(self, l):
+        self.kvc.kvc_stream_append(None, None, self.kvc.KVC_APPEND_TAIL, self.k_s[l],
+                                   self.v_s[l], len=self.lens[l], cache=self.caches[l])
 
-    def decodes(self, flags=0):
-        kvc, w = self.kvc, self.w
-        for l in range(w.layers):
-            kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
-                                   len=self.lens[l], out=self.out[l], ws=self.ws,
-                                   cache=self.caches[l])
+    def decode_layer(self, l, flags=0):
+        self.kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=self.w.scale, flags=flags,
+                                    len=self.lens[l], out=self.out[l], ws=self.ws,
+                                    cache=self.caches[l])
 
     def decode_bytes(self, first_step, n_steps):
         tot = 0
@@ -500,31 +521,29 @@ class H2O(DecodeWorkload):
         for dst, src in zip((self.t, self.free, self.pos, self.score, self.K, self.V), st):
             dst.copy_(src)
 
-    def appends(self):
-        kvc = self.kvc
-        for l in range(self.w.layers):
-            kvc.kvc_stream_append(None, None, kvc.KVC_APPEND_FREE_SLOT, self.k_s[l],
-                                  self.v_s[l], t=self.t, free_slot=self.free[l],
-                                  pos=self.pos[l], score=self.score[l], cache=self.caches[l])
+    def append_layer(self, l):
+        self.kvc.kvc_stream_append(None, None, self.kvc.KVC_APPEND_FREE_SLOT, self.k_s[l],
+                                   self.v_s[l], t=self.t, free_slot=self.free[l],
+                                   pos=self.pos[l], score=self.score[l], cache=self.caches[l])
 
-    def decodes(self, flags=0):
+    def decode_layer(self, l, flags=0):
         # Nothing in the decode of layer l + 1 reads layer l's scores or freed slot (only the
         # next step's append into layer l does), so each layer's accumulate/evict runs on a
-        # second stream once that layer's logits are out; the streams join before the
-        # position advance that ends the step.
+        # second stream once that layer's logits are out; end_step joins the streams before
+        # the position advance.
         kvc, w = self.kvc, self.w
-        main = torch.cuda.current_stream()
-        for l in range(w.layers):
-            kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
-                                   n_valid=self.cap, out=self.out[l], logits=self.logits[l],
-                                   lse=self.lse[l], ws=self.ws, cache=self.caches[l])
-            self.done[l].record(main)
-            self.side.wait_event(self.done[l])
-            kvc.kvc_h2o_accumulate_evict(self.logits[l], self.lse[l], self.score[l],
-                                         self.pos[l], self.free[l], n_slots=self.cap, t=self.t,
-                                         L_local=w.L_local, budget=w.budget, stream=self.side)
-        main.wait_stream(self.side)
-        kvc.kvc_position_advance(self.t, 1)
+        kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
+                               n_valid=self.cap, out=self.out[l], logits=self.logits[l],
+                               lse=self.lse[l], ws=self.ws, cache=self.caches[l])
+        self.done[l].record(torch.cuda.current_stream())
+        self.side.wait_event(self.done[l])
+        kvc.kvc_h2o_accumulate_evict(self.logits[l], self.lse[l], self.score[l],
+                                     self.pos[l], self.free[l], n_slots=self.cap, t=self.t,
+                                     L_local=w.L_local, budget=w.budget, stream=self.side)
+
+    def end_step(self):
+        torch.cuda.current_stream().wait_stream(self.side)
+        self.kvc.kvc_position_advance(self.t, 1)
 
     def decode_bytes(self, first_step, n_steps):
         w = self.w
@@ -670,8 +689,7 @@ def run_gpu(args):
     e0.record(stream)
     for i in range(args.steps):
         R.load_inputs(*host_in[i % total])
-        R.appends()
-        R.decodes()
+        R.step_interleaved()
         host_out.copy_(R.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
