@@ -7,7 +7,7 @@ with gcc into ``oracle/_build/``.  This module only marshals numpy arrays.
 
 Functions (each follows the page passage cited in ``kvc_oracle.c``):
   kv_bytes, pyramid_budgets, rope, attend, stream_window, stream_slot, stream_decode,
-  topk_ascending, snapkv_obs_scores, pool1d, snapkv_select, snapkv_stage_f32,
+  stream_decode_alibi, topk_ascending, snapkv_obs_scores, pool1d, snapkv_select, snapkv_stage_f32,
   h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_evict_f32.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against values the pages
@@ -63,6 +63,8 @@ _SIGS = {
     "orc_stream_slot": (_i64, [_i64, ctypes.c_int, ctypes.c_int]),
     "orc_stream_decode": (None, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64, _f64,
                                  _ptr, _ptr, _ptr, _ptr]),
+    "orc_stream_decode_alibi": (None, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64,
+                                       _f64, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
     "orc_topk_ascending": (None, [ctypes.c_int, ctypes.c_int, _ptr, _ptr]),
     "orc_snapkv_obs_scores": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64, _ptr,
                                      _ptr, _ptr]),
@@ -156,6 +158,21 @@ def stream_decode(t: int, S: int, W: int, q_pre, hist_k, hist_v, scale: float,
     out = np.empty(D)
     lib().orc_stream_decode(int(t), S, W, D, theta, scale, _p(q_pre), _p(hk), _p(hv), _p(out))
     return out
+
+
+def stream_decode_alibi(t: int, S: int, W: int, q, hist_k, hist_v, scale: float, slope: float):
+    """StreamingLLM decode with ALiBi at in-cache positions -> (out, logits in rank order, lse)."""
+    q = _f(q)
+    D = q.shape[0]
+    hk, hv = _f(hist_k), _f(hist_v)
+    assert hk.shape[0] >= t + 1 and hv.shape[0] >= t + 1 and hk.shape[1] == D
+    out = np.empty(D)
+    logits = np.empty(S + W + 1)
+    lse = np.empty(1)
+    lib().orc_stream_decode_alibi(int(t), S, W, D, float(slope), float(scale), _p(q), _p(hk),
+                                  _p(hv), _p(out), _p(logits), _p(lse))
+    n = min(int(t) + 1, S + W + 1)
+    return out, logits[:n].copy(), float(lse[0])
 
 
 def topk_ascending(score, k: int) -> np.ndarray:

@@ -182,6 +182,42 @@ void orc_stream_decode(int64_t t, int S, int W, int D, double theta, double scal
     free(tok); free(cpos); free(Kr); free(Vs); free(qr);
 }
 
+/* StreamingLLM with ALiBi.  [SINK] "como funciona": under ALiBi the linear bias is applied
+ * continuously at the in-cache positions (no jump over the evicted tokens), so distances never
+ * exceed the cache length.  The pages print no ALiBi formula; the reading taken is the usual
+ * one: the logit of the query at in-cache position p_q against a key at in-cache position p_k
+ * is scale * q.k - slope * (p_q - p_k), with `slope` the head's constant (given by the caller).
+ * Keys are used as stored (no rotation).  The attended set and the positions are those of
+ * orc_stream_window.  logits (nullable): per attended token in rank order; lse (nullable).    */
+void orc_stream_decode_alibi(int64_t t, int S, int W, int D, double slope, double scale,
+                             const double *q, const double *hist_k, const double *hist_v,
+                             double *out, double *logits, double *lse)
+{
+    const size_t cap = (size_t)(S + W + 1);
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * cap);
+    int64_t *cpos = (int64_t *)malloc(sizeof(int64_t) * cap);
+    int64_t qpos;
+    const int n = orc_stream_window(t, S, W, tok, cpos, &qpos);
+    double *l = (double *)malloc(sizeof(double) * (size_t)n);
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += q[d] * hist_k[(size_t)tok[j] * D + d];
+        l[j] = scale * acc - slope * (double)(qpos - cpos[j]);
+        if (l[j] > m) m = l[j];
+    }
+    double z = 0.0;
+    for (int j = 0; j < n; ++j) z += exp(l[j] - m);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int j = 0; j < n; ++j) {
+        const double p = exp(l[j] - m) / z;
+        for (int d = 0; d < D; ++d) out[d] += p * hist_v[(size_t)tok[j] * D + d];
+    }
+    if (logits) for (int j = 0; j < n; ++j) logits[j] = l[j];
+    if (lse) *lse = m + log(z);
+    free(tok); free(cpos); free(l);
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Top-k with the tie rule used throughout: keep the k largest scores, equal scores keep the
  * lower index; the kept indices are returned in ascending order (original order preserved).

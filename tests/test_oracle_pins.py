@@ -229,6 +229,78 @@ def test_window_attention_special_case():
     assert list(tok) == list(range(15, 21)) and qpos == 5
 
 
+def test_alibi_worked_example_bias_is_continuous():
+    """The pages' cache [0,1,2,3,6,7,8] decoding token 9 under ALiBi: with q = 0 the logits are
+    the bias alone, -slope * (7 - r) over in-cache positions r = 0..7 -- one unbroken line, not
+    the text distances 9,8,7,6,3,2,1,0 with their jump over the evicted tokens 4 and 5."""
+    g = _golden("stream_positions.json")
+    S, W, t, D = g["S"], g["W"], g["t"], 8
+    rng = np.random.default_rng(31)
+    hk, hv = rng.standard_normal((t + 1, D)), rng.standard_normal((t + 1, D))
+    slope = 0.375
+    _, logits, lse = oracle.stream_decode_alibi(t, S, W, np.zeros(D), hk, hv, 0.5, slope)
+    qp = g["query_position"]
+    want = [-slope * (qp - p) for p in g["positions"]]
+    assert list(logits) == want                               # exact: 0 * anything + bias
+    text = [-slope * (t - a) for a in g["attended_tokens"]]
+    assert list(logits) != text
+    rho = math.exp(-slope)                                    # log of a geometric sum
+    assert abs(lse - math.log((1 - rho ** 8) / (1 - rho))) <= 1e-14
+
+
+def test_alibi_geometric_closed_form_after_eviction():
+    """Equal keys make the weights proportional to rho^distance (rho = e^-slope) over the
+    n = S + W + 1 attended tokens: the mean in-cache position has a closed form."""
+    S, W, D, t = 4, 20, 6, 100
+    rng = np.random.default_rng(32)
+    k = rng.standard_normal(D)
+    hk = np.tile(k, (t + 1, 1))
+    hv = np.zeros((t + 1, D))
+    hv[:, 0] = 1.0
+    for a in range(t + 1):                                    # in-cache position of token a
+        hv[a, 1] = a if a < S else (S + a - (t - W) if a >= t - W else -1e9)
+    slope, n = 0.3, S + W + 1
+    out, _, _ = oracle.stream_decode_alibi(t, S, W, rng.standard_normal(D), hk, hv, 0.25, slope)
+    rho = math.exp(-slope)
+    mean_d = rho * (1 - n * rho ** (n - 1) + (n - 1) * rho ** n) / ((1 - rho) * (1 - rho ** n))
+    assert abs(out[0] - 1.0) <= 1e-14
+    assert abs(out[1] - ((n - 1) - mean_d)) <= 1e-12
+
+
+def test_alibi_reduces_to_library_attention():
+    """Slope 0: window attention over the attended tokens.  No eviction (t <= S + W): in-cache
+    and text positions coincide, so ALiBi is causal attention with the additive bias
+    -slope * (t - j) (library attention with a float mask)."""
+    rng = np.random.default_rng(33)
+    S, W, D = 4, 9, 16
+    T = 40
+    hk, hv = rng.standard_normal((T, D)), rng.standard_normal((T, D))
+    q = rng.standard_normal(D)
+    scale = 1 / math.sqrt(D)
+    t = T - 1
+    tok, _, _ = oracle.stream_window(t, S, W)
+    o, _, _ = oracle.stream_decode_alibi(t, S, W, q, hk, hv, scale, 0.0)
+    ref = _sdpa(q[None], hk[tok], hv[tok], scale, causal=False)[0]
+    assert np.max(np.abs(o - ref)) <= 1e-12
+    slope, t = 0.125, S + W                                   # the last step with no eviction
+    o, _, _ = oracle.stream_decode_alibi(t, 4, W, q, hk, hv, scale, slope)
+    bias = torch.tensor([[-slope * (t - j) for j in range(t + 1)]], dtype=torch.float64)
+    qq = torch.from_numpy(q)[None, None, None]
+    kk = torch.from_numpy(hk[:t + 1])[None, None]
+    vv = torch.from_numpy(hv[:t + 1])[None, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=bias,
+                                                           scale=scale)[0, 0, 0].numpy()
+    assert np.max(np.abs(o - ref)) <= 1e-12
+
+
+def test_alibi_steep_slope_attends_to_the_newest_token():
+    rng = np.random.default_rng(34)
+    S, W, D, t = 4, 7, 8, 30
+    hk, hv = rng.standard_normal((t + 1, D)), rng.standard_normal((t + 1, D))
+    o, _, _ = oracle.stream_decode_alibi(t, S, W, 0.1 * rng.standard_normal(D), hk, hv, 0.1, 80.0)
+    assert np.max(np.abs(o - hv[t])) <= 1e-12
+
+
 # ---------------------------------------------------------------------------- top-k
 def _brute_topk(score, k):
     n = len(score)
