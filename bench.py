@@ -10,7 +10,8 @@ the decode position advances.  Metric: tokens/s (batch x steps / time); the deco
 HBM bandwidth is reported against the measured copy peak.
 
 Other workloads (--workload): snapkv (select + compact + 256-step decode), h2o (prompt
-selection + per-step accumulate/evict), pyramid (per-layer budgets, D=256, GQA 6), tiny.
+selection + per-step accumulate/evict), pyramid (per-layer budgets, D=256, GQA 6), alibi (the
+streaming shape with ALiBi at in-cache positions instead of RoPE).
 
 Multi-GPU: the path shards into independent replicas (no exchange step); under torchrun every
 rank runs the same workload on its own GPU and rank 0 prints the aggregate.
@@ -336,6 +337,48 @@ class Streaming(DecodeWorkload):
                 f"workload's shape, extrapolated to {slices} slices per step (extrapolated)")
 
 
+class StreamingAlibi(Streaming):
+    """StreamingLLM decode with ALiBi at in-cache positions (no key rotation)."""
+
+    traffic_key = "decode_attn/alibi"
+
+    def __init__(self, w: I.Workload, dev, kvc):
+        super().__init__(w, dev, kvc)
+        self.slopes = kvc.kvc_alibi_slopes(w.n_heads_q).to(dev)
+        self.alibi = kvc.make_alibi(w.n_sink, w.window, self.t, self.slopes)
+
+    def decode_layer(self, l, flags=0):
+        self.kvc.kvc_decode_attn_alibi(self.q_s[l], None, None, scale=self.w.scale,
+                                       alibi=self.alibi, flags=flags, out=self.out[l],
+                                       ws=self.ws, cache=self.caches[l])
+
+    def describe(self):
+        d = super().describe()
+        d["workload"] = "streaming decode with ALiBi, Llama-2-7B attention shape"
+        d.pop("rope")
+        d["alibi"] = "in-cache positions, slopes 2^(-8(h+1)/32)"
+        return d
+
+    def oracle_sample(self, budget_s=12.0):
+        import oracle
+        w = self.w
+        rng = np.random.default_rng(0)
+        D, S, W, t = w.d_head, w.n_sink, w.window, w.prompt
+        hk = rng.standard_normal((t + 1, D))
+        hv = rng.standard_normal((t + 1, D))
+        q = rng.standard_normal(D)
+        oracle.stream_decode_alibi(t, S, W, q, hk, hv, w.scale, 0.5)
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.stream_decode_alibi(t, S, W, q, hk, hv, w.scale, 0.5)
+            n += 1
+        return (time.perf_counter() - t0) / n, w.batch * w.n_heads_q * w.layers, n
+
+    def sample_description(self, n, slices):
+        return (f"{n} oracle StreamingLLM ALiBi decodes of one (batch, head, layer) slice at the "
+                f"workload's shape, extrapolated to {slices} slices per step (extrapolated)")
+
+
 class SelectDecode(DecodeWorkload):
     """SnapKV selection per layer at the prompt, compaction, then TAIL-append decode steps.
     The per-layer budget is the workload's (or the PyramidKV ramp)."""
@@ -584,6 +627,8 @@ class H2O(DecodeWorkload):
 def make_workload(name, w, dev, kvc, max_steps):
     if name == "streaming":
         return Streaming(w, dev, kvc)
+    if name == "alibi":
+        return StreamingAlibi(w, dev, kvc)
     if name == "snapkv":
         return SelectDecode(w, dev, kvc, max_steps)
     if name == "pyramid":
@@ -593,7 +638,7 @@ def make_workload(name, w, dev, kvc, max_steps):
     raise ValueError(name)
 
 
-WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid"]
+WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid", "alibi"]
 
 
 # ----------------------------------------------------------------------------- main arms
@@ -744,7 +789,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     cls = {"streaming": Streaming, "snapkv": SelectDecode, "pyramid": SelectDecode,
-           "h2o": H2O}[args.workload]
+           "h2o": H2O, "alibi": StreamingAlibi}[args.workload]
     R = cls.__new__(cls)
     R.w = w
     R.budgets = ([w.budget] * w.layers if args.workload != "pyramid" else

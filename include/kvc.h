@@ -104,6 +104,21 @@ typedef struct {
     int32_t reserved;
 } kvc_rope;
 
+/* ALiBi at in-cache positions for a StreamingLLM cache ([SINK] "como funciona": under ALiBi
+ * the linear bias runs continuously over the in-cache positions, with no jump where tokens were
+ * evicted, so distances never exceed the cache).  Same sink + ring layout, attended set and
+ * in-cache positions as kvc_rope; keys are stored and used as given (no rotation).  The logit
+ * of query head h against the attended token at in-cache position r is
+ *     scale * q.k - slopes[h] * (qpos - r),   qpos = min(t, n_sink + window).
+ * The pages print no slope values: the caller passes them (kvc_alibi_slopes gives the usual
+ * geometric sequence).                                                                       */
+typedef struct {
+    int32_t n_sink;         /* S                                                             */
+    int32_t window;         /* W                                                             */
+    const int64_t *t;       /* device scalar: text position of the token being decoded       */
+    const float *slopes;    /* device fp32[n_heads_q]: the bias slope of each query head     */
+} kvc_alibi;
+
 /* ---------------------------------------------------------------------------------------- */
 /* Diagnostics                                                                               */
 
@@ -253,6 +268,23 @@ kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache 
                               float scale, float *out, float *logits, int64_t logits_stride,
                               float *lse, void *ws, size_t ws_bytes, uint32_t flags,
                               void *stream);
+
+/* Decode attention with ALiBi at in-cache positions over a StreamingLLM sink + ring cache
+ * ([SINK] "como funciona", the ALiBi alternative to RoPE; kvc_alibi gives the layout and the
+ * logit).  Same q, out, logits (indexed by slot), lse, workspace and flags as
+ * kvc_decode_attn_ex with a rope descriptor; the new token is appended with
+ * KVC_APPEND_RING first.  cap >= n_sink + window + 1 (else KVC_ERR_CAPACITY); alibi, its t and
+ * slopes must not be NULL (KVC_ERR_INVALID_ARG). */
+kvc_status kvc_decode_attn_alibi(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                                 const kvc_alibi *alibi, float scale, float *out, float *logits,
+                                 int64_t logits_stride, float *lse, void *ws, size_t ws_bytes,
+                                 uint32_t flags, void *stream);
+
+/* ALiBi slopes, host: out[h] = 2^(-8 (h+1) / n_heads) for h < n_heads, the geometric sequence
+ * of the ALiBi paper (Press et al., "Train Short, Test Long", 2022), defined there for a
+ * power-of-two head count; other counts return KVC_ERR_INVALID_ARG (pass your own slopes).
+ * out: host float[n_heads]. */
+kvc_status kvc_alibi_slopes(int32_t n_heads, float *out);
 
 /* Decode attention without a caller workspace.  No counterpart on the pages: this is a
  * deployment convenience of this library.  Some callers cannot allocate device memory at the

@@ -232,10 +232,12 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
                               logits_stride, lse, ws, ws_bytes, 0u, stream);
 }
 
-kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+// Shared body of the decode entry points: at most one of rope / alibi is given.
+static kvc_status decode_impl(const void *q, int32_t n_heads_q, const kvc_cache *cache,
                               const int32_t *len, int32_t n_valid, const kvc_rope *rope,
-                              float scale, float *out, float *logits, int64_t logits_stride,
-                              float *lse, void *ws, size_t ws_bytes, uint32_t flags, void *stream)
+                              const kvc_alibi *alibi, float scale, float *out, float *logits,
+                              int64_t logits_stride, float *lse, void *ws, size_t ws_bytes,
+                              uint32_t flags, void *stream)
 {
     if (flags & ~(uint32_t)(KVC_DECODE_KV_SETTLED | KVC_DECODE_BALANCE))
         return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: unknown flags 0x%x", flags);
@@ -263,6 +265,16 @@ kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache 
                         rope->n_pos, ring);
         if (!aligned16(rope->cos_sin))
             return fail(KVC_ERR_ALIGN, "kvc_decode_attn: cos_sin must be 16-byte aligned");
+        slots_max = (int)ring;
+    } else if (alibi != nullptr) {
+        if (alibi->t == nullptr || alibi->slopes == nullptr || alibi->n_sink < 0 ||
+            alibi->window < 0)
+            return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn_alibi: alibi descriptor");
+        const long long ring = (long long)alibi->n_sink + alibi->window + 1;
+        if (ring > cache->cap)
+            return fail(KVC_ERR_CAPACITY,
+                        "kvc_decode_attn_alibi: cap %d < n_sink + window + 1 = %lld", cache->cap,
+                        ring);
         slots_max = (int)ring;
     } else if (len == nullptr && (n_valid < 0 || n_valid > cache->cap)) {
         return fail(KVC_ERR_CAPACITY, "kvc_decode_attn: n_valid %d outside [0, cap %d]", n_valid,
@@ -293,6 +305,9 @@ kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache 
         p.rope = 1; p.S = rope->n_sink; p.W = rope->window; p.t = rope->t;
         p.cos_sin = rope->cos_sin;
         p.n_pos = rope->n_pos;
+    } else if (alibi != nullptr) {
+        p.S = alibi->n_sink; p.W = alibi->window; p.t = alibi->t;
+        p.alibi = alibi->slopes;
     }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = out; p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;
@@ -309,6 +324,12 @@ kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     bool used = false;
+    if (p.alibi != nullptr) {
+        e = cache->dtype == KVC_BF16 ? kvc::launch_decode_attn_bf16_alibi(p, cache->d_head, G, s)
+                                     : kvc::launch_decode_attn_f32_alibi(p, cache->d_head, G, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+        return ok();
+    }
     if (cache->dtype == KVC_BF16 && !p.rope && G > 1) {
         // query groups: the two matrix products of the group run on the tensor cores
         e = kvc::launch_decode_attn_mma(p, cache->d_head, G, s, &used);
@@ -322,6 +343,37 @@ kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache 
         e = p.rope ? kvc::launch_decode_attn_f32_rope(p, cache->d_head, G, s)
                    : kvc::launch_decode_attn_f32(p, cache->d_head, G, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    return ok();
+}
+
+kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                              const int32_t *len, int32_t n_valid, const kvc_rope *rope,
+                              float scale, float *out, float *logits, int64_t logits_stride,
+                              float *lse, void *ws, size_t ws_bytes, uint32_t flags, void *stream)
+{
+    return decode_impl(q, n_heads_q, cache, len, n_valid, rope, nullptr, scale, out, logits,
+                       logits_stride, lse, ws, ws_bytes, flags, stream);
+}
+
+kvc_status kvc_decode_attn_alibi(const void *q, int32_t n_heads_q, const kvc_cache *cache,
+                                 const kvc_alibi *alibi, float scale, float *out, float *logits,
+                                 int64_t logits_stride, float *lse, void *ws, size_t ws_bytes,
+                                 uint32_t flags, void *stream)
+{
+    if (alibi == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn_alibi: null alibi descriptor");
+    return decode_impl(q, n_heads_q, cache, nullptr, 0, nullptr, alibi, scale, out, logits,
+                       logits_stride, lse, ws, ws_bytes, flags, stream);
+}
+
+kvc_status kvc_alibi_slopes(int32_t n_heads, float *out)
+{
+    // Geometric sequence starting at and stepping by 2^(-8/n): head h gets 2^(-8(h+1)/n).
+    if (out == nullptr || n_heads <= 0 || (n_heads & (n_heads - 1)) != 0)
+        return fail(KVC_ERR_INVALID_ARG,
+                    "kvc_alibi_slopes: n_heads %d must be a positive power of two", n_heads);
+    for (int32_t h = 0; h < n_heads; ++h)
+        out[h] = (float)std::exp2(-8.0 * (double)(h + 1) / (double)n_heads);
     return ok();
 }
 

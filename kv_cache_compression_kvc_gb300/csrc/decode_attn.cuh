@@ -46,6 +46,12 @@
 // thread copies row |base| into the stage with the keys, so the per-key work reads only shared
 // memory.  A negative base (the newest tile) uses row |base| with the sine negated.
 //
+// ALiBi at in-cache positions ("attention sinks", "como funciona": the linear bias is applied
+// continuously over the cache, never with a jump where tokens were evicted).  The same rank-order
+// walk gives every key its distance qpos - r directly, and the logit becomes
+// scale * q.k - slope_h * (qpos - r), with the query head's slope from the caller; keys are not
+// rotated.
+//
 // Waits on mbarriers are bounded: after kMbarSpinLimit failed polls the thread records
 // KVC_DEV_TIMEOUT and carries on (results are then garbage, but the kernel always finishes).
 #pragma once
@@ -116,14 +122,17 @@ struct DecodeSmem {
     static constexpr int kBytes = kBarBytes + NS * kStageBytes + kMergeBytes;
 };
 
-// RM: 0 no RoPE, 1 RoPE with one table row per key, 2 factored RoPE (G == 1, n_pos >= TK).
+// RM: 0 no RoPE, 1 RoPE with one table row per key, 2 factored RoPE (G == 1, n_pos >= TK),
+// 3 ALiBi.  Modes 1-3 read the StreamingLLM sink + ring layout in rank order.
 template <typename T, int D, int G, int VW, int UNR, int RM, int CPS>
 __global__ void __launch_bounds__(kDecodeThreads, CPS)
 decode_attn_kernel(const DecodeParams p)
 {
     using SM = DecodeSmem<T, D, G, RM>;
-    constexpr bool ROPE = RM != 0;
+    constexpr bool RANKED = RM != 0;     // sink + ring layout, visited in rank order
+    constexpr bool ROPE = RM == 1 || RM == 2;
     constexpr bool FACT = RM == 2;
+    constexpr bool ALIBI = RM == 3;
     constexpr int TK = SM::TK;
     constexpr int NS = SM::NS;
     constexpr int NW = kDecodeWarps;
@@ -174,11 +183,11 @@ decode_attn_kernel(const DecodeParams p)
     }
 
     // ---- decode position (StreamingLLM layout) --------------------------------------------
-    // With RoPE the tiles run over ranks: rank r < S is sink slot r; rank r >= S is ring token
+    // With RoPE or ALiBi the tiles run over ranks: rank r < S is sink slot r; rank r >= S is ring token
     // a_old + (r - S), at slot S + (ring_off + r - S) mod (W + 1), a_old = max(S, t - W) being the
     // oldest ring token still attended.  n_att = min(t + 1, S + W + 1) ranks are attended.
     int qpos = 0, n_att = 0, ring_off = 0;
-    if (ROPE) {
+    if (RANKED) {
         int64_t tpos = *p.t;
         if (tpos < 0) {
             if (threadIdx.x == 0) record_code(p.dev_code, 4 /* KVC_DEV_BAD_POSITION */);
@@ -198,7 +207,7 @@ decode_attn_kernel(const DecodeParams p)
     };
     // number of work items (slots without RoPE, ranks with it) of pair q
     auto pair_slots = [&](int q) -> int {
-        if (ROPE) return n_att;
+        if (RANKED) return n_att;
         if (p.len != nullptr) {
             const int n = p.len[q];
             return n < 0 ? 0 : (n > p.cap ? p.cap : n);
@@ -253,7 +262,7 @@ decode_attn_kernel(const DecodeParams p)
             }
         };
         const int j1 = j0 + rows;
-        if (!ROPE) {
+        if (!RANKED) {
             copy_run(j0, j1, j0);
         } else {
             copy_run(j0, min(j1, p.S), j0);                          // sinks
@@ -282,6 +291,7 @@ decode_attn_kernel(const DecodeParams p)
     float2 pr[UNR][P2], pi[UNR][P2];            // factored RoPE: conj(q) e^{-i (TK-1-kk) th}
     float2 o1[G][P2], o2[G][P2];
     float m[G], l[G];
+    float slope2[G];           // ALiBi: the query heads' slopes times log2(e)
     int cur = -1;              // pair in progress
     int cur_slots = 0;
 
@@ -305,6 +315,7 @@ decode_attn_kernel(const DecodeParams p)
             }
             m[g] = kNegBig;
             l[g] = 0.f;
+            slope2[g] = ALIBI ? __ldg(p.alibi + kh * G + g) * kLog2e : 0.f;
         }
         if constexpr (FACT) {
 #pragma unroll
@@ -531,11 +542,17 @@ decode_attn_kernel(const DecodeParams p)
                         lg[u][g] += __shfl_xor_sync(0xffffffffu, lg[u][g], off);
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
+                if constexpr (ALIBI) {
+                    // the key of rank j sits qpos - j positions before the query
+                    const float dist = (float)(qpos - (j0 + kbase + u * KPW));
+#pragma unroll
+                    for (int g = 0; g < G; ++g) lg[u][g] = fmaf(-slope2[g], dist, lg[u][g]);
+                }
                 if (!valid[u]) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) lg[u][g] = -INFINITY;
                 } else if (lg_out != nullptr && lk == 0) {
-                    const int j = ROPE ? rank_slot(j0 + kbase + u * KPW) : j0 + kbase + u * KPW;
+                    const int j = RANKED ? rank_slot(j0 + kbase + u * KPW) : j0 + kbase + u * KPW;
 #pragma unroll
                     for (int g = 0; g < G; ++g)
                         lg_out[(size_t)g * p.logits_stride + j] = lg[u][g] * kLn2;
@@ -626,13 +643,20 @@ cudaError_t launch_decode_rm(const DecodeParams &p, cudaStream_t stream)
     return launch_pdl(kern, dim3((unsigned)C), dim3(kDecodeThreads), (size_t)SM::kBytes, stream, q);
 }
 
+// Position handling of an instantiation unit.
+constexpr int kDecodePlain = 0;   // valid slots 0 .. len-1, no positional term
+constexpr int kDecodeRope = 1;    // StreamingLLM layout, RoPE at in-cache positions
+constexpr int kDecodeAlibi = 2;   // StreamingLLM layout, ALiBi at in-cache positions
+
 // RoPE with one query head per KV head takes the factored rotation when the table covers the
 // per-lane offsets 0 .. TK-1; otherwise each key reads its table row.
-template <typename T, int D, int G, bool ROPE>
+template <typename T, int D, int G, int MODE>
 cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
 {
-    if constexpr (!ROPE) {
+    if constexpr (MODE == kDecodePlain) {
         return launch_decode_rm<T, D, G, 0>(p, stream);
+    } else if constexpr (MODE == kDecodeAlibi) {
+        return launch_decode_rm<T, D, G, 3>(p, stream);
     } else if constexpr (G == 1) {
         if (p.n_pos >= DecodeSmem<T, D, G, 2>::TK) return launch_decode_rm<T, D, G, 2>(p, stream);
         return launch_decode_rm<T, D, G, 1>(p, stream);
@@ -641,11 +665,11 @@ cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
     }
 }
 
-template <typename T, bool ROPE>
+template <typename T, int MODE>
 cudaError_t launch_decode_variant(const DecodeParams &p, int D, int G, cudaStream_t stream)
 {
 #define KVC_DECODE_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_decode_typed<T, DD, GG, ROPE>(p, stream);
+    if (D == DD && G == GG) return launch_decode_typed<T, DD, GG, MODE>(p, stream);
 #define KVC_DECODE_D(DD) \
     KVC_DECODE_CASE(DD, 1) KVC_DECODE_CASE(DD, 2) KVC_DECODE_CASE(DD, 4) \
     KVC_DECODE_CASE(DD, 6) KVC_DECODE_CASE(DD, 8)

@@ -4,6 +4,6 @@
 namespace kvc {
 cudaError_t launch_decode_attn_bf16_rope(const DecodeParams &p, int D, int G, cudaStream_t stream)
 {
-    return launch_decode_variant<__nv_bfloat16, true>(p, D, G, stream);
+    return launch_decode_variant<__nv_bfloat16, kDecodeRope>(p, D, G, stream);
 }
 }  // namespace kvc

@@ -4,6 +4,6 @@
 namespace kvc {
 cudaError_t launch_decode_attn_f32(const DecodeParams &p, int D, int G, cudaStream_t stream)
 {
-    return launch_decode_variant<float, false>(p, D, G, stream);
+    return launch_decode_variant<float, kDecodePlain>(p, D, G, stream);
 }
 }  // namespace kvc

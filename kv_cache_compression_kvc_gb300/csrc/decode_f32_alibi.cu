@@ -1,0 +1,9 @@
+// decode_f32_alibi.cu -- fp32-storage instantiations of the decode attention kernel with ALiBi at in-cache positions.
+#include "decode_attn.cuh"
+
+namespace kvc {
+cudaError_t launch_decode_attn_f32_alibi(const DecodeParams &p, int D, int G, cudaStream_t stream)
+{
+    return launch_decode_variant<float, kDecodeAlibi>(p, D, G, stream);
+}
+}  // namespace kvc

@@ -4,6 +4,6 @@
 namespace kvc {
 cudaError_t launch_decode_attn_f32_rope(const DecodeParams &p, int D, int G, cudaStream_t stream)
 {
-    return launch_decode_variant<float, true>(p, D, G, stream);
+    return launch_decode_variant<float, kDecodeRope>(p, D, G, stream);
 }
 }  // namespace kvc

@@ -44,6 +44,7 @@ struct DecodeParams {
     const int64_t *t;
     const float *cos_sin;        // [n_pos][2][D/2]: cosines then sines per distance
     int32_t n_pos;               // rows of cos_sin
+    const float *alibi;          // ALiBi slopes per query head [Hq] (same layout as RoPE) or null
     int32_t kv_settled;          // cache slots and lengths final before the previous launch began
     int32_t balance;             // split the tiles by the lengths (not by capacity)
     float scale_log2;            // scale * log2(e)
@@ -76,6 +77,9 @@ cudaError_t launch_decode_attn_mma(const DecodeParams &p, int D, int G, cudaStre
 cudaError_t launch_decode_attn_f32_rope(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16_rope(const DecodeParams &p, int D, int G,
                                          cudaStream_t stream);
+cudaError_t launch_decode_attn_f32_alibi(const DecodeParams &p, int D, int G, cudaStream_t stream);
+cudaError_t launch_decode_attn_bf16_alibi(const DecodeParams &p, int D, int G,
+                                          cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------
 // Append, gather, position advance.

@@ -18,6 +18,8 @@ Workloads (sizes as stated by the benchmark configuration):
               409 heavy hitters; keys scaled per position by a Zipf(1.1) draw on {1..8}; 512 steps.
   pyramid     16 layers, Hq=24, Hkv=4, D=256, bf16, B=2, N=131072; L_obs=64, pool 5; budgets
               fall linearly (ratio 4) around a mean of 8192; sink-boosted keys 0-3; 256 steps.
+  alibi       the streaming shape with ALiBi at in-cache positions in place of RoPE (slopes
+              2^(-8(h+1)/32) for the 32 heads); same cache, prompt and steps.
 """
 from __future__ import annotations
 
@@ -71,6 +73,8 @@ WORKLOADS = {
                     L_local=410),
     "pyramid": Workload("pyramid", 16, 2, 24, 4, 256, 131072, 256, torch.bfloat16, 1239,
                         L_obs=64, budget=8192),
+    "alibi": Workload("alibi", 32, 16, 32, 32, 128, 4096, 1024, torch.bfloat16, 1240,
+                      n_sink=4, window=2044),
 }
 
 

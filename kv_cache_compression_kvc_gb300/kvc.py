@@ -46,6 +46,11 @@ class kvc_rope(ctypes.Structure):
                 ("n_pos", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class kvc_alibi(ctypes.Structure):
+    _fields_ = [("n_sink", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("t", ctypes.c_void_p), ("slopes", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -55,6 +60,7 @@ _U32 = ctypes.c_uint32
 _F32 = ctypes.c_float
 _CACHE_P = ctypes.POINTER(kvc_cache)
 _ROPE_P = ctypes.POINTER(kvc_rope)
+_ALIBI_P = ctypes.POINTER(kvc_alibi)
 
 # name -> (restype, argtypes); every symbol declared in include/kvc.h
 SIGNATURES = {
@@ -75,6 +81,9 @@ SIGNATURES = {
                                _P, _SZ, _P]),
     "kvc_decode_attn_ex": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P, _I64,
                                   _P, _P, _SZ, _U32, _P]),
+    "kvc_decode_attn_alibi": (_I32, [_P, _I32, _CACHE_P, _ALIBI_P, _F32, _P, _P, _I64, _P, _P,
+                                     _SZ, _U32, _P]),
+    "kvc_alibi_slopes": (_I32, [_I32, _P]),
     "kvc_decode_attn_noalloc": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P,
                                        _I64, _P, _P]),
     "kvc_h2o_accumulate_evict": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P,
@@ -253,6 +262,42 @@ def kvc_decode_attn_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
     _check(load().kvc_decode_attn_ex(
         _ptr(q), Hq, ctypes.byref(c), _ptr(len), -1 if n_valid is None else int(n_valid),
         ctypes.byref(rope) if rope is not None else None, float(scale), _ptr(out),
+        _ptr(logits), lstride, _ptr(lse), wp, wb, int(flags), _stream(stream)))
+    return out
+
+
+def kvc_alibi_slopes(n_heads: int) -> torch.Tensor:
+    """Host fp32 [n_heads]: 2^(-8 (h+1) / n_heads) (power-of-two head counts)."""
+    out = torch.empty(n_heads, dtype=torch.float32)
+    _check(load().kvc_alibi_slopes(n_heads, _ptr(out)))
+    return out
+
+
+def make_alibi(n_sink: int, window: int, t: torch.Tensor, slopes: torch.Tensor) -> kvc_alibi:
+    a = kvc_alibi()
+    a.n_sink, a.window = n_sink, window
+    a.t = t.data_ptr()
+    a.slopes = slopes.data_ptr()
+    return a
+
+
+def kvc_decode_attn_alibi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,
+                          scale: float, alibi: kvc_alibi, flags: int = 0,
+                          out: Optional[torch.Tensor] = None,
+                          logits: Optional[torch.Tensor] = None,
+                          lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                          stream=None, cache: Optional[kvc_cache] = None) -> torch.Tensor:
+    """StreamingLLM decode with ALiBi at in-cache positions: q [B, Hq, D] -> out [B, Hq, D]."""
+    c = cache if cache is not None else cache_view(k_cache, v_cache)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(B, Hq, c.n_heads_kv, D, c.cap, q.device)
+    wp, wb = _ws_ptr(ws)
+    lstride = logits.stride(-2) if logits is not None else 0
+    _check(load().kvc_decode_attn_alibi(
+        _ptr(q), Hq, ctypes.byref(c), ctypes.byref(alibi), float(scale), _ptr(out),
         _ptr(logits), lstride, _ptr(lse), wp, wb, int(flags), _stream(stream)))
     return out
 

@@ -108,3 +108,34 @@ def test_validation_rejects_bad_calls_before_launch(kvc):
     assert st == 1                                                 # in place is refused
     assert lib.kvc_pyramid_budgets(0, 10, 4, 1, None) == 1
     assert kvc.kvc_last_error() != ""
+
+
+def test_alibi_slopes_geometric_sequence(kvc):
+    """Eight heads: 1/2, 1/4, ..., 1/256 (the ALiBi paper's example); sixteen heads interleave
+    the square roots; a head count that is not a power of two is refused."""
+    assert kvc.kvc_alibi_slopes(8).tolist() == [2.0 ** -(h + 1) for h in range(8)]
+    s16 = kvc.kvc_alibi_slopes(16).double().numpy()
+    assert np.allclose(s16, [2.0 ** (-(h + 1) / 2) for h in range(16)], rtol=1e-7, atol=0)
+    assert np.allclose(s16[1::2], [2.0 ** -(h + 1) for h in range(8)], rtol=0, atol=0)
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_alibi_slopes(6)
+
+
+def test_alibi_validation_before_launch(kvc):
+    lib = kvc.load()
+    c = kvc.kvc_cache()
+    c.k = c.v = 4096
+    c.dtype, c.batch, c.n_heads_kv, c.cap, c.d_head = kvc.KVC_BF16, 1, 1, 16, 128
+    c.stride_b, c.stride_h, c.stride_slot = 16 * 128, 16 * 128, 128
+    st = lib.kvc_decode_attn_alibi(4096, 1, ctypes.byref(c), None, 1.0, 4096, None, 0, None,
+                                   None, 0, 0, None)
+    assert st == 1 and "alibi" in kvc.kvc_last_error()            # no descriptor
+    a = kvc.kvc_alibi()
+    a.n_sink, a.window, a.t, a.slopes = 4, 20, 4096, 4096
+    st = lib.kvc_decode_attn_alibi(4096, 1, ctypes.byref(c), ctypes.byref(a), 1.0, 4096, None,
+                                   0, None, None, 0, 0, None)
+    assert st == 4                                                 # ring does not fit cap 16
+    a.window, a.slopes = 3, None
+    st = lib.kvc_decode_attn_alibi(4096, 1, ctypes.byref(c), ctypes.byref(a), 1.0, 4096, None,
+                                   0, None, None, 0, 0, None)
+    assert st == 1                                                 # no slopes

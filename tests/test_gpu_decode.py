@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, assert_close, cuda_or_skip, f64, lib
+from gpu_helpers import TOL, assert_close, assert_rel, cuda_or_skip, f64, lib
 from kv_cache_compression_kvc_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -275,3 +275,91 @@ def test_streaming_worked_example_positions(table_rows):
         want = 0.125 * float(np.dot(qr, oracle.rope(f64(ks[a, 0, 0]), int(pos))))
         got = float(lg[oracle.stream_slot(int(a), S, W)])
         assert abs(got - want) <= 1e-5 * max(1.0, abs(want)), f"logit of token {a}"
+
+
+# (dtype, D, G, S, W, wraps): ALiBi over the sink + ring layout, token by token from empty.
+@pytest.mark.parametrize("dtype,D,G,S,W,wraps", [
+    (torch.float32, 64, 1, 4, 20, 3),
+    (torch.bfloat16, 128, 1, 4, 150, 2),
+    (torch.bfloat16, 128, 4, 4, 37, 3),
+    (torch.float32, 256, 2, 2, 70, 2),
+    (torch.bfloat16, 64, 8, 0, 9, 3),
+    (torch.float32, 128, 1, 70, 20, 2),
+])
+def test_streaming_ring_alibi_matches_oracle_every_step(dtype, D, G, S, W, wraps):
+    """Ring append then decode with ALiBi at in-cache positions; every step's output, logits
+    (at their slots) and log-sum-exp against the oracle's ALiBi decode from the full history."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv = 2, 2
+    Hq = Hkv * G
+    T = S + wraps * (W + 1) + 5
+    cap = S + W + 1 + 3
+    K = torch.zeros((B, Hkv, cap, D), device=dev, dtype=dtype)
+    V = torch.zeros_like(K)
+    qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, T, 70 + D + W, dev, dtype)
+    slopes_h = kvc.kvc_alibi_slopes(Hq)
+    slopes = slopes_h.to(dev)
+    t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    alibi = kvc.make_alibi(S, W, t_dev, slopes)
+    scale = 1 / math.sqrt(D)
+    hk, hv = f64(ks), f64(vs)
+    logits = torch.full((B, Hq, cap), float("nan"), device=dev)
+    lse = torch.empty((B, Hq), device=dev)
+    for t in range(T):
+        t_dev.fill_(t)
+        kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_RING, ks[t], vs[t], t=t_dev, n_sink=S,
+                              window=W)
+        out_t = kvc.kvc_decode_attn_alibi(qs[t], K, V, scale=scale, alibi=alibi, logits=logits,
+                                          lse=lse)
+        t_dev.add_(0)        # a plain kernel: an ordering point after the append (kvc.h)
+        out_s = kvc.kvc_decode_attn_alibi(qs[t], K, V, scale=scale, alibi=alibi,
+                                          flags=kvc.KVC_DECODE_KV_SETTLED)
+        assert torch.equal(out_t, out_s), "settled-cache load order changed the result"
+        out, lg, ls = out_t.cpu().numpy(), logits.cpu().numpy(), lse.cpu().numpy()
+        tok, _, _ = oracle.stream_window(t, S, W)
+        slots = [oracle.stream_slot(int(a), S, W) for a in tok]
+        for b in range(B):
+            for h in range(Hq):
+                ref, ref_lg, ref_lse = oracle.stream_decode_alibi(
+                    t, S, W, f64(qs[t, b, h]), hk[:t + 1, b, h // G], hv[:t + 1, b, h // G],
+                    scale, float(slopes_h[h]))
+                assert_close(out[b, h], ref, TOL[dtype], f"t={t} b={b} h={h}")
+                assert_rel(lg[b, h, slots], ref_lg, 1e-5, 1e-4, f"logits t={t} b={b} h={h}")
+                assert abs(float(ls[b, h]) - ref_lse) <= 1e-4 * max(1.0, abs(ref_lse))
+    assert kvc.kvc_device_status() == 0
+
+
+def test_alibi_worked_example_continuous_bias():
+    """The pages' cache [0,1,2,3,6,7,8] decoding token 9 with q = 0: the logits at the tokens'
+    slots are the bias alone, -slope * (7 - r) over in-cache positions r = 0..7, and the output
+    mixes only the values of tokens 0,1,2,3,6,7,8,9."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    S, W, D = 4, 3, 64
+    K = torch.zeros((1, 1, S + W + 1, D), device=dev)
+    V = torch.zeros_like(K)
+    ks = I.randn((10, 1, 1, D), 81, dev)
+    vs = torch.zeros((10, 1, 1, D), device=dev)
+    for a in range(10):
+        vs[a, 0, 0, a] = 1.0
+    t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    for t in range(10):
+        t_dev.fill_(t)
+        kvc.kvc_stream_append(K, V, kvc.KVC_APPEND_RING, ks[t], vs[t], t=t_dev, n_sink=S,
+                              window=W)
+    slope = 0.375
+    slopes = torch.tensor([slope], device=dev)
+    logits = torch.zeros((1, 1, S + W + 1), device=dev)
+    q = torch.zeros((1, 1, D), device=dev)
+    out = kvc.kvc_decode_attn_alibi(q, K, V, scale=0.125, alibi=kvc.make_alibi(S, W, t_dev, slopes),
+                                    logits=logits)[0, 0].cpu().numpy()
+    assert np.all(out[[4, 5]] == 0) and np.all(out[[0, 1, 2, 3, 6, 7, 8, 9]] > 0)
+    tok, cpos, qpos = oracle.stream_window(9, S, W)
+    lg = logits[0, 0].cpu().numpy()
+    for a, r in zip(tok, cpos):
+        want = -slope * (qpos - int(r))
+        assert abs(float(lg[oracle.stream_slot(int(a), S, W)]) - want) <= 1e-5, int(a)
+    # weights fall off geometrically with the in-cache distance
+    w = out[[0, 1, 2, 3, 6, 7, 8, 9]]
+    assert np.allclose(w[1:] / w[:-1], math.exp(slope), rtol=1e-5)
