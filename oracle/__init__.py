@@ -8,7 +8,7 @@ with gcc into ``oracle/_build/``.  This module only marshals numpy arrays.
 Functions (each follows the page passage cited in ``kvc_oracle.c``):
   kv_bytes, pyramid_budgets, rope, attend, stream_window, stream_slot, stream_decode,
   stream_decode_alibi, topk_ascending, snapkv_obs_scores, pool1d, snapkv_select, snapkv_stage_f32,
-  h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_evict_f32.
+  h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_evict_f32, block_step, block_evict_f32.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against values the pages
 print, closed forms, invariants, library routines on special cases or brute force on tiny
@@ -77,6 +77,9 @@ _SIGS = {
     "orc_h2o_step": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _f64, _ptr, _ptr, _ptr, _ptr,
                                     _ptr, _i64, ctypes.c_int, ctypes.c_int, _ptr, _ptr]),
     "orc_h2o_evict_f32": (ctypes.c_int, [ctypes.c_int, _ptr, _ptr, _i64, ctypes.c_int]),
+    "orc_block_step": (ctypes.c_int, [ctypes.c_int] * 5 + [_f64, _ptr, _ptr, _ptr, _ptr,
+                                                           ctypes.c_int, ctypes.c_int, _ptr]),
+    "orc_block_evict_f32": (ctypes.c_int, [ctypes.c_int, _ptr, ctypes.c_int, ctypes.c_int]),
 }
 
 
@@ -259,3 +262,24 @@ def h2o_evict_f32(s_f32, pos, t: int, L_local: int) -> int:
     s = np.ascontiguousarray(np.asarray(s_f32, dtype=np.float32))
     pos = np.ascontiguousarray(np.asarray(pos, dtype=np.int64))
     return int(lib().orc_h2o_evict_f32(s.shape[0], _p(s), _p(pos), int(t), L_local))
+
+
+def block_step(q, K, V, score, bs: int, budget_blocks: int, recent_blocks: int, scale: float):
+    """One block-eviction decode step of one sequence.  q [Hq, D]; K, V [Hkv, n_tok, D] in
+    page-table order; score [nb] (not modified).  Returns (out [Hq, D], score_new, released
+    block index or -1)."""
+    q, K, V = _f(q), _f(K), _f(V)
+    Hq, D = q.shape
+    Hkv, n_tok = K.shape[0], K.shape[1]
+    nb = (n_tok + bs - 1) // bs
+    s_new = _f(score).copy()
+    assert s_new.shape[0] == nb
+    out = np.empty((Hq, D))
+    ev = lib().orc_block_step(Hq, Hkv, D, n_tok, bs, scale, _p(q), _p(K), _p(V), _p(s_new),
+                              budget_blocks, recent_blocks, _p(out))
+    return out, s_new, int(ev)
+
+
+def block_evict_f32(score_f32, budget_blocks: int, recent_blocks: int) -> int:
+    s = np.ascontiguousarray(np.asarray(score_f32, dtype=np.float32))
+    return int(lib().orc_block_evict_f32(s.shape[0], _p(s), budget_blocks, recent_blocks))

@@ -457,3 +457,58 @@ int orc_h2o_evict_f32(int n_slots, const float *s, const int64_t *pos, int64_t t
     }
     return ev;
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* Block-level eviction.  [KVC] "Implementação prática em vLLM e SGLang": the cache lives in
+ * physical blocks of 16 or 32 tokens reached through a page table; the engine rates a whole
+ * block by the sum of its tokens' importance, Score(block) = sum over t in the block of s_t,
+ * and when memory runs out the scheduler releases the lowest-scoring blocks from the page
+ * table; they return to the free pool without copying any data.
+ * Readings (the pages leave these open):
+ *   - s_t is H2O's accumulated attention of token t ([KVC] H2O: s_j = sum over steps of
+ *     alpha), summed over the query heads: a block holds every head's keys and values of its
+ *     tokens, so only a per-token total can rank it;
+ *   - step order as for H2O: the new token is appended (opening a new block when the last one
+ *     is full), every head attends over all cached tokens (itself included), each block's score
+ *     grows by its share of this step's attention, and then, if the sequence holds more than
+ *     budget_blocks blocks, one block is released;
+ *   - the recent_blocks newest blocks (the partly filled one included) are never released,
+ *     the counterpart of H2O's recent quota; among the others the lowest score goes, equal
+ *     scores releasing the newer block (the larger index; the older one is kept, as in H2O).
+ *
+ * One decode step of one sequence, computed as written.  The cache holds n_tok tokens in
+ * page-table order; block i holds tokens i*bs .. min(n_tok, (i+1)*bs) - 1.  Query head h
+ * (h < Hq) reads KV head h / (Hq / Hkv).  q: [Hq][D]; K, V: [Hkv][n_tok][D] (tokens gathered
+ * in table order); score: [nb] block scores, updated in place.  out: [Hq][D].
+ * Returns the index of the released block, or -1.                                             */
+int orc_block_step(int Hq, int Hkv, int D, int n_tok, int bs, double scale, const double *q,
+                   const double *K, const double *V, double *score, int budget_blocks,
+                   int recent_blocks, double *out)
+{
+    const int G = Hq / Hkv;
+    const int nb = (n_tok + bs - 1) / bs;
+    double *l = (double *)malloc(sizeof(double) * (size_t)(n_tok > 0 ? n_tok : 1));
+    for (int h = 0; h < Hq; ++h) {
+        const int kh = h / G;
+        double lse;
+        orc_attend(n_tok, D, scale, q + (size_t)h * D, K + (size_t)kh * n_tok * D,
+                   V + (size_t)kh * n_tok * D, out + (size_t)h * D, l, &lse);
+        for (int j = 0; j < n_tok; ++j) score[j / bs] += exp(l[j] - lse);
+    }
+    free(l);
+    if (nb <= budget_blocks) return -1;
+    int ev = -1;
+    for (int i = 0; i < nb - recent_blocks; ++i)
+        if (ev < 0 || score[i] <= score[ev]) ev = i;     /* <=: equal scores take the newer */
+    return ev;
+}
+
+/* The release decision alone, in fp32, on given fp32 block scores (the GPU's own). */
+int orc_block_evict_f32(int nb, const float *score, int budget_blocks, int recent_blocks)
+{
+    if (nb <= budget_blocks) return -1;
+    int ev = -1;
+    for (int i = 0; i < nb - recent_blocks; ++i)
+        if (ev < 0 || score[i] <= score[ev]) ev = i;
+    return ev;
+}

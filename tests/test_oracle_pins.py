@@ -555,3 +555,74 @@ def test_snapkv_stage_f32_divides_after_summing():
     idx = oracle.snapkv_stage_f32(s, L, budget=L + 1)
     expect_first = 0 if div_tie else 9  # tie keeps the lower index; else b's window wins
     assert list(idx) == [expect_first, n, n + 1]
+
+
+# ---------------------------------------------------------------------------- block eviction
+def test_block_step_with_one_token_blocks_is_h2o():
+    """Blocks of one token and one head: the block scores are H2O's per-token scores, the
+    recent-block quota is H2O's recent quota (the newest tokens sit at consecutive positions),
+    and the released block is H2O's evicted token -- including an exact tie among candidates,
+    which releases the newer one."""
+    rng = np.random.default_rng(41)
+    D, L_local, budget = 8, 3, 6
+    n = budget + 1
+    K, V = rng.standard_normal((n, D)), rng.standard_normal((n, D))
+    t = 50
+    pos = np.array([2, 5, 9, 11, t - 2, t - 1, t])
+    for q, s0 in ((rng.standard_normal(D), rng.random(n)),
+                  (np.zeros(D), np.array([0.5, 0.25, 0.25, 0.25, 0.1, 0.2, 0.0]))):
+        o_h, s_h, _, ev_h = oracle.h2o_step(q, K, V, pos, s0, t, L_local, budget, 0.3)
+        o_b, s_b, ev_b = oracle.block_step(q[None], K[None], V[None], s0, 1, budget, L_local, 0.3)
+        assert ev_b == ev_h and np.array_equal(s_b, s_h) and np.array_equal(o_b[0], o_h)
+    assert ev_b == 3                      # uniform attention: ties 1,2,3 -> the newest goes
+
+
+def test_block_score_is_the_sum_of_its_token_scores():
+    """Score(block) = sum of s_t over its tokens ([KVC] block-level eviction), s_t summed over
+    the query heads: blocks of 4 against blocks of 1 on the same grouped-query inputs, several
+    steps with no release, the last block partly filled."""
+    rng = np.random.default_rng(42)
+    Hq, Hkv, D, bs = 4, 2, 8, 4
+    s1 = np.zeros(0)
+    s4 = np.zeros(0)
+    for n_tok in (9, 10, 11, 12, 13):
+        K, V = rng.standard_normal((Hkv, n_tok, D)), rng.standard_normal((Hkv, n_tok, D))
+        q = rng.standard_normal((Hq, D))
+        s1 = np.concatenate([s1, np.zeros(n_tok - len(s1))])
+        s4 = np.concatenate([s4, np.zeros((n_tok + bs - 1) // bs - len(s4))])
+        _, s1, e1 = oracle.block_step(q, K, V, s1, 1, 100, 1, 0.35)
+        _, s4, e4 = oracle.block_step(q, K, V, s4, bs, 100, 1, 0.35)
+        assert e1 == e4 == -1
+        pad = np.concatenate([s1, np.zeros(len(s4) * bs - len(s1))])
+        assert np.max(np.abs(pad.reshape(-1, bs).sum(axis=1) - s4)) <= 1e-12
+
+
+def test_block_step_against_library_softmax_brute_force():
+    rng = np.random.default_rng(43)
+    Hq, Hkv, D, bs, n_tok = 4, 2, 8, 4, 23          # 6 blocks, the last holds 3 tokens
+    budget, recent = 5, 2
+    G = Hq // Hkv
+    K, V = rng.standard_normal((Hkv, n_tok, D)), rng.standard_normal((Hkv, n_tok, D))
+    q = rng.standard_normal((Hq, D))
+    s0 = rng.random(6) * 3
+    scale = 1 / math.sqrt(D)
+    out, s_new, ev = oracle.block_step(q, K, V, s0, bs, budget, recent, scale)
+    want = s0.copy()
+    for h in range(Hq):
+        lg = torch.from_numpy(K[h // G] @ q[h] * scale)
+        a = torch.softmax(lg, dim=0).numpy()
+        want += np.concatenate([a, np.zeros(6 * bs - n_tok)]).reshape(6, bs).sum(axis=1)
+        ref = _sdpa(q[h][None], K[h // G], V[h // G], scale, causal=False)[0]
+        assert np.max(np.abs(out[h] - ref)) <= 1e-12
+    assert np.max(np.abs(s_new - want)) <= 1e-12
+    assert abs((s_new - s0).sum() - Hq) <= 1e-12          # every head's attention sums to 1
+    cands = sorted(range(6 - recent), key=lambda i: (want[i], -i))
+    assert ev == cands[0]
+
+
+def test_block_release_rules():
+    s = np.array([0.5, 0.25, 0.25, 0.9, 0.0, 0.0], dtype=np.float32)
+    assert oracle.block_evict_f32(s, 6, 2) == -1            # within budget: nothing released
+    assert oracle.block_evict_f32(s, 5, 2) == 2             # tie 1/2: the newer goes
+    assert oracle.block_evict_f32(s, 5, 1) == 4             # recent quota of one block
+    assert oracle.block_evict_f32(s, 5, 5) == 0             # only the oldest is a candidate
