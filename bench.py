@@ -11,7 +11,8 @@ HBM bandwidth is reported against the measured copy peak.
 
 Other workloads (--workload): snapkv (select + compact + 256-step decode), h2o (prompt
 selection + per-step accumulate/evict), pyramid (per-layer budgets, D=256, GQA 6), alibi (the
-streaming shape with ALiBi at in-cache positions instead of RoPE).
+streaming shape with ALiBi at in-cache positions instead of RoPE), paged (block-level eviction
+over page tables at the H2O shape).
 
 Multi-GPU: the path shards into independent replicas (no exchange step); under torchrun every
 rank runs the same workload on its own GPU and rank 0 prints the aggregate.
@@ -624,6 +625,142 @@ class H2O(DecodeWorkload):
                 f"slice, extrapolated to {slices} slices per step (extrapolated)")
 
 
+class PagedBlocks(DecodeWorkload):
+    """Block-level eviction over page tables at the H2O shape: per layer a pool of 32-token
+    blocks and a page table per sequence (26 blocks = 832 tokens, the 13 newest protected);
+    per step: paged append, paged decode with logits, and the block score update + release
+    (on a second stream beside the next layer's decode, as for H2O)."""
+
+    traffic_key = "decode_attn/paged"
+
+    def __init__(self, w: I.Workload, dev, kvc):
+        super().__init__(w, dev, kvc)
+        L, B, H, D = w.layers, w.batch, w.n_heads_kv, w.d_head
+        self.bs, self.nb, self.recent = self.block_shape(w)
+        bs = self.bs
+        self.mb = self.nb + 1
+        self.n_pool = B * self.mb + B
+        self.kp = torch.empty((L, self.n_pool, H, bs, D), dtype=w.dtype, device=dev)
+        self.vp = torch.empty_like(self.kp)
+        for l in range(L):
+            g = I.generator(w.seed * 1000 + l, dev)
+            self.kp[l].normal_(generator=g)
+            self.vp[l].normal_(generator=g)
+        self.table = torch.empty((L, B, self.mb), dtype=torch.int32, device=dev)
+        self.ids = torch.empty((L, self.n_pool), dtype=torch.int32, device=dev)
+        self.top = torch.empty((L, 1), dtype=torch.int32, device=dev)
+        for l in range(L):
+            perm = torch.randperm(self.n_pool, generator=torch.Generator().manual_seed(l))
+            used = perm[:B * self.nb].reshape(B, self.nb)
+            self.table[l].fill_(-1)
+            self.table[l, :, :self.nb] = used.to(torch.int32).to(dev)
+            free = perm[B * self.nb:].to(torch.int32)
+            self.ids[l].fill_(-1)
+            self.ids[l, :free.numel()] = free.to(dev)
+            self.top[l] = free.numel()
+        self.n_blk = torch.full((L, B), self.nb, dtype=torch.int32, device=dev)
+        self.len = torch.full((L, B), self.nb * bs, dtype=torch.int32, device=dev)
+        self.score = torch.zeros((L, B, self.mb), dtype=torch.float32, device=dev)
+        self.cap = self.mb * bs
+        self.logits = torch.empty((L, B, w.n_heads_q, self.cap), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((L, B, w.n_heads_q), dtype=torch.float32, device=dev)
+        self.pools = [kvc.block_pool_view(self.kp[l], self.vp[l]) for l in range(L)]
+        self.pts = [kvc.page_table_view(self.table[l], self.n_blk[l], self.len[l], self.score[l])
+                    for l in range(L)]
+        self.fps = [kvc.free_pool_view(self.ids[l], self.top[l]) for l in range(L)]
+        self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.cap, dev)
+        self.launches_per_step = 3 * L
+        self.side = torch.cuda.Stream(device=dev)
+        self.done = [torch.cuda.Event() for _ in range(L)]
+
+    @staticmethod
+    def block_shape(w):
+        """(block size, budget in blocks, protected newest blocks): the token budget and the
+        recent quota rounded up to whole blocks."""
+        bs = w.extra["block_size"]
+        return bs, -(-w.budget // bs), -(-w.L_local // bs)
+
+    def save_state(self):
+        # appends only write past each sequence's length or into free blocks, so the live
+        # contents of the pools need no saving
+        return tuple(x.clone() for x in (self.table, self.ids, self.top, self.n_blk, self.len,
+                                         self.score))
+
+    def restore_state(self, st):
+        for dst, src in zip((self.table, self.ids, self.top, self.n_blk, self.len, self.score),
+                            st):
+            dst.copy_(src)
+
+    def append_layer(self, l):
+        self.kvc.kvc_paged_append(self.pools[l], self.pts[l], self.fps[l], self.k_s[l],
+                                  self.v_s[l])
+
+    def decode_layer(self, l, flags=0):
+        kvc, w = self.kvc, self.w
+        kvc.kvc_decode_attn_paged(self.q_s[l], self.pools[l], self.pts[l], scale=w.scale,
+                                  flags=flags, out=self.out[l], logits=self.logits[l],
+                                  lse=self.lse[l], ws=self.ws)
+        self.done[l].record(torch.cuda.current_stream())
+        self.side.wait_event(self.done[l])
+        kvc.kvc_block_accumulate_evict(self.logits[l], self.lse[l], self.pts[l], self.fps[l],
+                                       block_size=self.bs, budget_blocks=self.nb,
+                                       recent_blocks=self.recent, stream=self.side)
+
+    def end_step(self):
+        torch.cuda.current_stream().wait_stream(self.side)
+
+    def tokens_at(self, step):
+        """Tokens each sequence attends at decode step `step` (0-based from the start): the
+        cache starts with nb full blocks; a step that opens a block attends nb*bs + 1 tokens and
+        then releases one, after which the last block refills."""
+        k = step % self.bs
+        return self.nb * self.bs + 1 if k == 0 else (self.nb - 1) * self.bs + 1 + k
+
+    def decode_bytes(self, first_step, n_steps):
+        w = self.w
+        tot = 0
+        for st in range(first_step, first_step + n_steps):
+            n = self.tokens_at(st)
+            tot += self.kv_bytes(n) + self.qo_bytes() + w.batch * w.n_heads_q * (n + 1) * 4
+        return tot // n_steps
+
+    def describe(self):
+        w = self.w
+        return {"workload": "block-level eviction over page tables (H2O shape)",
+                "layers": w.layers, "batch": w.batch, "n_heads": w.n_heads_q,
+                "d_head": w.d_head, "block_size": self.bs, "budget_blocks": self.nb,
+                "recent_blocks": self.recent, "tokens_per_step": "801..833 (mean 817.5)",
+                "kv_dtype": "bf16", "l2": "inputs larger than L2 (7 GB of KV per step)",
+                "init": "page tables start with 26 full blocks of N(0,1) keys/values, zero "
+                        "scores (no prompt selection in this workload)",
+                "graph": "appends, then paged decode + block update per layer (the update of "
+                         "layer l on a second stream beside the decode of layer l + 1), as two "
+                         "CUDA graphs"}
+
+    def oracle_sample(self, budget_s=12.0):
+        import oracle
+        w = self.w
+        bs, nb, recent = self.block_shape(w)
+        rng = np.random.default_rng(0)
+        n = nb * bs + 1
+        G = w.n_heads_q // w.n_heads_kv
+        K = rng.standard_normal((1, n, w.d_head))
+        V = rng.standard_normal((1, n, w.d_head))
+        q = rng.standard_normal((G, w.d_head))
+        s = rng.random(nb + 1)
+        oracle.block_step(q, K, V, s, bs, nb, recent, w.scale)
+        cnt, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.block_step(q, K, V, s, bs, nb, recent, w.scale)
+            cnt += 1
+        # one call covers one KV head's query heads of one sequence and layer
+        return (time.perf_counter() - t0) / cnt, w.batch * w.n_heads_kv * w.layers, cnt
+
+    def sample_description(self, n, slices):
+        return (f"{n} oracle block-eviction steps (attend, block scores, release) of one (batch, "
+                f"KV head, layer) slice, extrapolated to {slices} slices per step (extrapolated)")
+
+
 def make_workload(name, w, dev, kvc, max_steps):
     if name == "streaming":
         return Streaming(w, dev, kvc)
@@ -635,10 +772,12 @@ def make_workload(name, w, dev, kvc, max_steps):
         return SelectDecode(w, dev, kvc, max_steps, pyramid=True)
     if name == "h2o":
         return H2O(w, dev, kvc)
+    if name == "paged":
+        return PagedBlocks(w, dev, kvc)
     raise ValueError(name)
 
 
-WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid", "alibi"]
+WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid", "alibi", "paged"]
 
 
 # ----------------------------------------------------------------------------- main arms
@@ -789,7 +928,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     cls = {"streaming": Streaming, "snapkv": SelectDecode, "pyramid": SelectDecode,
-           "h2o": H2O, "alibi": StreamingAlibi}[args.workload]
+           "h2o": H2O, "alibi": StreamingAlibi, "paged": PagedBlocks}[args.workload]
     R = cls.__new__(cls)
     R.w = w
     R.budgets = ([w.budget] * w.layers if args.workload != "pyramid" else

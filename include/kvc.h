@@ -61,7 +61,10 @@ enum {
     KVC_DEV_BAD_LENGTH = 5,     /* len outside [0, cap]                                       */
     KVC_DEV_NO_CANDIDATE = 6,   /* H2O: cache over budget but no historical token to evict    */
     KVC_DEV_TIMEOUT = 7,        /* a bounded wait inside a kernel gave up (results invalid)   */
-    KVC_DEV_SCHEDULE = 8        /* internal schedule bound violated (results invalid)         */
+    KVC_DEV_SCHEDULE = 8,       /* internal schedule bound violated (results invalid)         */
+    KVC_DEV_BAD_BLOCK = 9,      /* page-table or free-stack entry outside the block pool      */
+    KVC_DEV_POOL_EMPTY = 10,    /* a sequence needed a new block and the free stack was empty */
+    KVC_DEV_POOL_OVERFLOW = 11  /* a released block did not fit on the free stack             */
 };
 
 /* A KV cache (or a prompt's keys/values) in device memory.
@@ -118,6 +121,44 @@ typedef struct {
     const int64_t *t;       /* device scalar: text position of the token being decoded       */
     const float *slopes;    /* device fp32[n_heads_q]: the bias slope of each query head     */
 } kvc_alibi;
+
+/* Paged KV cache for block-level eviction ([KVC] "Implementação prática em vLLM e SGLang": the
+ * cache is allocated in blocks of 16 or 32 tokens reached through a page table; blocks leave
+ * the page table and return to the free pool without their contents being copied).
+ * One pool, one set of page tables and one free stack per layer.
+ * Element (blk, h, j, d) of K is at k + ((blk*n_heads_kv + h)*block_size + j)*d_head + d
+ * (v likewise): a block holds block_size consecutive tokens of every KV head.              */
+typedef struct {
+    void *k;                /* device [n_blocks][n_heads_kv][block_size][d_head]             */
+    void *v;
+    int32_t dtype;          /* kvc_dtype                                                     */
+    int32_t n_blocks;       /* physical blocks in the pool                                   */
+    int32_t n_heads_kv;
+    int32_t block_size;     /* tokens per block                                              */
+    int32_t d_head;
+    int32_t reserved;
+} kvc_block_pool;
+
+/* Page tables of a batch of sequences.  Sequence b holds len[b] tokens in n_blocks[b] blocks:
+ * logical block i is physical block table[b*max_blocks + i]; tokens fill the blocks in table
+ * order, so only the last block may be partly filled (n_blocks[b] = ceil(len[b]/block_size)).
+ * score[b*max_blocks + i] is logical block i's score (kvc_block_accumulate_evict).           */
+typedef struct {
+    int32_t *table;         /* device int32[batch][max_blocks]                               */
+    int32_t *n_blocks;      /* device int32[batch]                                           */
+    int32_t *len;           /* device int32[batch]                                           */
+    float *score;           /* device fp32[batch][max_blocks]                                */
+    int32_t batch;
+    int32_t max_blocks;
+} kvc_page_table;
+
+/* The free pool: a stack of free physical block ids, ids[0 .. *top - 1]. */
+typedef struct {
+    int32_t *ids;           /* device int32[capacity]                                        */
+    int32_t *top;           /* device int32 scalar: number of free ids                       */
+    int32_t capacity;
+    int32_t reserved;
+} kvc_free_pool;
 
 /* ---------------------------------------------------------------------------------------- */
 /* Diagnostics                                                                               */
@@ -285,6 +326,55 @@ kvc_status kvc_decode_attn_alibi(const void *q, int32_t n_heads_q, const kvc_cac
  * power-of-two head count; other counts return KVC_ERR_INVALID_ARG (pass your own slopes).
  * out: host float[n_heads]. */
 kvc_status kvc_alibi_slopes(int32_t n_heads, float *out);
+
+/* Block-level eviction: append one token per sequence to a paged cache.
+ * For every sequence b: if len[b] is a multiple of block_size, a block is popped from the free
+ * stack, appended to the page table (n_blocks[b] += 1) with score 0; then the new token's keys
+ * and values (every KV head) are written at offset len[b] % block_size of the last block and
+ * len[b] += 1.  pos (nullable, with t): device int32[n_blocks][block_size], the text position
+ * *t is stored at the token's place in its physical block (it moves with the block).
+ * k_new, v_new: [batch][n_heads_kv][d_head], pool dtype, contiguous.
+ * When several sequences pop in one call, which free id each receives depends on timing (the
+ * page tables stay valid; their logical contents do not depend on it).  An empty free stack
+ * records KVC_DEV_POOL_EMPTY and skips that sequence; inconsistent lengths record
+ * KVC_DEV_BAD_LENGTH; a table entry outside the pool KVC_DEV_BAD_BLOCK. */
+kvc_status kvc_paged_append(const kvc_block_pool *pool, const kvc_page_table *pt,
+                            const kvc_free_pool *free_pool, const void *k_new, const void *v_new,
+                            const int64_t *t, int32_t *pos, void *stream);
+
+/* Decode attention over a paged cache ("Implementação prática...": FlashDecoding over the
+ * blocks the page tables list): for every query head h of sequence b,
+ *   out[b,h] = sum_j softmax_j(scale * q[b,h].k_j) v_j
+ * over the len[b] tokens of its page table (KV head h / (n_heads_q / n_heads_kv)).
+ * q, out, lse, flags and the workspace are those of kvc_decode_attn_ex, with
+ * cap = max_blocks * block_size (kvc_decode_attn_workspace_bytes(batch, n_heads_q,
+ * n_heads_kv, d_head, cap)); logits (nullable) are indexed by logical slot j = i*block_size +
+ * offset, logits_stride >= cap.  KVC_DECODE_KV_SETTLED extends to the page tables. */
+kvc_status kvc_decode_attn_paged(const void *q, int32_t n_heads_q, const kvc_block_pool *pool,
+                                 const kvc_page_table *pt, float scale, float *out,
+                                 float *logits, int64_t logits_stride, float *lse, void *ws,
+                                 size_t ws_bytes, uint32_t flags, void *stream);
+
+/* Block-level eviction for one decode step ([KVC] "Implementação prática...": Score(block) =
+ * sum over t in the block of s_t; the lowest-scoring blocks leave the page table for the free
+ * pool, without copies).  For every sequence b:
+ *   score[b,i] += sum over query heads h and tokens j of block i of exp(logits[b,h,j] - lse[b,h])
+ *   (s_t is H2O's accumulated attention, summed over the heads: a block holds every head's
+ *   keys and values of its tokens);
+ *   if n_blocks[b] > budget_blocks: among the logical blocks 0 .. n_blocks[b]-recent_blocks-1
+ *   the lowest score is released (equal scores: the newer block); the table and scores after
+ *   it move down one entry, n_blocks[b] -= 1, len[b] -= block_size, and its physical id is
+ *   pushed onto the free stack.  released (nullable): device int32[batch], the released
+ *   logical index or -1.
+ * logits: [batch][n_heads_q][logits_stride] from kvc_decode_attn_paged; lse: [batch][n_heads_q].
+ * recent_blocks >= 1 (the partly filled block is never released), budget_blocks >= recent_blocks,
+ * n_heads_q <= 1024, batch <= 65535.  Two kernels: the score update (one thread block per
+ * table entry and sequence), then the release (one warp per sequence). */
+kvc_status kvc_block_accumulate_evict(const float *logits, int64_t logits_stride,
+                                      const float *lse, int32_t n_heads_q, int32_t block_size,
+                                      const kvc_page_table *pt, const kvc_free_pool *free_pool,
+                                      int32_t budget_blocks, int32_t recent_blocks,
+                                      int32_t *released, void *stream);
 
 /* Decode attention without a caller workspace.  No counterpart on the pages: this is a
  * deployment convenience of this library.  Some callers cannot allocate device memory at the

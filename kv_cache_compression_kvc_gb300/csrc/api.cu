@@ -232,12 +232,19 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
                               logits_stride, lse, ws, ws_bytes, 0u, stream);
 }
 
-// Shared body of the decode entry points: at most one of rope / alibi is given.
+// Paged decode: the page tables of a paged cache (pool described by the kvc_cache view).
+struct PagedView {
+    const int32_t *table;
+    const int32_t *len;
+    int32_t max_blocks, bs, n_pool;
+};
+
+// Shared body of the decode entry points: at most one of rope / alibi / paged is given.
 static kvc_status decode_impl(const void *q, int32_t n_heads_q, const kvc_cache *cache,
                               const int32_t *len, int32_t n_valid, const kvc_rope *rope,
-                              const kvc_alibi *alibi, float scale, float *out, float *logits,
-                              int64_t logits_stride, float *lse, void *ws, size_t ws_bytes,
-                              uint32_t flags, void *stream)
+                              const kvc_alibi *alibi, const PagedView *paged, float scale,
+                              float *out, float *logits, int64_t logits_stride, float *lse,
+                              void *ws, size_t ws_bytes, uint32_t flags, void *stream)
 {
     if (flags & ~(uint32_t)(KVC_DECODE_KV_SETTLED | KVC_DECODE_BALANCE))
         return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: unknown flags 0x%x", flags);
@@ -276,6 +283,8 @@ static kvc_status decode_impl(const void *q, int32_t n_heads_q, const kvc_cache 
                         "kvc_decode_attn_alibi: cap %d < n_sink + window + 1 = %lld", cache->cap,
                         ring);
         slots_max = (int)ring;
+    } else if (paged != nullptr) {
+        slots_max = cache->cap;
     } else if (len == nullptr && (n_valid < 0 || n_valid > cache->cap)) {
         return fail(KVC_ERR_CAPACITY, "kvc_decode_attn: n_valid %d outside [0, cap %d]", n_valid,
                     cache->cap);
@@ -308,6 +317,12 @@ static kvc_status decode_impl(const void *q, int32_t n_heads_q, const kvc_cache 
     } else if (alibi != nullptr) {
         p.S = alibi->n_sink; p.W = alibi->window; p.t = alibi->t;
         p.alibi = alibi->slopes;
+    } else if (paged != nullptr) {
+        p.len = paged->len;
+        p.table = paged->table;
+        p.max_blocks = paged->max_blocks;
+        p.bs = paged->bs;
+        p.n_pool = paged->n_pool;
     }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = out; p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;
@@ -324,6 +339,12 @@ static kvc_status decode_impl(const void *q, int32_t n_heads_q, const kvc_cache 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     bool used = false;
+    if (p.table != nullptr) {
+        e = cache->dtype == KVC_BF16 ? kvc::launch_decode_attn_bf16_paged(p, cache->d_head, G, s)
+                                     : kvc::launch_decode_attn_f32_paged(p, cache->d_head, G, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+        return ok();
+    }
     if (p.alibi != nullptr) {
         e = cache->dtype == KVC_BF16 ? kvc::launch_decode_attn_bf16_alibi(p, cache->d_head, G, s)
                                      : kvc::launch_decode_attn_f32_alibi(p, cache->d_head, G, s);
@@ -351,8 +372,8 @@ kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache 
                               float scale, float *out, float *logits, int64_t logits_stride,
                               float *lse, void *ws, size_t ws_bytes, uint32_t flags, void *stream)
 {
-    return decode_impl(q, n_heads_q, cache, len, n_valid, rope, nullptr, scale, out, logits,
-                       logits_stride, lse, ws, ws_bytes, flags, stream);
+    return decode_impl(q, n_heads_q, cache, len, n_valid, rope, nullptr, nullptr, scale, out,
+                       logits, logits_stride, lse, ws, ws_bytes, flags, stream);
 }
 
 kvc_status kvc_decode_attn_alibi(const void *q, int32_t n_heads_q, const kvc_cache *cache,
@@ -362,8 +383,126 @@ kvc_status kvc_decode_attn_alibi(const void *q, int32_t n_heads_q, const kvc_cac
 {
     if (alibi == nullptr)
         return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn_alibi: null alibi descriptor");
-    return decode_impl(q, n_heads_q, cache, nullptr, 0, nullptr, alibi, scale, out, logits,
-                       logits_stride, lse, ws, ws_bytes, flags, stream);
+    return decode_impl(q, n_heads_q, cache, nullptr, 0, nullptr, alibi, nullptr, scale, out,
+                       logits, logits_stride, lse, ws, ws_bytes, flags, stream);
+}
+
+// ------------------------------------------------------------------------------------------
+// Block-level eviction over page tables.
+static kvc_status check_paged(const kvc_block_pool *pool, const kvc_page_table *pt,
+                              const char *name, kvc_cache *view)
+{
+    if (pool == nullptr || pt == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "%s: null pool or page-table descriptor", name);
+    if (pt->table == nullptr || pt->n_blocks == nullptr || pt->len == nullptr ||
+        pt->score == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "%s: null page-table array", name);
+    if (pool->n_blocks <= 0 || pool->block_size <= 0 || pt->batch <= 0 || pt->max_blocks <= 0)
+        return fail(KVC_ERR_SHAPE, "%s: n_blocks %d block_size %d batch %d max_blocks %d", name,
+                    pool->n_blocks, pool->block_size, pt->batch, pt->max_blocks);
+    if ((long long)pt->max_blocks * pool->block_size > (1LL << 30))
+        return fail(KVC_ERR_SHAPE, "%s: max_blocks * block_size too large", name);
+    kvc_cache c{};
+    c.k = pool->k;
+    c.v = pool->v;
+    c.dtype = pool->dtype;
+    c.batch = pt->batch;
+    c.n_heads_kv = pool->n_heads_kv;
+    c.cap = pt->max_blocks * pool->block_size;
+    c.d_head = pool->d_head;
+    c.stride_b = 0;
+    c.stride_h = (int64_t)pool->block_size * pool->d_head;
+    c.stride_slot = pool->d_head;
+    *view = c;
+    return check_cache(&c, name, true);
+}
+
+static kvc_status check_free_pool(const kvc_free_pool *fp, const char *name)
+{
+    if (fp == nullptr || fp->ids == nullptr || fp->top == nullptr || fp->capacity <= 0)
+        return fail(KVC_ERR_INVALID_ARG, "%s: free pool descriptor", name);
+    return KVC_OK;
+}
+
+kvc_status kvc_paged_append(const kvc_block_pool *pool, const kvc_page_table *pt,
+                            const kvc_free_pool *free_pool, const void *k_new, const void *v_new,
+                            const int64_t *t, int32_t *pos, void *stream)
+{
+    kvc_cache view;
+    kvc_status st = check_paged(pool, pt, "kvc_paged_append", &view);
+    if (st != KVC_OK) return st;
+    st = check_free_pool(free_pool, "kvc_paged_append");
+    if (st != KVC_OK) return st;
+    if (k_new == nullptr || v_new == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_paged_append: null k_new/v_new");
+    if (!aligned16(k_new) || !aligned16(v_new))
+        return fail(KVC_ERR_ALIGN, "kvc_paged_append: k_new/v_new must be 16-byte aligned");
+    int32_t *code = nullptr;
+    st = device_info(&code, nullptr);
+    if (st != KVC_OK) return st;
+    kvc::PagedParams p{};
+    p.k = pool->k; p.v = pool->v;
+    p.n_pool = pool->n_blocks; p.Hkv = pool->n_heads_kv; p.bs = pool->block_size;
+    p.D = pool->d_head; p.B = pt->batch; p.max_blocks = pt->max_blocks;
+    p.table = pt->table; p.n_blocks = pt->n_blocks; p.len = pt->len; p.score = pt->score;
+    p.free_ids = free_pool->ids; p.free_top = free_pool->top; p.free_cap = free_pool->capacity;
+    p.k_new = k_new; p.v_new = v_new; p.t = t; p.pos = pos;
+    p.dev_code = code;
+    cudaError_t e = kvc::launch_paged_append(p, elem_bytes(pool->dtype),
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged append launch");
+    return ok();
+}
+
+kvc_status kvc_decode_attn_paged(const void *q, int32_t n_heads_q, const kvc_block_pool *pool,
+                                 const kvc_page_table *pt, float scale, float *out,
+                                 float *logits, int64_t logits_stride, float *lse, void *ws,
+                                 size_t ws_bytes, uint32_t flags, void *stream)
+{
+    kvc_cache view;
+    kvc_status st = check_paged(pool, pt, "kvc_decode_attn_paged", &view);
+    if (st != KVC_OK) return st;
+    PagedView pv{pt->table, pt->len, pt->max_blocks, pool->block_size, pool->n_blocks};
+    return decode_impl(q, n_heads_q, &view, nullptr, 0, nullptr, nullptr, &pv, scale, out,
+                       logits, logits_stride, lse, ws, ws_bytes, flags, stream);
+}
+
+kvc_status kvc_block_accumulate_evict(const float *logits, int64_t logits_stride,
+                                      const float *lse, int32_t n_heads_q, int32_t block_size,
+                                      const kvc_page_table *pt, const kvc_free_pool *free_pool,
+                                      int32_t budget_blocks, int32_t recent_blocks,
+                                      int32_t *released, void *stream)
+{
+    if (pt == nullptr || pt->table == nullptr || pt->n_blocks == nullptr || pt->len == nullptr ||
+        pt->score == nullptr || logits == nullptr || lse == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_block_accumulate_evict: null argument");
+    kvc_status st = check_free_pool(free_pool, "kvc_block_accumulate_evict");
+    if (st != KVC_OK) return st;
+    if (pt->batch <= 0 || pt->batch > 65535 || pt->max_blocks <= 0 || block_size <= 0 ||
+        n_heads_q <= 0 || n_heads_q > 1024)
+        return fail(KVC_ERR_SHAPE, "kvc_block_accumulate_evict: batch %d max_blocks %d "
+                    "block_size %d n_heads_q %d", pt->batch, pt->max_blocks, block_size,
+                    n_heads_q);
+    if (recent_blocks < 1 || budget_blocks < recent_blocks)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_block_accumulate_evict: recent_blocks %d must be "
+                    ">= 1 and <= budget_blocks %d", recent_blocks, budget_blocks);
+    if (logits_stride < (int64_t)pt->max_blocks * block_size)
+        return fail(KVC_ERR_CAPACITY, "kvc_block_accumulate_evict: logits_stride %lld < %lld",
+                    (long long)logits_stride, (long long)pt->max_blocks * block_size);
+    int32_t *code = nullptr;
+    st = device_info(&code, nullptr);
+    if (st != KVC_OK) return st;
+    kvc::PagedParams p{};
+    p.bs = block_size; p.B = pt->batch; p.max_blocks = pt->max_blocks;
+    p.table = pt->table; p.n_blocks = pt->n_blocks; p.len = pt->len; p.score = pt->score;
+    p.free_ids = free_pool->ids; p.free_top = free_pool->top; p.free_cap = free_pool->capacity;
+    p.logits = logits; p.logits_stride = logits_stride; p.lse = lse; p.Hq = n_heads_q;
+    p.budget_blocks = budget_blocks; p.recent_blocks = recent_blocks; p.released = released;
+    p.n_pool = 0x7fffffff;
+    p.dev_code = code;
+    cudaError_t e = kvc::launch_block_accumulate_evict(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "block accumulate/evict launch");
+    return ok();
 }
 
 kvc_status kvc_alibi_slopes(int32_t n_heads, float *out)

@@ -52,6 +52,12 @@
 // scale * q.k - slope_h * (qpos - r), with the query head's slope from the caller; keys are not
 // rotated.
 //
+// Paged cache ("Implementação prática em vLLM e SGLang": blocks of 16 or 32 tokens behind a page
+// table).  The slots of a sequence are its page table's blocks in order; a tile of TK logical
+// slots is copied run by run, one bulk copy per block it touches, from the pool's
+// [block][head][slot][d] rows, so the compute loop is unchanged.  A table entry outside the pool
+// records KVC_DEV_BAD_BLOCK and reads block 0 instead (the copy sizes stay as announced).
+//
 // Waits on mbarriers are bounded: after kMbarSpinLimit failed polls the thread records
 // KVC_DEV_TIMEOUT and carries on (results are then garbage, but the kernel always finishes).
 #pragma once
@@ -123,13 +129,15 @@ struct DecodeSmem {
 };
 
 // RM: 0 no RoPE, 1 RoPE with one table row per key, 2 factored RoPE (G == 1, n_pos >= TK),
-// 3 ALiBi.  Modes 1-3 read the StreamingLLM sink + ring layout in rank order.
+// 3 ALiBi, 4 paged (no positional term).  Modes 1-3 read the StreamingLLM sink + ring layout in
+// rank order.
 template <typename T, int D, int G, int VW, int UNR, int RM, int CPS>
 __global__ void __launch_bounds__(kDecodeThreads, CPS)
 decode_attn_kernel(const DecodeParams p)
 {
     using SM = DecodeSmem<T, D, G, RM>;
-    constexpr bool RANKED = RM != 0;     // sink + ring layout, visited in rank order
+    constexpr bool RANKED = RM >= 1 && RM <= 3;   // sink + ring layout, visited in rank order
+    constexpr bool PAGED = RM == 4;
     constexpr bool ROPE = RM == 1 || RM == 2;
     constexpr bool FACT = RM == 2;
     constexpr bool ALIBI = RM == 3;
@@ -153,6 +161,9 @@ decode_attn_kernel(const DecodeParams p)
     const uint32_t bar_full = sbase;                 // NS x 8 bytes
     const uint32_t bar_empty = sbase + 8 * NS;       // NS x 8 bytes
     const uint32_t stage0 = sbase + SM::kBarBytes;
+    // bytes 128..255 of the barrier area: the issuing thread's cache of page-table entries
+    static_assert(16 * NS <= 128, "barriers fit below the table cache");
+    constexpr int kTabCache = 32;
     float *sm_m = reinterpret_cast<float *>(smem + SM::kBarBytes + NS * SM::kStageBytes);
     float *sm_l = sm_m + NW * G;
     float *sm_o = sm_l + NW * G;                     // [NW][G][D]
@@ -208,6 +219,10 @@ decode_attn_kernel(const DecodeParams p)
     // number of work items (slots without RoPE, ranks with it) of pair q
     auto pair_slots = [&](int q) -> int {
         if (RANKED) return n_att;
+        if (PAGED) {
+            const int n = p.len[q / p.Hkv];
+            return n < 0 ? 0 : (n > p.cap ? p.cap : n);
+        }
         if (p.len != nullptr) {
             const int n = p.len[q];
             return n < 0 ? 0 : (n > p.cap ? p.cap : n);
@@ -220,6 +235,23 @@ decode_attn_kernel(const DecodeParams p)
     // The issuing thread keeps the slot count of the pair it is loading: one global read per
     // pair, not one per tile on the critical path of every copy.
     int iss_q = -1, iss_slots = 0;
+    // Paged: it also keeps up to kTabCache page-table entries of the sequence it is loading in
+    // shared memory, fetched together with cp.async (one round trip per refill, not one per
+    // block on the critical path of every copy).
+    int tab_b = -1, tab_lo = 0, tab_cnt = 0;
+    auto table_entry = [&](int b, int lb) -> int {
+        if (b != tab_b || lb < tab_lo || lb >= tab_lo + tab_cnt) {
+            tab_b = b;
+            tab_lo = lb;
+            tab_cnt = min(kTabCache, p.max_blocks - lb);
+            const int32_t *src = p.table + (size_t)b * p.max_blocks + lb;
+            for (int k = 0; k < tab_cnt; ++k)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                             :: "r"(sbase + 128 + 4 * k), "l"(src + k) : "memory");
+            asm volatile("cp.async.wait_all;" ::: "memory");
+        }
+        return reinterpret_cast<const int32_t *>(smem + 128)[lb - tab_lo];
+    };
     auto issue_tile = [&](int i) {
         const long long t = t_begin + i;
         const int s = i % NS;
@@ -262,7 +294,24 @@ decode_attn_kernel(const DecodeParams p)
             }
         };
         const int j1 = j0 + rows;
-        if (!RANKED) {
+        if constexpr (PAGED) {
+            // one run per block of the page table the tile touches
+            const size_t blk_elems = (size_t)p.Hkv * p.bs * D;
+            for (int r = j0; r < j1;) {
+                const int lb = r / p.bs, off = r - lb * p.bs;
+                const int n = min(j1 - r, p.bs - off);
+                int phys = table_entry(b, lb);
+                if (phys < 0 || phys >= p.n_pool) {
+                    record_code(p.dev_code, 9 /* KVC_DEV_BAD_BLOCK */);
+                    phys = 0;
+                }
+                const size_t src = (size_t)phys * blk_elems + ((size_t)kh * p.bs + off) * D;
+                const uint32_t doff = (uint32_t)((r - j0) * D * EB);
+                bulk_g2s(kdst + doff, static_cast<const T *>(p.k) + src, n * D * EB, full);
+                bulk_g2s(vdst + doff, static_cast<const T *>(p.v) + src, n * D * EB, full);
+                r += n;
+            }
+        } else if (!RANKED) {
             copy_run(j0, j1, j0);
         } else {
             copy_run(j0, min(j1, p.S), j0);                          // sinks
@@ -647,6 +696,7 @@ cudaError_t launch_decode_rm(const DecodeParams &p, cudaStream_t stream)
 constexpr int kDecodePlain = 0;   // valid slots 0 .. len-1, no positional term
 constexpr int kDecodeRope = 1;    // StreamingLLM layout, RoPE at in-cache positions
 constexpr int kDecodeAlibi = 2;   // StreamingLLM layout, ALiBi at in-cache positions
+constexpr int kDecodePaged = 3;   // page-table cache, no positional term
 
 // RoPE with one query head per KV head takes the factored rotation when the table covers the
 // per-lane offsets 0 .. TK-1; otherwise each key reads its table row.
@@ -657,6 +707,8 @@ cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
         return launch_decode_rm<T, D, G, 0>(p, stream);
     } else if constexpr (MODE == kDecodeAlibi) {
         return launch_decode_rm<T, D, G, 3>(p, stream);
+    } else if constexpr (MODE == kDecodePaged) {
+        return launch_decode_rm<T, D, G, 4>(p, stream);
     } else if constexpr (G == 1) {
         if (p.n_pos >= DecodeSmem<T, D, G, 2>::TK) return launch_decode_rm<T, D, G, 2>(p, stream);
         return launch_decode_rm<T, D, G, 1>(p, stream);

@@ -45,6 +45,9 @@ struct DecodeParams {
     const float *cos_sin;        // [n_pos][2][D/2]: cosines then sines per distance
     int32_t n_pos;               // rows of cos_sin
     const float *alibi;          // ALiBi slopes per query head [Hq] (same layout as RoPE) or null
+    // paged cache: K/V pool [n_pool][Hkv][bs][D]; len is per sequence [B]; cap = max_blocks*bs
+    const int32_t *table;        // [B][max_blocks] physical block of each logical block
+    int32_t max_blocks, bs, n_pool;
     int32_t kv_settled;          // cache slots and lengths final before the previous launch began
     int32_t balance;             // split the tiles by the lengths (not by capacity)
     float scale_log2;            // scale * log2(e)
@@ -77,6 +80,9 @@ cudaError_t launch_decode_attn_mma(const DecodeParams &p, int D, int G, cudaStre
 cudaError_t launch_decode_attn_f32_rope(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16_rope(const DecodeParams &p, int D, int G,
                                          cudaStream_t stream);
+cudaError_t launch_decode_attn_f32_paged(const DecodeParams &p, int D, int G, cudaStream_t stream);
+cudaError_t launch_decode_attn_bf16_paged(const DecodeParams &p, int D, int G,
+                                          cudaStream_t stream);
 cudaError_t launch_decode_attn_f32_alibi(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16_alibi(const DecodeParams &p, int D, int G,
                                           cudaStream_t stream);
@@ -168,6 +174,35 @@ cudaError_t launch_topk_rows(const float *score, int64_t score_stride, int rows,
                              int tail, int32_t *idx, int64_t idx_stride, cudaStream_t stream);
 cudaError_t launch_iota_rows(int32_t *idx, int64_t idx_stride, int rows, int n,
                              cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// Block-level eviction over page tables.
+struct PagedParams {
+    void *k;                     // pool [n_pool][Hkv][bs][D]
+    void *v;
+    int32_t n_pool, Hkv, bs, D, B, max_blocks;
+    int32_t *table;              // [B][max_blocks]
+    int32_t *n_blocks;           // [B]
+    int32_t *len;                // [B]
+    float *score;                // [B][max_blocks]
+    int32_t *free_ids;           // [free_cap] stack of free physical blocks
+    int32_t *free_top;           // number of ids on the stack
+    int32_t free_cap;
+    // append
+    const void *k_new;           // [B][Hkv][D]
+    const void *v_new;
+    const int64_t *t;            // nullable
+    int32_t *pos;                // nullable [n_pool][bs]
+    // accumulate / release
+    const float *logits;         // [B*Hq][logits_stride], logical slots
+    int64_t logits_stride;
+    const float *lse;            // [B*Hq]
+    int32_t Hq, budget_blocks, recent_blocks;
+    int32_t *released;           // nullable [B]
+    int32_t *dev_code;
+};
+cudaError_t launch_paged_append(const PagedParams &p, int elem_bytes, cudaStream_t stream);
+cudaError_t launch_block_accumulate_evict(const PagedParams &p, cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------
 // H2O.

@@ -20,6 +20,9 @@ Workloads (sizes as stated by the benchmark configuration):
               fall linearly (ratio 4) around a mean of 8192; sink-boosted keys 0-3; 256 steps.
   alibi       the streaming shape with ALiBi at in-cache positions in place of RoPE (slopes
               2^(-8(h+1)/32) for the 32 heads); same cache, prompt and steps.
+  paged       the h2o shape with block-level eviction: blocks of 32 tokens, 26 blocks (832
+              tokens, >= the 819 budget) per sequence, the 13 newest (>= 410 recent tokens)
+              protected; pools of N(0,1) keys and values.
 """
 from __future__ import annotations
 
@@ -75,6 +78,8 @@ WORKLOADS = {
                         L_obs=64, budget=8192),
     "alibi": Workload("alibi", 32, 16, 32, 32, 128, 4096, 1024, torch.bfloat16, 1240,
                       n_sink=4, window=2044),
+    "paged": Workload("paged", 32, 16, 32, 32, 128, 4096, 512, torch.bfloat16, 1241,
+                      budget=819, L_local=410, extra={"block_size": 32}),
 }
 
 

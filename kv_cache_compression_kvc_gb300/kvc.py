@@ -51,6 +51,24 @@ class kvc_alibi(ctypes.Structure):
                 ("t", ctypes.c_void_p), ("slopes", ctypes.c_void_p)]
 
 
+class kvc_block_pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dtype", ctypes.c_int32),
+                ("n_blocks", ctypes.c_int32), ("n_heads_kv", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("d_head", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class kvc_page_table(ctypes.Structure):
+    _fields_ = [("table", ctypes.c_void_p), ("n_blocks", ctypes.c_void_p),
+                ("len", ctypes.c_void_p), ("score", ctypes.c_void_p),
+                ("batch", ctypes.c_int32), ("max_blocks", ctypes.c_int32)]
+
+
+class kvc_free_pool(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("top", ctypes.c_void_p),
+                ("capacity", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -61,6 +79,9 @@ _F32 = ctypes.c_float
 _CACHE_P = ctypes.POINTER(kvc_cache)
 _ROPE_P = ctypes.POINTER(kvc_rope)
 _ALIBI_P = ctypes.POINTER(kvc_alibi)
+_POOL_P = ctypes.POINTER(kvc_block_pool)
+_PT_P = ctypes.POINTER(kvc_page_table)
+_FREE_P = ctypes.POINTER(kvc_free_pool)
 
 # name -> (restype, argtypes); every symbol declared in include/kvc.h
 SIGNATURES = {
@@ -84,6 +105,11 @@ SIGNATURES = {
     "kvc_decode_attn_alibi": (_I32, [_P, _I32, _CACHE_P, _ALIBI_P, _F32, _P, _P, _I64, _P, _P,
                                      _SZ, _U32, _P]),
     "kvc_alibi_slopes": (_I32, [_I32, _P]),
+    "kvc_paged_append": (_I32, [_POOL_P, _PT_P, _FREE_P, _P, _P, _P, _P, _P]),
+    "kvc_decode_attn_paged": (_I32, [_P, _I32, _POOL_P, _PT_P, _F32, _P, _P, _I64, _P, _P, _SZ,
+                                     _U32, _P]),
+    "kvc_block_accumulate_evict": (_I32, [_P, _I64, _P, _I32, _I32, _PT_P, _FREE_P, _I32, _I32,
+                                          _P, _P]),
     "kvc_decode_attn_noalloc": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P,
                                        _I64, _P, _P]),
     "kvc_h2o_accumulate_evict": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P,
@@ -300,6 +326,85 @@ def kvc_decode_attn_alibi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         _ptr(q), Hq, ctypes.byref(c), ctypes.byref(alibi), float(scale), _ptr(out),
         _ptr(logits), lstride, _ptr(lse), wp, wb, int(flags), _stream(stream)))
     return out
+
+
+def block_pool_view(k_pool: torch.Tensor, v_pool: torch.Tensor) -> kvc_block_pool:
+    """Describe a block pool: K and V tensors [n_blocks, n_heads_kv, block_size, d_head],
+    contiguous."""
+    if k_pool.dim() != 4 or not k_pool.is_contiguous() or v_pool.shape != k_pool.shape or \
+            not v_pool.is_contiguous() or v_pool.dtype != k_pool.dtype:
+        raise ValueError("block pools are contiguous [n_blocks, n_heads_kv, block_size, d_head]")
+    c = kvc_block_pool()
+    c.k, c.v = k_pool.data_ptr(), v_pool.data_ptr()
+    c.dtype = _dtype_code(k_pool.dtype)
+    c.n_blocks, c.n_heads_kv, c.block_size, c.d_head = (int(x) for x in k_pool.shape)
+    return c
+
+
+def page_table_view(table: torch.Tensor, n_blocks: torch.Tensor, len: torch.Tensor,
+                    score: torch.Tensor) -> kvc_page_table:
+    """table int32 [batch, max_blocks], n_blocks / len int32 [batch], score fp32
+    [batch, max_blocks], all contiguous."""
+    B, mb = table.shape
+    if table.dtype != torch.int32 or n_blocks.dtype != torch.int32 or len.dtype != torch.int32 \
+            or score.dtype != torch.float32 or tuple(score.shape) != (B, mb) or \
+            not (table.is_contiguous() and score.is_contiguous()):
+        raise ValueError("page table: int32 table [B, max_blocks], int32 n_blocks/len [B], "
+                         "fp32 score [B, max_blocks]")
+    c = kvc_page_table()
+    c.table, c.n_blocks, c.len, c.score = (table.data_ptr(), n_blocks.data_ptr(), len.data_ptr(),
+                                           score.data_ptr())
+    c.batch, c.max_blocks = B, mb
+    return c
+
+
+def free_pool_view(ids: torch.Tensor, top: torch.Tensor) -> kvc_free_pool:
+    """ids int32 [capacity] (a stack, ids[:top]), top int32 [1]."""
+    c = kvc_free_pool()
+    c.ids, c.top = ids.data_ptr(), top.data_ptr()
+    c.capacity = ids.numel()
+    return c
+
+
+def kvc_paged_append(pool: kvc_block_pool, pt: kvc_page_table, free_pool: kvc_free_pool,
+                     k_new: torch.Tensor, v_new: torch.Tensor, *,
+                     t: Optional[torch.Tensor] = None, pos: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    _check(load().kvc_paged_append(ctypes.byref(pool), ctypes.byref(pt), ctypes.byref(free_pool),
+                                   _ptr(k_new), _ptr(v_new), _ptr(t), _ptr(pos),
+                                   _stream(stream)))
+
+
+def kvc_decode_attn_paged(q: torch.Tensor, pool: kvc_block_pool, pt: kvc_page_table, *,
+                          scale: float, flags: int = 0, out: Optional[torch.Tensor] = None,
+                          logits: Optional[torch.Tensor] = None,
+                          lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """q [B, Hq, D] -> out [B, Hq, D] fp32 over each sequence's page table."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(B, Hq, pool.n_heads_kv, D, pt.max_blocks * pool.block_size,
+                              q.device)
+    wp, wb = _ws_ptr(ws)
+    lstride = logits.stride(-2) if logits is not None else 0
+    _check(load().kvc_decode_attn_paged(
+        _ptr(q), Hq, ctypes.byref(pool), ctypes.byref(pt), float(scale), _ptr(out),
+        _ptr(logits), lstride, _ptr(lse), wp, wb, int(flags), _stream(stream)))
+    return out
+
+
+def kvc_block_accumulate_evict(logits: torch.Tensor, lse: torch.Tensor, pt: kvc_page_table,
+                               free_pool: kvc_free_pool, *, block_size: int, budget_blocks: int,
+                               recent_blocks: int, released: Optional[torch.Tensor] = None,
+                               stream=None) -> None:
+    """logits [B, Hq, >= max_blocks*block_size], lse [B, Hq]."""
+    B, Hq = lse.shape
+    _check(load().kvc_block_accumulate_evict(
+        _ptr(logits), logits.stride(-2), _ptr(lse), Hq, int(block_size), ctypes.byref(pt),
+        ctypes.byref(free_pool), int(budget_blocks), int(recent_blocks), _ptr(released),
+        _stream(stream)))
 
 
 def kvc_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,

@@ -139,3 +139,36 @@ def test_alibi_validation_before_launch(kvc):
     st = lib.kvc_decode_attn_alibi(4096, 1, ctypes.byref(c), ctypes.byref(a), 1.0, 4096, None,
                                    0, None, None, 0, 0, None)
     assert st == 1                                                 # no slopes
+
+
+def test_paged_validation_before_launch(kvc):
+    lib = kvc.load()
+    pool = kvc.kvc_block_pool()
+    pool.k = pool.v = 4096
+    pool.dtype, pool.n_blocks, pool.n_heads_kv, pool.block_size, pool.d_head = \
+        kvc.KVC_BF16, 8, 2, 16, 96
+    pt = kvc.kvc_page_table()
+    pt.table = pt.n_blocks = pt.len = pt.score = 4096
+    pt.batch, pt.max_blocks = 2, 4
+    fp = kvc.kvc_free_pool()
+    fp.ids, fp.top, fp.capacity = 4096, 4096, 8
+    B = ctypes.byref
+    st = lib.kvc_decode_attn_paged(4096, 2, B(pool), B(pt), 1.0, 4096, None, 0, None, None, 0,
+                                   0, None)
+    assert st == 2 and "d_head" in kvc.kvc_last_error()           # KVC_ERR_SHAPE
+    pool.d_head = 128
+    pt.table = None
+    st = lib.kvc_paged_append(B(pool), B(pt), B(fp), 4096, 4096, None, None, None)
+    assert st == 1                                                 # null page-table array
+    pt.table = 4096
+    fp.capacity = 0
+    st = lib.kvc_paged_append(B(pool), B(pt), B(fp), 4096, 4096, None, None, None)
+    assert st == 1                                                 # empty free-pool descriptor
+    fp.capacity = 8
+    st = lib.kvc_block_accumulate_evict(4096, 64, 4096, 4, 16, B(pt), B(fp), 3, 0, None, None)
+    assert st == 1 and "recent_blocks" in kvc.kvc_last_error()    # recent quota of 0 blocks
+    st = lib.kvc_block_accumulate_evict(4096, 63, 4096, 4, 16, B(pt), B(fp), 3, 1, None, None)
+    assert st == 4                                                 # logits_stride < 4 * 16
+    st = lib.kvc_decode_attn_paged(4096, 2, B(pool), B(pt), 1.0, 4096, 4096, 32, None, None, 0,
+                                   0, None)
+    assert st == 4                                                 # logits_stride < cap 64
