@@ -235,16 +235,18 @@ decode_attn_kernel(const DecodeParams p)
     // The issuing thread keeps the slot count of the pair it is loading: one global read per
     // pair, not one per tile on the critical path of every copy.
     int iss_q = -1, iss_slots = 0;
-    // Paged: it also keeps up to kTabCache page-table entries of the sequence it is loading in
-    // shared memory, fetched together with cp.async (one round trip per refill, not one per
-    // block on the critical path of every copy).
+    // Paged: it also keeps a window of kTabCache page-table entries of the sequence it is
+    // loading in shared memory, fetched together with cp.async (one round trip per window, not
+    // one per block on the critical path of every copy).
     int tab_b = -1, tab_lo = 0, tab_cnt = 0;
     auto table_entry = [&](int b, int lb) -> int {
         if (b != tab_b || lb < tab_lo || lb >= tab_lo + tab_cnt) {
+            // aligned windows: every head of a sequence restarts at block 0, and a sequence of
+            // at most kTabCache blocks is fetched once
             tab_b = b;
-            tab_lo = lb;
-            tab_cnt = min(kTabCache, p.max_blocks - lb);
-            const int32_t *src = p.table + (size_t)b * p.max_blocks + lb;
+            tab_lo = lb - lb % kTabCache;
+            tab_cnt = min(kTabCache, p.max_blocks - tab_lo);
+            const int32_t *src = p.table + (size_t)b * p.max_blocks + tab_lo;
             for (int k = 0; k < tab_cnt; ++k)
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
                              :: "r"(sbase + 128 + 4 * k), "l"(src + k) : "memory");
@@ -258,8 +260,9 @@ decode_attn_kernel(const DecodeParams p)
         const int q = (int)(t / p.NT);
         const int j0 = (int)(t % p.NT) * TK;
         if (q != iss_q) {
+            // paged: the pairs of a sequence share its length
+            if (!PAGED || iss_q < 0 || q / p.Hkv != iss_q / p.Hkv) iss_slots = pair_slots(q);
             iss_q = q;
-            iss_slots = pair_slots(q);
         }
         const int rows = max(0, min(TK, iss_slots - j0));
         const uint32_t full = bar_full + 8 * s;
@@ -343,10 +346,15 @@ decode_attn_kernel(const DecodeParams p)
     float slope2[G];           // ALiBi: the query heads' slopes times log2(e)
     int cur = -1;              // pair in progress
     int cur_slots = 0;
+    int cur_li = -1;           // whose length cur_slots holds (paged: the pairs of a sequence share it)
 
     auto start_pair = [&](int q) {
         cur = q;
-        cur_slots = pair_slots(q);
+        const int li = PAGED ? q / p.Hkv : q;
+        if (li != cur_li) {
+            cur_li = li;
+            cur_slots = pair_slots(q);
+        }
         const int b = q / p.Hkv, kh = q % p.Hkv;
         const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)kh * G) * D;
 #pragma unroll
