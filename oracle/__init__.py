@@ -8,7 +8,7 @@ with gcc into ``oracle/_build/``.  This module only marshals numpy arrays.
 Functions (each follows the page passage cited in ``kvc_oracle.c``):
   kv_bytes, pyramid_budgets, rope, attend, stream_window, stream_slot, stream_decode,
   stream_decode_alibi, topk_ascending, snapkv_obs_scores, pool1d, snapkv_select, snapkv_stage_f32,
-  h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_evict_f32, block_step, block_evict_f32.
+  h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_step_group, h2o_evict_f32, block_step, block_evict_f32.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against values the pages
 print, closed forms, invariants, library routines on special cases or brute force on tiny
@@ -77,6 +77,9 @@ _SIGS = {
     "orc_h2o_step": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _f64, _ptr, _ptr, _ptr, _ptr,
                                     _ptr, _i64, ctypes.c_int, ctypes.c_int, _ptr, _ptr]),
     "orc_h2o_evict_f32": (ctypes.c_int, [ctypes.c_int, _ptr, _ptr, _i64, ctypes.c_int]),
+    "orc_h2o_step_group": (ctypes.c_int, [ctypes.c_int] * 3 + [_f64, _ptr, _ptr, _ptr, _ptr,
+                                                               _ptr, _i64, ctypes.c_int,
+                                                               ctypes.c_int, _ptr]),
     "orc_block_step": (ctypes.c_int, [ctypes.c_int] * 5 + [_f64, _ptr, _ptr, _ptr, _ptr,
                                                            ctypes.c_int, ctypes.c_int, _ptr]),
     "orc_block_evict_f32": (ctypes.c_int, [ctypes.c_int, _ptr, ctypes.c_int, ctypes.c_int]),
@@ -256,6 +259,20 @@ def h2o_step(q, K, V, pos, s, t: int, L_local: int, budget: int, scale: float):
     ev = lib().orc_h2o_step(n, D, scale, _p(q), _p(K), _p(V), _p(pos), _p(s_new), int(t),
                             L_local, budget, _p(out), _p(alpha))
     return out, s_new, alpha[:n].copy(), int(ev)
+
+
+def h2o_step_group(q, K, V, pos, s, t: int, L_local: int, budget: int, scale: float):
+    """One decode step of a grouped-query KV head: q [G, D]; returns (out [G, D], s_new,
+    evicted slot or -1).  s is not modified."""
+    q, K, V = _f(q), _f(K), _f(V)
+    G, D = q.shape
+    n = K.shape[0]
+    pos = np.ascontiguousarray(np.asarray(pos, dtype=np.int64))
+    s_new = _f(s).copy()
+    out = np.empty((G, D))
+    ev = lib().orc_h2o_step_group(G, n, D, scale, _p(q), _p(K), _p(V), _p(pos), _p(s_new),
+                                  int(t), L_local, budget, _p(out))
+    return out, s_new, int(ev)
 
 
 def h2o_evict_f32(s_f32, pos, t: int, L_local: int) -> int:

@@ -447,6 +447,32 @@ int orc_h2o_step(int n_slots, int D, double scale, const double *q, const double
     return ev;
 }
 
+/* H2O on a grouped-query cache.  [KVC] H2O fixes s_j = sum over steps of alpha_j for one
+ * head; with grouped-query attention ([KVCL] "01 · Conceito": several query heads share one
+ * KV head) a cached row serves G query heads and can only be evicted for all of them.
+ * Reading: the row's score is the sum over the group of its query heads' attention,
+ * s_j += sum_g alpha_{g,j}; the eviction rule is that of orc_h2o_step.  q: [G][D];
+ * out: [G][D].  Returns the evicted slot or -1.                                              */
+int orc_h2o_step_group(int G, int n_slots, int D, double scale, const double *q,
+                       const double *K, const double *V, const int64_t *pos, double *s,
+                       int64_t t, int L_local, int budget, double *out)
+{
+    double *l = (double *)malloc(sizeof(double) * (size_t)(n_slots > 0 ? n_slots : 1));
+    for (int g = 0; g < G; ++g) {
+        double lse;
+        orc_attend(n_slots, D, scale, q + (size_t)g * D, K, V, out + (size_t)g * D, l, &lse);
+        for (int j = 0; j < n_slots; ++j) s[j] += exp(l[j] - lse);
+    }
+    free(l);
+    if (n_slots <= budget) return -1;
+    int ev = -1;
+    for (int j = 0; j < n_slots; ++j) {
+        if (pos[j] > t - L_local) continue;
+        if (ev < 0 || s[j] < s[ev] || (s[j] == s[ev] && pos[j] > pos[ev])) ev = j;
+    }
+    return ev;
+}
+
 /* The eviction decision alone, in fp32, on given fp32 scores (the GPU's own). */
 int orc_h2o_evict_f32(int n_slots, const float *s, const int64_t *pos, int64_t t, int L_local)
 {

@@ -626,3 +626,41 @@ def test_block_release_rules():
     assert oracle.block_evict_f32(s, 5, 2) == 2             # tie 1/2: the newer goes
     assert oracle.block_evict_f32(s, 5, 1) == 4             # recent quota of one block
     assert oracle.block_evict_f32(s, 5, 5) == 0             # only the oldest is a candidate
+
+
+# ---------------------------------------------------------------------------- grouped-query H2O
+def test_h2o_group_of_one_is_h2o():
+    rng = np.random.default_rng(51)
+    n, D, t, L_local, budget = 9, 8, 40, 3, 8
+    K, V = rng.standard_normal((n, D)), rng.standard_normal((n, D))
+    pos = np.array([0, 5, 7, 12, 20, 30, 38, 39, 40])
+    s0 = rng.random(n)
+    q = rng.standard_normal(D)
+    o1, s1, _, e1 = oracle.h2o_step(q, K, V, pos, s0, t, L_local, budget, 0.3)
+    og, sg, eg = oracle.h2o_step_group(q[None], K, V, pos, s0, t, L_local, budget, 0.3)
+    assert eg == e1 and np.array_equal(sg, s1) and np.array_equal(og[0], o1)
+
+
+def test_h2o_group_sums_the_heads_attention():
+    """Library softmax per query head, summed over the group; the increments total G; the
+    evicted row is the brute-force minimum over the candidates (ties: larger position)."""
+    rng = np.random.default_rng(52)
+    G, n, D, t, L_local, budget = 4, 12, 8, 60, 4, 11
+    K, V = rng.standard_normal((n, D)), rng.standard_normal((n, D))
+    pos = np.array([1, 3, 9, 10, 14, 22, 31, 44, 57, 58, 59, 60])
+    q = rng.standard_normal((G, D))
+    s0 = rng.random(n) * 2
+    scale = 1 / math.sqrt(D)
+    out, s_new, ev = oracle.h2o_step_group(q, K, V, pos, s0, t, L_local, budget, scale)
+    want = s0.copy()
+    for g in range(G):
+        want += torch.softmax(torch.from_numpy(K @ q[g] * scale), dim=0).numpy()
+        ref = _sdpa(q[g][None], K, V, scale, causal=False)[0]
+        assert np.max(np.abs(out[g] - ref)) <= 1e-12
+    assert np.max(np.abs(s_new - want)) <= 1e-12
+    assert abs((s_new - s0).sum() - G) <= 1e-12
+    cands = [j for j in range(n) if pos[j] <= t - L_local]
+    assert ev == sorted(cands, key=lambda j: (want[j], -pos[j]))[0]
+    # one head of the group alone gives different scores: every head counts
+    _, s_one, ev_one = oracle.h2o_step_group(q[:1], K, V, pos, s0, t, L_local, budget, scale)
+    assert not np.allclose(s_one, s_new)
