@@ -12,7 +12,8 @@ HBM bandwidth is reported against the measured copy peak.
 Other workloads (--workload): snapkv (select + compact + 256-step decode), h2o (prompt
 selection + per-step accumulate/evict), pyramid (per-layer budgets, D=256, GQA 6), alibi (the
 streaming shape with ALiBi at in-cache positions instead of RoPE), paged (block-level eviction
-over page tables at the H2O shape).
+over page tables at the H2O shape), h2o_gqa (H2O on a grouped-query cache, 32 query heads over 8
+KV heads).
 
 Multi-GPU: the path shards into independent replicas (no exchange step); under torchrun every
 rank runs the same workload on its own GPU and rank 0 prints the aggregate.
@@ -625,6 +626,91 @@ class H2O(DecodeWorkload):
                 f"slice, extrapolated to {slices} slices per step (extrapolated)")
 
 
+class H2OGrouped(H2O):
+    """H2O on a grouped-query cache (Hq=32, Hkv=8): per step, free-slot append, decode on the
+    tensor cores with logits, and the grouped score update (the attention of the four query
+    heads of a KV head summed), on a second stream beside the next layer's decode."""
+
+    traffic_key = "decode_mma/h2o_gqa"
+    kernel_file = "decode_mma.cu"
+    kernel_name = "decode_mma_kernel"
+
+    def __init__(self, w: I.Workload, dev, kvc):
+        DecodeWorkload.__init__(self, w, dev, kvc)
+        L, B, H, D = w.layers, w.batch, w.n_heads_kv, w.d_head
+        self.cap = w.budget + 1
+        self.K = torch.empty((L, B, H, self.cap, D), dtype=w.dtype, device=dev)
+        self.V = torch.empty_like(self.K)
+        self.pos = torch.full((L, B, H, self.cap), -1, dtype=torch.int32, device=dev)
+        self.score = torch.zeros((L, B, H, self.cap), dtype=torch.float32, device=dev)
+        rng = np.random.default_rng(w.seed)
+        K_hh = w.budget - w.L_local
+        for l in range(L):
+            g = I.generator(w.seed * 1000 + l, dev)
+            self.K[l].normal_(generator=g)
+            self.V[l].normal_(generator=g)
+            old = np.sort(rng.random((B * H, w.prompt - w.L_local)).argsort(axis=1)[:, :K_hh],
+                          axis=1)
+            recent = np.tile(np.arange(w.prompt - w.L_local, w.prompt), (B * H, 1))
+            self.pos[l, :, :, :w.budget] = torch.from_numpy(
+                np.concatenate([old, recent], axis=1).astype(np.int32)).reshape(B, H, -1).to(dev)
+            self.score[l, :, :, :w.budget] = torch.from_numpy(
+                rng.random((B, H, w.budget)).astype(np.float32) * w.group).to(dev)
+        self.free = torch.full((L, B * H), w.budget, dtype=torch.int32, device=dev)
+        self.logits = torch.empty((L, B, w.n_heads_q, self.cap), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((L, B, w.n_heads_q), dtype=torch.float32, device=dev)
+        self.t = torch.tensor([w.prompt], dtype=torch.int64, device=dev)
+        self.caches = [kvc.cache_view(self.K[l], self.V[l]) for l in range(L)]
+        self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.cap, dev)
+        self.launches_per_step = 3 * L + 1
+        self.side = torch.cuda.Stream(device=dev)
+        self.done = [torch.cuda.Event() for _ in range(L)]
+
+    def decode_layer(self, l, flags=0):
+        kvc, w = self.kvc, self.w
+        kvc.kvc_decode_attn_ex(self.q_s[l], None, None, scale=w.scale, flags=flags,
+                               n_valid=self.cap, out=self.out[l], logits=self.logits[l],
+                               lse=self.lse[l], ws=self.ws, cache=self.caches[l])
+        self.done[l].record(torch.cuda.current_stream())
+        self.side.wait_event(self.done[l])
+        kvc.kvc_h2o_accumulate_evict_gqa(self.logits[l], self.lse[l], self.score[l],
+                                         self.pos[l], self.free[l], n_slots=self.cap, t=self.t,
+                                         L_local=w.L_local, budget=w.budget, stream=self.side)
+
+    def describe(self):
+        w = self.w
+        return {"workload": "H2O eviction during decode, grouped-query cache", "layers": w.layers,
+                "batch": w.batch, "n_heads_q": w.n_heads_q, "n_heads_kv": w.n_heads_kv,
+                "d_head": w.d_head, "budget": w.budget, "L_local": w.L_local,
+                "K_hh": w.budget - w.L_local, "kv_dtype": "bf16", "l2": "inputs larger than L2",
+                "init": "caches of N(0,1) keys/values at the 410 newest and 409 random older "
+                        "prompt positions, random scores (no prompt selection in this workload)",
+                "graph": "appends, then decode + grouped accumulate/evict per layer (the update "
+                         "of layer l on a second stream beside the decode of layer l + 1), as "
+                         "two CUDA graphs"}
+
+    def oracle_sample(self, budget_s=12.0):
+        import oracle
+        w = self.w
+        rng = np.random.default_rng(0)
+        n = w.budget + 1
+        K, V = rng.standard_normal((n, w.d_head)), rng.standard_normal((n, w.d_head))
+        q = rng.standard_normal((w.group, w.d_head))
+        pos = np.arange(n)
+        s = rng.random(n)
+        oracle.h2o_step_group(q, K, V, pos, s, n, w.L_local, w.budget, w.scale)
+        cnt, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.h2o_step_group(q, K, V, pos, s, n, w.L_local, w.budget, w.scale)
+            cnt += 1
+        return (time.perf_counter() - t0) / cnt, w.batch * w.n_heads_kv * w.layers, cnt
+
+    def sample_description(self, n, slices):
+        return (f"{n} oracle grouped H2O steps (attend for the group, accumulate, evict) of one "
+                f"(batch, KV head, layer) slice, extrapolated to {slices} slices per step "
+                f"(extrapolated)")
+
+
 class PagedBlocks(DecodeWorkload):
     """Block-level eviction over page tables at the H2O shape: per layer a pool of 32-token
     blocks and a page table per sequence (26 blocks = 832 tokens, the 13 newest protected);
@@ -774,10 +860,12 @@ def make_workload(name, w, dev, kvc, max_steps):
         return H2O(w, dev, kvc)
     if name == "paged":
         return PagedBlocks(w, dev, kvc)
+    if name == "h2o_gqa":
+        return H2OGrouped(w, dev, kvc)
     raise ValueError(name)
 
 
-WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid", "alibi", "paged"]
+WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid", "alibi", "paged", "h2o_gqa"]
 
 
 # ----------------------------------------------------------------------------- main arms
@@ -928,7 +1016,8 @@ def run_reference(args):
     import oracle
     oracle.build()
     cls = {"streaming": Streaming, "snapkv": SelectDecode, "pyramid": SelectDecode,
-           "h2o": H2O, "alibi": StreamingAlibi, "paged": PagedBlocks}[args.workload]
+           "h2o": H2O, "alibi": StreamingAlibi, "paged": PagedBlocks,
+           "h2o_gqa": H2OGrouped}[args.workload]
     R = cls.__new__(cls)
     R.w = w
     R.budgets = ([w.budget] * w.layers if args.workload != "pyramid" else

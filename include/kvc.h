@@ -415,6 +415,22 @@ kvc_status kvc_h2o_accumulate_evict(const float *logits, int64_t logits_stride, 
                                     int32_t n_slots, const int64_t *t, int32_t L_local,
                                     int32_t budget, void *stream);
 
+/* kvc_h2o_accumulate_evict for a grouped-query cache (n_heads_q = G * n_heads_kv; query head
+ * h reads KV head h / G).  A cached row serves the G query heads of its KV head and is evicted
+ * for all of them, so its score adds their attention ([KVC] H2O, s_j = sum_t alpha_{t,j}, over
+ * the group -- a reading, the pages treat one head):
+ *   score[b,kh,j] += sum_g exp(logits[b,kh*G+g,j] - lse[b,kh*G+g])   (g in head order);
+ * then the eviction rule of kvc_h2o_accumulate_evict per (b, kh).  score, pos, free_slot are
+ * per KV head ([batch][n_heads_kv][stride], device int32[batch*n_heads_kv]); logits and lse per
+ * query head ([batch][n_heads_q][logits_stride], [batch][n_heads_q]), as kvc_decode_attn writes
+ * them.  n_heads_q == n_heads_kv is kvc_h2o_accumulate_evict (same bits). */
+kvc_status kvc_h2o_accumulate_evict_gqa(const float *logits, int64_t logits_stride,
+                                        const float *lse, float *score, int32_t *pos,
+                                        int64_t stride, int32_t *free_slot, int32_t batch,
+                                        int32_t n_heads_q, int32_t n_heads_kv, int32_t n_slots,
+                                        const int64_t *t, int32_t L_local, int32_t budget,
+                                        void *stream);
+
 /* H2O at the end of the prompt: full causal attention of the prompt (every query row), the
  * column sums s_j = sum_t alpha_{t,j}, then the one-shot compression to the budget: the
  * L_local newest positions plus the K_hh largest s among the older ones (equal scores keep

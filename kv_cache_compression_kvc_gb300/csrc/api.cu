@@ -728,12 +728,25 @@ kvc_status kvc_h2o_accumulate_evict(const float *logits, int64_t logits_stride, 
                                     int32_t n_slots, const int64_t *t, int32_t L_local,
                                     int32_t budget, void *stream)
 {
+    return kvc_h2o_accumulate_evict_gqa(logits, logits_stride, lse, score, pos, stride, free_slot,
+                                        batch, n_heads, n_heads, n_slots, t, L_local, budget,
+                                        stream);
+}
+
+kvc_status kvc_h2o_accumulate_evict_gqa(const float *logits, int64_t logits_stride,
+                                        const float *lse, float *score, int32_t *pos,
+                                        int64_t stride, int32_t *free_slot, int32_t batch,
+                                        int32_t n_heads_q, int32_t n_heads_kv, int32_t n_slots,
+                                        const int64_t *t, int32_t L_local, int32_t budget,
+                                        void *stream)
+{
     if (logits == nullptr || lse == nullptr || score == nullptr || pos == nullptr ||
         free_slot == nullptr || t == nullptr)
         return fail(KVC_ERR_INVALID_ARG, "kvc_h2o_accumulate_evict: null pointer");
-    if (batch <= 0 || n_heads <= 0 || n_slots < 0 || L_local < 0 || budget < 0 ||
-        logits_stride < n_slots || stride < n_slots)
+    if (batch <= 0 || n_heads_kv <= 0 || n_heads_q < n_heads_kv || n_heads_q % n_heads_kv ||
+        n_slots < 0 || L_local < 0 || budget < 0 || logits_stride < n_slots || stride < n_slots)
         return fail(KVC_ERR_SHAPE, "kvc_h2o_accumulate_evict: sizes");
+    const int n_heads = n_heads_kv;
     int32_t *code = nullptr;
     kvc_status st = device_info(&code, nullptr);
     if (st != KVC_OK) return st;
@@ -741,6 +754,7 @@ kvc_status kvc_h2o_accumulate_evict(const float *logits, int64_t logits_stride, 
     p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;
     p.score = score; p.pos = pos; p.stride = stride; p.free_slot = free_slot;
     p.rows = batch * n_heads; p.n_slots = n_slots; p.L_local = L_local; p.budget = budget;
+    p.G = n_heads_q / n_heads_kv;
     p.t = t; p.dev_code = code;
     cudaError_t e = kvc::launch_h2o_accumulate_evict(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "H2O launch");

@@ -10,6 +10,11 @@
 // own best candidate, and the block reduces (s, pos, slot) with shuffles and one shared-memory
 // step.  The order (lower s first, then larger pos) is total since positions are distinct, so
 // the result does not depend on how the reduction is split.
+//
+// Grouped-query caches (G query heads per KV head): a row is evicted for the whole group, so
+// its score adds the attention of all G heads, s_j += sum_g exp(logit_{g,j} - lse_g), the terms
+// taken in head order.  The query heads of KV row r are rows r*G .. r*G + G - 1 of the logits
+// and lse.  The one-head case keeps its own instance.
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,6 +41,7 @@ __device__ __forceinline__ void h2o_fold(float &bs, int &bp, int &bj, float os, 
     }
 }
 
+template <bool GROUPED>
 __global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const H2OParams p)
 {
     __shared__ float w_s[H2O_THREADS / 32];
@@ -45,10 +51,11 @@ __global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const
     pdl_trigger();
     pdl_wait();                                 // logits and lse come from the decode kernel
     const int64_t t = *p.t;
-    const float *__restrict__ lg = p.logits + (size_t)row * p.logits_stride;
+    const int G = GROUPED ? p.G : 1;
+    const float *__restrict__ lg = p.logits + (size_t)row * G * p.logits_stride;
     float *__restrict__ s = p.score + (size_t)row * p.stride;
     const int32_t *__restrict__ pos = p.pos + (size_t)row * p.stride;
-    const float lse = p.lse[row];
+    const float lse = p.lse[(size_t)row * G];
     const int64_t limit = t - p.L_local;
     const int n = p.n_slots;
 
@@ -66,11 +73,24 @@ __global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const
                 pv[u] = __ldg(pos + j);
             }
         }
+        if constexpr (GROUPED) {
+            // the group's other heads, in head order after head 0
+            for (int g = 1; g < G; ++g) {
+                const float *__restrict__ lgg = lg + (size_t)g * p.logits_stride;
+                const float lse_g = p.lse[(size_t)row * G + g];
+#pragma unroll
+                for (int u = 0; u < H2O_BATCH; ++u) {
+                    const int j = j0 + u * H2O_THREADS;
+                    if (j < n) lv[u] = g == 1 ? expf(lv[u] - lse) + expf(__ldg(lgg + j) - lse_g)
+                                              : lv[u] + expf(__ldg(lgg + j) - lse_g);
+                }
+            }
+        }
 #pragma unroll
         for (int u = 0; u < H2O_BATCH; ++u) {
             const int j = j0 + u * H2O_THREADS;
             if (j < n) {
-                const float sj = sv[u] + expf(lv[u] - lse);
+                const float sj = sv[u] + ((GROUPED && G > 1) ? lv[u] : expf(lv[u] - lse));
                 s[j] = sj;
                 if ((int64_t)pv[u] <= limit) h2o_fold(best_s, best_p, best_j, sj, pv[u], j);
             }
@@ -110,8 +130,11 @@ __global__ void gather_scores_kernel(const float *s_full, int64_t s_stride, cons
 cudaError_t launch_h2o_accumulate_evict(const H2OParams &p, cudaStream_t stream)
 {
     if (p.rows == 0) return cudaSuccess;
-    return launch_pdl(h2o_accumulate_evict_kernel, dim3((unsigned)p.rows), dim3(H2O_THREADS), 0,
-                      stream, p);
+    if (p.G > 1)
+        return launch_pdl(h2o_accumulate_evict_kernel<true>, dim3((unsigned)p.rows),
+                          dim3(H2O_THREADS), 0, stream, p);
+    return launch_pdl(h2o_accumulate_evict_kernel<false>, dim3((unsigned)p.rows),
+                      dim3(H2O_THREADS), 0, stream, p);
 }
 
 cudaError_t launch_gather_scores(const float *s_full, int64_t s_stride, const int32_t *idx,

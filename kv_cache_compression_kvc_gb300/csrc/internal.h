@@ -215,6 +215,7 @@ struct H2OParams {
     int64_t stride;
     int32_t *free_slot;
     int32_t rows, n_slots, L_local, budget;
+    int32_t G;                   // query heads per KV row (1: MHA)
     const int64_t *t;
     int32_t *dev_code;
 };

@@ -23,6 +23,8 @@ Workloads (sizes as stated by the benchmark configuration):
   paged       the h2o shape with block-level eviction: blocks of 32 tokens, 26 blocks (832
               tokens, >= the 819 budget) per sequence, the 13 newest (>= 410 recent tokens)
               protected; pools of N(0,1) keys and values.
+  h2o_gqa     the h2o shape on a grouped-query cache: 32 query heads over 8 KV heads; caches of
+              N(0,1) keys/values at the 410 newest and 409 random older prompt positions.
 """
 from __future__ import annotations
 
@@ -80,6 +82,8 @@ WORKLOADS = {
                       n_sink=4, window=2044),
     "paged": Workload("paged", 32, 16, 32, 32, 128, 4096, 512, torch.bfloat16, 1241,
                       budget=819, L_local=410, extra={"block_size": 32}),
+    "h2o_gqa": Workload("h2o_gqa", 32, 16, 32, 8, 128, 4096, 512, torch.bfloat16, 1242,
+                        budget=819, L_local=410),
 }
 
 

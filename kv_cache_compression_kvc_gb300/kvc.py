@@ -114,6 +114,8 @@ SIGNATURES = {
                                        _I64, _P, _P]),
     "kvc_h2o_accumulate_evict": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _P,
                                         _I32, _I32, _P]),
+    "kvc_h2o_accumulate_evict_gqa": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
+                                            _I32, _P, _I32, _I32, _P]),
     "kvc_h2o_prefill_workspace_bytes": (_SZ, [_I32] * 4),
     "kvc_h2o_prefill_select": (_I32, [_P, _CACHE_P, _I32, _I32, _I32, _F32, _P, _P, _P, _P,
                                       _SZ, _P]),
@@ -491,6 +493,21 @@ def kvc_h2o_accumulate_evict(logits: torch.Tensor, lse: torch.Tensor, score: tor
     _check(load().kvc_h2o_accumulate_evict(
         _ptr(logits), logits.stride(-2), _ptr(lse), _ptr(score), _ptr(pos), score.stride(-2),
         _ptr(free_slot), B, H, int(n_slots), _ptr(t), int(L_local), int(budget),
+        _stream(stream)))
+
+
+def kvc_h2o_accumulate_evict_gqa(logits: torch.Tensor, lse: torch.Tensor, score: torch.Tensor,
+                                 pos: torch.Tensor, free_slot: torch.Tensor, *, n_slots: int,
+                                 t: torch.Tensor, L_local: int, budget: int,
+                                 stream=None) -> None:
+    """logits [B, Hq, >=n_slots], lse [B, Hq]; score/pos [B, Hkv, stride], free_slot [B, Hkv]."""
+    B, Hq = lse.shape
+    Hkv = score.shape[1]
+    if score.stride(-2) != pos.stride(-2):
+        raise ValueError("score and pos must share a row stride")
+    _check(load().kvc_h2o_accumulate_evict_gqa(
+        _ptr(logits), logits.stride(-2), _ptr(lse), _ptr(score), _ptr(pos), score.stride(-2),
+        _ptr(free_slot), B, Hq, Hkv, int(n_slots), _ptr(t), int(L_local), int(budget),
         _stream(stream)))
 
 

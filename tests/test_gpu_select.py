@@ -302,3 +302,56 @@ def test_h2o_evict_candidates_and_no_candidate_code():
     kvc.kvc_h2o_accumulate_evict(logits, lse, sc, pos, free, n_slots=n, t=t, L_local=2, budget=5)
     assert kvc.kvc_device_status() == 6    # KVC_DEV_NO_CANDIDATE (row 0)
     assert int(free[1]) == 0               # row 1: position 0 is the only candidate
+
+
+@pytest.mark.parametrize("dtype,G,D", [(torch.bfloat16, 4, 128), (torch.float32, 2, 64),
+                                       (torch.bfloat16, 8, 64)])
+def test_h2o_grouped_query_steps_teacher_forced(dtype, G, D):
+    """H2O on a grouped-query cache: free-slot append, decode (tensor cores for bf16 groups)
+    with logits, then the grouped score update; every step from the GPU's own state: output,
+    scores (the sum over the group's heads) and the evicted slot, exactly, given the GPU's
+    fp32 scores."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv, N, budget, L_local, steps = 2, 2, 300, 70, 35, 24
+    Hq = Hkv * G
+    cap = budget + 1
+    rng = np.random.default_rng(60 + G + D)
+    Kc = I.randn((B, Hkv, cap, D), 61 + G, dev, dtype)
+    Vc = I.randn((B, Hkv, cap, D), 62 + G, dev, dtype)
+    pos_np = np.full((B, Hkv, cap), -1, dtype=np.int32)
+    for b in range(B):
+        for h in range(Hkv):
+            old = np.sort(rng.choice(N - L_local, budget - L_local, replace=False))
+            pos_np[b, h, :budget] = np.concatenate([old, np.arange(N - L_local, N)])
+    pos = torch.tensor(pos_np, device=dev)
+    sc = torch.tensor(rng.random((B, Hkv, cap)) * 3, dtype=torch.float32, device=dev)
+    free = torch.full((B * Hkv,), budget, dtype=torch.int32, device=dev)
+    t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, steps, 63 + G, dev, dtype)
+    logits = torch.empty((B, Hq, cap), device=dev)
+    lse = torch.empty((B, Hq), device=dev)
+    scale = 1 / math.sqrt(D)
+    for step in range(steps):
+        t = N + step
+        t_dev.fill_(t)
+        kvc.kvc_stream_append(Kc, Vc, kvc.KVC_APPEND_FREE_SLOT, ks[step], vs[step], t=t_dev,
+                              free_slot=free, pos=pos, score=sc)
+        K0, V0 = f64(Kc), f64(Vc)
+        pos0, s0 = pos.cpu().numpy().astype(np.int64), sc.cpu().numpy().astype(np.float64)
+        out = kvc.kvc_decode_attn(qs[step], Kc, Vc, scale=scale, n_valid=cap, logits=logits,
+                                  lse=lse)
+        kvc.kvc_h2o_accumulate_evict_gqa(logits, lse, sc, pos, free, n_slots=cap, t=t_dev,
+                                         L_local=L_local, budget=budget)
+        assert kvc.kvc_device_status() == 0
+        o_gpu, s_gpu, f_gpu = out.cpu().numpy(), sc.cpu().numpy(), free.cpu().numpy()
+        for b in range(B):
+            for kh in range(Hkv):
+                qg = f64(qs[step, b, kh * G:(kh + 1) * G])
+                o_ref, s_ref, _ = oracle.h2o_step_group(qg, K0[b, kh], V0[b, kh], pos0[b, kh],
+                                                        s0[b, kh], t, L_local, budget, scale)
+                assert_close(o_gpu[b, kh * G:(kh + 1) * G], o_ref, TOL[dtype],
+                             f"out step {step} ({b},{kh})")
+                assert_rel(s_gpu[b, kh], s_ref, 1e-4, 1e-5, f"s step {step} ({b},{kh})")
+                ev = oracle.h2o_evict_f32(s_gpu[b, kh], pos0[b, kh], t, L_local)
+                assert ev == int(f_gpu[b * Hkv + kh]), f"evictee step {step} ({b},{kh})"
