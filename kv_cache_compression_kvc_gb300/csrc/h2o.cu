@@ -14,7 +14,8 @@
 // Grouped-query caches (G query heads per KV head): a row is evicted for the whole group, so
 // its score adds the attention of all G heads, s_j += sum_g exp(logit_{g,j} - lse_g), the terms
 // taken in head order.  The query heads of KV row r are rows r*G .. r*G + G - 1 of the logits
-// and lse.  The one-head case keeps its own instance.
+// and lse.  One instance per group size the decode supports (2, 4, 6, 8) issues the loads of
+// all G heads together; another G takes a generic instance; one head keeps its own.
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,9 +42,11 @@ __device__ __forceinline__ void h2o_fold(float &bs, int &bp, int &bj, float os, 
     }
 }
 
-template <bool GROUPED>
+// GT: 1 one head; 2..8 that group size; 0 any group size (p.G)
+template <int GT>
 __global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const H2OParams p)
 {
+    constexpr bool GROUPED = GT != 1;
     __shared__ float w_s[H2O_THREADS / 32];
     __shared__ int w_p[H2O_THREADS / 32], w_j[H2O_THREADS / 32];
     const int row = blockIdx.x;
@@ -51,13 +54,18 @@ __global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const
     pdl_trigger();
     pdl_wait();                                 // logits and lse come from the decode kernel
     const int64_t t = *p.t;
-    const int G = GROUPED ? p.G : 1;
+    const int G = GT == 0 ? p.G : GT;
     const float *__restrict__ lg = p.logits + (size_t)row * G * p.logits_stride;
     float *__restrict__ s = p.score + (size_t)row * p.stride;
     const int32_t *__restrict__ pos = p.pos + (size_t)row * p.stride;
     const float lse = p.lse[(size_t)row * G];
     const int64_t limit = t - p.L_local;
     const int n = p.n_slots;
+    float lse_g[GT > 1 ? GT : 1];               // the group's log-sum-exps (head 0 is lse)
+    if constexpr (GT > 1) {
+#pragma unroll
+        for (int g = 1; g < GT; ++g) lse_g[g] = p.lse[(size_t)row * GT + g];
+    }
 
     float best_s = INFINITY;
     int best_p = -1, best_j = -1;
@@ -67,13 +75,31 @@ __global__ void __launch_bounds__(H2O_THREADS) h2o_accumulate_evict_kernel(const
 #pragma unroll
         for (int u = 0; u < H2O_BATCH; ++u) {
             const int j = j0 + u * H2O_THREADS;
+            lv[u] = 0.f;
             if (j < n) {
                 sv[u] = s[j];
                 lv[u] = __ldg(lg + j);
                 pv[u] = __ldg(pos + j);
             }
         }
-        if constexpr (GROUPED) {
+        if constexpr (GT > 1) {
+            // every head's logits in flight at once, then the terms in head order
+            float lx[GT - 1][H2O_BATCH];
+#pragma unroll
+            for (int g = 1; g < GT; ++g)
+#pragma unroll
+                for (int u = 0; u < H2O_BATCH; ++u) {
+                    const int j = j0 + u * H2O_THREADS;
+                    lx[g - 1][u] = j < n ? __ldg(lg + (size_t)g * p.logits_stride + j) : 0.f;
+                }
+#pragma unroll
+            for (int u = 0; u < H2O_BATCH; ++u) {
+                float acc = expf(lv[u] - lse);
+#pragma unroll
+                for (int g = 1; g < GT; ++g) acc += expf(lx[g - 1][u] - lse_g[g]);
+                lv[u] = acc;
+            }
+        } else if constexpr (GT == 0) {
             // the group's other heads, in head order after head 0
             for (int g = 1; g < G; ++g) {
                 const float *__restrict__ lgg = lg + (size_t)g * p.logits_stride;
@@ -130,11 +156,15 @@ __global__ void gather_scores_kernel(const float *s_full, int64_t s_stride, cons
 cudaError_t launch_h2o_accumulate_evict(const H2OParams &p, cudaStream_t stream)
 {
     if (p.rows == 0) return cudaSuccess;
-    if (p.G > 1)
-        return launch_pdl(h2o_accumulate_evict_kernel<true>, dim3((unsigned)p.rows),
-                          dim3(H2O_THREADS), 0, stream, p);
-    return launch_pdl(h2o_accumulate_evict_kernel<false>, dim3((unsigned)p.rows),
-                      dim3(H2O_THREADS), 0, stream, p);
+    const dim3 grid((unsigned)p.rows), block(H2O_THREADS);
+    switch (p.G) {
+    case 1: return launch_pdl(h2o_accumulate_evict_kernel<1>, grid, block, 0, stream, p);
+    case 2: return launch_pdl(h2o_accumulate_evict_kernel<2>, grid, block, 0, stream, p);
+    case 4: return launch_pdl(h2o_accumulate_evict_kernel<4>, grid, block, 0, stream, p);
+    case 6: return launch_pdl(h2o_accumulate_evict_kernel<6>, grid, block, 0, stream, p);
+    case 8: return launch_pdl(h2o_accumulate_evict_kernel<8>, grid, block, 0, stream, p);
+    default: return launch_pdl(h2o_accumulate_evict_kernel<0>, grid, block, 0, stream, p);
+    }
 }
 
 cudaError_t launch_gather_scores(const float *s_full, int64_t s_stride, const int32_t *idx,
