@@ -8,7 +8,8 @@ with gcc into ``oracle/_build/``.  This module only marshals numpy arrays.
 Functions (each follows the page passage cited in ``kvc_oracle.c``):
   kv_bytes, pyramid_budgets, rope, attend, stream_window, stream_slot, stream_decode,
   stream_decode_alibi, topk_ascending, snapkv_obs_scores, pool1d, snapkv_select, snapkv_stage_f32,
-  h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_step_group, h2o_evict_f32, block_step, block_evict_f32.
+  h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_step_group, h2o_evict_f32, block_step, block_evict_f32,
+  duo_decode, duo_kv_bytes.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against values the pages
 print, closed forms, invariants, library routines on special cases or brute force on tiny
@@ -83,6 +84,9 @@ _SIGS = {
     "orc_block_step": (ctypes.c_int, [ctypes.c_int] * 5 + [_f64, _ptr, _ptr, _ptr, _ptr,
                                                            ctypes.c_int, ctypes.c_int, _ptr]),
     "orc_block_evict_f32": (ctypes.c_int, [ctypes.c_int, _ptr, ctypes.c_int, ctypes.c_int]),
+    "orc_duo_decode": (None, [ctypes.c_int, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              _f64, _ptr, _ptr, _ptr, _ptr]),
+    "orc_duo_kv_bytes": (_u64, [_u64] * 9),
 }
 
 
@@ -300,3 +304,22 @@ def block_step(q, K, V, score, bs: int, budget_blocks: int, recent_blocks: int, 
 def block_evict_f32(score_f32, budget_blocks: int, recent_blocks: int) -> int:
     s = np.ascontiguousarray(np.asarray(score_f32, dtype=np.float32))
     return int(lib().orc_block_evict_f32(s.shape[0], _p(s), budget_blocks, recent_blocks))
+
+
+def duo_decode(retrieval: bool, t: int, S: int, W: int, q, hist_k, hist_v, scale: float):
+    """DuoAttention decode of one head at text position t: full history for a retrieval head,
+    the StreamingLLM set (sinks + window + t) for a streaming head."""
+    q = _f(q)
+    D = q.shape[0]
+    hk, hv = _f(hist_k), _f(hist_v)
+    assert hk.shape[0] >= t + 1 and hv.shape[0] >= t + 1 and hk.shape[1] == D
+    out = np.empty(D)
+    lib().orc_duo_decode(int(bool(retrieval)), int(t), S, W, D, float(scale), _p(q), _p(hk),
+                         _p(hv), _p(out))
+    return out
+
+
+def duo_kv_bytes(n_layers, n_retrieval, n_streaming, d_head, seq_len, n_sink, window,
+                 bytes_per_elem, batch) -> int:
+    return int(lib().orc_duo_kv_bytes(n_layers, n_retrieval, n_streaming, d_head, seq_len,
+                                      n_sink, window, bytes_per_elem, batch))

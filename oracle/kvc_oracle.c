@@ -538,3 +538,47 @@ int orc_block_evict_f32(int nb, const float *score, int budget_blocks, int recen
         if (ev < 0 || score[i] <= score[ev]) ev = i;
     return ev;
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* DuoAttention, inference half.  [KVC] "Decomposição funcional com o DuoAttention": retrieval
+ * heads (gamma = 1, 20-30 % of the heads) keep the full KV cache; streaming heads (gamma = 0)
+ * keep a constant buffer of 64 local tokens and 4 attention sinks.  The mask gamma comes from a
+ * calibration (training), out of scope here: it is an input.
+ * Readings: a streaming head attends to the set StreamingLLM attends to (orc_stream_window: the
+ * n_sink first tokens, the `window` tokens before t and t itself); no positional term is added
+ * (keys as stored, already position-encoded); a retrieval head attends to tokens 0..t.
+ * hist_k, hist_v: [t+1][D], the head's keys and values of text positions 0..t.              */
+void orc_duo_decode(int retrieval, int64_t t, int S, int W, int D, double scale,
+                    const double *q, const double *hist_k, const double *hist_v, double *out)
+{
+    if (retrieval) {
+        orc_attend((int)(t + 1), D, scale, q, hist_k, hist_v, out, NULL, NULL);
+        return;
+    }
+    const size_t cap = (size_t)(S + W + 1);
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * cap);
+    int64_t *cpos = (int64_t *)malloc(sizeof(int64_t) * cap);
+    int64_t qpos;
+    const int n = orc_stream_window(t, S, W, tok, cpos, &qpos);
+    double *K = (double *)malloc(sizeof(double) * (size_t)n * D);
+    double *V = (double *)malloc(sizeof(double) * (size_t)n * D);
+    for (int j = 0; j < n; ++j) {
+        memcpy(K + (size_t)j * D, hist_k + (size_t)tok[j] * D, sizeof(double) * (size_t)D);
+        memcpy(V + (size_t)j * D, hist_v + (size_t)tok[j] * D, sizeof(double) * (size_t)D);
+    }
+    orc_attend(n, D, scale, q, K, V, out, NULL, NULL);
+    free(tok); free(cpos); free(K); free(V);
+}
+
+/* KV bytes under DuoAttention: the memory formula of [KVC] "O gargalo de memória..." with the
+ * sequence length replaced per head: seq_len tokens for a retrieval head, at most
+ * n_sink + window + 1 for a streaming head (its buffer, the token being decoded included).   */
+uint64_t orc_duo_kv_bytes(uint64_t n_layers, uint64_t n_retrieval, uint64_t n_streaming,
+                          uint64_t d_head, uint64_t seq_len, uint64_t n_sink, uint64_t window,
+                          uint64_t bytes_per_elem, uint64_t batch)
+{
+    uint64_t buf = n_sink + window + 1;
+    if (buf > seq_len) buf = seq_len;
+    return 2ull * n_layers * d_head * bytes_per_elem * batch *
+           (n_retrieval * seq_len + n_streaming * buf);
+}
