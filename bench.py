@@ -13,7 +13,7 @@ Other workloads (--workload): snapkv (select + compact + 256-step decode), h2o (
 selection + per-step accumulate/evict), pyramid (per-layer budgets, D=256, GQA 6), alibi (the
 streaming shape with ALiBi at in-cache positions instead of RoPE), paged (block-level eviction
 over page tables at the H2O shape), h2o_gqa (H2O on a grouped-query cache, 32 query heads over 8
-KV heads).
+KV heads), duo (DuoAttention at 128k tokens: a quarter of the heads retrieving).
 
 Multi-GPU: the path shards into independent replicas (no exchange step); under torchrun every
 rank runs the same workload on its own GPU and rank 0 prints the aggregate.
@@ -711,6 +711,109 @@ class H2OGrouped(H2O):
                 f"(extrapolated)")
 
 
+class DuoAttention(DecodeWorkload):
+    """DuoAttention's inference half at 128k tokens: per layer 8 of the 32 KV heads (a seeded
+    fixed mask) keep the full cache, the others 4 sinks + 64 recent tokens; per step, the
+    append routes each head's row to its cache and one decode launch covers both kinds."""
+
+    traffic_key = "decode_attn/duo"
+
+    def __init__(self, w: I.Workload, dev, kvc, max_steps):
+        super().__init__(w, dev, kvc)
+        L, B, H, D, N = w.layers, w.batch, w.n_heads_kv, w.d_head, w.prompt
+        S, W = w.n_sink, w.window
+        n_ret = w.extra["n_retrieval"]
+        self.n_ret, self.n_str = n_ret, H - n_ret
+        self.cap = N + max_steps + 8
+        self.ring_cap = S + W + 1
+        rng = np.random.default_rng(w.seed)
+        self.ret_heads = [sorted(rng.choice(H, n_ret, replace=False).tolist()) for _ in range(L)]
+        self.fk = torch.empty((L, B, n_ret, self.cap, D), dtype=w.dtype, device=dev)
+        self.fv = torch.empty_like(self.fk)
+        self.rk = torch.empty((L, B, self.n_str, self.ring_cap, D), dtype=w.dtype, device=dev)
+        self.rv = torch.empty_like(self.rk)
+        for l in range(L):
+            g = I.generator(w.seed * 1000 + l, dev)
+            for x in (self.fk[l], self.fv[l], self.rk[l], self.rv[l]):
+                x.normal_(generator=g)
+        self.len = torch.full((L, B * n_ret), N, dtype=torch.int32, device=dev)
+        self.t = torch.tensor([N], dtype=torch.int64, device=dev)
+        self.fulls = [kvc.cache_view(self.fk[l], self.fv[l]) for l in range(L)]
+        self.rings = [kvc.cache_view(self.rk[l], self.rv[l]) for l in range(L)]
+        self.duos = [kvc.Duo(self.ret_heads[l], S, W, self.t) for l in range(L)]
+        self.ws = torch.zeros(kvc.kvc_decode_attn_duo_workspace_bytes(
+            B, w.n_heads_q, H, D, self.cap, n_ret) + 256, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 2 * L + 1
+
+    def save_state(self):
+        return self.t.clone(), self.len.clone()
+
+    def restore_state(self, st):
+        self.t.copy_(st[0])
+        self.len.copy_(st[1])
+
+    def append_layer(self, l):
+        self.kvc.kvc_duo_append(self.fulls[l], self.len[l], self.rings[l], self.duos[l],
+                                self.k_s[l], self.v_s[l])
+
+    def decode_layer(self, l, flags=0):
+        self.kvc.kvc_decode_attn_duo(self.q_s[l], self.fulls[l], self.rings[l], self.duos[l],
+                                     scale=self.w.scale, len=self.len[l], flags=flags,
+                                     out=self.out[l], ws=self.ws)
+
+    def end_step(self):
+        self.kvc.kvc_position_advance(self.t, 1)
+
+    def decode_bytes(self, first_step, n_steps):
+        w = self.w
+        eb = elem_bytes(w.dtype)
+        tot = 0
+        for st in range(first_step, first_step + n_steps):
+            n_full = w.prompt + st + 1
+            tot += 2 * w.batch * w.d_head * eb * (self.n_ret * n_full + self.n_str * self.ring_cap)
+            tot += self.qo_bytes()
+        return tot // n_steps
+
+    def describe(self):
+        w = self.w
+        return {"workload": "DuoAttention decode at 128k tokens", "layers": w.layers,
+                "batch": w.batch, "n_heads": w.n_heads_q, "d_head": w.d_head,
+                "context": w.prompt, "retrieval_heads": f"{self.n_ret} of {w.n_heads_kv} per layer "
+                "(seeded fixed mask; no calibration)", "streaming_buffer":
+                f"{w.n_sink} sinks + {w.window} recent + the current token",
+                "kv_dtype": "bf16", "l2": "inputs larger than L2 (17 GB of KV per step)",
+                "kv_memory_vs_full": round(self.kvc.kvc_duo_kv_bytes(
+                    w.layers, self.n_ret, self.n_str, w.d_head, w.prompt, w.n_sink, w.window, 2,
+                    w.batch) / self.kvc.kvc_kv_bytes(w.layers, w.n_heads_kv, w.d_head, w.prompt,
+                                                     2, w.batch), 4),
+                "graph": "appends and decodes captured as two CUDA graphs per step"}
+
+    def oracle_sample(self, budget_s=12.0):
+        import oracle
+        w = self.w
+        rng = np.random.default_rng(0)
+        # a retrieval head at the full context dominates: time those, scale by the head mix
+        t = w.prompt
+        hk = rng.standard_normal((t + 1, w.d_head))
+        hv = rng.standard_normal((t + 1, w.d_head))
+        q = rng.standard_normal(w.d_head)
+        oracle.duo_decode(True, t, w.n_sink, w.window, q, hk, hv, w.scale)
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            oracle.duo_decode(True, t, w.n_sink, w.window, q, hk, hv, w.scale)
+            n += 1
+        per = (time.perf_counter() - t0) / n
+        per_str = per * (w.n_sink + w.window + 1) / (t + 1)
+        n_ret = w.extra["n_retrieval"]
+        slices = w.batch * w.layers
+        return per * n_ret + per_str * (w.n_heads_kv - n_ret), slices, n
+
+    def sample_description(self, n, slices):
+        return (f"{n} oracle retrieval-head decodes at the full context, scaled by the head mix "
+                f"(streaming heads by their buffer) and extrapolated to {slices} (batch, layer) "
+                f"slices per step (extrapolated)")
+
+
 class PagedBlocks(DecodeWorkload):
     """Block-level eviction over page tables at the H2O shape: per layer a pool of 32-token
     blocks and a page table per sequence (26 blocks = 832 tokens, the 13 newest protected);
@@ -862,10 +965,12 @@ def make_workload(name, w, dev, kvc, max_steps):
         return PagedBlocks(w, dev, kvc)
     if name == "h2o_gqa":
         return H2OGrouped(w, dev, kvc)
+    if name == "duo":
+        return DuoAttention(w, dev, kvc, max_steps)
     raise ValueError(name)
 
 
-WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid", "alibi", "paged", "h2o_gqa"]
+WORKLOAD_NAMES = ["streaming", "snapkv", "h2o", "pyramid", "alibi", "paged", "h2o_gqa", "duo"]
 
 
 # ----------------------------------------------------------------------------- main arms
@@ -1017,7 +1122,7 @@ def run_reference(args):
     oracle.build()
     cls = {"streaming": Streaming, "snapkv": SelectDecode, "pyramid": SelectDecode,
            "h2o": H2O, "alibi": StreamingAlibi, "paged": PagedBlocks,
-           "h2o_gqa": H2OGrouped}[args.workload]
+           "h2o_gqa": H2OGrouped, "duo": DuoAttention}[args.workload]
     R = cls.__new__(cls)
     R.w = w
     R.budgets = ([w.budget] * w.layers if args.workload != "pyramid" else

@@ -160,6 +160,25 @@ typedef struct {
     int32_t reserved;
 } kvc_free_pool;
 
+/* DuoAttention's inference half ([KVC] "Decomposição funcional com o DuoAttention"): the KV
+ * heads of a layer are split by a fixed mask gamma (its calibration is training and out of
+ * scope).  Retrieval heads (gamma = 1, 20-30 % of the heads on the page) keep the full cache;
+ * streaming heads (gamma = 0) keep a constant buffer of n_sink attention sinks and the window
+ * tokens before the current one, laid out as the StreamingLLM sink + ring cache of kvc_rope (no
+ * positional term: keys are used as stored).  Two caches per layer:
+ *   full: [batch][n_retrieval][cap][d_head], tokens at the tail (len per retrieval pair);
+ *   ring: [batch][n_streaming][>= n_sink+window+1][d_head].
+ * Model KV head h is retrieval index r if retrieval_heads[r] == h, else the next streaming
+ * index in ascending head order.                                                             */
+typedef struct {
+    int32_t n_retrieval;            /* retrieval KV heads (>= 1; the ring holds >= 1 head too) */
+    int32_t n_sink;                 /* S (4 on the page)                                        */
+    int32_t window;                 /* W (64 on the page)                                       */
+    int32_t reserved;
+    const int32_t *retrieval_heads; /* HOST int32[n_retrieval]: model KV heads, ascending       */
+    const int64_t *t;               /* device scalar: text position of the token being decoded  */
+} kvc_duo;
+
 /* ---------------------------------------------------------------------------------------- */
 /* Diagnostics                                                                               */
 
@@ -375,6 +394,39 @@ kvc_status kvc_block_accumulate_evict(const float *logits, int64_t logits_stride
                                       const kvc_page_table *pt, const kvc_free_pool *free_pool,
                                       int32_t budget_blocks, int32_t recent_blocks,
                                       int32_t *released, void *stream);
+
+/* KV bytes under DuoAttention, host: the memory formula of kvc_kv_bytes with seq_len tokens
+ * per retrieval head and min(n_sink + window + 1, seq_len) per streaming head.  With 30 % of
+ * the heads retrieving at 128k tokens the saving over kvc_kv_bytes is 70 % ([KVC] DuoAttention:
+ * "economizando até 70% de VRAM"). */
+uint64_t kvc_duo_kv_bytes(uint64_t n_layers, uint64_t n_retrieval, uint64_t n_streaming,
+                          uint64_t d_head, uint64_t seq_len, uint64_t n_sink, uint64_t window,
+                          uint64_t bytes_per_elem, uint64_t batch);
+
+/* DuoAttention: append the new token of every KV head to its cache -- a retrieval head's row at
+ * the tail of the full cache (slot len[b*n_retrieval+r], then len += 1; a full row records
+ * KVC_DEV_TAIL_FULL and is skipped), a streaming head's row at the ring slot of text position
+ * *duo->t (slot t for t < n_sink, else n_sink + (t - n_sink) mod (window + 1)).
+ * k_new, v_new: [batch][n_heads_kv][d_head] in model head order, cache dtype, contiguous. */
+kvc_status kvc_duo_append(const kvc_cache *full, int32_t *len, const kvc_cache *ring,
+                          const kvc_duo *duo, const void *k_new, const void *v_new, void *stream);
+
+/* DuoAttention decode ([KVC] DuoAttention with "FlashDecoding esparso"): one launch for both
+ * kinds of heads.  Query head h (model order, KV head h / G) attends to all len (or n_valid)
+ * slots of its retrieval cache row, or to the min(*t + 1, n_sink + window + 1) valid slots of
+ * its ring.  q: [batch][n_heads_q][d_head]; out, lse as kvc_decode_attn; logits (nullable)
+ * [batch][n_heads_q][logits_stride] indexed by the slot of the head's own cache,
+ * logits_stride >= max(cap, n_sink + window + 1).  Slots of both caches must be dense
+ * (stride_slot == d_head).  The work is divided by tiles of each kind, so the streaming heads
+ * cost their buffer only.  Flags: KVC_DECODE_KV_SETTLED (as kvc_decode_attn_ex, covering len
+ * and *t).  Workspace: kvc_decode_attn_duo_workspace_bytes(); zero-filled once, kept zeroed. */
+size_t kvc_decode_attn_duo_workspace_bytes(int32_t batch, int32_t n_heads_q, int32_t n_heads_kv,
+                                           int32_t d_head, int32_t cap, int32_t n_retrieval);
+kvc_status kvc_decode_attn_duo(const void *q, int32_t n_heads_q, const kvc_cache *full,
+                               const int32_t *len, int32_t n_valid, const kvc_cache *ring,
+                               const kvc_duo *duo, float scale, float *out, float *logits,
+                               int64_t logits_stride, float *lse, void *ws, size_t ws_bytes,
+                               uint32_t flags, void *stream);
 
 /* Decode attention without a caller workspace.  No counterpart on the pages: this is a
  * deployment convenience of this library.  Some callers cannot allocate device memory at the

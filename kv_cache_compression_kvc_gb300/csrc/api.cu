@@ -117,7 +117,7 @@ namespace kvc {
 
 void set_last_error(const char *msg) { g_last_error = msg; }
 
-DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm)
+DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm, int seg_pairs)
 {
     // The decode kernel divides the P = B*Hkv pairs' slot tiles evenly over at most C = 2*n_sm
     // persistent blocks (two per SM).  A pair's tiles then meet at most floor(C / P) + 2
@@ -127,7 +127,8 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm)
     DecodePlan pl{};
     const long long pairs = (long long)B * Hkv;
     const long long ctas = 2LL * (n_sm > 0 ? n_sm : 152);
-    long long max_seg = ctas / pairs + 2;
+    const long long alike = seg_pairs > 0 && seg_pairs < pairs ? seg_pairs : pairs;
+    long long max_seg = ctas / alike + 2;
     if (max_seg > ctas) max_seg = ctas;
     pl.max_seg = (int)max_seg;
     const size_t G = (size_t)(Hq / Hkv);
@@ -385,6 +386,184 @@ kvc_status kvc_decode_attn_alibi(const void *q, int32_t n_heads_q, const kvc_cac
         return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn_alibi: null alibi descriptor");
     return decode_impl(q, n_heads_q, cache, nullptr, 0, nullptr, alibi, nullptr, scale, out,
                        logits, logits_stride, lse, ws, ws_bytes, flags, stream);
+}
+
+// ------------------------------------------------------------------------------------------
+// DuoAttention.
+namespace {
+
+struct DuoMap {
+    int n_ret = 0, n_str = 0, Hkv = 0;
+    uint8_t head_of[256] = {};    // retrieval heads in the given order, then the others ascending
+    uint8_t index_of[256] = {};   // inverse of head_of
+};
+
+kvc_status duo_check(const kvc_cache *full, const kvc_cache *ring, const kvc_duo *duo,
+                     const char *name, DuoMap *m)
+{
+    if (duo == nullptr || duo->t == nullptr || duo->n_retrieval < 0 || duo->n_sink < 0 ||
+        duo->window < 0 || (duo->n_retrieval > 0 && duo->retrieval_heads == nullptr))
+        return fail(KVC_ERR_INVALID_ARG, "%s: duo descriptor", name);
+    if (full == nullptr || ring == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "%s: null cache descriptor", name);
+    kvc_status st = check_cache(full, name, true);
+    if (st != KVC_OK) return st;
+    st = check_cache(ring, name, true);
+    if (st != KVC_OK) return st;
+    if (full->dtype != ring->dtype || full->d_head != ring->d_head || full->batch != ring->batch)
+        return fail(KVC_ERR_SHAPE, "%s: the two caches differ in dtype, d_head or batch", name);
+    if (full->stride_slot != full->d_head || ring->stride_slot != ring->d_head)
+        return fail(KVC_ERR_SHAPE, "%s: cache slots must be dense (stride_slot == d_head)", name);
+    if (full->n_heads_kv != duo->n_retrieval)
+        return fail(KVC_ERR_SHAPE, "%s: full cache has %d heads, n_retrieval is %d", name,
+                    full->n_heads_kv, duo->n_retrieval);
+    const long long ring_cap = (long long)duo->n_sink + duo->window + 1;
+    if (ring->cap < ring_cap)
+        return fail(KVC_ERR_CAPACITY, "%s: ring cap %d < n_sink + window + 1 = %lld", name,
+                    ring->cap, ring_cap);
+    m->n_ret = duo->n_retrieval;
+    m->n_str = ring->n_heads_kv;
+    m->Hkv = m->n_ret + m->n_str;
+    if (m->Hkv > 256) return fail(KVC_ERR_SHAPE, "%s: more than 256 KV heads", name);
+    bool used[256] = {};
+    for (int r = 0; r < m->n_ret; ++r) {
+        const int h = duo->retrieval_heads[r];
+        if (h < 0 || h >= m->Hkv || used[h] || (r > 0 && h <= duo->retrieval_heads[r - 1]))
+            return fail(KVC_ERR_INVALID_ARG, "%s: retrieval_heads must be ascending, distinct "
+                        "KV heads below %d", name, m->Hkv);
+        used[h] = true;
+        m->head_of[r] = (uint8_t)h;
+        m->index_of[h] = (uint8_t)r;
+    }
+    int i = m->n_ret;
+    for (int h = 0; h < m->Hkv; ++h)
+        if (!used[h]) {
+            m->head_of[i] = (uint8_t)h;
+            m->index_of[h] = (uint8_t)i;
+            ++i;
+        }
+    return KVC_OK;
+}
+
+}  // namespace
+
+uint64_t kvc_duo_kv_bytes(uint64_t n_layers, uint64_t n_retrieval, uint64_t n_streaming,
+                          uint64_t d_head, uint64_t seq_len, uint64_t n_sink, uint64_t window,
+                          uint64_t bytes_per_elem, uint64_t batch)
+{
+    // per head: seq_len tokens (retrieval) or the constant buffer, never more than seq_len
+    const uint64_t buffer = std::min<uint64_t>(n_sink + window + 1, seq_len);
+    return 2ull * n_layers * d_head * bytes_per_elem * batch *
+           (n_retrieval * seq_len + n_streaming * buffer);
+}
+
+kvc_status kvc_duo_append(const kvc_cache *full, int32_t *len, const kvc_cache *ring,
+                          const kvc_duo *duo, const void *k_new, const void *v_new, void *stream)
+{
+    DuoMap m;
+    kvc_status st = duo_check(full, ring, duo, "kvc_duo_append", &m);
+    if (st != KVC_OK) return st;
+    if (k_new == nullptr || v_new == nullptr || (m.n_ret > 0 && len == nullptr))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_duo_append: null k_new/v_new/len");
+    if (!aligned16(k_new) || !aligned16(v_new))
+        return fail(KVC_ERR_ALIGN, "kvc_duo_append: k_new/v_new must be 16-byte aligned");
+    int32_t *code = nullptr;
+    st = device_info(&code, nullptr);
+    if (st != KVC_OK) return st;
+    kvc::DuoAppendParams p{};
+    p.k = full->k; p.v = full->v;
+    p.sb = full->stride_b; p.sh = full->stride_h; p.ss = full->stride_slot; p.cap = full->cap;
+    p.len = len;
+    p.k2 = ring->k; p.v2 = ring->v;
+    p.sb2 = ring->stride_b; p.sh2 = ring->stride_h; p.ss2 = ring->stride_slot;
+    p.S = duo->n_sink; p.W = duo->window; p.t = duo->t;
+    p.k_new = k_new; p.v_new = v_new;
+    p.B = full->batch; p.Hkv = m.Hkv; p.D = full->d_head; p.eb = elem_bytes(full->dtype);
+    p.n_ret = m.n_ret;
+    std::memcpy(p.index_of, m.index_of, sizeof(p.index_of));
+    p.dev_code = code;
+    cudaError_t e = kvc::launch_duo_append(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "duo append launch");
+    return ok();
+}
+
+size_t kvc_decode_attn_duo_workspace_bytes(int32_t batch, int32_t n_heads_q, int32_t n_heads_kv,
+                                           int32_t d_head, int32_t cap, int32_t n_retrieval)
+{
+    if (batch <= 0 || n_heads_q <= 0 || n_heads_kv <= 0 || d_head <= 0 || cap < 0 ||
+        n_retrieval < 0 || n_retrieval > n_heads_kv)
+        return 0;
+    return kvc::decode_plan(batch, n_heads_q, n_heads_kv, d_head, cap, sm_count_or_default(),
+                            batch * (n_retrieval > 0 ? n_retrieval : 1))
+        .bytes;
+}
+
+kvc_status kvc_decode_attn_duo(const void *q, int32_t n_heads_q, const kvc_cache *full,
+                               const int32_t *len, int32_t n_valid, const kvc_cache *ring,
+                               const kvc_duo *duo, float scale, float *out, float *logits,
+                               int64_t logits_stride, float *lse, void *ws, size_t ws_bytes,
+                               uint32_t flags, void *stream)
+{
+    if (flags & ~(uint32_t)KVC_DECODE_KV_SETTLED)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn_duo: unknown flags 0x%x", flags);
+    DuoMap m;
+    kvc_status st = duo_check(full, ring, duo, "kvc_decode_attn_duo", &m);
+    if (st != KVC_OK) return st;
+    if (q == nullptr || out == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn_duo: null q/out");
+    if (!aligned16(q)) return fail(KVC_ERR_ALIGN, "kvc_decode_attn_duo: q must be 16-byte aligned");
+    if (n_heads_q <= 0 || n_heads_q % m.Hkv)
+        return fail(KVC_ERR_SHAPE, "kvc_decode_attn_duo: n_heads_q %d not a multiple of %d KV "
+                    "heads", n_heads_q, m.Hkv);
+    const int G = n_heads_q / m.Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 6 && G != 8)
+        return fail(KVC_ERR_SHAPE, "kvc_decode_attn_duo: group size %d (supported: 1,2,4,6,8)", G);
+    if (!std::isfinite(scale)) return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn_duo: scale");
+    if (len == nullptr && (n_valid < 0 || n_valid > full->cap))
+        return fail(KVC_ERR_CAPACITY, "kvc_decode_attn_duo: n_valid %d outside [0, cap %d]",
+                    n_valid, full->cap);
+    const int ring_cap = duo->n_sink + duo->window + 1;
+    if (logits != nullptr && logits_stride < std::max(full->cap, ring_cap))
+        return fail(KVC_ERR_CAPACITY, "kvc_decode_attn_duo: logits_stride %lld too small",
+                    (long long)logits_stride);
+    int32_t *code = nullptr;
+    int n_sm = 0;
+    st = device_info(&code, &n_sm);
+    if (st != KVC_OK) return st;
+    const int B = full->batch;
+    const kvc::DecodePlan pl = kvc::decode_plan(B, n_heads_q, m.Hkv, full->d_head, full->cap,
+                                                n_sm, B * (m.n_ret > 0 ? m.n_ret : 1));
+    if (ws == nullptr || ws_bytes < pl.bytes)
+        return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn_duo: workspace needs %zu bytes, got %zu",
+                    pl.bytes, ws_bytes);
+    if (!aligned256(ws)) return fail(KVC_ERR_WORKSPACE, "kvc_decode_attn_duo: workspace alignment");
+    kvc::DecodeParams p{};
+    p.q = q;
+    p.k = full->k; p.v = full->v;
+    p.sb = full->stride_b; p.sh = full->stride_h; p.ss = full->stride_slot;
+    p.B = B; p.Hq = n_heads_q; p.Hkv = m.Hkv; p.cap = full->cap;
+    p.len = len; p.n_valid = n_valid;
+    p.t = duo->t;
+    p.n_ret = m.n_ret; p.n_str = m.n_str; p.ring_cap = ring_cap;
+    p.k2 = ring->k; p.v2 = ring->v; p.sb2 = ring->stride_b; p.sh2 = ring->stride_h;
+    std::memcpy(p.head_of, m.head_of, sizeof(p.head_of));
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out; p.logits = logits; p.logits_stride = logits_stride; p.lse = lse;
+    char *wsb = static_cast<char *>(ws);
+    p.ws_o = reinterpret_cast<float *>(wsb + pl.off_o);
+    p.ws_ml = reinterpret_cast<float *>(wsb + pl.off_ml);
+    p.ws_cnt = reinterpret_cast<int32_t *>(wsb + pl.off_cnt);
+    p.P = B * m.Hkv;
+    p.max_seg = pl.max_seg;
+    p.n_sm = n_sm > 0 ? n_sm : 152;
+    p.kv_settled = (flags & KVC_DECODE_KV_SETTLED) ? 1 : 0;
+    p.dev_code = code;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = full->dtype == KVC_BF16
+                        ? kvc::launch_decode_attn_bf16_duo(p, full->d_head, G, s)
+                        : kvc::launch_decode_attn_f32_duo(p, full->d_head, G, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    return ok();
 }
 
 // ------------------------------------------------------------------------------------------

@@ -58,6 +58,14 @@
 // [block][head][slot][d] rows, so the compute loop is unchanged.  A table entry outside the pool
 // records KVC_DEV_BAD_BLOCK and reads block 0 instead (the copy sizes stay as announced).
 //
+// DuoAttention ("Decomposição funcional com o DuoAttention": retrieval heads keep the full
+// cache, streaming heads a constant buffer of sinks and recent tokens).  One launch covers both
+// kinds.  The tiles of the retrieval pairs (B x n_ret, full caches, NT tiles each) are split
+// evenly over the blocks as usual; each streaming pair (B x n_str, ring caches, NT2 tiles) goes
+// whole to one block, round-robin, ahead of that block's retrieval range -- a streaming pair is
+// almost all fixed cost (its q, its output), so spreading them keeps any block from collecting
+// many.  head_of maps each pair back to the model's KV head for q, the outputs and the logits.
+//
 // Waits on mbarriers are bounded: after kMbarSpinLimit failed polls the thread records
 // KVC_DEV_TIMEOUT and carries on (results are then garbage, but the kernel always finishes).
 #pragma once
@@ -129,8 +137,8 @@ struct DecodeSmem {
 };
 
 // RM: 0 no RoPE, 1 RoPE with one table row per key, 2 factored RoPE (G == 1, n_pos >= TK),
-// 3 ALiBi, 4 paged (no positional term).  Modes 1-3 read the StreamingLLM sink + ring layout in
-// rank order.
+// 3 ALiBi, 4 paged (no positional term), 5 DuoAttention (no positional term).  Modes 1-3 read
+// the StreamingLLM sink + ring layout in rank order.
 template <typename T, int D, int G, int VW, int UNR, int RM, int CPS>
 __global__ void __launch_bounds__(kDecodeThreads, CPS)
 decode_attn_kernel(const DecodeParams p)
@@ -138,6 +146,7 @@ decode_attn_kernel(const DecodeParams p)
     using SM = DecodeSmem<T, D, G, RM>;
     constexpr bool RANKED = RM >= 1 && RM <= 3;   // sink + ring layout, visited in rank order
     constexpr bool PAGED = RM == 4;
+    constexpr bool DUO = RM == 5;
     constexpr bool ROPE = RM == 1 || RM == 2;
     constexpr bool FACT = RM == 2;
     constexpr bool ALIBI = RM == 3;
@@ -173,10 +182,16 @@ decode_attn_kernel(const DecodeParams p)
     const int lane = threadIdx.x & 31;
     const int C = gridDim.x;
     const int cta = blockIdx.x;
-    const long long T_all = (long long)p.P * p.NT;
+    // DuoAttention: the even split covers the T_ret retrieval tiles only; streaming pairs
+    // cta, cta + C, ... (n_own of them) come first in this block's list
+    const long long T_ret = DUO ? (long long)p.B * p.n_ret * p.NT : 0;
+    const int P_ret = DUO ? p.B * p.n_ret : 0;
+    const int P_str = DUO ? p.B * p.n_str : 0;
+    const int n_own = DUO ? (cta < P_str ? (P_str - 1 - cta) / C + 1 : 0) : 0;
+    const long long T_all = DUO ? T_ret : (long long)p.P * p.NT;
     const long long t_begin = (long long)cta * T_all / C;
     const long long t_end = (long long)(cta + 1) * T_all / C;
-    const int n_tiles = (int)(t_end - t_begin);
+    const int n_tiles = (int)(t_end - t_begin) + n_own * (DUO ? p.NT2 : 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -198,6 +213,15 @@ decode_attn_kernel(const DecodeParams p)
     // a_old + (r - S), at slot S + (ring_off + r - S) mod (W + 1), a_old = max(S, t - W) being the
     // oldest ring token still attended.  n_att = min(t + 1, S + W + 1) ranks are attended.
     int qpos = 0, n_att = 0, ring_off = 0;
+    int n_ring = 0;            // DuoAttention: valid slots of a streaming head's ring
+    if (DUO) {
+        int64_t tpos = *p.t;
+        if (tpos < 0) {
+            if (threadIdx.x == 0) record_code(p.dev_code, 4 /* KVC_DEV_BAD_POSITION */);
+            tpos = 0;
+        }
+        n_ring = (int)(tpos + 1 < (int64_t)p.ring_cap ? tpos + 1 : (int64_t)p.ring_cap);
+    }
     if (RANKED) {
         int64_t tpos = *p.t;
         if (tpos < 0) {
@@ -216,9 +240,48 @@ decode_attn_kernel(const DecodeParams p)
         if (x > p.W) x -= p.W + 1;
         return p.S + x;
     };
+    // ---- pairs and tiles -------------------------------------------------------------------
+    // this block's tile i -> its pair q and first slot j0
+    auto locate = [&](int i, int &q, int &j0) {
+        if constexpr (DUO) {
+            const int own = n_own * p.NT2;
+            if (i < own) {
+                q = P_ret + cta + (i / p.NT2) * C;
+                j0 = (i % p.NT2) * TK;
+            } else {
+                const long long t = t_begin + (i - own);
+                q = (int)(t / p.NT);
+                j0 = (int)(t % p.NT) * TK;
+            }
+        } else {
+            const long long t = t_begin + i;
+            q = (int)(t / p.NT);
+            j0 = (int)(t % p.NT) * TK;
+        }
+    };
+    // first tile and tile count of pair q in the even split (DuoAttention: retrieval pairs;
+    // a streaming pair is one block's alone)
+    auto pair_first = [&](int q) -> long long { return (long long)q * p.NT; };
+    auto pair_tiles = [&](int q) -> int { return p.NT; };
+    // batch row and model KV head of pair q
+    auto pair_bk = [&](int q, int &b, int &kh) {
+        if constexpr (DUO) {
+            if (q < P_ret) {
+                b = q / p.n_ret;
+                kh = p.head_of[q % p.n_ret];
+            } else {
+                b = (q - P_ret) / p.n_str;
+                kh = p.head_of[p.n_ret + (q - P_ret) % p.n_str];
+            }
+        } else {
+            b = q / p.Hkv;
+            kh = q % p.Hkv;
+        }
+    };
     // number of work items (slots without RoPE, ranks with it) of pair q
     auto pair_slots = [&](int q) -> int {
         if (RANKED) return n_att;
+        if (DUO && q >= P_ret) return n_ring;
         if (PAGED) {
             const int n = p.len[q / p.Hkv];
             return n < 0 ? 0 : (n > p.cap ? p.cap : n);
@@ -255,10 +318,9 @@ decode_attn_kernel(const DecodeParams p)
         return reinterpret_cast<const int32_t *>(smem + 128)[lb - tab_lo];
     };
     auto issue_tile = [&](int i) {
-        const long long t = t_begin + i;
         const int s = i % NS;
-        const int q = (int)(t / p.NT);
-        const int j0 = (int)(t % p.NT) * TK;
+        int q, j0;
+        locate(i, q, j0);
         if (q != iss_q) {
             // paged: the pairs of a sequence share its length
             if (!PAGED || iss_q < 0 || q / p.Hkv != iss_q / p.Hkv) iss_slots = pair_slots(q);
@@ -269,9 +331,24 @@ decode_attn_kernel(const DecodeParams p)
         const uint32_t kdst = stage0 + s * SM::kStageBytes;
         const uint32_t vdst = kdst + SM::kTileBytes;
         const int b = q / p.Hkv, kh = q % p.Hkv;
-        const size_t base = (size_t)b * p.sb + (size_t)kh * p.sh;
-        const T *kb = static_cast<const T *>(p.k) + base;
-        const T *vb = static_cast<const T *>(p.v) + base;
+        const T *kb, *vb;
+        if constexpr (DUO) {
+            // the pair's own cache: a retrieval head's full cache or a streaming head's ring
+            if (q < P_ret) {
+                const size_t base = (size_t)(q / p.n_ret) * p.sb + (size_t)(q % p.n_ret) * p.sh;
+                kb = static_cast<const T *>(p.k) + base;
+                vb = static_cast<const T *>(p.v) + base;
+            } else {
+                const int qs = q - P_ret;
+                const size_t base = (size_t)(qs / p.n_str) * p.sb2 + (size_t)(qs % p.n_str) * p.sh2;
+                kb = static_cast<const T *>(p.k2) + base;
+                vb = static_cast<const T *>(p.v2) + base;
+            }
+        } else {
+            const size_t base = (size_t)b * p.sb + (size_t)kh * p.sh;
+            kb = static_cast<const T *>(p.k) + base;
+            vb = static_cast<const T *>(p.v) + base;
+        }
         if (rows == 0) {
             mbar_arrive(full);
             return;
@@ -355,7 +432,8 @@ decode_attn_kernel(const DecodeParams p)
             cur_li = li;
             cur_slots = pair_slots(q);
         }
-        const int b = q / p.Hkv, kh = q % p.Hkv;
+        int b, kh;
+        pair_bk(q, b, kh);
         const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)kh * G) * D;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -440,14 +518,17 @@ decode_attn_kernel(const DecodeParams p)
             }
         }
         __syncthreads();
-        const long long t_first = (long long)q * p.NT;
-        const int c_lo = cta_of_tile(t_first, T_all, C);
-        const int c_hi = cta_of_tile(t_first + p.NT - 1, T_all, C);
+        const long long t_first = pair_first(q);
+        const bool whole = DUO && q >= P_ret;        // a streaming pair: this block alone
+        const int c_lo = whole ? cta : cta_of_tile(t_first, T_all, C);
+        const int c_hi = whole ? cta : cta_of_tile(t_first + pair_tiles(q) - 1, T_all, C);
         const int nseg = c_hi - c_lo + 1;
         const int seg = cta - c_lo;
         const bool seg_ok = nseg <= p.max_seg;   // guaranteed by the host plan; checked anyway
         if (!seg_ok && threadIdx.x == 0) record_code(p.dev_code, kDevCodeSchedule);
-        const int rows0 = (q / p.Hkv) * p.Hq + (q % p.Hkv) * G;
+        int pb, pkh;
+        pair_bk(q, pb, pkh);
+        const int rows0 = pb * p.Hq + pkh * G;
         for (int i = threadIdx.x; i < G * D; i += kDecodeThreads) {
             const int g = i / D, d = i % D;
             float M = sm_m[g];
@@ -489,20 +570,20 @@ decode_attn_kernel(const DecodeParams p)
     };
 
     for (int i = 0; i < n_tiles; ++i) {
-        const long long t = t_begin + i;
         const int s = i % NS;
-        const int q = (int)(t / p.NT);
+        int q, j0;
+        locate(i, q, j0);
         if (q != cur) {
             if (cur >= 0) finish_pair(cur);
             start_pair(q);
         }
         mbar_wait(bar_full + 8 * s, (i / NS) & 1, p.dev_code);
-        const int j0 = (int)(t % p.NT) * TK;
         const uint32_t kst = stage0 + s * SM::kStageBytes;
         const uint32_t vst = kst + SM::kTileBytes;
+        int lb_, lkh_;
+        pair_bk(q, lb_, lkh_);
         float *lg_out =
-            p.logits ? p.logits + (size_t)((q / p.Hkv) * p.Hq + (q % p.Hkv) * G) * p.logits_stride
-                     : nullptr;
+            p.logits ? p.logits + (size_t)(lb_ * p.Hq + lkh_ * G) * p.logits_stride : nullptr;
         // factored RoPE: the tile's base row e^{-i base th} (cosines, sines signed by base)
         float2 cb[P2], ncb[P2], sb[P2];
         if constexpr (FACT) {
@@ -694,7 +775,14 @@ cudaError_t launch_decode_rm(const DecodeParams &p, cudaStream_t stream)
     DecodeParams q = p;
     q.NT = p.cap > 0 ? (p.cap + SM::TK - 1) / SM::TK : 1;
     if (q.NT < 1) q.NT = 1;
-    const long long T_all = (long long)q.P * q.NT;
+    long long T_all = (long long)q.P * q.NT;
+    if constexpr (RM == 5) {
+        // retrieval tiles split evenly; at least as many blocks as streaming pairs would use
+        q.NT2 = p.ring_cap > 0 ? (p.ring_cap + SM::TK - 1) / SM::TK : 1;
+        const long long t_ret = (long long)p.B * p.n_ret * q.NT;
+        const long long p_str = (long long)p.B * p.n_str;
+        T_all = t_ret > p_str ? t_ret : p_str;
+    }
     const long long max_ctas = (long long)p.n_sm * SM::CPS;
     const int C = (int)(T_all < max_ctas ? T_all : max_ctas);
     return launch_pdl(kern, dim3((unsigned)C), dim3(kDecodeThreads), (size_t)SM::kBytes, stream, q);
@@ -705,6 +793,7 @@ constexpr int kDecodePlain = 0;   // valid slots 0 .. len-1, no positional term
 constexpr int kDecodeRope = 1;    // StreamingLLM layout, RoPE at in-cache positions
 constexpr int kDecodeAlibi = 2;   // StreamingLLM layout, ALiBi at in-cache positions
 constexpr int kDecodePaged = 3;   // page-table cache, no positional term
+constexpr int kDecodeDuo = 4;     // DuoAttention: full and ring caches in one launch
 
 // RoPE with one query head per KV head takes the factored rotation when the table covers the
 // per-lane offsets 0 .. TK-1; otherwise each key reads its table row.
@@ -717,6 +806,8 @@ cudaError_t launch_decode_typed(const DecodeParams &p, cudaStream_t stream)
         return launch_decode_rm<T, D, G, 3>(p, stream);
     } else if constexpr (MODE == kDecodePaged) {
         return launch_decode_rm<T, D, G, 4>(p, stream);
+    } else if constexpr (MODE == kDecodeDuo) {
+        return launch_decode_rm<T, D, G, 5>(p, stream);
     } else if constexpr (G == 1) {
         if (p.n_pos >= DecodeSmem<T, D, G, 2>::TK) return launch_decode_rm<T, D, G, 2>(p, stream);
         return launch_decode_rm<T, D, G, 1>(p, stream);

@@ -48,6 +48,15 @@ struct DecodeParams {
     // paged cache: K/V pool [n_pool][Hkv][bs][D]; len is per sequence [B]; cap = max_blocks*bs
     const int32_t *table;        // [B][max_blocks] physical block of each logical block
     int32_t max_blocks, bs, n_pool;
+    // DuoAttention: pairs 0 .. B*n_ret-1 are retrieval heads over k/v ([B][n_ret][cap][D], len
+    // per pair or n_valid); pairs B*n_ret .. are streaming heads over the ring caches k2/v2
+    // ([B][n_str][ring_cap][D]) with min(*t + 1, ring_cap) valid slots.  head_of maps retrieval
+    // index r (then n_ret + streaming index s) to the model's KV head.
+    int32_t n_ret, n_str, NT2, ring_cap;
+    const void *k2;
+    const void *v2;
+    int64_t sb2, sh2;
+    uint8_t head_of[256];
     int32_t kv_settled;          // cache slots and lengths final before the previous launch began
     int32_t balance;             // split the tiles by the lengths (not by capacity)
     float scale_log2;            // scale * log2(e)
@@ -68,7 +77,9 @@ struct DecodePlan {
     size_t off_o, off_ml, off_cnt, bytes;
 };
 
-DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm);
+// seg_pairs: pairs of the longest kind (0: all B*Hkv pairs are alike); a pair's tiles meet at
+// most C / seg_pairs + 2 blocks.
+DecodePlan decode_plan(int B, int Hq, int Hkv, int D, int cap, int n_sm, int seg_pairs = 0);
 // Sets the calling thread's kvc_last_error() message.
 void set_last_error(const char *msg);
 cudaError_t launch_decode_attn_f32(const DecodeParams &p, int D, int G, cudaStream_t stream);
@@ -83,6 +94,8 @@ cudaError_t launch_decode_attn_bf16_rope(const DecodeParams &p, int D, int G,
 cudaError_t launch_decode_attn_f32_paged(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16_paged(const DecodeParams &p, int D, int G,
                                           cudaStream_t stream);
+cudaError_t launch_decode_attn_f32_duo(const DecodeParams &p, int D, int G, cudaStream_t stream);
+cudaError_t launch_decode_attn_bf16_duo(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_f32_alibi(const DecodeParams &p, int D, int G, cudaStream_t stream);
 cudaError_t launch_decode_attn_bf16_alibi(const DecodeParams &p, int D, int G,
                                           cudaStream_t stream);
@@ -174,6 +187,25 @@ cudaError_t launch_topk_rows(const float *score, int64_t score_stride, int rows,
                              int tail, int32_t *idx, int64_t idx_stride, cudaStream_t stream);
 cudaError_t launch_iota_rows(int32_t *idx, int64_t idx_stride, int rows, int n,
                              cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// DuoAttention append: model KV head kh of the new token goes to retrieval cache index
+// index_of[kh] (< n_ret, tail slot len) or streaming ring index index_of[kh] - n_ret.
+struct DuoAppendParams {
+    void *k, *v;                 // retrieval caches [B][n_ret][cap][D]
+    int64_t sb, sh, ss;
+    int32_t cap;
+    int32_t *len;                // [B*n_ret]
+    void *k2, *v2;               // streaming rings [B][n_str][S+W+1][D]
+    int64_t sb2, sh2, ss2;
+    int32_t S, W;
+    const int64_t *t;
+    const void *k_new, *v_new;   // [B][Hkv][D]
+    int32_t B, Hkv, D, eb, n_ret;
+    uint8_t index_of[256];
+    int32_t *dev_code;
+};
+cudaError_t launch_duo_append(const DuoAppendParams &p, cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------
 // Block-level eviction over page tables.

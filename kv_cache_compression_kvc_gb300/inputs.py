@@ -25,6 +25,9 @@ Workloads (sizes as stated by the benchmark configuration):
               protected; pools of N(0,1) keys and values.
   h2o_gqa     the h2o shape on a grouped-query cache: 32 query heads over 8 KV heads; caches of
               N(0,1) keys/values at the 410 newest and 409 random older prompt positions.
+  duo         DuoAttention at 128k tokens: 32 layers, MHA 32 heads, D=128, bf16, batch 1; per
+              layer a seeded fixed choice of 8 retrieval heads (25 %) with full caches of N(0,1)
+              keys/values, the other 24 with 4 sinks + 64 recent tokens; 256 steps.
 """
 from __future__ import annotations
 
@@ -84,6 +87,8 @@ WORKLOADS = {
                       budget=819, L_local=410, extra={"block_size": 32}),
     "h2o_gqa": Workload("h2o_gqa", 32, 16, 32, 8, 128, 4096, 512, torch.bfloat16, 1242,
                         budget=819, L_local=410),
+    "duo": Workload("duo", 32, 1, 32, 32, 128, 131072, 256, torch.bfloat16, 1243, n_sink=4,
+                    window=64, extra={"n_retrieval": 8}),
 }
 
 

@@ -69,6 +69,12 @@ class kvc_free_pool(ctypes.Structure):
                 ("capacity", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class kvc_duo(ctypes.Structure):
+    _fields_ = [("n_retrieval", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("retrieval_heads", ctypes.c_void_p), ("t", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -82,6 +88,7 @@ _ALIBI_P = ctypes.POINTER(kvc_alibi)
 _POOL_P = ctypes.POINTER(kvc_block_pool)
 _PT_P = ctypes.POINTER(kvc_page_table)
 _FREE_P = ctypes.POINTER(kvc_free_pool)
+_DUO_P = ctypes.POINTER(kvc_duo)
 
 # name -> (restype, argtypes); every symbol declared in include/kvc.h
 SIGNATURES = {
@@ -105,6 +112,11 @@ SIGNATURES = {
     "kvc_decode_attn_alibi": (_I32, [_P, _I32, _CACHE_P, _ALIBI_P, _F32, _P, _P, _I64, _P, _P,
                                      _SZ, _U32, _P]),
     "kvc_alibi_slopes": (_I32, [_I32, _P]),
+    "kvc_duo_kv_bytes": (_U64, [_U64] * 9),
+    "kvc_duo_append": (_I32, [_CACHE_P, _P, _CACHE_P, _DUO_P, _P, _P, _P]),
+    "kvc_decode_attn_duo_workspace_bytes": (_SZ, [_I32] * 6),
+    "kvc_decode_attn_duo": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _CACHE_P, _DUO_P, _F32, _P, _P,
+                                   _I64, _P, _P, _SZ, _U32, _P]),
     "kvc_paged_append": (_I32, [_POOL_P, _PT_P, _FREE_P, _P, _P, _P, _P, _P]),
     "kvc_decode_attn_paged": (_I32, [_P, _I32, _POOL_P, _PT_P, _F32, _P, _P, _I64, _P, _P, _SZ,
                                      _U32, _P]),
@@ -407,6 +419,61 @@ def kvc_block_accumulate_evict(logits: torch.Tensor, lse: torch.Tensor, pt: kvc_
         _ptr(logits), logits.stride(-2), _ptr(lse), Hq, int(block_size), ctypes.byref(pt),
         ctypes.byref(free_pool), int(budget_blocks), int(recent_blocks), _ptr(released),
         _stream(stream)))
+
+
+class Duo:
+    """A kvc_duo descriptor with the host array of retrieval heads it points to kept alive."""
+
+    def __init__(self, retrieval_heads, n_sink: int, window: int, t: torch.Tensor):
+        heads = [int(h) for h in retrieval_heads]
+        self._heads = (ctypes.c_int32 * max(1, len(heads)))(*heads)
+        self.desc = kvc_duo()
+        self.desc.n_retrieval = len(heads)
+        self.desc.n_sink, self.desc.window = n_sink, window
+        self.desc.retrieval_heads = ctypes.cast(self._heads, ctypes.c_void_p)
+        self.desc.t = t.data_ptr()
+
+
+def kvc_duo_kv_bytes(n_layers, n_retrieval, n_streaming, d_head, seq_len, n_sink, window,
+                     bytes_per_elem, batch) -> int:
+    return int(load().kvc_duo_kv_bytes(n_layers, n_retrieval, n_streaming, d_head, seq_len,
+                                       n_sink, window, bytes_per_elem, batch))
+
+
+def kvc_duo_append(full: kvc_cache, len: torch.Tensor, ring: kvc_cache, duo: Duo,
+                   k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    _check(load().kvc_duo_append(ctypes.byref(full), _ptr(len), ctypes.byref(ring),
+                                 ctypes.byref(duo.desc), _ptr(k_new), _ptr(v_new),
+                                 _stream(stream)))
+
+
+def kvc_decode_attn_duo_workspace_bytes(batch, n_heads_q, n_heads_kv, d_head, cap,
+                                        n_retrieval) -> int:
+    return int(load().kvc_decode_attn_duo_workspace_bytes(batch, n_heads_q, n_heads_kv, d_head,
+                                                          cap, n_retrieval))
+
+
+def kvc_decode_attn_duo(q: torch.Tensor, full: kvc_cache, ring: kvc_cache, duo: Duo, *,
+                        scale: float, len: Optional[torch.Tensor] = None,
+                        n_valid: Optional[int] = None, flags: int = 0,
+                        out: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+                        lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """q [B, Hq, D] (model head order) -> out [B, Hq, D] fp32."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = _zeroed_workspace(kvc_decode_attn_duo_workspace_bytes(
+            B, Hq, full.n_heads_kv + ring.n_heads_kv, D, full.cap, duo.desc.n_retrieval),
+            q.device)
+    wp, wb = _ws_ptr(ws)
+    lstride = logits.stride(-2) if logits is not None else 0
+    _check(load().kvc_decode_attn_duo(
+        _ptr(q), Hq, ctypes.byref(full), _ptr(len), -1 if n_valid is None else int(n_valid),
+        ctypes.byref(ring), ctypes.byref(duo.desc), float(scale), _ptr(out), _ptr(logits),
+        lstride, _ptr(lse), wp, wb, int(flags), _stream(stream)))
+    return out
 
 
 def kvc_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, *,

@@ -7,6 +7,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 
@@ -172,3 +173,33 @@ def test_paged_validation_before_launch(kvc):
     st = lib.kvc_decode_attn_paged(4096, 2, B(pool), B(pt), 1.0, 4096, 4096, 32, None, None, 0,
                                    0, None)
     assert st == 4                                                 # logits_stride < cap 64
+
+
+def test_duo_kv_bytes_matches_oracle(kvc):
+    for args in [(32, 3, 7, 128, 131072, 4, 64, 2, 1), (1, 1, 1, 64, 10, 4, 64, 4, 2),
+                 (16, 8, 24, 256, 4096, 4, 64, 2, 8)]:
+        assert kvc.kvc_duo_kv_bytes(*args) == oracle.duo_kv_bytes(*args)
+
+
+def test_duo_validation_before_launch(kvc):
+    lib = kvc.load()
+    full, ring = kvc.kvc_cache(), kvc.kvc_cache()
+    for c, h, cap in ((full, 2, 64), (ring, 6, 69)):
+        c.k = c.v = 4096
+        c.dtype, c.batch, c.n_heads_kv, c.cap, c.d_head = kvc.KVC_BF16, 1, h, cap, 128
+        c.stride_b, c.stride_h, c.stride_slot = h * cap * 128, cap * 128, 128
+    duo = kvc.Duo([1, 5], 4, 64, torch.zeros(1, dtype=torch.int64))
+    B = ctypes.byref
+    st = lib.kvc_decode_attn_duo(4096, 6, B(full), None, 10, B(ring), B(duo.desc), 1.0, 4096,
+                                 None, 0, None, None, 0, 0, None)
+    assert st == 2                                                 # 6 query heads over 8 KV heads
+    bad = kvc.Duo([5, 1], 4, 64, torch.zeros(1, dtype=torch.int64))
+    st = lib.kvc_decode_attn_duo(4096, 8, B(full), None, 10, B(ring), B(bad.desc), 1.0, 4096,
+                                 None, 0, None, None, 0, 0, None)
+    assert st == 1 and "ascending" in kvc.kvc_last_error()
+    three = kvc.Duo([0, 1, 2], 4, 64, torch.zeros(1, dtype=torch.int64))
+    st = lib.kvc_duo_append(B(full), 4096, B(ring), B(three.desc), 4096, 4096, None)
+    assert st == 2                                                 # full cache holds 2 heads
+    ring.cap = 68
+    st = lib.kvc_duo_append(B(full), 4096, B(ring), B(duo.desc), 4096, 4096, None)
+    assert st == 4                                                 # ring < 4 + 64 + 1 slots
