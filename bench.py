@@ -829,7 +829,7 @@ class PagedBlocks(DecodeWorkload):
         bs = self.bs
         self.mb = self.nb + 1
         self.n_pool = B * self.mb + B
-        self.kp = torch.empty((L, self.n_pool, H, bs, D), dtype=w.dtype, device=dev)
+        self.kp = torch.empty((L, H, self.n_pool, bs, D), dtype=w.dtype, device=dev)
         self.vp = torch.empty_like(self.kp)
         for l in range(L):
             g = I.generator(w.seed * 1000 + l, dev)

@@ -126,10 +126,12 @@ typedef struct {
  * cache is allocated in blocks of 16 or 32 tokens reached through a page table; blocks leave
  * the page table and return to the free pool without their contents being copied).
  * One pool, one set of page tables and one free stack per layer.
- * Element (blk, h, j, d) of K is at k + ((blk*n_heads_kv + h)*block_size + j)*d_head + d
- * (v likewise): a block holds block_size consecutive tokens of every KV head.              */
+ * Element (blk, h, j, d) of K is at k + ((h*n_blocks + blk)*block_size + j)*d_head + d
+ * (v likewise): block blk holds block_size consecutive tokens of every KV head, each head's
+ * part in that head's region of the pool (head-major, so the blocks one head reads stay
+ * close together whatever ids the page table holds).                                          */
 typedef struct {
-    void *k;                /* device [n_blocks][n_heads_kv][block_size][d_head]             */
+    void *k;                /* device [n_heads_kv][n_blocks][block_size][d_head]             */
     void *v;
     int32_t dtype;          /* kvc_dtype                                                     */
     int32_t n_blocks;       /* physical blocks in the pool                                   */

@@ -590,7 +590,7 @@ static kvc_status check_paged(const kvc_block_pool *pool, const kvc_page_table *
     c.cap = pt->max_blocks * pool->block_size;
     c.d_head = pool->d_head;
     c.stride_b = 0;
-    c.stride_h = (int64_t)pool->block_size * pool->d_head;
+    c.stride_h = (int64_t)pool->n_blocks * pool->block_size * pool->d_head;   // head-major
     c.stride_slot = pool->d_head;
     *view = c;
     return check_cache(&c, name, true);

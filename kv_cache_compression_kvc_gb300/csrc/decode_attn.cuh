@@ -55,7 +55,9 @@
 // Paged cache ("Implementação prática em vLLM e SGLang": blocks of 16 or 32 tokens behind a page
 // table).  The slots of a sequence are its page table's blocks in order; a tile of TK logical
 // slots is copied run by run, one bulk copy per block it touches, from the pool's
-// [block][head][slot][d] rows, so the compute loop is unchanged.  A table entry outside the pool
+// [head][block][slot][d] rows, so the compute loop is unchanged.  The pool is head-major: all
+// of one head's blocks lie in one region (n_blocks * block_size rows), so the blocks a (sequence,
+// head) pair reads stay within a few large pages wherever the page table puts them.  A table entry outside the pool
 // records KVC_DEV_BAD_BLOCK and reads block 0 instead (the copy sizes stay as announced).
 //
 // DuoAttention ("Decomposição funcional com o DuoAttention": retrieval heads keep the full
@@ -376,7 +378,7 @@ decode_attn_kernel(const DecodeParams p)
         const int j1 = j0 + rows;
         if constexpr (PAGED) {
             // one run per block of the page table the tile touches
-            const size_t blk_elems = (size_t)p.Hkv * p.bs * D;
+            const size_t head_elems = (size_t)p.n_pool * p.bs * D;   // a head's pool region
             for (int r = j0; r < j1;) {
                 const int lb = r / p.bs, off = r - lb * p.bs;
                 const int n = min(j1 - r, p.bs - off);
@@ -385,7 +387,7 @@ decode_attn_kernel(const DecodeParams p)
                     record_code(p.dev_code, 9 /* KVC_DEV_BAD_BLOCK */);
                     phys = 0;
                 }
-                const size_t src = (size_t)phys * blk_elems + ((size_t)kh * p.bs + off) * D;
+                const size_t src = (size_t)kh * head_elems + ((size_t)phys * p.bs + off) * D;
                 const uint32_t doff = (uint32_t)((r - j0) * D * EB);
                 bulk_g2s(kdst + doff, static_cast<const T *>(p.k) + src, n * D * EB, full);
                 bulk_g2s(vdst + doff, static_cast<const T *>(p.v) + src, n * D * EB, full);

@@ -45,7 +45,7 @@ struct DecodeParams {
     const float *cos_sin;        // [n_pos][2][D/2]: cosines then sines per distance
     int32_t n_pos;               // rows of cos_sin
     const float *alibi;          // ALiBi slopes per query head [Hq] (same layout as RoPE) or null
-    // paged cache: K/V pool [n_pool][Hkv][bs][D]; len is per sequence [B]; cap = max_blocks*bs
+    // paged cache: K/V pool [Hkv][n_pool][bs][D]; len is per sequence [B]; cap = max_blocks*bs
     const int32_t *table;        // [B][max_blocks] physical block of each logical block
     int32_t max_blocks, bs, n_pool;
     // DuoAttention: pairs 0 .. B*n_ret-1 are retrieval heads over k/v ([B][n_ret][cap][D], len
@@ -210,7 +210,7 @@ cudaError_t launch_duo_append(const DuoAppendParams &p, cudaStream_t stream);
 // ------------------------------------------------------------------------------------------
 // Block-level eviction over page tables.
 struct PagedParams {
-    void *k;                     // pool [n_pool][Hkv][bs][D]
+    void *k;                     // pool [Hkv][n_pool][bs][D]
     void *v;
     int32_t n_pool, Hkv, bs, D, B, max_blocks;
     int32_t *table;              // [B][max_blocks]

@@ -4,7 +4,8 @@
 // Score(block) = sum over t in the block of s_t; when memory runs out the lowest-scoring blocks
 // leave the page table and return to the free pool with no copy of their contents).
 //
-// State per layer: a pool of physical blocks K/V [n_pool][Hkv][bs][D]; per sequence b a page
+// State per layer: a pool of physical blocks K/V [Hkv][n_pool][bs][D] (head-major: one head's
+// blocks share a region); per sequence b a page
 // table (physical ids in logical order), its block count, its token count and one score per
 // table entry; a stack of free physical ids shared by the sequences.
 //
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kAppendThreads) paged_append_kernel(const Page
     char *vd = static_cast<char *>(p.v);
     for (int i = threadIdx.x; i < total; i += kAppendThreads) {
         const int h = i / vpr, c = i - h * vpr;
-        const size_t dst = ((((size_t)blk * p.Hkv + h) * p.bs + off) * row_bytes) + (size_t)c * 16;
+        const size_t dst = ((((size_t)h * p.n_pool + blk) * p.bs + off) * row_bytes) + (size_t)c * 16;
         const size_t src = (size_t)h * row_bytes + (size_t)c * 16;
         const uint4 kx = __ldg(reinterpret_cast<const uint4 *>(kn + src));
         const uint4 vx = __ldg(reinterpret_cast<const uint4 *>(vn + src));

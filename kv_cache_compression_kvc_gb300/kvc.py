@@ -343,15 +343,15 @@ def kvc_decode_attn_alibi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
 
 
 def block_pool_view(k_pool: torch.Tensor, v_pool: torch.Tensor) -> kvc_block_pool:
-    """Describe a block pool: K and V tensors [n_blocks, n_heads_kv, block_size, d_head],
-    contiguous."""
+    """Describe a block pool: K and V tensors [n_heads_kv, n_blocks, block_size, d_head]
+    (head-major), contiguous."""
     if k_pool.dim() != 4 or not k_pool.is_contiguous() or v_pool.shape != k_pool.shape or \
             not v_pool.is_contiguous() or v_pool.dtype != k_pool.dtype:
-        raise ValueError("block pools are contiguous [n_blocks, n_heads_kv, block_size, d_head]")
+        raise ValueError("block pools are contiguous [n_heads_kv, n_blocks, block_size, d_head]")
     c = kvc_block_pool()
     c.k, c.v = k_pool.data_ptr(), v_pool.data_ptr()
     c.dtype = _dtype_code(k_pool.dtype)
-    c.n_blocks, c.n_heads_kv, c.block_size, c.d_head = (int(x) for x in k_pool.shape)
+    c.n_heads_kv, c.n_blocks, c.block_size, c.d_head = (int(x) for x in k_pool.shape)
     return c
 
 

@@ -19,11 +19,11 @@ def _gather(k_pool, v_pool, table, n, bs):
     ks, vs = [], []
     for i in range(nb):
         fill = min(bs, n - i * bs)
-        ks.append(k_pool[table[i], :, :fill])
-        vs.append(v_pool[table[i], :, :fill])
+        ks.append(k_pool[:, table[i], :fill])
+        vs.append(v_pool[:, table[i], :fill])
     D = k_pool.shape[-1]
     if not ks:
-        return np.zeros((k_pool.shape[1], 0, D)), np.zeros((k_pool.shape[1], 0, D))
+        return np.zeros((k_pool.shape[0], 0, D)), np.zeros((k_pool.shape[0], 0, D))
     return np.concatenate(ks, axis=1), np.concatenate(vs, axis=1)
 
 
@@ -39,8 +39,8 @@ def test_paged_decode_matches_oracle(dtype, D, G, bs):
     Hq = Hkv * G
     n_pool = B * mb + 3
     seed = 200 + D + G + bs
-    kp = I.randn((n_pool, Hkv, bs, D), seed, dev, dtype)
-    vp = I.randn((n_pool, Hkv, bs, D), seed + 1, dev, dtype)
+    kp = I.randn((Hkv, n_pool, bs, D), seed, dev, dtype)
+    vp = I.randn((Hkv, n_pool, bs, D), seed + 1, dev, dtype)
     q = I.randn((B, Hq, D), seed + 2, dev, dtype)
     rng = np.random.default_rng(seed)
     perm = rng.permutation(n_pool)[:B * mb].reshape(B, mb)
@@ -93,7 +93,7 @@ def test_block_eviction_steps_teacher_forced(dtype, D, G, bs, budget, recent):
     n_pool = B * mb + 2
     T = (budget + 3) * bs + 5
     scale = 1 / math.sqrt(D)
-    kp = torch.zeros((n_pool, Hkv, bs, D), device=dev, dtype=dtype)
+    kp = torch.zeros((Hkv, n_pool, bs, D), device=dev, dtype=dtype)
     vp = torch.zeros_like(kp)
     qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, T, 300 + D + bs, dev, dtype)
     rng = np.random.default_rng(5)
@@ -183,7 +183,7 @@ def test_block_scores_accumulate_like_the_oracle():
     Hq = Hkv * G
     n_pool = B * mb
     dtype = torch.float32
-    kp = torch.zeros((n_pool, Hkv, bs, D), device=dev, dtype=dtype)
+    kp = torch.zeros((Hkv, n_pool, bs, D), device=dev, dtype=dtype)
     vp = torch.zeros_like(kp)
     T = mb * bs - 3
     qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, T, 401, dev, dtype)
@@ -226,7 +226,7 @@ def test_paged_append_reports_an_empty_pool():
     dev = cuda_or_skip()
     kvc = lib()
     B, Hkv, D, bs, mb = 2, 1, 64, 16, 2
-    kp = torch.zeros((1, Hkv, bs, D), device=dev)
+    kp = torch.zeros((Hkv, 1, bs, D), device=dev)
     vp = torch.zeros_like(kp)
     ids = torch.tensor([0], dtype=torch.int32, device=dev)
     top = torch.tensor([1], dtype=torch.int32, device=dev)
