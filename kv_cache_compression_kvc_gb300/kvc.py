@@ -259,6 +259,7 @@ def make_rope(n_sink: int, window: int, t: torch.Tensor, cos_sin: torch.Tensor) 
     r.t = t.data_ptr()
     r.cos_sin = cos_sin.data_ptr()
     r.n_pos = cos_sin.shape[0]
+    r._keep = (t, cos_sin)          # the descriptor holds their addresses: keep them alive
     return r
 
 
@@ -318,6 +319,7 @@ def make_alibi(n_sink: int, window: int, t: torch.Tensor, slopes: torch.Tensor) 
     a.n_sink, a.window = n_sink, window
     a.t = t.data_ptr()
     a.slopes = slopes.data_ptr()
+    a._keep = (t, slopes)           # the descriptor holds their addresses: keep them alive
     return a
 
 
@@ -432,6 +434,7 @@ class Duo:
         self.desc.n_sink, self.desc.window = n_sink, window
         self.desc.retrieval_heads = ctypes.cast(self._heads, ctypes.c_void_p)
         self.desc.t = t.data_ptr()
+        self._t = t                     # the descriptor holds its address: keep it alive
 
 
 def kvc_duo_kv_bytes(n_layers, n_retrieval, n_streaming, d_head, seq_len, n_sink, window,
