@@ -193,6 +193,7 @@ def cache_view(k: torch.Tensor, v: Optional[torch.Tensor] = None) -> kvc_cache:
     c.dtype = _dtype_code(k.dtype)
     c.batch, c.n_heads_kv, c.cap, c.d_head = (int(x) for x in k.shape)
     c.stride_b, c.stride_h, c.stride_slot = k.stride(0), k.stride(1), k.stride(2)
+    c._keep = (k, v)                # the descriptor holds their addresses: keep them alive
     return c
 
 
@@ -354,6 +355,7 @@ def block_pool_view(k_pool: torch.Tensor, v_pool: torch.Tensor) -> kvc_block_poo
     c.k, c.v = k_pool.data_ptr(), v_pool.data_ptr()
     c.dtype = _dtype_code(k_pool.dtype)
     c.n_heads_kv, c.n_blocks, c.block_size, c.d_head = (int(x) for x in k_pool.shape)
+    c._keep = (k_pool, v_pool)
     return c
 
 
@@ -371,6 +373,7 @@ def page_table_view(table: torch.Tensor, n_blocks: torch.Tensor, len: torch.Tens
     c.table, c.n_blocks, c.len, c.score = (table.data_ptr(), n_blocks.data_ptr(), len.data_ptr(),
                                            score.data_ptr())
     c.batch, c.max_blocks = B, mb
+    c._keep = (table, n_blocks, len, score)
     return c
 
 
@@ -379,6 +382,7 @@ def free_pool_view(ids: torch.Tensor, top: torch.Tensor) -> kvc_free_pool:
     c = kvc_free_pool()
     c.ids, c.top = ids.data_ptr(), top.data_ptr()
     c.capacity = ids.numel()
+    c._keep = (ids, top)
     return c
 
 
