@@ -422,16 +422,25 @@ class SelectDecode(DecodeWorkload):
                                       idx_out=idx, ws=ws)
                 kvc.kvc_compact_gather(k, v, idx, self.budgets[l], Kc, Vc, len_dst=self.lens[l])
                 warm = False
-            flush.fill_(l & 0xff)
+            # device time of the selection and the compaction: both captured as CUDA graphs
+            # (host work such as tensor-map encoding happens at capture, untimed, as it would
+            # in a captured or pipelined prefill), replayed after an L2 flush
+            g_sel, g_gat = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_sel):
+                kvc.kvc_snapkv_select(q_obs, k, seq_len=w.prompt, L_obs=w.L_obs,
+                                      budget=self.budgets[l], scale=w.scale, pool_k=w.pool_k,
+                                      idx_out=idx, ws=ws)
+            with torch.cuda.graph(g_gat):
+                kvc.kvc_compact_gather(k, v, idx, self.budgets[l], Kc, Vc, len_dst=self.lens[l])
             torch.cuda.synchronize()
+            flush.fill_(l & 0xff)
             e[0].record()
-            kvc.kvc_snapkv_select(q_obs, k, seq_len=w.prompt, L_obs=w.L_obs,
-                                  budget=self.budgets[l], scale=w.scale, pool_k=w.pool_k,
-                                  idx_out=idx, ws=ws)
+            g_sel.replay()
             e[1].record()
-            kvc.kvc_compact_gather(k, v, idx, self.budgets[l], Kc, Vc, len_dst=self.lens[l])
+            g_gat.replay()
             e[2].record()
             torch.cuda.synchronize()
+            del g_sel, g_gat
             sel_ms.append(e[0].elapsed_time(e[1]))
             gat_ms.append(e[1].elapsed_time(e[2]))
             self.K.append(Kc)
