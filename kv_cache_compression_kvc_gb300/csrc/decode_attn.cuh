@@ -377,21 +377,26 @@ decode_attn_kernel(const DecodeParams p)
         };
         const int j1 = j0 + rows;
         if constexpr (PAGED) {
-            // one run per block of the page table the tile touches
-            const size_t head_elems = (size_t)p.n_pool * p.bs * D;   // a head's pool region
-            for (int r = j0; r < j1;) {
-                const int lb = r / p.bs, off = r - lb * p.bs;
+            // one run per block of the page table the tile touches; one division per tile
+            const T *kh_k = static_cast<const T *>(p.k) + (size_t)kh * p.n_pool * p.bs * D;
+            const T *kh_v = static_cast<const T *>(p.v) + (size_t)kh * p.n_pool * p.bs * D;
+            int lb = j0 / p.bs;
+            int off = j0 - lb * p.bs;
+            uint32_t doff = 0;
+            for (int r = j0; r < j1; ++lb) {
                 const int n = min(j1 - r, p.bs - off);
                 int phys = table_entry(b, lb);
                 if (phys < 0 || phys >= p.n_pool) {
                     record_code(p.dev_code, 9 /* KVC_DEV_BAD_BLOCK */);
                     phys = 0;
                 }
-                const size_t src = (size_t)kh * head_elems + ((size_t)phys * p.bs + off) * D;
-                const uint32_t doff = (uint32_t)((r - j0) * D * EB);
-                bulk_g2s(kdst + doff, static_cast<const T *>(p.k) + src, n * D * EB, full);
-                bulk_g2s(vdst + doff, static_cast<const T *>(p.v) + src, n * D * EB, full);
+                const size_t src = (size_t)phys * p.bs * D + (size_t)off * D;
+                const uint32_t bytes = (uint32_t)n * (uint32_t)(D * EB);
+                bulk_g2s(kdst + doff, kh_k + src, bytes, full);
+                bulk_g2s(vdst + doff, kh_v + src, bytes, full);
+                doff += bytes;
                 r += n;
+                off = 0;
             }
         } else if (!RANKED) {
             copy_run(j0, j1, j0);
