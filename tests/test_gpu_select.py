@@ -355,3 +355,67 @@ def test_h2o_grouped_query_steps_teacher_forced(dtype, G, D):
                 assert_rel(s_gpu[b, kh], s_ref, 1e-4, 1e-5, f"s step {step} ({b},{kh})")
                 ev = oracle.h2o_evict_f32(s_gpu[b, kh], pos0[b, kh], t, L_local)
                 assert ev == int(f_gpu[b * Hkv + kh]), f"evictee step {step} ({b},{kh})"
+
+
+@pytest.mark.parametrize("dtype,G", [(torch.float32, 1), (torch.bfloat16, 4)])
+def test_h2o_streamed_prompt_teacher_forced(dtype, G):
+    """The streamed-prompt reading of H2O: the prompt goes through the decode-time step token
+    by token from an empty cache, eviction active as soon as the cache exceeds the budget.
+    Tail appends fill the cache (len counts the tokens), then each token takes the slot the
+    previous step freed; decode and score update run over the tokens held so far.  Every step
+    from the GPU's own state against the oracle's step: output, scores, evictee (exact, given
+    the GPU's fp32 scores)."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv, D, N, budget, L_local = 2, 2, 64, 150, 48, 24
+    Hq = Hkv * G
+    cap = budget + 1
+    Kc = torch.zeros((B, Hkv, cap, D), device=dev, dtype=dtype)
+    Vc = torch.zeros_like(Kc)
+    pos = torch.full((B, Hkv, cap), -1, dtype=torch.int32, device=dev)
+    sc = torch.zeros((B, Hkv, cap), device=dev)
+    ln = torch.zeros(B * Hkv, dtype=torch.int32, device=dev)
+    free = torch.zeros(B * Hkv, dtype=torch.int32, device=dev)
+    t_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    qs, ks, vs = I.decode_qkv(B, Hq, Hkv, D, N, 77 + G, dev, dtype)
+    logits = torch.empty((B, Hq, cap), device=dev)
+    lse = torch.empty((B, Hq), device=dev)
+    scale = 1 / math.sqrt(D)
+    n_evicted = 0
+    for t in range(N):
+        t_dev.fill_(t)
+        n = min(t + 1, cap)
+        if t < cap:
+            kvc.kvc_stream_append(Kc, Vc, kvc.KVC_APPEND_TAIL, ks[t], vs[t], t=t_dev, len=ln,
+                                  pos=pos, score=sc)
+        else:
+            kvc.kvc_stream_append(Kc, Vc, kvc.KVC_APPEND_FREE_SLOT, ks[t], vs[t], t=t_dev,
+                                  free_slot=free, pos=pos, score=sc)
+        K0, V0 = f64(Kc), f64(Vc)
+        pos0, s0 = pos.cpu().numpy().astype(np.int64), sc.cpu().numpy().astype(np.float64)
+        out = kvc.kvc_decode_attn(qs[t], Kc, Vc, scale=scale, n_valid=n, logits=logits, lse=lse)
+        kvc.kvc_h2o_accumulate_evict_gqa(logits, lse, sc, pos, free, n_slots=n, t=t_dev,
+                                         L_local=L_local, budget=budget)
+        assert kvc.kvc_device_status() == 0, f"t={t}"
+        o_gpu, s_gpu, f_gpu = out.cpu().numpy(), sc.cpu().numpy(), free.cpu().numpy()
+        for b in range(B):
+            for kh in range(Hkv):
+                qg = f64(qs[t, b, kh * G:(kh + 1) * G])
+                o_ref, s_ref, ev_ref = oracle.h2o_step_group(qg, K0[b, kh, :n], V0[b, kh, :n],
+                                                             pos0[b, kh, :n], s0[b, kh, :n], t,
+                                                             L_local, budget, scale)
+                assert_close(o_gpu[b, kh * G:(kh + 1) * G], o_ref, TOL[dtype], f"out t={t}")
+                assert_rel(s_gpu[b, kh, :n], s_ref, 1e-4, 1e-5, f"s t={t} ({b},{kh})")
+                if n > budget:
+                    ev = oracle.h2o_evict_f32(s_gpu[b, kh, :n], pos0[b, kh, :n], t, L_local)
+                    assert ev == int(f_gpu[b * Hkv + kh]), f"evictee t={t} ({b},{kh})"
+                    n_evicted += 1
+                else:
+                    assert ev_ref == -1
+    assert n_evicted == B * Hkv * (N - budget)
+    # the cache ends with the L_local newest prompt tokens and budget - L_local older ones
+    p_end = pos.cpu().numpy()
+    for b in range(B):
+        for kh in range(Hkv):
+            held = sorted(int(x) for x in p_end[b, kh])
+            assert held[-L_local:] == list(range(N - L_local, N))
