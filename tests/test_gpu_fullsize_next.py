@@ -1,4 +1,4 @@
-"""GPU parity of the survey's next rows at the bench workloads' full sizes, in the launch
+"""GPU parity of ALiBi, DuoAttention, block eviction and grouped-query H2O at the bench workloads' full sizes, in the launch
 configuration bench.py times (one layer, same shapes and calls), on sampled outputs the oracle
 computes one by one, plus properties that hold at any size."""
 import numpy as np
