@@ -1,6 +1,7 @@
-"""GPU parity of ALiBi, DuoAttention, block eviction and grouped-query H2O at the bench workloads' full sizes, in the launch
-configuration bench.py times (one layer, same shapes and calls), on sampled outputs the oracle
-computes one by one, plus properties that hold at any size."""
+"""GPU parity of ALiBi, DuoAttention, block eviction and grouped-query H2O at the bench
+workloads' full sizes, in the launch configuration bench.py times (one layer, same shapes and
+calls), on sampled outputs the oracle computes one by one, plus properties that hold at any
+size."""
 import numpy as np
 import pytest
 import torch
