@@ -9,7 +9,7 @@ Functions (each follows the page passage cited in ``kvc_oracle.c``):
   kv_bytes, pyramid_budgets, rope, attend, stream_window, stream_slot, stream_decode,
   stream_decode_alibi, topk_ascending, snapkv_obs_scores, pool1d, snapkv_select, snapkv_stage_f32,
   h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_step_group, h2o_evict_f32, block_step, block_evict_f32,
-  duo_decode, duo_kv_bytes.
+  duo_decode, duo_kv_bytes, block_prompt_select.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against values the pages
 print, closed forms, invariants, library routines on special cases or brute force on tiny
@@ -87,6 +87,8 @@ _SIGS = {
     "orc_duo_decode": (None, [ctypes.c_int, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                               _f64, _ptr, _ptr, _ptr, _ptr]),
     "orc_duo_kv_bytes": (_u64, [_u64] * 9),
+    "orc_block_prompt_select": (ctypes.c_int, [ctypes.c_int] * 3 + [_ptr, ctypes.c_int,
+                                                                   ctypes.c_int, _ptr, _ptr]),
 }
 
 
@@ -323,3 +325,15 @@ def duo_kv_bytes(n_layers, n_retrieval, n_streaming, d_head, seq_len, n_sink, wi
                  bytes_per_elem, batch) -> int:
     return int(lib().orc_duo_kv_bytes(n_layers, n_retrieval, n_streaming, d_head, seq_len,
                                       n_sink, window, bytes_per_elem, batch))
+
+
+def block_prompt_select(s, bs: int, budget_blocks: int, recent_blocks: int):
+    """s [H, N] per-token scores -> (kept block indices ascending, block scores [nblk])."""
+    s = _f(s)
+    H, N = s.shape
+    nblk = (N + bs - 1) // bs
+    keep = np.empty(max(nblk, 1), dtype=np.int32)
+    sc = np.empty(max(nblk, 1))
+    n = lib().orc_block_prompt_select(H, N, bs, _p(s), budget_blocks, recent_blocks, _p(sc),
+                                      _p(keep))
+    return keep[:n].copy(), sc[:nblk].copy()

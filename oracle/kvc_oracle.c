@@ -582,3 +582,37 @@ uint64_t orc_duo_kv_bytes(uint64_t n_layers, uint64_t n_retrieval, uint64_t n_st
     return 2ull * n_layers * d_head * bytes_per_elem * batch *
            (n_retrieval * seq_len + n_streaming * buf);
 }
+
+/* Block-level eviction at the end of the prompt: the prompt's tokens are grouped into blocks
+ * of bs (block i holds tokens i*bs .. min(N, (i+1)*bs) - 1), each block is rated by
+ * Score(block) = sum over its tokens t and the H heads of s[h][t] (the prompt's accumulated
+ * attention, [KVC] H2O column sums), and the cache keeps the recent_blocks newest blocks plus
+ * the budget_blocks - recent_blocks highest-scoring older ones (equal scores keep the lower
+ * index, as for tokens), in ascending order.  Reading: the one-shot prompt compression of H2O
+ * ([KVC] H2O), taken at block granularity as "Implementação prática em vLLM e SGLang" rates
+ * blocks.  s: [H][N]; score_blk (nullable): [nblk] block scores; keep: [nblk] ascending kept
+ * block indices.  Returns the number kept.                                                   */
+int orc_block_prompt_select(int H, int N, int bs, const double *s, int budget_blocks,
+                            int recent_blocks, double *score_blk, int32_t *keep)
+{
+    const int nblk = (N + bs - 1) / bs;
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(nblk > 0 ? nblk : 1));
+    for (int i = 0; i < nblk; ++i) sc[i] = 0.0;
+    for (int h = 0; h < H; ++h)
+        for (int t = 0; t < N; ++t) sc[t / bs] += s[(size_t)h * N + t];
+    if (score_blk) for (int i = 0; i < nblk; ++i) score_blk[i] = sc[i];
+    int n_keep;
+    if (nblk <= budget_blocks) {
+        for (int i = 0; i < nblk; ++i) keep[i] = i;
+        n_keep = nblk;
+    } else {
+        const int recent = recent_blocks < nblk ? recent_blocks : nblk;
+        const int n_old = nblk - recent;
+        const int k_old = budget_blocks - recent;
+        orc_topk_ascending(n_old, k_old, sc, keep);
+        for (int j = 0; j < recent; ++j) keep[k_old + j] = n_old + j;
+        n_keep = k_old + recent;
+    }
+    free(sc);
+    return n_keep;
+}

@@ -704,3 +704,32 @@ def test_duo_heads_against_library_attention():
         a = oracle.duo_decode(True, t, S, W, q, hk, hv, scale)
         b = oracle.duo_decode(False, t, S, W, q, hk, hv, scale)
         assert np.max(np.abs(a - b)) <= 1e-15
+
+
+def test_block_prompt_select_one_token_blocks_is_h2o_prompt_select():
+    rng = np.random.default_rng(81)
+    N, L_local, K_hh = 200, 30, 45
+    s = rng.random(N) * 3
+    s[[10, 11, 12]] = 1.5                                    # exact ties among candidates
+    keep, sc = oracle.block_prompt_select(s[None], 1, L_local + K_hh, L_local)
+    assert np.array_equal(keep, oracle.h2o_prompt_select(s, L_local, K_hh))
+    assert np.array_equal(sc, s)
+
+
+def test_block_prompt_select_block_scores_and_rules():
+    """Uniform scores give H * block_size per block (the partial last block: H * its tokens);
+    the recent blocks are always kept, the rest by score with ties to the lower index; a
+    prompt within the budget keeps every block."""
+    H, N, bs = 3, 70, 16                                     # 5 blocks, the last holds 6 tokens
+    keep, sc = oracle.block_prompt_select(np.ones((H, N)), bs, 3, 1)
+    assert list(sc) == [48.0, 48.0, 48.0, 48.0, 18.0]
+    assert list(keep) == [0, 1, 4]                           # ties: lower indices, + newest
+    s = np.zeros((H, N))
+    s[1, 20] = 5.0                                           # block 1
+    s[2, 50:53] = 1.0                                        # block 3
+    keep, _ = oracle.block_prompt_select(s, bs, 3, 1)
+    assert list(keep) == [1, 3, 4]
+    keep, _ = oracle.block_prompt_select(s, bs, 2, 2)
+    assert list(keep) == [3, 4]                              # only the recent blocks
+    keep, _ = oracle.block_prompt_select(s, bs, 5, 1)
+    assert list(keep) == [0, 1, 2, 3, 4]
