@@ -840,34 +840,49 @@ class PagedBlocks(DecodeWorkload):
         self.n_pool = B * self.mb + B
         self.kp = torch.empty((L, H, self.n_pool, bs, D), dtype=w.dtype, device=dev)
         self.vp = torch.empty_like(self.kp)
-        for l in range(L):
-            g = I.generator(w.seed * 1000 + l, dev)
-            self.kp[l].normal_(generator=g)
-            self.vp[l].normal_(generator=g)
-        self.table = torch.empty((L, B, self.mb), dtype=torch.int32, device=dev)
+        self.table = torch.full((L, B, self.mb), -1, dtype=torch.int32, device=dev)
         self.ids = torch.empty((L, self.n_pool), dtype=torch.int32, device=dev)
-        self.top = torch.empty((L, 1), dtype=torch.int32, device=dev)
+        self.top = torch.full((L, 1), self.n_pool, dtype=torch.int32, device=dev)
         for l in range(L):
             perm = torch.randperm(self.n_pool, generator=torch.Generator().manual_seed(l))
-            used = perm[:B * self.nb].reshape(B, self.nb)
-            self.table[l].fill_(-1)
-            self.table[l, :, :self.nb] = used.to(torch.int32).to(dev)
-            free = perm[B * self.nb:].to(torch.int32)
-            self.ids[l].fill_(-1)
-            self.ids[l, :free.numel()] = free.to(dev)
-            self.top[l] = free.numel()
-        self.n_blk = torch.full((L, B), self.nb, dtype=torch.int32, device=dev)
-        self.len = torch.full((L, B), self.nb * bs, dtype=torch.int32, device=dev)
+            self.ids[l] = perm.to(torch.int32).to(dev)
+        self.n_blk = torch.zeros((L, B), dtype=torch.int32, device=dev)
+        self.len = torch.zeros((L, B), dtype=torch.int32, device=dev)
         self.score = torch.zeros((L, B, self.mb), dtype=torch.float32, device=dev)
-        self.cap = self.mb * bs
-        self.logits = torch.empty((L, B, w.n_heads_q, self.cap), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((L, B, w.n_heads_q), dtype=torch.float32, device=dev)
         self.pools = [kvc.block_pool_view(self.kp[l], self.vp[l]) for l in range(L)]
         self.pts = [kvc.page_table_view(self.table[l], self.n_blk[l], self.len[l], self.score[l])
                     for l in range(L)]
         self.fps = [kvc.free_pool_view(self.ids[l], self.top[l]) for l in range(L)]
+        # the prompt: H2O's column sums over the whole prompt (the H2O workload's inputs), then
+        # the one-shot block compression to the budget; the latter is timed on the device while
+        # the scoring kernels run ahead of the host
+        ws_h = torch.zeros(kvc.kvc_h2o_prefill_workspace_bytes(B, H, D, w.prompt) + 256,
+                           dtype=torch.uint8, device=dev)
+        s_full = torch.empty((B, H, w.prompt), dtype=torch.float32, device=dev)
+        sel_ms = []
+        for l in range(L):
+            q, k, v = I.h2o_layer(w, l, dev)
+            kvc.kvc_h2o_prefill_select(q, k, seq_len=w.prompt, L_local=w.L_local,
+                                       K_hh=w.budget - w.L_local, scale=w.scale, s_full=s_full,
+                                       ws=ws_h)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            kvc.kvc_block_prompt_select(s_full, k, v, self.pools[l], self.pts[l], self.fps[l],
+                                        seq_len=w.prompt, budget_blocks=self.nb,
+                                        recent_blocks=self.recent)
+            e1.record()
+            torch.cuda.synchronize()
+            sel_ms.append(e0.elapsed_time(e1))
+            del q, k, v
+        code = kvc.kvc_device_status()
+        if code != 0:
+            raise RuntimeError(f"prompt block selection: device range check {code}")
+        self.extra["block_prompt_select_ms"] = round(sum(sel_ms), 3)
+        self.cap = self.mb * bs
+        self.logits = torch.empty((L, B, w.n_heads_q, self.cap), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((L, B, w.n_heads_q), dtype=torch.float32, device=dev)
         self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.cap, dev)
-        self.launches_per_step = 3 * L
+        self.launches_per_step = 4 * L          # append, decode, score update, release
         self.side = torch.cuda.Stream(device=dev)
         self.done = [torch.cuda.Event() for _ in range(L)]
 
@@ -929,8 +944,8 @@ class PagedBlocks(DecodeWorkload):
                 "d_head": w.d_head, "block_size": self.bs, "budget_blocks": self.nb,
                 "recent_blocks": self.recent, "tokens_per_step": "801..833 (mean 817.5)",
                 "kv_dtype": "bf16", "l2": "inputs larger than L2 (7 GB of KV per step)",
-                "init": "page tables start with 26 full blocks of N(0,1) keys/values, zero "
-                        "scores (no prompt selection in this workload)",
+                "prompt": f"{w.prompt} tokens (the h2o workload's Zipf-scaled keys), compressed "
+                          "to 26 blocks by block scores from the prompt's column sums",
                 "graph": "appends, then paged decode + block update per layer (the update of "
                          "layer l on a second stream beside the decode of layer l + 1), as two "
                          "CUDA graphs"}

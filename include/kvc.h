@@ -376,6 +376,30 @@ kvc_status kvc_decode_attn_paged(const void *q, int32_t n_heads_q, const kvc_blo
                                  float *logits, int64_t logits_stride, float *lse, void *ws,
                                  size_t ws_bytes, uint32_t flags, void *stream);
 
+/* Block-level eviction at the end of the prompt (the one-shot prompt compression of [KVC] H2O,
+ * at the block granularity of "Implementação prática em vLLM e SGLang").  For every sequence:
+ * prompt block i holds tokens i*block_size .. min(seq_len, (i+1)*block_size) - 1 and scores
+ *   Score(i) = sum over the n_heads_kv heads h and its tokens t of s[b][h][t]
+ * (s: the prompt's per-token scores, e.g. the column sums kvc_h2o_prefill_select writes to
+ * s_full; [batch][n_heads_kv][s_stride] fp32).  The recent_blocks newest blocks are kept with
+ * the budget_blocks - recent_blocks highest-scoring older ones (equal scores keep the lower
+ * index; a prompt of at most budget_blocks blocks is kept whole).  The kept blocks, in
+ * ascending order, take consecutive page-table entries and one contiguous range of ids popped
+ * from the free stack; their keys and values are copied from the prompt cache
+ * ([batch][n_heads_kv][>= seq_len][d_head]) into the pool; the entries' scores are the block
+ * scores; n_blocks and len are set (only the newest block may be partial).
+ * The sequences' tables must be empty (n_blocks == 0; else KVC_DEV_BAD_LENGTH); too few free
+ * blocks records KVC_DEV_POOL_EMPTY and leaves that sequence empty.
+ * 1 <= recent_blocks <= budget_blocks <= max_blocks.  Three kernels: block scores, selection,
+ * copy.  Workspace: kvc_block_prompt_select_workspace_bytes(), 256-byte aligned. */
+size_t kvc_block_prompt_select_workspace_bytes(int32_t batch, int32_t seq_len,
+                                               int32_t block_size, int32_t budget_blocks);
+kvc_status kvc_block_prompt_select(const float *s, int64_t s_stride, const kvc_cache *prompt,
+                                   int32_t seq_len, const kvc_block_pool *pool,
+                                   const kvc_page_table *pt, const kvc_free_pool *free_pool,
+                                   int32_t budget_blocks, int32_t recent_blocks, void *ws,
+                                   size_t ws_bytes, void *stream);
+
 /* Block-level eviction for one decode step ([KVC] "Implementação prática...": Score(block) =
  * sum over t in the block of s_t; the lowest-scoring blocks leave the page table for the free
  * pool, without copies).  For every sequence b:

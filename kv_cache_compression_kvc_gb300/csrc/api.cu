@@ -646,6 +646,72 @@ kvc_status kvc_decode_attn_paged(const void *q, int32_t n_heads_q, const kvc_blo
                        logits, logits_stride, lse, ws, ws_bytes, flags, stream);
 }
 
+size_t kvc_block_prompt_select_workspace_bytes(int32_t batch, int32_t seq_len,
+                                               int32_t block_size, int32_t budget_blocks)
+{
+    if (batch <= 0 || seq_len <= 0 || block_size <= 0 || budget_blocks <= 0) return 0;
+    const size_t nblk = ((size_t)seq_len + block_size - 1) / block_size;
+    return align256((size_t)batch * nblk * sizeof(float)) +
+           align256((size_t)batch * budget_blocks * sizeof(int32_t));
+}
+
+kvc_status kvc_block_prompt_select(const float *s, int64_t s_stride, const kvc_cache *prompt,
+                                   int32_t seq_len, const kvc_block_pool *pool,
+                                   const kvc_page_table *pt, const kvc_free_pool *free_pool,
+                                   int32_t budget_blocks, int32_t recent_blocks, void *ws,
+                                   size_t ws_bytes, void *stream)
+{
+    kvc_cache view;
+    kvc_status st = check_paged(pool, pt, "kvc_block_prompt_select", &view);
+    if (st != KVC_OK) return st;
+    st = check_free_pool(free_pool, "kvc_block_prompt_select");
+    if (st != KVC_OK) return st;
+    st = check_cache(prompt, "kvc_block_prompt_select", true);
+    if (st != KVC_OK) return st;
+    if (s == nullptr) return fail(KVC_ERR_INVALID_ARG, "kvc_block_prompt_select: null scores");
+    if (prompt->dtype != pool->dtype || prompt->n_heads_kv != pool->n_heads_kv ||
+        prompt->d_head != pool->d_head || prompt->batch != pt->batch)
+        return fail(KVC_ERR_SHAPE, "kvc_block_prompt_select: prompt and pool differ in dtype, "
+                    "heads, d_head or batch");
+    if (seq_len <= 0 || seq_len > prompt->cap || s_stride < seq_len)
+        return fail(KVC_ERR_CAPACITY, "kvc_block_prompt_select: seq_len %d (prompt cap %d, "
+                    "score stride %lld)", seq_len, prompt->cap, (long long)s_stride);
+    if (recent_blocks < 1 || budget_blocks < recent_blocks || budget_blocks > pt->max_blocks)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_block_prompt_select: need 1 <= recent_blocks <= "
+                    "budget_blocks <= max_blocks (%d, %d, %d)", recent_blocks, budget_blocks,
+                    pt->max_blocks);
+    if (pt->batch > 65535 || pool->n_heads_kv > 65535)
+        return fail(KVC_ERR_SHAPE, "kvc_block_prompt_select: batch %d, heads %d", pt->batch,
+                    pool->n_heads_kv);
+    const size_t need = kvc_block_prompt_select_workspace_bytes(pt->batch, seq_len,
+                                                                pool->block_size, budget_blocks);
+    if (ws == nullptr || ws_bytes < need || !aligned256(ws))
+        return fail(KVC_ERR_WORKSPACE, "kvc_block_prompt_select: workspace needs %zu bytes "
+                    "(256-byte aligned), got %zu", need, ws_bytes);
+    int32_t *code = nullptr;
+    st = device_info(&code, nullptr);
+    if (st != KVC_OK) return st;
+    kvc::BlockPromptParams p{};
+    p.s = s; p.s_stride = s_stride;
+    p.pk = prompt->k; p.pv = prompt->v;
+    p.sb = prompt->stride_b; p.sh = prompt->stride_h; p.ss = prompt->stride_slot;
+    p.k = pool->k; p.v = pool->v;
+    p.B = pt->batch; p.H = pool->n_heads_kv; p.N = seq_len; p.bs = pool->block_size;
+    p.nblk = (seq_len + pool->block_size - 1) / pool->block_size;
+    p.eb = elem_bytes(pool->dtype); p.row_bytes = pool->d_head * p.eb;
+    p.n_pool = pool->n_blocks; p.max_blocks = pt->max_blocks;
+    p.table = pt->table; p.n_blocks = pt->n_blocks; p.len = pt->len; p.score = pt->score;
+    p.free_ids = free_pool->ids; p.free_top = free_pool->top; p.free_cap = free_pool->capacity;
+    p.budget_blocks = budget_blocks; p.recent_blocks = recent_blocks;
+    char *wsb = static_cast<char *>(ws);
+    p.ws_score = reinterpret_cast<float *>(wsb);
+    p.ws_src = reinterpret_cast<int32_t *>(wsb + align256((size_t)p.B * p.nblk * sizeof(float)));
+    p.dev_code = code;
+    cudaError_t e = kvc::launch_block_prompt_select(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "block prompt selection launch");
+    return ok();
+}
+
 kvc_status kvc_block_accumulate_evict(const float *logits, int64_t logits_stride,
                                       const float *lse, int32_t n_heads_q, int32_t block_size,
                                       const kvc_page_table *pt, const kvc_free_pool *free_pool,

@@ -234,6 +234,24 @@ struct PagedParams {
     int32_t *dev_code;
 };
 cudaError_t launch_paged_append(const PagedParams &p, int elem_bytes, cudaStream_t stream);
+
+// The prompt's block selection: block scores, the pick, the copy into pool blocks.
+struct BlockPromptParams {
+    const float *s;              // [B][H][s_stride] per-token scores of the prompt
+    int64_t s_stride;
+    const void *pk, *pv;         // prompt K/V [B][H][>= N][D] (cache strides, elements)
+    int64_t sb, sh, ss;
+    void *k, *v;                 // pool [H][n_pool][bs][D]
+    int32_t B, H, N, bs, nblk, eb, row_bytes, n_pool, max_blocks;
+    int32_t *table, *n_blocks, *len;
+    float *score;
+    int32_t *free_ids, *free_top;
+    int32_t free_cap, budget_blocks, recent_blocks;
+    float *ws_score;             // [B][nblk]
+    int32_t *ws_src;             // [B][budget_blocks] prompt block of each kept entry
+    int32_t *dev_code;
+};
+cudaError_t launch_block_prompt_select(const BlockPromptParams &p, cudaStream_t stream);
 cudaError_t launch_block_accumulate_evict(const PagedParams &p, cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------

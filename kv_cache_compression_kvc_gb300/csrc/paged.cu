@@ -36,6 +36,7 @@ namespace {
 
 constexpr int kAppendThreads = 128;
 constexpr int kEvictThreads = 128;
+constexpr int kPickThreads = 256;
 constexpr int kDevBadLength = 5;
 constexpr int kDevNoCandidate = 6;
 constexpr int kDevBadBlock = 9;
@@ -230,6 +231,136 @@ __global__ void __launch_bounds__(32) block_release_kernel(const PagedParams p)
     }
 }
 
+// ---- the prompt: one-shot compression to budget_blocks blocks ----------------------------
+// Score of prompt block i of sequence b: the sum over the H heads and its tokens of the
+// prompt's per-token scores, in a fixed order (threads over (head, offset), shuffle tree).
+__global__ void __launch_bounds__(kEvictThreads) block_prompt_score_kernel(const BlockPromptParams p)
+{
+    constexpr int NW = kEvictThreads / 32;
+    __shared__ float s_part[NW];
+    const int i = blockIdx.x, b = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
+    pdl_wait();                                 // the scores may come from the previous kernel
+    const int fill = min(p.bs, p.N - i * p.bs);
+    const float *s0 = p.s + (size_t)b * p.H * p.s_stride + (size_t)i * p.bs;
+    float part = 0.f;
+    for (int x = tid; x < p.H * p.bs; x += kEvictThreads) {
+        const int h = x / p.bs, off = x - h * p.bs;
+        if (off < fill) part += __ldg(s0 + (size_t)h * p.s_stride + off);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) s_part[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = s_part[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) tot += s_part[w];
+        p.ws_score[(size_t)b * p.nblk + i] = tot;
+    }
+}
+
+// Selection: block i < n_old is kept when fewer than k_old older blocks outrank it (a higher
+// score, or an equal score and a lower index); the recent blocks always.  The kept blocks take
+// consecutive table entries in ascending order and one contiguous range of free ids.
+__global__ void __launch_bounds__(kPickThreads) block_prompt_pick_kernel(const BlockPromptParams p)
+{
+    __shared__ int s_keep[kPickThreads];
+    __shared__ int s_base, s_ok;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    const float *sc = p.ws_score + (size_t)b * p.nblk;
+    const int recent = min(p.recent_blocks, p.nblk);
+    const int n_old = p.nblk - recent;
+    const int k_old = p.nblk <= p.budget_blocks ? n_old : p.budget_blocks - recent;
+    const int n_keep = k_old + recent;
+    if (tid == 0) {
+        s_ok = 1;
+        if (p.n_blocks[b] != 0) {               // the table must start empty
+            record_code(p.dev_code, kDevBadLength);
+            s_ok = 0;
+        } else {
+            const int old = atomicSub(p.free_top, n_keep);
+            if (old < n_keep || old > p.free_cap) {
+                atomicAdd(p.free_top, n_keep);
+                record_code(p.dev_code, kDevPoolEmpty);
+                s_ok = 0;
+            } else {
+                s_base = old - n_keep;
+            }
+        }
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    int written = 0;                            // entries before this chunk of blocks
+    for (int c0 = 0; c0 < p.nblk; c0 += kPickThreads) {
+        const int i = c0 + tid;
+        int keep = 0;
+        if (i < p.nblk) {
+            if (i >= n_old || k_old >= n_old) {
+                keep = 1;
+            } else {
+                const float v = sc[i];
+                int rank = 0;
+                for (int j = 0; j < n_old && rank < k_old; ++j) {
+                    const float u = sc[j];
+                    rank += (u > v || (u == v && j < i)) ? 1 : 0;
+                }
+                keep = rank < k_old;
+            }
+        }
+        s_keep[tid] = keep;
+        __syncthreads();
+        // exclusive scan of the flags, in thread order (the chunk is at most kPickThreads)
+        int before = written;
+        for (int j = 0; j < tid; ++j) before += s_keep[j];
+        if (keep) {
+            const int id = p.free_ids[s_base + before];
+            p.table[(size_t)b * p.max_blocks + before] = id;
+            p.score[(size_t)b * p.max_blocks + before] = sc[i];
+            p.ws_src[(size_t)b * p.budget_blocks + before] = i;
+        }
+        int total = 0;
+        for (int j = 0; j < kPickThreads; ++j) total += s_keep[j];
+        written += total;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        p.n_blocks[b] = n_keep;
+        p.len[b] = (n_keep - 1) * p.bs + (p.N - (p.nblk - 1) * p.bs);   // the newest may be partial
+    }
+}
+
+// Copy: kept block e of sequence b, head h -> its pool block, the tokens of K and V.
+__global__ void __launch_bounds__(kAppendThreads) block_prompt_gather_kernel(const BlockPromptParams p)
+{
+    const int e = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+    pdl_trigger();
+    pdl_wait();
+    if (e >= p.n_blocks[b]) return;
+    const int src_blk = p.ws_src[(size_t)b * p.budget_blocks + e];
+    const int phys = p.table[(size_t)b * p.max_blocks + e];
+    if (src_blk < 0 || src_blk >= p.nblk || phys < 0 || phys >= p.n_pool) {
+        if (threadIdx.x == 0) record_code(p.dev_code, kDevBadBlock);
+        return;
+    }
+    const int fill = min(p.bs, p.N - src_blk * p.bs);
+    const int vpr = p.row_bytes / 16;
+    for (int x = threadIdx.x; x < fill * vpr; x += kAppendThreads) {
+        const int r = x / vpr, c = x - r * vpr;
+        const size_t src = ((size_t)b * p.sb + (size_t)h * p.sh + (size_t)(src_blk * p.bs + r) * p.ss) *
+                               (size_t)p.eb + (size_t)c * 16;
+        const size_t dst = (((size_t)h * p.n_pool + phys) * p.bs + r) * (size_t)p.row_bytes +
+                           (size_t)c * 16;
+        const uint4 kx = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(p.pk) + src));
+        const uint4 vx = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(p.pv) + src));
+        *reinterpret_cast<uint4 *>(static_cast<char *>(p.k) + dst) = kx;
+        *reinterpret_cast<uint4 *>(static_cast<char *>(p.v) + dst) = vx;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_paged_append(const PagedParams &p, int elem_bytes, cudaStream_t stream)
@@ -246,6 +377,19 @@ cudaError_t launch_block_accumulate_evict(const PagedParams &p, cudaStream_t str
                                dim3(kEvictThreads), 0, stream, p);
     if (e != cudaSuccess) return e;
     return launch_pdl(block_release_kernel, dim3((unsigned)p.B), dim3(32), 0, stream, p);
+}
+
+cudaError_t launch_block_prompt_select(const BlockPromptParams &p, cudaStream_t stream)
+{
+    if (p.B == 0 || p.nblk == 0) return cudaSuccess;
+    cudaError_t e = launch_pdl(block_prompt_score_kernel, dim3((unsigned)p.nblk, (unsigned)p.B),
+                               dim3(kEvictThreads), 0, stream, p);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(block_prompt_pick_kernel, dim3((unsigned)p.B), dim3(kPickThreads), 0, stream, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(block_prompt_gather_kernel,
+                      dim3((unsigned)p.budget_blocks, (unsigned)p.B, (unsigned)p.H),
+                      dim3(kAppendThreads), 0, stream, p);
 }
 
 }  // namespace kvc

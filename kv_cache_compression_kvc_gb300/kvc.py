@@ -120,6 +120,9 @@ SIGNATURES = {
     "kvc_paged_append": (_I32, [_POOL_P, _PT_P, _FREE_P, _P, _P, _P, _P, _P]),
     "kvc_decode_attn_paged": (_I32, [_P, _I32, _POOL_P, _PT_P, _F32, _P, _P, _I64, _P, _P, _SZ,
                                      _U32, _P]),
+    "kvc_block_prompt_select_workspace_bytes": (_SZ, [_I32] * 4),
+    "kvc_block_prompt_select": (_I32, [_P, _I64, _CACHE_P, _I32, _POOL_P, _PT_P, _FREE_P, _I32,
+                                       _I32, _P, _SZ, _P]),
     "kvc_block_accumulate_evict": (_I32, [_P, _I64, _P, _I32, _I32, _PT_P, _FREE_P, _I32, _I32,
                                           _P, _P]),
     "kvc_decode_attn_noalloc": (_I32, [_P, _I32, _CACHE_P, _P, _I32, _ROPE_P, _F32, _P, _P,
@@ -413,6 +416,22 @@ def kvc_decode_attn_paged(q: torch.Tensor, pool: kvc_block_pool, pt: kvc_page_ta
         _ptr(q), Hq, ctypes.byref(pool), ctypes.byref(pt), float(scale), _ptr(out),
         _ptr(logits), lstride, _ptr(lse), wp, wb, int(flags), _stream(stream)))
     return out
+
+
+def kvc_block_prompt_select(s: torch.Tensor, k_prompt: torch.Tensor, v_prompt: torch.Tensor,
+                            pool: kvc_block_pool, pt: kvc_page_table, free_pool: kvc_free_pool, *,
+                            seq_len: int, budget_blocks: int, recent_blocks: int,
+                            ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    """s [B, Hkv, >= seq_len] per-token prompt scores; k/v_prompt [B, Hkv, cap, D]."""
+    c = cache_view(k_prompt, v_prompt)
+    if ws is None:
+        ws = _zeroed_workspace(int(load().kvc_block_prompt_select_workspace_bytes(
+            pt.batch, seq_len, pool.block_size, budget_blocks)), s.device)
+    wp, wb = _ws_ptr(ws)
+    _check(load().kvc_block_prompt_select(
+        _ptr(s), s.stride(-2), ctypes.byref(c), int(seq_len), ctypes.byref(pool),
+        ctypes.byref(pt), ctypes.byref(free_pool), int(budget_blocks), int(recent_blocks), wp, wb,
+        _stream(stream)))
 
 
 def kvc_block_accumulate_evict(logits: torch.Tensor, lse: torch.Tensor, pt: kvc_page_table,

@@ -240,3 +240,62 @@ def test_paged_append_reports_an_empty_pool():
     kvc.kvc_paged_append(pool, pt, fp, k, k)
     assert kvc.kvc_device_status() == 10                 # KVC_DEV_POOL_EMPTY
     assert sorted(ln.cpu().tolist()) == [0, 1] and int(top) == 0
+
+
+@pytest.mark.parametrize("dtype,budget,recent", [(torch.float32, 7, 2), (torch.bfloat16, 5, 1),
+                                                 (torch.bfloat16, 40, 3)])
+def test_block_prompt_select_matches_oracle(dtype, budget, recent):
+    """The prompt's one-shot block compression: integer-valued per-token scores make every block
+    sum exact (ties included), so the kept blocks, their order and scores must equal the
+    oracle's, the pool blocks must hold the kept prompt rows bit for bit, the free stack must
+    have given each sequence distinct ids, and a decode over the result must equal attention
+    over the kept tokens.  budget 40 keeps the whole 19-block prompt."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, H, D, N, bs = 2, 3, 64, 300, 16
+    nblk = (N + bs - 1) // bs
+    n_keep = min(budget, nblk)
+    mb = max(budget, nblk) + 1
+    n_pool = B * mb + 3
+    rng = np.random.default_rng(budget)
+    s_np = rng.integers(0, 4, size=(B, H, N)).astype(np.float32)
+    s = torch.tensor(s_np, device=dev)
+    kpr = I.randn((B, H, N + 5, D), 41, dev, dtype)
+    vpr = I.randn((B, H, N + 5, D), 42, dev, dtype)
+    kp = torch.zeros((H, n_pool, bs, D), device=dev, dtype=dtype)
+    vp = torch.zeros_like(kp)
+    ids = torch.tensor(rng.permutation(n_pool), dtype=torch.int32, device=dev)
+    top = torch.tensor([n_pool], dtype=torch.int32, device=dev)
+    table = torch.full((B, mb), -1, dtype=torch.int32, device=dev)
+    nbl = torch.zeros(B, dtype=torch.int32, device=dev)
+    ln = torch.zeros(B, dtype=torch.int32, device=dev)
+    score = torch.zeros((B, mb), device=dev)
+    pool, pt = kvc.block_pool_view(kp, vp), kvc.page_table_view(table, nbl, ln, score)
+    fp = kvc.free_pool_view(ids, top)
+    kvc.kvc_block_prompt_select(s, kpr, vpr, pool, pt, fp, seq_len=N, budget_blocks=budget,
+                                recent_blocks=recent)
+    assert kvc.kvc_device_status() == 0
+    assert nbl.cpu().tolist() == [n_keep] * B
+    assert ln.cpu().tolist() == [(n_keep - 1) * bs + (N - (nblk - 1) * bs)] * B
+    assert int(top) == n_pool - B * n_keep
+    tab, sc = table.cpu().numpy(), score.cpu().numpy()
+    used = tab[:, :n_keep].flatten().tolist()
+    assert len(set(used)) == len(used) and set(used) <= set(ids.cpu().tolist()[int(top):])
+    kp_h, vp_h, kpr_h, vpr_h = kp.cpu(), vp.cpu(), kpr.cpu(), vpr.cpu()
+    q = I.randn((B, H, D), 43, dev, dtype)
+    out = kvc.kvc_decode_attn_paged(q, pool, pt, scale=1 / math.sqrt(D)).cpu().numpy()
+    for b in range(B):
+        keep, bsc = oracle.block_prompt_select(s_np[b].astype(np.float64), bs, budget, recent)
+        assert len(keep) == n_keep
+        assert np.array_equal(sc[b, :n_keep], bsc[keep].astype(np.float32))
+        toks = []
+        for e, i in enumerate(keep):
+            fill = min(bs, N - i * bs)
+            phys = int(tab[b, e])
+            assert torch.equal(kp_h[:, phys, :fill], kpr_h[b, :, i * bs:i * bs + fill])
+            assert torch.equal(vp_h[:, phys, :fill], vpr_h[b, :, i * bs:i * bs + fill])
+            toks += list(range(i * bs, i * bs + fill))
+        for h in range(H):
+            ref, _, _ = oracle.attend(f64(q[b, h]), f64(kpr[b, h, toks]), f64(vpr[b, h, toks]),
+                                      1 / math.sqrt(D))
+            assert_close(out[b, h], ref, TOL[dtype], f"decode over the kept prompt b={b} h={h}")
