@@ -1084,13 +1084,23 @@ def run_gpu(args):
     host_out = torch.empty(R.out.shape, dtype=R.out.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host_in[0])
     d2h = host_out.numel() * host_out.element_size()
+    # The step as a model runs it (per layer: append, then decode), captured once from the same
+    # C-ABI calls and replayed as a serving loop does; --e2e-eager makes the calls every step.
+    g_step = None
+    if not args.e2e_eager:
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            R.step_interleaved()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(stream)
     for i in range(args.steps):
         R.load_inputs(*host_in[i % total])
-        R.step_interleaved()
+        if g_step is not None:
+            g_step.replay()
+        else:
+            R.step_interleaved()
         host_out.copy_(R.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -1126,7 +1136,11 @@ def run_gpu(args):
                      "traffic": kernel_traffic(R.kernel_file, R.traffic_key)},
         "e2e": {"value": round(job_tokens_per_s(w.batch, args.steps, world, e2e_ms), 2),
                 "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "mode": "eager C-ABI calls every step" if args.e2e_eager else
+                        "per step: pinned host-to-device copy of the inputs, the step captured "
+                        "once from the C-ABI calls (per layer: append, then decode) replayed as "
+                        "a CUDA graph, device-to-host copy of the outputs"},
         "gpu_launches": R.launches_per_step * args.steps,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
@@ -1186,6 +1200,8 @@ def main():
     ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
     ap.add_argument("--workload", choices=WORKLOAD_NAMES, default="streaming")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-eager", action="store_true",
+                    help="end to end: make the C-ABI calls every step instead of replaying them")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
