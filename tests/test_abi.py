@@ -203,3 +203,38 @@ def test_duo_validation_before_launch(kvc):
     ring.cap = 68
     st = lib.kvc_duo_append(B(full), 4096, B(ring), B(duo.desc), 4096, 4096, None)
     assert st == 4                                                 # ring < 4 + 64 + 1 slots
+
+
+def test_block_prompt_select_validation_before_launch(kvc):
+    lib = kvc.load()
+    B = ctypes.byref
+    pool = kvc.kvc_block_pool()
+    pool.k = pool.v = 4096
+    pool.dtype, pool.n_blocks, pool.n_heads_kv, pool.block_size, pool.d_head = \
+        kvc.KVC_BF16, 32, 2, 16, 128
+    pt = kvc.kvc_page_table()
+    pt.table = pt.n_blocks = pt.len = pt.score = 4096
+    pt.batch, pt.max_blocks = 1, 8
+    fp = kvc.kvc_free_pool()
+    fp.ids, fp.top, fp.capacity = 4096, 4096, 32
+    pr = kvc.kvc_cache()
+    pr.k = pr.v = 4096
+    pr.dtype, pr.batch, pr.n_heads_kv, pr.cap, pr.d_head = kvc.KVC_BF16, 1, 2, 100, 128
+    pr.stride_b, pr.stride_h, pr.stride_slot = 2 * 100 * 128, 100 * 128, 128
+    st = lib.kvc_block_prompt_select(4096, 100, B(pr), 100, B(pool), B(pt), B(fp), 4, 0, 4096,
+                                     1 << 20, None)
+    assert st == 1 and "recent_blocks" in kvc.kvc_last_error()    # recent quota of 0 blocks
+    st = lib.kvc_block_prompt_select(4096, 100, B(pr), 100, B(pool), B(pt), B(fp), 9, 1, 4096,
+                                     1 << 20, None)
+    assert st == 1                                                 # budget beyond max_blocks
+    st = lib.kvc_block_prompt_select(4096, 100, B(pr), 101, B(pool), B(pt), B(fp), 4, 1, 4096,
+                                     1 << 20, None)
+    assert st == 4                                                 # seq_len beyond the prompt
+    st = lib.kvc_block_prompt_select(4096, 50, B(pr), 100, B(pool), B(pt), B(fp), 4, 1, 4096,
+                                     1 << 20, None)
+    assert st == 4                                                 # score rows too short
+    pr.n_heads_kv, pr.stride_b = 3, 3 * 100 * 128
+    st = lib.kvc_block_prompt_select(4096, 100, B(pr), 100, B(pool), B(pt), B(fp), 4, 1, 4096,
+                                     1 << 20, None)
+    assert st == 2                                                 # prompt heads != pool heads
+    assert lib.kvc_block_prompt_select_workspace_bytes(1, 100, 16, 4) == 256 + 256

@@ -114,3 +114,32 @@ def test_duo_long_retrieval_heads_many_blocks():
                 slots = [oracle.stream_slot(int(a), S, W) for a in tok]
                 want = scale * (hk[tok, b, kh] @ f64(q[b, h]))
                 assert_close(lg[b, h, slots], want, 1e-3, f"ring logits b={b} h={h}")
+
+
+def test_duo_empty_retrieval_caches():
+    """Retrieval heads with no token yet (len 0) give out = 0 and lse = -inf; the streaming
+    heads at t = 0 attend their one slot."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv, G, D, S, W = 2, 3, 2, 64, 4, 8
+    Hq = Hkv * G
+    fk, fv, rk, rv = _caches(B, 1, Hkv - 1, 16, S + W + 1, D, torch.float32, dev)
+    rk[:, :, 0] = I.randn((B, Hkv - 1, D), 601, dev)
+    rv[:, :, 0] = I.randn((B, Hkv - 1, D), 602, dev)
+    full, ring = kvc.cache_view(fk, fv), kvc.cache_view(rk, rv)
+    ln = torch.zeros(B, dtype=torch.int32, device=dev)
+    t = torch.zeros(1, dtype=torch.int64, device=dev)
+    duo = kvc.Duo([1], S, W, t)
+    q = I.randn((B, Hq, D), 603, dev)
+    lse = torch.empty((B, Hq), device=dev)
+    out = kvc.kvc_decode_attn_duo(q, full, ring, duo, scale=0.125, len=ln, lse=lse)
+    assert kvc.kvc_device_status() == 0
+    o, ls = out.cpu(), lse.cpu()
+    for h in range(Hq):
+        if h // G == 1:                                     # the retrieval head
+            assert torch.all(o[:, h] == 0) and torch.all(torch.isneginf(ls[:, h]))
+        else:                                               # one slot: its value
+            s_idx = 0 if h // G == 0 else 1
+            assert torch.allclose(o[:, h], rv[:, s_idx, 0].cpu(), atol=1e-6)
+            assert torch.allclose(ls[:, h], 0.125 * (q[:, h] * rk[:, s_idx, 0]).sum(-1).cpu(),
+                                  atol=1e-4)
