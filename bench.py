@@ -21,12 +21,10 @@ rank runs the same workload on its own GPU and rank 0 prints the aggregate.
 from __future__ import annotations
 
 import argparse
-import ctypes
 import dataclasses
 import datetime
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess

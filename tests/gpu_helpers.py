@@ -1,5 +1,4 @@
 """Shared helpers for the GPU parity tests (imported by tests only)."""
-import math
 
 import numpy as np
 import pytest

@@ -2,7 +2,6 @@
 over sink + ring buffers, one decode launch), through the C ABI, against the oracle."""
 import math
 
-import numpy as np
 import pytest
 import torch
 

@@ -1,7 +1,6 @@
 """GPU parity at the benchmark workloads' full sizes, in the launch configuration bench.py times
 (one layer of each workload, same shapes and calls), on sampled outputs the oracle can compute
 one by one, plus properties that hold at any size."""
-import math
 
 import numpy as np
 import pytest
