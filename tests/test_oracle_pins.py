@@ -672,12 +672,12 @@ def test_duo_memory_saving_matches_the_pages():
     70 % of the KV memory at 128k tokens: with 30 % retrieval heads (a 4 + 64 token buffer for
     the others) the saving is 70 % to within 0.1 %, with 20 % it is 80 %; no streaming heads is
     the plain memory formula."""
-    N, S, W = 131072, 4, 64
+    g = _golden("duo_memory.json")
+    N, S, W = g["seq_len"], g["n_sink"], g["window"]
     full = oracle.kv_bytes(32, 10, 128, N, 2, 1)
-    duo = oracle.duo_kv_bytes(32, 3, 7, 128, N, S, W, 2, 1)
-    assert abs((1 - duo / full) - 0.70) < 1e-3
-    duo20 = oracle.duo_kv_bytes(32, 2, 8, 128, N, S, W, 2, 1)
-    assert abs((1 - duo20 / full) - 0.80) < 1e-3
+    for c in g["cases"]:
+        duo = oracle.duo_kv_bytes(32, c["n_retrieval"], c["n_streaming"], 128, N, S, W, 2, 1)
+        assert abs((1 - duo / full) - c["saving"]) < 1e-3, c["what"]
     assert oracle.duo_kv_bytes(32, 10, 0, 128, N, S, W, 2, 1) == full
     # a streaming head's buffer is constant: O(1) in the sequence length
     a = oracle.duo_kv_bytes(1, 0, 1, 128, 10 ** 6, S, W, 2, 1)
