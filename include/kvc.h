@@ -154,7 +154,11 @@ typedef struct {
     int32_t max_blocks;
 } kvc_page_table;
 
-/* The free pool: a stack of free physical block ids, ids[0 .. *top - 1]. */
+/* The free pool: a stack of free physical block ids, ids[0 .. *top - 1].  Within one call the
+ * pops (kvc_paged_append, kvc_block_prompt_select) or the pushes (kvc_block_accumulate_evict)
+ * of several sequences take distinct entries through an atomic on *top; calls that use the
+ * same free pool must not overlap on the GPU (order them on one stream, or join the streams
+ * between them), since a pop racing a push could read an entry before it is written. */
 typedef struct {
     int32_t *ids;           /* device int32[capacity]                                        */
     int32_t *top;           /* device int32 scalar: number of free ids                       */
