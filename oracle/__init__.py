@@ -8,7 +8,8 @@ with gcc into ``oracle/_build/``.  This module only marshals numpy arrays.
 Functions (each follows the page passage cited in ``kvc_oracle.c``):
   kv_bytes, pyramid_budgets, rope, attend, stream_window, stream_slot, stream_decode,
   stream_decode_alibi, topk_ascending, snapkv_obs_scores, pool1d, snapkv_select, snapkv_stage_f32,
-  h2o_prompt_scores, h2o_prompt_select, h2o_step, h2o_step_group, h2o_evict_f32, block_step, block_evict_f32,
+  h2o_prompt_scores, h2o_prompt_scores_group, h2o_prompt_select, h2o_step, h2o_step_group,
+  h2o_evict_f32, block_step, block_evict_f32,
   duo_decode, duo_kv_bytes, block_prompt_select.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against values the pages
@@ -75,6 +76,8 @@ _SIGS = {
     "orc_snapkv_stage_f32": (ctypes.c_int, [ctypes.c_int] * 5 + [_ptr, _ptr]),
     "orc_h2o_prompt_scores": (None, [ctypes.c_int, ctypes.c_int, _f64, _ptr, _ptr, _ptr]),
     "orc_h2o_prompt_select": (ctypes.c_int, [ctypes.c_int] * 3 + [_ptr, _ptr]),
+    "orc_h2o_prompt_scores_group": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64, _ptr,
+                                           _ptr, _ptr]),
     "orc_h2o_step": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _f64, _ptr, _ptr, _ptr, _ptr,
                                     _ptr, _i64, ctypes.c_int, ctypes.c_int, _ptr, _ptr]),
     "orc_h2o_evict_f32": (ctypes.c_int, [ctypes.c_int, _ptr, _ptr, _i64, ctypes.c_int]),
@@ -243,6 +246,15 @@ def h2o_prompt_scores(Q, K, scale: float) -> np.ndarray:
     N, D = Q.shape
     s = np.empty(N)
     lib().orc_h2o_prompt_scores(N, D, scale, _p(Q), _p(K), _p(s))
+    return s
+
+
+def h2o_prompt_scores_group(Q, K, scale: float) -> np.ndarray:
+    """Q [G, N, D] the group's query heads, K [N, D] -> s [N] summed over the group."""
+    Q, K = _f(Q), _f(K)
+    G, N, D = Q.shape
+    s = np.empty(N)
+    lib().orc_h2o_prompt_scores_group(G, N, D, scale, _p(Q), _p(K), _p(s))
     return s
 
 

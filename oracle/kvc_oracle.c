@@ -403,6 +403,22 @@ void orc_h2o_prompt_scores(int N, int D, double scale, const double *Q, const do
     free(row);
 }
 
+/* Prompt scores of a grouped-query KV head.  Reading (as for the decode steps of a grouped
+ * cache): a cached row serves the G query heads of its KV head and is kept or dropped for all
+ * of them, so its score is the sum over the group of each query head's column sum.
+ * Q: [G][N][D] (the group's query heads); K: [N][D]; s: [N].                                 */
+void orc_h2o_prompt_scores_group(int G, int N, int D, double scale, const double *Q,
+                                 const double *K, double *s)
+{
+    double *sg = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    for (int j = 0; j < N; ++j) s[j] = 0.0;
+    for (int g = 0; g < G; ++g) {
+        orc_h2o_prompt_scores(N, D, scale, Q + (size_t)g * N * D, K, sg);
+        for (int j = 0; j < N; ++j) s[j] += sg[j];
+    }
+    free(sg);
+}
+
 /* One-shot compression at the end of the prompt.  Reading: the L_local newest prompt positions
  * are kept (recent quota), the K_HH largest s among the older positions are kept (ties: lower
  * position), the kept positions are returned ascending.  If N <= L_local + K_HH everything is

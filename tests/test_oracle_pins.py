@@ -733,3 +733,18 @@ def test_block_prompt_select_block_scores_and_rules():
     assert list(keep) == [3, 4]                              # only the recent blocks
     keep, _ = oracle.block_prompt_select(s, bs, 5, 1)
     assert list(keep) == [0, 1, 2, 3, 4]
+
+
+def test_h2o_prompt_scores_group():
+    """A group of one is H2O's prompt scores; the group's sum is the sum of library causal
+    softmax columns over its heads; every head's rows sum to one, so the total is G * N."""
+    rng = np.random.default_rng(91)
+    G, N, D = 3, 40, 8
+    Q, K = rng.standard_normal((G, N, D)), rng.standard_normal((N, D))
+    scale = 1 / math.sqrt(D)
+    one = oracle.h2o_prompt_scores_group(Q[:1], K, scale)
+    assert np.array_equal(one, oracle.h2o_prompt_scores(Q[0], K, scale))
+    s = oracle.h2o_prompt_scores_group(Q, K, scale)
+    want = sum(_causal_probs(Q[g], K, scale).sum(axis=0) for g in range(G))
+    assert np.max(np.abs(s - want)) <= 1e-12
+    assert abs(s.sum() - G * N) <= 1e-9
