@@ -650,19 +650,26 @@ class H2OGrouped(H2O):
         self.V = torch.empty_like(self.K)
         self.pos = torch.full((L, B, H, self.cap), -1, dtype=torch.int32, device=dev)
         self.score = torch.zeros((L, B, H, self.cap), dtype=torch.float32, device=dev)
-        rng = np.random.default_rng(w.seed)
         K_hh = w.budget - w.L_local
+        ws = torch.zeros(kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, H, D, w.prompt, kvc.KVC_BF16)
+                         + 256, dtype=torch.uint8, device=dev)
+        init_ms = []
         for l in range(L):
-            g = I.generator(w.seed * 1000 + l, dev)
-            self.K[l].normal_(generator=g)
-            self.V[l].normal_(generator=g)
-            old = np.sort(rng.random((B * H, w.prompt - w.L_local)).argsort(axis=1)[:, :K_hh],
-                          axis=1)
-            recent = np.tile(np.arange(w.prompt - w.L_local, w.prompt), (B * H, 1))
-            self.pos[l, :, :, :w.budget] = torch.from_numpy(
-                np.concatenate([old, recent], axis=1).astype(np.int32)).reshape(B, H, -1).to(dev)
-            self.score[l, :, :, :w.budget] = torch.from_numpy(
-                rng.random((B, H, w.budget)).astype(np.float32) * w.group).to(dev)
+            # the prompt (N(0,1), sink-boosted keys), its grouped column sums and the one-shot
+            # compression to the budget, then the kept rows gathered into the cache
+            q, k, v = I.prompt_qkv(B, w.n_heads_q, H, w.prompt, D, w.seed * 1000 + l, dev, w.dtype)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            idx, sc = kvc.kvc_h2o_prefill_select_gqa(q, k, seq_len=w.prompt, L_local=w.L_local,
+                                                     K_hh=K_hh, scale=w.scale, ws=ws)
+            e1.record()
+            kvc.kvc_compact_gather(k, v, idx, w.budget, self.K[l], self.V[l],
+                                   pos_dst=self.pos[l])
+            self.score[l, :, :, :w.budget] = sc
+            torch.cuda.synchronize()
+            init_ms.append(e0.elapsed_time(e1))
+            del q, k, v
+        self.extra["h2o_prompt_select_ms"] = round(sum(init_ms), 3)
         self.free = torch.full((L, B * H), w.budget, dtype=torch.int32, device=dev)
         self.logits = torch.empty((L, B, w.n_heads_q, self.cap), dtype=torch.float32, device=dev)
         self.lse = torch.empty((L, B, w.n_heads_q), dtype=torch.float32, device=dev)
@@ -690,8 +697,8 @@ class H2OGrouped(H2O):
                 "batch": w.batch, "n_heads_q": w.n_heads_q, "n_heads_kv": w.n_heads_kv,
                 "d_head": w.d_head, "budget": w.budget, "L_local": w.L_local,
                 "K_hh": w.budget - w.L_local, "kv_dtype": "bf16", "l2": "inputs larger than L2",
-                "init": "caches of N(0,1) keys/values at the 410 newest and 409 random older "
-                        "prompt positions, random scores (no prompt selection in this workload)",
+                "prompt": f"{w.prompt} tokens, compressed by the grouped prompt column sums "
+                          "(410 newest + 409 heavy hitters per KV head)",
                 "graph": "appends, then decode + grouped accumulate/evict per layer (the update "
                          "of layer l on a second stream beside the decode of layer l + 1), as "
                          "two CUDA graphs"}

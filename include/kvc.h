@@ -528,6 +528,22 @@ kvc_status kvc_h2o_prefill_select(const void *q, const kvc_cache *prompt, int32_
                                   float *score_out, float *s_full, void *ws, size_t ws_bytes,
                                   void *stream);
 
+/* kvc_h2o_prefill_select for a grouped-query cache (n_heads_q = G * n_heads_kv; query head h
+ * reads KV head h / G).  A cached row is kept or dropped for the whole group, so its score is
+ * the sum over the group of each query head's causal column sum ([KVC] H2O, s_j = sum_t
+ * alpha_{t,j}, added over the G heads in head order -- a reading, the pages treat one head);
+ * then the same compression per (batch, KV head).  q: [batch][n_heads_q][seq_len][d_head]
+ * (prompt->dtype, contiguous); idx_out, score_out: [batch][n_heads_kv][n_keep];
+ * s_full (nullable): [batch][n_heads_kv][seq_len].  Each group member's heads are copied into
+ * the workspace and scored by the one-head kernels.  Workspace:
+ * kvc_h2o_prefill_gqa_workspace_bytes() (dtype: kvc_dtype of the prompt), 256-byte aligned. */
+size_t kvc_h2o_prefill_gqa_workspace_bytes(int32_t batch, int32_t n_heads_kv, int32_t d_head,
+                                           int32_t seq_len, int32_t dtype);
+kvc_status kvc_h2o_prefill_select_gqa(const void *q, int32_t n_heads_q, const kvc_cache *prompt,
+                                      int32_t seq_len, int32_t L_local, int32_t K_hh,
+                                      float scale, int32_t *idx_out, float *score_out,
+                                      float *s_full, void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1078,4 +1078,99 @@ kvc_status kvc_h2o_prefill_select(const void *q, const kvc_cache *prompt, int32_
     return ok();
 }
 
+// Grouped-query prompt selection: [s_acc][s_g][q of one group member][scoring plan].
+static size_t h2o_gqa_layout(int B, int Hkv, int N, int D, int eb, int n_sm, size_t *off_g,
+                             size_t *off_q, kvc::ScorePlan *pl)
+{
+    const size_t s_bytes = align256((size_t)B * Hkv * N * sizeof(float));
+    *off_g = s_bytes;
+    *off_q = 2 * s_bytes;
+    const size_t base = *off_q + align256((size_t)B * Hkv * N * D * eb);
+    *pl = kvc::score_plan(B, Hkv, 1, N, N, n_sm, base);
+    return pl->bytes;
+}
+
+size_t kvc_h2o_prefill_gqa_workspace_bytes(int32_t batch, int32_t n_heads_kv, int32_t d_head,
+                                           int32_t seq_len, int32_t dtype)
+{
+    if (batch <= 0 || n_heads_kv <= 0 || seq_len <= 0 || d_head <= 0 ||
+        (dtype != KVC_F32 && dtype != KVC_BF16))
+        return 0;
+    size_t og, oq;
+    kvc::ScorePlan pl;
+    return h2o_gqa_layout(batch, n_heads_kv, seq_len, d_head, elem_bytes(dtype),
+                          sm_count_or_default(), &og, &oq, &pl);
+}
+
+kvc_status kvc_h2o_prefill_select_gqa(const void *q, int32_t n_heads_q, const kvc_cache *prompt,
+                                      int32_t seq_len, int32_t L_local, int32_t K_hh,
+                                      float scale, int32_t *idx_out, float *score_out,
+                                      float *s_full, void *ws, size_t ws_bytes, void *stream)
+{
+    kvc_status st = check_cache(prompt, "kvc_h2o_prefill_select_gqa", false);
+    if (st != KVC_OK) return st;
+    if (q == nullptr || idx_out == nullptr || score_out == nullptr)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_h2o_prefill_select_gqa: null pointer");
+    if (!aligned16(q)) return fail(KVC_ERR_ALIGN, "kvc_h2o_prefill_select_gqa: q alignment");
+    const int Hkv = prompt->n_heads_kv;
+    if (n_heads_q <= 0 || n_heads_q % Hkv)
+        return fail(KVC_ERR_SHAPE, "kvc_h2o_prefill_select_gqa: n_heads_q %d not a multiple of "
+                    "%d KV heads", n_heads_q, Hkv);
+    if (seq_len <= 0 || seq_len > prompt->cap || L_local < 0 || K_hh < 0)
+        return fail(KVC_ERR_SHAPE, "kvc_h2o_prefill_select_gqa: sizes");
+    if (!std::isfinite(scale))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_h2o_prefill_select_gqa: scale");
+    int32_t *code = nullptr;
+    int n_sm = 0;
+    st = device_info(&code, &n_sm);
+    if (st != KVC_OK) return st;
+    const int B = prompt->batch, N = seq_len, D = prompt->d_head, G = n_heads_q / Hkv;
+    const int eb = elem_bytes(prompt->dtype);
+    size_t off_g, off_q;
+    kvc::ScorePlan pl;
+    const size_t need = h2o_gqa_layout(B, Hkv, N, D, eb, n_sm, &off_g, &off_q, &pl);
+    if (ws == nullptr || ws_bytes < need || !aligned256(ws))
+        return fail(KVC_ERR_WORKSPACE, "kvc_h2o_prefill_select_gqa: workspace needs %zu aligned "
+                    "bytes", need);
+    char *wsb = static_cast<char *>(ws);
+    float *acc = s_full ? s_full : reinterpret_cast<float *>(wsb);
+    float *sg = reinterpret_cast<float *>(wsb + off_g);
+    void *qg = wsb + off_q;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kvc::ScoreParams sp{};
+    sp.q = qg; sp.k = prompt->k;
+    sp.sb = prompt->stride_b; sp.sh = prompt->stride_h; sp.ss = prompt->stride_slot;
+    sp.B = B; sp.Hq = Hkv; sp.Hkv = Hkv; sp.G = 1; sp.D = D; sp.N = N; sp.L_obs = N;
+    sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.n_cols = N;
+    sp.col_mult = 1.0f;
+    sp.row_ml = reinterpret_cast<float *>(wsb + pl.off_ml);
+    sp.row_lse2 = reinterpret_cast<float *>(wsb + pl.off_lse);
+    sp.n_chunks = pl.n_chunks;
+    sp.chunk = pl.chunk;
+    cudaError_t e;
+    for (int g = 0; g < G; ++g) {
+        // member g of every group, then its causal column sums, added in head order
+        e = kvc::launch_group_member_copy(q, qg, B, Hkv, G, g, N, D * eb, s);
+        if (e != cudaSuccess) return cuda_fail(e, "group member copy launch");
+        sp.s_out = g == 0 ? acc : sg;
+        e = run_scores(sp, prompt->dtype, scale, code, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prompt scores launch");
+        if (g > 0) {
+            e = kvc::launch_add_rows(acc, sg, (long long)B * Hkv * N, s);
+            if (e != cudaSuccess) return cuda_fail(e, "group sum launch");
+        }
+    }
+    const long long keep_ll = (long long)K_hh + L_local;
+    const int n_keep = (int)std::min<long long>(N, keep_ll);
+    if (N <= keep_ll)
+        e = kvc::launch_iota_rows(idx_out, n_keep, B * Hkv, n_keep, s);
+    else
+        e = kvc::launch_topk_rows(acc, N, B * Hkv, N - L_local, K_hh, L_local, idx_out, n_keep, s);
+    if (e != cudaSuccess) return cuda_fail(e, "H2O selection launch");
+    e = kvc::launch_gather_scores(acc, N, idx_out, n_keep, B * Hkv, n_keep, score_out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "score gather launch");
+    return ok();
+}
+
 }  // extern "C"

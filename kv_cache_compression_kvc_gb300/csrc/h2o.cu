@@ -151,6 +151,33 @@ __global__ void gather_scores_kernel(const float *s_full, int64_t s_stride, cons
     out[(size_t)r * n_keep + j] = s_full[(size_t)r * s_stride + idx[(size_t)r * idx_stride + j]];
 }
 
+// Grouped-query prompt scores: query heads kh*G + g (member g of every group) copied into a
+// contiguous [B][Hkv][N][D] buffer, so the one-head scoring runs on them unchanged.
+__global__ void group_member_copy_kernel(const char *__restrict__ q, char *__restrict__ dst,
+                                         int Hkv, int G, int g, int N, int row_bytes,
+                                         long long n_vec)
+{
+    const int vpr = row_bytes / 16;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / vpr;
+        const int c = (int)(i - r * vpr);
+        const long long bk = r / N;              // b * Hkv + kh
+        const int n = (int)(r - bk * N);
+        const long long src_row = (bk * G + g) * N + n;
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(q + src_row * row_bytes) + c);
+        reinterpret_cast<uint4 *>(dst + r * row_bytes)[c] = x;
+    }
+}
+
+// acc += x, element by element (the group's members added in head order)
+__global__ void add_rows_kernel(float *__restrict__ acc, const float *__restrict__ x, long long n)
+{
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        acc[i] += x[i];
+}
+
 }  // namespace
 
 cudaError_t launch_h2o_accumulate_evict(const H2OParams &p, cudaStream_t stream)
@@ -175,6 +202,25 @@ cudaError_t launch_gather_scores(const float *s_full, int64_t s_stride, const in
     if (total == 0) return cudaSuccess;
     gather_scores_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(
         s_full, s_stride, idx, idx_stride, rows, n_keep, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_group_member_copy(const void *q, void *dst, int B, int Hkv, int G, int g, int N,
+                                     int row_bytes, cudaStream_t stream)
+{
+    const long long n_vec = (long long)B * Hkv * N * (row_bytes / 16);
+    if (n_vec == 0) return cudaSuccess;
+    const long long blocks = (n_vec + 255) / 256;
+    group_member_copy_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+        static_cast<const char *>(q), static_cast<char *>(dst), Hkv, G, g, N, row_bytes, n_vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_add_rows(float *acc, const float *x, long long n, cudaStream_t stream)
+{
+    if (n == 0) return cudaSuccess;
+    const long long blocks = (n + 255) / 256;
+    add_rows_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(acc, x, n);
     return cudaGetLastError();
 }
 

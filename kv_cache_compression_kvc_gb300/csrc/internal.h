@@ -270,6 +270,9 @@ struct H2OParams {
     int32_t *dev_code;
 };
 cudaError_t launch_h2o_accumulate_evict(const H2OParams &p, cudaStream_t stream);
+cudaError_t launch_group_member_copy(const void *q, void *dst, int B, int Hkv, int G, int g, int N,
+                                     int row_bytes, cudaStream_t stream);
+cudaError_t launch_add_rows(float *acc, const float *x, long long n, cudaStream_t stream);
 cudaError_t launch_gather_scores(const float *s_full, int64_t s_stride, const int32_t *idx,
                                  int64_t idx_stride, int rows, int n_keep, float *out,
                                  cudaStream_t stream);

@@ -132,6 +132,9 @@ SIGNATURES = {
     "kvc_h2o_accumulate_evict_gqa": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
                                             _I32, _P, _I32, _I32, _P]),
     "kvc_h2o_prefill_workspace_bytes": (_SZ, [_I32] * 4),
+    "kvc_h2o_prefill_gqa_workspace_bytes": (_SZ, [_I32] * 5),
+    "kvc_h2o_prefill_select_gqa": (_I32, [_P, _I32, _CACHE_P, _I32, _I32, _I32, _F32, _P, _P, _P,
+                                          _P, _SZ, _P]),
     "kvc_h2o_prefill_select": (_I32, [_P, _CACHE_P, _I32, _I32, _I32, _F32, _P, _P, _P, _P,
                                       _SZ, _P]),
 }
@@ -627,5 +630,34 @@ def kvc_h2o_prefill_select(q: torch.Tensor, k_prompt: torch.Tensor, *, seq_len: 
     wp, wb = _ws_ptr(ws)
     _check(load().kvc_h2o_prefill_select(
         _ptr(q), ctypes.byref(c), seq_len, L_local, K_hh, float(scale), _ptr(idx_out),
+        _ptr(score_out), _ptr(s_full), wp, wb, _stream(stream)))
+    return idx_out, score_out
+
+
+def kvc_h2o_prefill_gqa_workspace_bytes(batch, n_heads_kv, d_head, seq_len, dtype) -> int:
+    return int(load().kvc_h2o_prefill_gqa_workspace_bytes(batch, n_heads_kv, d_head, seq_len,
+                                                           dtype))
+
+
+def kvc_h2o_prefill_select_gqa(q: torch.Tensor, k_prompt: torch.Tensor, *, seq_len: int,
+                               L_local: int, K_hh: int, scale: float,
+                               idx_out: Optional[torch.Tensor] = None,
+                               score_out: Optional[torch.Tensor] = None,
+                               s_full: Optional[torch.Tensor] = None,
+                               ws: Optional[torch.Tensor] = None, stream=None):
+    """q [B, Hq, N, D]; k_prompt [B, Hkv, cap, D] -> (idx [B, Hkv, n_keep], score [B, Hkv, n_keep])."""
+    c = cache_view(k_prompt)
+    B, Hq = q.shape[0], q.shape[1]
+    n_keep = min(seq_len, K_hh + L_local)
+    if idx_out is None:
+        idx_out = torch.empty((B, c.n_heads_kv, n_keep), dtype=torch.int32, device=q.device)
+    if score_out is None:
+        score_out = torch.empty((B, c.n_heads_kv, n_keep), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = _zeroed_workspace(kvc_h2o_prefill_gqa_workspace_bytes(
+            B, c.n_heads_kv, c.d_head, seq_len, c.dtype), q.device)
+    wp, wb = _ws_ptr(ws)
+    _check(load().kvc_h2o_prefill_select_gqa(
+        _ptr(q), Hq, ctypes.byref(c), seq_len, L_local, K_hh, float(scale), _ptr(idx_out),
         _ptr(score_out), _ptr(s_full), wp, wb, _stream(stream)))
     return idx_out, score_out

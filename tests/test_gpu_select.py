@@ -419,3 +419,31 @@ def test_h2o_streamed_prompt_teacher_forced(dtype, G):
         for kh in range(Hkv):
             held = sorted(int(x) for x in p_end[b, kh])
             assert held[-L_local:] == list(range(N - L_local, N))
+
+
+@pytest.mark.parametrize("dtype,D,G", [(torch.float32, 64, 4), (torch.bfloat16, 128, 4),
+                                       (torch.bfloat16, 128, 2)])
+def test_h2o_prompt_select_grouped_query(dtype, D, G):
+    """H2O's prompt compression on a grouped-query cache: each KV head's column sums added over
+    its query heads (against the oracle, relative 1e-4; G * N in total), the kept positions
+    bit-exact given the GPU's scores, the kept scores gathered from them."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    B, Hkv, N, L_local, K_hh = 2, 2, 333, 40, 60
+    Hq = Hkv * G
+    q, k, v = I.prompt_qkv(B, Hq, Hkv, N, D, 123 + D + G, dev, dtype)
+    scale = 1 / math.sqrt(D)
+    s_full = torch.empty((B, Hkv, N), device=dev)
+    idx, score = kvc.kvc_h2o_prefill_select_gqa(q, k, seq_len=N, L_local=L_local, K_hh=K_hh,
+                                                scale=scale, s_full=s_full)
+    assert kvc.kvc_device_status() == 0
+    sf, ix, sc = s_full.cpu().numpy(), idx.cpu().numpy(), score.cpu().numpy()
+    for b in range(B):
+        for kh in range(Hkv):
+            ref = oracle.h2o_prompt_scores_group(f64(q[b, kh * G:(kh + 1) * G]), f64(k[b, kh]),
+                                                 scale)
+            assert_rel(sf[b, kh], ref, 1e-4, 1e-5, f"group column sums ({b},{kh})")
+            assert abs(float(sf[b, kh].sum()) - G * N) < 1e-3 * G * N
+            assert np.array_equal(oracle.h2o_prompt_select(sf[b, kh].astype(np.float64), L_local,
+                                                           K_hh), ix[b, kh]), "stage-exact"
+            assert np.array_equal(sc[b, kh], sf[b, kh][ix[b, kh]])
