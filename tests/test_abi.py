@@ -238,3 +238,19 @@ def test_block_prompt_select_validation_before_launch(kvc):
                                      1 << 20, None)
     assert st == 2                                                 # prompt heads != pool heads
     assert lib.kvc_block_prompt_select_workspace_bytes(1, 100, 16, 4) == 256 + 256
+
+
+def test_workspace_queries_of_the_added_entry_points(kvc):
+    """Host sizing: the DuoAttention decode allows more blocks per retrieval pair than the
+    plain decode of the same shape; the grouped H2O prompt selection holds one group member's
+    queries and two score arrays beside the one-head scoring state; bad arguments give 0."""
+    plain = kvc.kvc_decode_attn_workspace_bytes(1, 32, 32, 128, 131080)
+    duo = kvc.kvc_decode_attn_duo_workspace_bytes(1, 32, 32, 128, 131080, 8)
+    assert duo > plain > 0
+    B, Hkv, D, N = 16, 8, 128, 4096
+    gqa = kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, kvc.KVC_BF16)
+    assert gqa >= B * Hkv * N * D * 2 + 2 * B * Hkv * N * 4
+    assert gqa > kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, kvc.KVC_BF16) - 1
+    assert kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, kvc.KVC_F32) > gqa
+    assert kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, 7) == 0
+    assert kvc.kvc_decode_attn_duo_workspace_bytes(1, 32, 32, 128, 100, 33) == 0
