@@ -250,7 +250,6 @@ def test_workspace_queries_of_the_added_entry_points(kvc):
     B, Hkv, D, N = 16, 8, 128, 4096
     gqa = kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, kvc.KVC_BF16)
     assert gqa >= B * Hkv * N * D * 2 + 2 * B * Hkv * N * 4
-    assert gqa > kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, kvc.KVC_BF16) - 1
     assert kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, kvc.KVC_F32) > gqa
     assert kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, 7) == 0
     assert kvc.kvc_decode_attn_duo_workspace_bytes(1, 32, 32, 128, 100, 33) == 0
