@@ -15,6 +15,10 @@ streaming shape with ALiBi at in-cache positions instead of RoPE), paged (block-
 over page tables at the H2O shape), h2o_gqa (H2O on a grouped-query cache, 32 query heads over 8
 KV heads), duo (DuoAttention at 128k tokens: a quarter of the heads retrieving).
 
+Every line also carries "snapkv_select": SnapKV's prefill selection and compaction over the
+SnapKV workload's 32 layers (device time, fraction of its one-read HBM roofline), measured in the
+same run (--no-select skips it).
+
 Multi-GPU: the path shards into independent replicas (no exchange step); under torchrun every
 rank runs the same workload on its own GPU and rank 0 prints the aggregate.
 """
@@ -184,6 +188,120 @@ def kernel_traffic(kernel_file: str, key: str):
 
 
 # ----------------------------------------------------------------------------- workloads
+def graph_device_ms(fns, flush, reps=3):
+    """Device time (ms, median of `reps` replays) of each callable's work, each captured as a
+    CUDA graph and the graphs replayed in order after an L2 flush.  Host-side work such as
+    tensor-map encoding happens at capture, untimed, as in a captured or pipelined prefill."""
+    graphs = []
+    for fn in fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    times = [[] for _ in fns]
+    for r in range(reps):
+        flush.fill_(r & 0xff)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+        ev[0].record()
+        for i, g in enumerate(graphs):
+            g.replay()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        for i in range(len(fns)):
+            times[i].append(ev[i].elapsed_time(ev[i + 1]))
+    del graphs
+    return [statistics.median(t) for t in times]
+
+
+def snapkv_selection(w: I.Workload, dev, kvc, budgets, caps=None, pyramid=False, reps=3):
+    """SnapKV selection (kvc_snapkv_select) and compaction (kvc_compact_gather) of every layer
+    of a workload, each layer's prompt generated in turn, device-timed after an L2 flush.
+    Returns (summary, compacted caches [(K, V)] or None, lengths [L, B*Hkv]).  With caps the
+    compacted caches (cap slots per pair) are kept for decoding; without, they are dropped."""
+    L, B, Hkv, D = w.layers, w.batch, w.n_heads_kv, w.d_head
+    lens = torch.zeros((L, B * Hkv), dtype=torch.int32, device=dev)
+    ws = torch.zeros(kvc.kvc_snapkv_select_workspace_bytes(
+        B, w.n_heads_q, Hkv, D, w.prompt, w.L_obs) + 256, dtype=torch.uint8, device=dev)
+    gen = I.pyramid_layer if pyramid else I.snapkv_layer
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # twice the L2
+    kept, sel_ms, gat_ms = [], [], []
+    for l in range(L):
+        q_obs, k, v = gen(w, l, dev)
+        cap = caps[l] if caps is not None else budgets[l]
+        idx = torch.empty((B, Hkv, budgets[l]), dtype=torch.int32, device=dev)
+        Kc = torch.empty((B, Hkv, cap, D), dtype=w.dtype, device=dev)
+        Vc = torch.empty_like(Kc)
+
+        def select():
+            kvc.kvc_snapkv_select(q_obs, k, seq_len=w.prompt, L_obs=w.L_obs, budget=budgets[l],
+                                  scale=w.scale, pool_k=w.pool_k, idx_out=idx, ws=ws)
+
+        def compact():
+            kvc.kvc_compact_gather(k, v, idx, budgets[l], Kc, Vc, len_dst=lens[l])
+
+        if l == 0:                          # one-time set-up (attributes, tensor maps) untimed
+            select()
+            compact()
+        t_sel, t_gat = graph_device_ms([select, compact], flush, reps)
+        sel_ms.append(t_sel)
+        gat_ms.append(t_gat)
+        if caps is not None:
+            kept.append((Kc, Vc))
+        del q_obs, k, v, idx
+    code = kvc.kvc_device_status()
+    if code != 0:
+        raise RuntimeError(f"device range check fired during the selection: {code}")
+    eb = elem_bytes(w.dtype)
+    sel_bytes = L * (B * Hkv * w.prompt * D * eb + B * w.n_heads_q * w.L_obs * D * eb)
+    sel_flop = L * 2.0 * B * w.n_heads_q * w.L_obs * w.prompt * D
+    gat_bytes = sum(2 * 2 * B * Hkv * b * D * eb + B * Hkv * b * 4 for b in budgets)
+    peak, peak_kind = measured_peak()
+    tflops = measured_tensor_peak()
+    sel_roof = max(sel_bytes / (peak * 1e9), sel_flop / (tflops * 1e12)) * 1e3
+    gat_roof = gat_bytes / (peak * 1e9) * 1e3
+    summary = {
+        "workload": (f"{w.name}: {L} layers, batch {B}, {w.n_heads_q}/{Hkv} heads, d_head {D}, "
+                     f"prompt {w.prompt}, L_obs {w.L_obs}, pool {w.pool_k}, budget "
+                     + (f"{budgets[0]}..{budgets[-1]}" if pyramid else f"{budgets[0]}")),
+        "layers": L, "select_ms": round(sum(sel_ms), 3),
+        "select_ms_per_layer": round(sum(sel_ms) / L, 4),
+        "compact_ms": round(sum(gat_ms), 3),
+        "compact_ms_max_layer": round(max(gat_ms), 3),
+        "select_roofline_ms": round(sel_roof, 3),
+        "select_frac": round(sel_roof / sum(sel_ms), 4),
+        "compact_roofline_ms": round(gat_roof, 3),
+        "compact_frac": round(gat_roof / sum(gat_ms), 4),
+        "peak_kind": peak_kind,
+        "algorithmic_select_bytes": sel_bytes, "select_flop": sel_flop,
+        "bound": "hbm" if sel_bytes / (peak * 1e9) >= sel_flop / (tflops * 1e12) else "tensor",
+        "timing": f"per layer: selection and compaction captured as CUDA graphs, replayed "
+                  f"{reps} times after an L2 flush, median"}
+    del flush, ws
+    return summary, (kept if caps is not None else None), lens
+
+
+def prompt_select_summary(w: I.Workload, n_heads_q, layer_ms):
+    """H2O's prompt scoring + one-shot compression, per layer and in total, against its
+    roofline: one causal Q.K^T pass over the prompt (the column sums need the row statistics
+    first, so the kernels make two; the second is implementation overhead) and one read of Q
+    and K."""
+    L, B, D, N = w.layers, w.batch, w.d_head, w.prompt
+    eb = elem_bytes(w.dtype)
+    flop = 2.0 * B * n_heads_q * (N * (N + 1) / 2) * D               # per layer, causal half
+    nbytes = B * (n_heads_q + w.n_heads_kv) * N * D * eb              # Q and K once
+    peak, peak_kind = measured_peak()
+    tflops = measured_tensor_peak()
+    roof = max(nbytes / (peak * 1e9), flop / (tflops * 1e12)) * 1e3   # ms per layer
+    total = sum(layer_ms)
+    return {"layers": L, "ms": round(total, 3), "ms_per_layer": round(total / L, 4),
+            "roofline_ms_per_layer": round(roof, 4), "frac": round(roof * L / total, 4),
+            "bound": "tensor" if flop / (tflops * 1e12) >= nbytes / (peak * 1e9) else "hbm",
+            "flop_per_layer": flop, "bytes_per_layer": nbytes, "peak_kind": peak_kind,
+            "timing": "per layer: captured as a CUDA graph, replayed 3 times after an L2 flush, "
+                      "median"}
+
+
 def elem_bytes(dtype) -> int:
     return torch.tensor([], dtype=dtype).element_size()
 
@@ -399,71 +517,12 @@ class SelectDecode(DecodeWorkload):
             self.budgets = [w.budget] * L
         self.pre = max_steps
         self.caps = [b + max_steps for b in self.budgets]
-        self.K, self.V, self.caches = [], [], []
-        self.lens = torch.zeros((L, B * Hkv), dtype=torch.int32, device=dev)
-        sel_ms, gat_ms = [], []
-        ws = torch.zeros(kvc.kvc_snapkv_select_workspace_bytes(
-            B, w.n_heads_q, Hkv, D, w.prompt, w.L_obs) + 256, dtype=torch.uint8, device=dev)
-        gen = I.pyramid_layer if pyramid else I.snapkv_layer
-        # L2 is flushed before each timed selection (the generator has just written the prompt)
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        warm = True
-        for l in range(L):
-            q_obs, k, v = gen(w, l, dev)
-            idx = torch.empty((B, Hkv, self.budgets[l]), dtype=torch.int32, device=dev)
-            Kc = torch.empty((B, Hkv, self.caps[l], D), dtype=w.dtype, device=dev)
-            Vc = torch.empty_like(Kc)
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-            if warm:                        # one-time setup (attributes, tensor maps) untimed
-                kvc.kvc_snapkv_select(q_obs, k, seq_len=w.prompt, L_obs=w.L_obs,
-                                      budget=self.budgets[l], scale=w.scale, pool_k=w.pool_k,
-                                      idx_out=idx, ws=ws)
-                kvc.kvc_compact_gather(k, v, idx, self.budgets[l], Kc, Vc, len_dst=self.lens[l])
-                warm = False
-            # device time of the selection and the compaction: both captured as CUDA graphs
-            # (host work such as tensor-map encoding happens at capture, untimed, as it would
-            # in a captured or pipelined prefill), replayed after an L2 flush
-            g_sel, g_gat = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_sel):
-                kvc.kvc_snapkv_select(q_obs, k, seq_len=w.prompt, L_obs=w.L_obs,
-                                      budget=self.budgets[l], scale=w.scale, pool_k=w.pool_k,
-                                      idx_out=idx, ws=ws)
-            with torch.cuda.graph(g_gat):
-                kvc.kvc_compact_gather(k, v, idx, self.budgets[l], Kc, Vc, len_dst=self.lens[l])
-            torch.cuda.synchronize()
-            flush.fill_(l & 0xff)
-            e[0].record()
-            g_sel.replay()
-            e[1].record()
-            g_gat.replay()
-            e[2].record()
-            torch.cuda.synchronize()
-            del g_sel, g_gat
-            sel_ms.append(e[0].elapsed_time(e[1]))
-            gat_ms.append(e[1].elapsed_time(e[2]))
-            self.K.append(Kc)
-            self.V.append(Vc)
-            self.caches.append(kvc.cache_view(Kc, Vc))
-            del q_obs, k, v
-        del flush
-        eb = elem_bytes(w.dtype)
-        sel_bytes = L * (B * Hkv * w.prompt * D * eb + B * w.n_heads_q * w.L_obs * D * eb)
-        sel_flop = L * 2.0 * B * w.n_heads_q * w.L_obs * w.prompt * D
-        gat_bytes = sum(2 * 2 * B * Hkv * b * D * eb + B * Hkv * b * 4 for b in self.budgets)
-        peak, _ = measured_peak()
-        tflops = measured_tensor_peak()
-        sel_roof = max(sel_bytes / (peak * 1e9), sel_flop / (tflops * 1e12)) * 1e3
-        gat_roof = gat_bytes / (peak * 1e9) * 1e3
-        self.extra["snapkv_select"] = {
-            "layers": L, "select_ms": round(sum(sel_ms), 3),
-            "compact_ms": round(sum(gat_ms), 3),
-            "compact_ms_max_layer": round(max(gat_ms), 3),
-            "select_roofline_ms": round(sel_roof, 3),
-            "select_frac": round(sel_roof / sum(sel_ms), 4),
-            "compact_roofline_ms": round(gat_roof, 3),
-            "compact_frac": round(gat_roof / sum(gat_ms), 4),
-            "algorithmic_select_bytes": sel_bytes, "select_flop": sel_flop,
-            "bound": "hbm" if sel_bytes / (peak * 1e9) >= sel_flop / (tflops * 1e12) else "tensor"}
+        summary, kept, self.lens = snapkv_selection(w, dev, kvc, self.budgets, self.caps,
+                                                    pyramid=pyramid)
+        self.K = [kc for kc, _ in kept]
+        self.V = [vc for _, vc in kept]
+        self.caches = [kvc.cache_view(kc, vc) for kc, vc in kept]
+        self.extra["snapkv_select"] = summary
         self.ws = kvc.decode_workspace(B, w.n_heads_q, Hkv, D, max(self.caps), dev)
         self.launches_per_step = 2 * L
         self.appended = 0
@@ -543,20 +602,26 @@ class H2O(DecodeWorkload):
         ws = torch.zeros(kvc.kvc_h2o_prefill_workspace_bytes(B, H, D, w.prompt) + 256,
                          dtype=torch.uint8, device=dev)
         init_ms = []
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        idx = torch.empty((B, H, w.budget), dtype=torch.int32, device=dev)
+        sc = torch.empty((B, H, w.budget), dtype=torch.float32, device=dev)
         for l in range(L):
             q, k, v = I.h2o_layer(w, l, dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            idx, sc = kvc.kvc_h2o_prefill_select(q, k, seq_len=w.prompt, L_local=w.L_local,
-                                                 K_hh=K_hh, scale=w.scale, ws=ws)
-            e1.record()
+
+            def select():
+                kvc.kvc_h2o_prefill_select(q, k, seq_len=w.prompt, L_local=w.L_local, K_hh=K_hh,
+                                           scale=w.scale, idx_out=idx, score_out=sc, ws=ws)
+
+            if l == 0:                      # one-time set-up (attributes, tensor maps) untimed
+                select()
+            init_ms.append(graph_device_ms([select], flush)[0])
             kvc.kvc_compact_gather(k, v, idx, w.budget, self.K[l], self.V[l],
                                    pos_dst=self.pos[l])
             self.score[l, :, :, :w.budget] = sc
             torch.cuda.synchronize()
-            init_ms.append(e0.elapsed_time(e1))
             del q, k, v
-        self.extra["h2o_prompt_select_ms"] = round(sum(init_ms), 3)
+        del flush
+        self.extra["h2o_prompt_select"] = prompt_select_summary(w, w.n_heads_q, init_ms)
         self.t = torch.tensor([w.prompt], dtype=torch.int64, device=dev)
         self.caches = [kvc.cache_view(self.K[l], self.V[l]) for l in range(L)]
         self.ws = kvc.decode_workspace(B, w.n_heads_q, H, D, self.cap, dev)
@@ -654,22 +719,29 @@ class H2OGrouped(H2O):
         ws = torch.zeros(kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, H, D, w.prompt, kvc.KVC_BF16)
                          + 256, dtype=torch.uint8, device=dev)
         init_ms = []
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        idx = torch.empty((B, H, w.budget), dtype=torch.int32, device=dev)
+        sc = torch.empty((B, H, w.budget), dtype=torch.float32, device=dev)
         for l in range(L):
             # the prompt (N(0,1), sink-boosted keys), its grouped column sums and the one-shot
             # compression to the budget, then the kept rows gathered into the cache
             q, k, v = I.prompt_qkv(B, w.n_heads_q, H, w.prompt, D, w.seed * 1000 + l, dev, w.dtype)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            idx, sc = kvc.kvc_h2o_prefill_select_gqa(q, k, seq_len=w.prompt, L_local=w.L_local,
-                                                     K_hh=K_hh, scale=w.scale, ws=ws)
-            e1.record()
+
+            def select():
+                kvc.kvc_h2o_prefill_select_gqa(q, k, seq_len=w.prompt, L_local=w.L_local,
+                                               K_hh=K_hh, scale=w.scale, idx_out=idx,
+                                               score_out=sc, ws=ws)
+
+            if l == 0:                      # one-time set-up (attributes, tensor maps) untimed
+                select()
+            init_ms.append(graph_device_ms([select], flush)[0])
             kvc.kvc_compact_gather(k, v, idx, w.budget, self.K[l], self.V[l],
                                    pos_dst=self.pos[l])
             self.score[l, :, :, :w.budget] = sc
             torch.cuda.synchronize()
-            init_ms.append(e0.elapsed_time(e1))
             del q, k, v
-        self.extra["h2o_prompt_select_ms"] = round(sum(init_ms), 3)
+        del flush
+        self.extra["h2o_prompt_select"] = prompt_select_summary(w, w.n_heads_q, init_ms)
         self.free = torch.full((L, B * H), w.budget, dtype=torch.int32, device=dev)
         self.logits = torch.empty((L, B, w.n_heads_q, self.cap), dtype=torch.float32, device=dev)
         self.lse = torch.empty((L, B, w.n_heads_q), dtype=torch.float32, device=dev)
@@ -1155,6 +1227,11 @@ def run_gpu(args):
     }
     line.update(R.extra)
     line["decode_share_of_step"] = round(dec_share, 4)
+    if "snapkv_select" not in line and not args.no_select:
+        # the metric's third leg: SnapKV prefill selection (and compaction) on the SnapKV
+        # workload's 32 layers, timed on the device in this same run
+        ws_ = I.WORKLOADS["snapkv"]
+        line["snapkv_select"], _, _ = snapkv_selection(ws_, dev, kvc, [ws_.budget] * ws_.layers)
     print(json.dumps(line), flush=True)
 
 
@@ -1208,6 +1285,9 @@ def main():
     ap.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
     ap.add_argument("--workload", choices=WORKLOAD_NAMES, default="streaming")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-select", action="store_true",
+                    help="skip the SnapKV selection leg (32 layers of the SnapKV workload) that "
+                         "decode-only workloads report beside their decode line")
     ap.add_argument("--e2e-eager", action="store_true",
                     help="end to end: make the C-ABI calls every step instead of replaying them")
     args = ap.parse_args()

@@ -326,9 +326,18 @@ kvc_status kvc_decode_attn(const void *q, int32_t n_heads_q, const kvc_cache *ca
  * cap; when they differ widely (a ragged batch) the pairs' blocks finish at very different
  * times, and this flag balances them at the price of a scan of the lengths at the start of
  * every block.  Same results either way (the log-sum-exp merge order may differ).
+ * KVC_DECODE_TEST_STARVE: a test hook with no counterpart on the pages, for exercising the
+ * kernels' bounded waits without a GPU fault.  The kernel issues no cache loads at all, so its
+ * first wait for a tile runs out after a short bounded spin; the block then stops (no loads
+ * are in flight), every block still finishes, the workspace is left zeroed, and
+ * kvc_device_status() reports KVC_DEV_TIMEOUT.  The outputs of such a call are undefined; the
+ * next call without the flag is unaffected.  Every wait inside the decode kernels behaves the
+ * same way when it gives up for a real reason (a lost arrival): the block stops issuing loads,
+ * waits (bounded) for the loads it has in flight, and exits with invalid outputs.
  * Other bits must be 0 (KVC_ERR_INVALID_ARG). */
 #define KVC_DECODE_KV_SETTLED 1u
 #define KVC_DECODE_BALANCE 2u
+#define KVC_DECODE_TEST_STARVE 0x80000000u
 kvc_status kvc_decode_attn_ex(const void *q, int32_t n_heads_q, const kvc_cache *cache,
                               const int32_t *len, int32_t n_valid, const kvc_rope *rope,
                               float scale, float *out, float *logits, int64_t logits_stride,

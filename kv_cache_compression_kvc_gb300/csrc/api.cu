@@ -22,6 +22,8 @@ thread_local std::string g_last_error;
 __device__ int32_t g_dev_code;
 
 constexpr int kMaxDevices = 64;
+// polls before a wait gives up under KVC_DECODE_TEST_STARVE (a short, bounded stall)
+constexpr uint32_t kTestSpinLimit = 1024;
 std::mutex g_mutex;
 int32_t *g_code_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
@@ -247,7 +249,7 @@ static kvc_status decode_impl(const void *q, int32_t n_heads_q, const kvc_cache 
                               float *out, float *logits, int64_t logits_stride, float *lse,
                               void *ws, size_t ws_bytes, uint32_t flags, void *stream)
 {
-    if (flags & ~(uint32_t)(KVC_DECODE_KV_SETTLED | KVC_DECODE_BALANCE))
+    if (flags & ~(uint32_t)(KVC_DECODE_KV_SETTLED | KVC_DECODE_BALANCE | KVC_DECODE_TEST_STARVE))
         return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attn: unknown flags 0x%x", flags);
     kvc_status st = check_cache(cache, "kvc_decode_attn", true);
     if (st != KVC_OK) return st;
@@ -336,6 +338,10 @@ static kvc_status decode_impl(const void *q, int32_t n_heads_q, const kvc_cache 
     p.n_sm = n_sm > 0 ? n_sm : 152;
     p.kv_settled = (flags & KVC_DECODE_KV_SETTLED) ? 1 : 0;
     p.balance = (flags & KVC_DECODE_BALANCE) ? 1 : 0;
+    if (flags & KVC_DECODE_TEST_STARVE) {
+        p.starve = 1;
+        p.spin_limit = kTestSpinLimit;
+    }
     p.dev_code = code;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;

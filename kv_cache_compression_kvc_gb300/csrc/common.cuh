@@ -109,8 +109,10 @@ __device__ __forceinline__ float warp_sum(float x)
 }
 
 // ---- mbarriers, bulk copies (PTX) ---------------------------------------------------------------
-// Waits are bounded: after kMbarSpinLimit failed polls the thread records KVC_DEV_TIMEOUT and
-// returns as if the phase had completed, so a kernel can never hang on a lost arrival.
+// Waits are bounded: after kMbarSpinLimit failed polls the thread gives up, so a kernel can
+// never hang on a lost arrival.  mbar_wait records KVC_DEV_TIMEOUT and returns as if the phase
+// had completed; mbar_wait_ok only reports the outcome, for kernels that then stop issuing
+// work and wait (again bounded) for their own copies in flight before they exit.
 constexpr uint32_t kMbarSpinLimit = 1u << 22;
 constexpr int kDevCodeTimeout = 7;           // KVC_DEV_TIMEOUT
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -146,6 +148,26 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int32_t
     for (uint32_t it = 0; it < kMbarSpinLimit; ++it)
         if (mbar_try_wait(bar, parity)) return;
     record_code(code, kDevCodeTimeout);
+}
+// true once the phase with the given parity has completed; false after `limit` failed polls
+__device__ __forceinline__ bool mbar_wait_ok(uint32_t bar, uint32_t parity, uint32_t limit)
+{
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// The same wait for a block that may be aborting: when the first poll fails it keeps polling
+// but also gives up as soon as another thread of the block has raised *abort (checked every
+// 64 polls, off the fast path), so after one wait has run out the others end quickly.
+__device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity, uint32_t limit,
+                                                    const volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    for (uint32_t it = 1; it < limit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u && *abort != 0) return false;
+    }
+    return false;
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
                                          uint32_t bar)

@@ -68,8 +68,14 @@
 // almost all fixed cost (its q, its output), so spreading them keeps any block from collecting
 // many.  head_of maps each pair back to the model's KV head for q, the outputs and the logits.
 //
-// Waits on mbarriers are bounded: after kMbarSpinLimit failed polls the thread records
-// KVC_DEV_TIMEOUT and carries on (results are then garbage, but the kernel always finishes).
+// Waits on mbarriers are bounded (p.spin_limit polls).  A wait that gives up records
+// KVC_DEV_TIMEOUT and raises the block's abort flag: the issuing thread loads nothing more,
+// the other waits of the block give up at once, and the block still walks its tiles (computing
+// on whatever the stages hold) and takes part in the merge tickets, so every block finishes
+// and the tickets are left zeroed.  Before exiting, the issuing thread waits (again bounded)
+// for the loads it issued last, so no copy is still landing in the block's shared memory when
+// it exits.  The outputs of such a call are invalid.  The flag is read only once a first poll
+// has failed, so the waits that succeed at once cost what they did without it.
 #pragma once
 
 #include "common.cuh"
@@ -179,6 +185,7 @@ decode_attn_kernel(const DecodeParams p)
     float *sm_l = sm_m + NW * G;
     float *sm_o = sm_l + NW * G;                     // [NW][G][D]
     int *sm_flag = reinterpret_cast<int *>(sm_o + NW * G * D);
+    volatile int *sm_abort = sm_flag + 1;            // set once a bounded wait has given up
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -200,6 +207,7 @@ decode_attn_kernel(const DecodeParams p)
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, NW);
         }
+        *sm_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -319,7 +327,10 @@ decode_attn_kernel(const DecodeParams p)
         }
         return reinterpret_cast<const int32_t *>(smem + 128)[lb - tab_lo];
     };
+    int last_issued = -1;      // the issuing thread's last tile (the drain after an abort)
     auto issue_tile = [&](int i) {
+        if (p.starve) return;  // test hook: no loads, no arrivals (the waits run out)
+        last_issued = i;
         const int s = i % NS;
         int q, j0;
         locate(i, q, j0);
@@ -584,7 +595,10 @@ decode_attn_kernel(const DecodeParams p)
             if (cur >= 0) finish_pair(cur);
             start_pair(q);
         }
-        mbar_wait(bar_full + 8 * s, (i / NS) & 1, p.dev_code);
+        if (!mbar_wait_abortable(bar_full + 8 * s, (i / NS) & 1, p.spin_limit, sm_abort)) {
+            record_code(p.dev_code, kDevCodeTimeout);
+            *sm_abort = 1;
+        }
         const uint32_t kst = stage0 + s * SM::kStageBytes;
         const uint32_t vst = kst + SM::kTileBytes;
         int lb_, lkh_;
@@ -746,13 +760,24 @@ decode_attn_kernel(const DecodeParams p)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        if (threadIdx.x == 0 && i + NS < n_tiles) {
-            // every warp has released stage s: refill it with tile i + NS
-            mbar_wait(bar_empty + 8 * s, (i / NS) & 1, p.dev_code);
-            issue_tile(i + NS);
+        if (threadIdx.x == 0 && i + NS < n_tiles && *sm_abort == 0) {
+            // every warp has released stage s: refill it with tile i + NS (a warp that gave up
+            // on this stage set the abort flag before it released it, so the refill never lands
+            // on a load still in flight)
+            if (!mbar_wait_abortable(bar_empty + 8 * s, (i / NS) & 1, p.spin_limit, sm_abort)) {
+                record_code(p.dev_code, kDevCodeTimeout);
+                *sm_abort = 1;
+            } else if (*sm_abort == 0) {
+                issue_tile(i + NS);
+            }
         }
     }
     if (cur >= 0) finish_pair(cur);
+    // after an abort the last NS tiles issued (one per stage) may still be landing: wait for
+    // them, bounded, before the block's shared memory is released
+    if (threadIdx.x == 0 && *sm_abort != 0)
+        for (int i = max(0, last_issued - NS + 1); i <= last_issued; ++i)
+            mbar_wait_ok(bar_full + 8 * (i % NS), (i / NS) & 1, p.spin_limit);
 }
 
 // Elements per lane-half by (type, group size): keeps q and o (4*G*VW floats) in registers.
@@ -780,6 +805,7 @@ cudaError_t launch_decode_rm(const DecodeParams &p, cudaStream_t stream)
         configured[dev] = true;
     }
     DecodeParams q = p;
+    if (q.spin_limit == 0) q.spin_limit = kMbarSpinLimit;
     q.NT = p.cap > 0 ? (p.cap + SM::TK - 1) / SM::TK : 1;
     if (q.NT < 1) q.NT = 1;
     long long T_all = (long long)q.P * q.NT;

@@ -17,8 +17,17 @@
 // updates its online-softmax state (lazy running max, base-2 exponentials), converts the
 // probabilities in place into the A operand of the P.V product (the accumulator layout of
 // m16n8 is the operand layout of m16k16) and accumulates o.  For D = 256 two warps share the
-// same 16 keys and split the head dimension of o.  P is rounded to bf16 for the P.V product;
-// the sums l are kept in fp32.
+// same 16 keys and split the head dimension of o.  The probabilities P enter the P.V product as
+// two bf16 terms, P = hi + lo with hi = bf16(P) and lo = bf16(P - hi), each multiplied by V on
+// the tensor cores into the same fp32 accumulator: P is carried to 16 significant bits (a
+// relative error below 2^-17, against 2^-9 for P rounded once), so the arithmetic stays fp32
+// class while the inputs are bf16.  The sums l are kept in fp32.
+//
+// Bounded waits (p.spin_limit polls): one that gives up records KVC_DEV_TIMEOUT and raises the
+// block's abort flag -- no more loads, the other waits give up at once, the tiles and merge
+// tickets are still walked so that every block finishes -- and the issuing thread waits
+// (bounded) for its last loads before the block exits.  The outputs of such a call are invalid.
+// The flag is read only after a first poll has failed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -231,6 +240,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     float *sm_l = sm_m + PL::KGROUPS * G;
     float *sm_o = sm_l + PL::KGROUPS * G;      // [KGROUPS][G][D]
     int *sm_flag = reinterpret_cast<int *>(sm_o + PL::KGROUPS * G * D);
+    volatile int *sm_abort = sm_flag + 1;      // set once a bounded wait has given up
     int *sm_pref = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(sm_m) + PL::MERGE_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -245,6 +255,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mbar_init(bar_empty + 8 * s, MW);
         }
         mbar_init(bar_merge, 1);
+        *sm_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -339,7 +350,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // pair, not one per tile on the critical path of every copy.
     Cursor ic{};
     int iss_q = -1, iss_slots = 0;
+    int last_issued = -1;                      // the issuing thread's last tile (abort drain)
     auto issue_tile = [&](int i) {
+        if (p.starve) return;                  // test hook: no loads, no arrivals
+        last_issued = i;
         const long long t = t_begin + i;
         const int s = i % NS;
         advance(ic, t);
@@ -453,7 +467,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                              ML_BYTES, bar_merge);
                 }
             }
-            mbar_wait(bar_merge, phase & 1u, p.dev_code);
+            const bool got = mbar_wait_abortable(bar_merge, phase & 1u, p.spin_limit, sm_abort);
             ++phase;
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
@@ -473,7 +487,17 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
                 M[k] = mb;
             }
-            __syncthreads();                   // the next group's copies reuse the ring
+            // the next group's copies reuse the ring; a wait that gave up ends the merge after
+            // a bounded wait for this group's copies
+            if (__syncthreads_or(!got)) {
+                if (threadIdx.x == 0) {
+                    record_code(p.dev_code, kDevCodeTimeout);
+                    *sm_abort = 1;
+                    mbar_wait_ok(bar_merge, (phase - 1) & 1u, p.spin_limit);
+                }
+                __syncthreads();
+                break;
+            }
         }
 #pragma unroll
         for (int k = 0; k < CPT; ++k) {
@@ -543,7 +567,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (*sm_flag) {
                 const long long tb_lo = (long long)c_lo * T / Ce;  // first tile of block c_lo
                 const int slot0 = 2 * c_lo + (tb_lo < q_lo ? 1 : 0);
-                if (ring_idle && nseg > 8)         // one batch of register loads covers <= 8
+                // (an aborting block's ring may still receive tile loads: not used then)
+                if (ring_idle && nseg > 8 && *sm_abort == 0)   // one batch of registers <= 8
                     merge_staged(slot0, c_lo, nseg, rows0);
                 else
                     merge_segments<G, D>(p.ws_o, p.ws_ml, slot0, c_lo, nseg, p.out, p.lse, rows0);
@@ -568,7 +593,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             cur_hi = mc.hi;
             start_pair(cur);
         }
-        mbar_wait(bar_full + 8 * s, (i / NS) & 1, p.dev_code);
+        if (!mbar_wait_abortable(bar_full + 8 * s, (i / NS) & 1, p.spin_limit, sm_abort)) {
+            record_code(p.dev_code, kDevCodeTimeout);
+            *sm_abort = 1;
+        }
         const int j0 = (int)(t - cur_lo) * TK;
         const int key0 = kg * 16;                          // this warp's 16 keys in the tile
         if (j0 + key0 < cur_slots) {
@@ -621,6 +649,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
             const uint32_t pa0 = pack_bf16(pr[0][0], pr[0][1]);   // keys 2tq, 2tq+1
             const uint32_t pa2 = pack_bf16(pr[1][0], pr[1][1]);   // keys 8+2tq, 9+2tq
+            // the rounding residuals (exact in fp32), themselves rounded to bf16
+            const uint32_t pb0 = pack_bf16(pr[0][0] - bf16_lo(pa0), pr[0][1] - bf16_hi(pa0));
+            const uint32_t pb2 = pack_bf16(pr[1][0] - bf16_lo(pa2), pr[1][1] - bf16_hi(pa2));
             // ---- o[16 x DW] += P[16 x 16 keys] . V[16 keys x DW] --------------------------------
             // Slots past the pair's length are still in the tile (the cache may hold any bytes
             // there); their probabilities are 0, but 0 * NaN would poison the product, so the
@@ -648,16 +679,27 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 ldsm_x4_t(vst + sw_off(vrow, chunk, TK), b0, b1, b2, b3);
                 mma16816(o[n], pa0, pa2, b0, b1);
                 mma16816(o[n + 1], pa0, pa2, b2, b3);
+                mma16816(o[n], pb0, pb2, b0, b1);
+                mma16816(o[n + 1], pb0, pb2, b2, b3);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        if (threadIdx.x == 0 && i + NS < n_tiles) {
-            mbar_wait(bar_empty + 8 * s, (i / NS) & 1, p.dev_code);
-            issue_tile(i + NS);
+        if (threadIdx.x == 0 && i + NS < n_tiles && *sm_abort == 0) {
+            // a warp that gave up on this stage set the abort flag before releasing it
+            if (!mbar_wait_abortable(bar_empty + 8 * s, (i / NS) & 1, p.spin_limit, sm_abort)) {
+                record_code(p.dev_code, kDevCodeTimeout);
+                *sm_abort = 1;
+            } else if (*sm_abort == 0) {
+                issue_tile(i + NS);
+            }
         }
     }
     if (cur >= 0) finish_pair(cur, cur_lo, cur_hi, true);
+    // after an abort the last NS tiles issued (one per stage) may still be landing
+    if (threadIdx.x == 0 && *sm_abort != 0)
+        for (int i = max(0, last_issued - NS + 1); i <= last_issued; ++i)
+            mbar_wait_ok(bar_full + 8 * (i % NS), (i / NS) & 1, p.spin_limit);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
@@ -707,6 +749,7 @@ cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream, bool *used)
         configured[dev] = true;
     }
     DecodeParams q = p;
+    if (q.spin_limit == 0) q.spin_limit = kMbarSpinLimit;
     q.NT = p.cap > 0 ? (p.cap + PL::TK - 1) / PL::TK : 1;
     const long long T_all = (long long)q.P * q.NT;
     long long C = T_all < p.n_sm ? T_all : p.n_sm;

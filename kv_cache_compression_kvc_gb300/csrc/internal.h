@@ -59,6 +59,8 @@ struct DecodeParams {
     uint8_t head_of[256];
     int32_t kv_settled;          // cache slots and lengths final before the previous launch began
     int32_t balance;             // split the tiles by the lengths (not by capacity)
+    uint32_t spin_limit;         // polls before a bounded wait gives up (0: the default)
+    int32_t starve;              // test hook: issue no cache loads, so the first wait runs out
     float scale_log2;            // scale * log2(e)
     float *out;                  // [B][Hq][D]
     float *logits;               // nullable, [B*Hq][logits_stride]

@@ -21,6 +21,7 @@ KVC_F32, KVC_BF16 = 0, 1
 KVC_APPEND_TAIL, KVC_APPEND_RING, KVC_APPEND_FREE_SLOT = 0, 1, 2
 KVC_DECODE_KV_SETTLED = 1
 KVC_DECODE_BALANCE = 2
+KVC_DECODE_TEST_STARVE = 0x80000000
 STATUS_NAMES = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_SHAPE", 3: "KVC_ERR_ALIGN",
                 4: "KVC_ERR_CAPACITY", 5: "KVC_ERR_CUDA", 6: "KVC_ERR_WORKSPACE",
                 7: "KVC_ERR_DEVICE"}
@@ -648,6 +649,17 @@ def kvc_h2o_prefill_select_gqa(q: torch.Tensor, k_prompt: torch.Tensor, *, seq_l
     """q [B, Hq, N, D]; k_prompt [B, Hkv, cap, D] -> (idx [B, Hkv, n_keep], score [B, Hkv, n_keep])."""
     c = cache_view(k_prompt)
     B, Hq = q.shape[0], q.shape[1]
+    # the library reads q as a contiguous [batch][Hq][seq_len][d_head] array of the prompt's type
+    # and writes batch * Hkv * seq_len floats to s_full: check both before handing over pointers
+    if q.dim() != 4 or not q.is_contiguous() or q.dtype != k_prompt.dtype or \
+            tuple(q.shape) != (c.batch, Hq, int(seq_len), c.d_head):
+        raise ValueError(f"q must be a contiguous {k_prompt.dtype} tensor "
+                         f"[{c.batch}, n_heads_q, {seq_len}, {c.d_head}], got "
+                         f"{q.dtype} {tuple(q.shape)}")
+    if s_full is not None and (s_full.dtype != torch.float32 or not s_full.is_contiguous() or
+                               tuple(s_full.shape) != (c.batch, c.n_heads_kv, int(seq_len))):
+        raise ValueError(f"s_full must be a contiguous float32 tensor "
+                         f"[{c.batch}, {c.n_heads_kv}, {seq_len}]")
     n_keep = min(seq_len, K_hh + L_local)
     if idx_out is None:
         idx_out = torch.empty((B, c.n_heads_kv, n_keep), dtype=torch.int32, device=q.device)

@@ -21,8 +21,21 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Scratch for one call.  The oracle has no error path for a failed allocation: it stops the
+ * process with a message rather than compute from a null pointer.                            */
+static void *orc_alloc(size_t bytes)
+{
+    void *p = malloc(bytes > 0 ? bytes : 1);
+    if (p == NULL) {
+        fprintf(stderr, "kvc oracle: out of host memory (%zu bytes)\n", bytes);
+        abort();
+    }
+    return p;
+}
 
 /* ------------------------------------------------------------------------------------------ */
 /* KV memory model.  [KVC] "O gargalo de memória do KV Cache em contextos longos", equation
@@ -54,7 +67,7 @@ int orc_pyramid_budgets(int n_layers, int64_t b_target, int64_t ratio_num, int64
     const int64_t Q = (ratio_num + ratio_den) * nl1;
     const int64_t base_num = 2 * b_target * ratio_den * nl1;                 /* B_base * Q    */
     const int64_t delta_num = 2 * b_target * (ratio_num - ratio_den);        /* dB * Q/(N_L-1) */
-    int64_t *rem = (int64_t *)malloc(sizeof(int64_t) * (size_t)n_layers);
+    int64_t *rem = (int64_t *)orc_alloc(sizeof(int64_t) * (size_t)n_layers);
     int64_t total = 0;
     for (int l = 0; l < n_layers; ++l) {
         const int64_t num = base_num + delta_num * (nl1 - l);               /* B_l * Q      */
@@ -107,7 +120,7 @@ void orc_attend(int n, int D, double scale, const double *q, const double *K, co
         if (lse) *lse = -INFINITY;
         return;
     }
-    double *l = (double *)malloc(sizeof(double) * (size_t)n);
+    double *l = (double *)orc_alloc(sizeof(double) * (size_t)n);
     double m = -INFINITY;
     for (int j = 0; j < n; ++j) {
         double acc = 0.0;
@@ -166,13 +179,13 @@ void orc_stream_decode(int64_t t, int S, int W, int D, double theta, double scal
                        double *out)
 {
     const size_t cap = (size_t)(S + W + 1);
-    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * cap);
-    int64_t *cpos = (int64_t *)malloc(sizeof(int64_t) * cap);
+    int64_t *tok = (int64_t *)orc_alloc(sizeof(int64_t) * cap);
+    int64_t *cpos = (int64_t *)orc_alloc(sizeof(int64_t) * cap);
     int64_t qpos;
     const int n = orc_stream_window(t, S, W, tok, cpos, &qpos);
-    double *Kr = (double *)malloc(sizeof(double) * (size_t)n * D);
-    double *Vs = (double *)malloc(sizeof(double) * (size_t)n * D);
-    double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+    double *Kr = (double *)orc_alloc(sizeof(double) * (size_t)n * D);
+    double *Vs = (double *)orc_alloc(sizeof(double) * (size_t)n * D);
+    double *qr = (double *)orc_alloc(sizeof(double) * (size_t)D);
     for (int j = 0; j < n; ++j) {
         orc_rope(D, theta, cpos[j], hist_k + (size_t)tok[j] * D, Kr + (size_t)j * D);
         memcpy(Vs + (size_t)j * D, hist_v + (size_t)tok[j] * D, sizeof(double) * (size_t)D);
@@ -194,11 +207,11 @@ void orc_stream_decode_alibi(int64_t t, int S, int W, int D, double slope, doubl
                              double *out, double *logits, double *lse)
 {
     const size_t cap = (size_t)(S + W + 1);
-    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * cap);
-    int64_t *cpos = (int64_t *)malloc(sizeof(int64_t) * cap);
+    int64_t *tok = (int64_t *)orc_alloc(sizeof(int64_t) * cap);
+    int64_t *cpos = (int64_t *)orc_alloc(sizeof(int64_t) * cap);
     int64_t qpos;
     const int n = orc_stream_window(t, S, W, tok, cpos, &qpos);
-    double *l = (double *)malloc(sizeof(double) * (size_t)n);
+    double *l = (double *)orc_alloc(sizeof(double) * (size_t)n);
     double m = -INFINITY;
     for (int j = 0; j < n; ++j) {
         double acc = 0.0;
@@ -242,7 +255,7 @@ void orc_topk_ascending(int n, int k, const double *score, int32_t *idx)
 {
     if (k > n) k = n;
     if (k <= 0) return;
-    orc_scored *e = (orc_scored *)malloc(sizeof(orc_scored) * (size_t)n);
+    orc_scored *e = (orc_scored *)orc_alloc(sizeof(orc_scored) * (size_t)n);
     for (int i = 0; i < n; ++i) { e[i].v = score[i]; e[i].i = i; }
     qsort(e, (size_t)n, sizeof(orc_scored), orc_cmp_desc);
     for (int j = 0; j < k; ++j) idx[j] = e[j].i;
@@ -265,7 +278,7 @@ void orc_topk_ascending(int n, int k, const double *score, int32_t *idx)
 void orc_snapkv_obs_scores(int L_obs, int N, int D, double scale, const double *Qobs,
                            const double *K, double *s)
 {
-    double *row = (double *)malloc(sizeof(double) * (size_t)N);
+    double *row = (double *)orc_alloc(sizeof(double) * (size_t)N);
     for (int i = 0; i < N; ++i) s[i] = 0.0;
     for (int t = 0; t < L_obs; ++t) {
         const int p = N - L_obs + t;            /* text position of this query */
@@ -311,9 +324,9 @@ int orc_snapkv_select(int G, int L_obs, int N, int D, int pool_k, int budget, do
         budget < L_obs)
         return -1;
     const int n = N - L_obs;
-    double *s = (double *)malloc(sizeof(double) * (size_t)G * N);
-    double *p = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
-    double *score = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double *s = (double *)orc_alloc(sizeof(double) * (size_t)G * N);
+    double *p = (double *)orc_alloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double *score = (double *)orc_alloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     for (int g = 0; g < G; ++g)
         orc_snapkv_obs_scores(L_obs, N, D, scale, Qobs + (size_t)g * L_obs * D, K,
                               s + (size_t)g * N);
@@ -355,7 +368,7 @@ int orc_snapkv_stage_f32(int G, int n_prefix, int pool_k, int L_obs, int budget,
         return N;
     }
     const int r = (pool_k - 1) / 2;
-    double *score = (double *)malloc(sizeof(double) * (size_t)(n_prefix > 0 ? n_prefix : 1));
+    double *score = (double *)orc_alloc(sizeof(double) * (size_t)(n_prefix > 0 ? n_prefix : 1));
     for (int i = 0; i < n_prefix; ++i) {
         float best = -INFINITY;
         for (int g = 0; g < G; ++g) {
@@ -386,7 +399,7 @@ int orc_snapkv_stage_f32(int G, int n_prefix, int pool_k, int L_obs, int budget,
 void orc_h2o_prompt_scores(int N, int D, double scale, const double *Q, const double *K,
                            double *s)
 {
-    double *row = (double *)malloc(sizeof(double) * (size_t)N);
+    double *row = (double *)orc_alloc(sizeof(double) * (size_t)N);
     for (int j = 0; j < N; ++j) s[j] = 0.0;
     for (int t = 0; t < N; ++t) {
         double m = -INFINITY;
@@ -410,7 +423,7 @@ void orc_h2o_prompt_scores(int N, int D, double scale, const double *Q, const do
 void orc_h2o_prompt_scores_group(int G, int N, int D, double scale, const double *Q,
                                  const double *K, double *s)
 {
-    double *sg = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double *sg = (double *)orc_alloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     for (int j = 0; j < N; ++j) s[j] = 0.0;
     for (int g = 0; g < G; ++g) {
         orc_h2o_prompt_scores(N, D, scale, Q + (size_t)g * N * D, K, sg);
@@ -445,7 +458,7 @@ int orc_h2o_step(int n_slots, int D, double scale, const double *q, const double
                  const double *V, const int64_t *pos, double *s, int64_t t, int L_local,
                  int budget, double *out, double *alpha)
 {
-    double *l = (double *)malloc(sizeof(double) * (size_t)(n_slots > 0 ? n_slots : 1));
+    double *l = (double *)orc_alloc(sizeof(double) * (size_t)(n_slots > 0 ? n_slots : 1));
     double lse;
     orc_attend(n_slots, D, scale, q, K, V, out, l, &lse);
     for (int j = 0; j < n_slots; ++j) {
@@ -473,7 +486,7 @@ int orc_h2o_step_group(int G, int n_slots, int D, double scale, const double *q,
                        const double *K, const double *V, const int64_t *pos, double *s,
                        int64_t t, int L_local, int budget, double *out)
 {
-    double *l = (double *)malloc(sizeof(double) * (size_t)(n_slots > 0 ? n_slots : 1));
+    double *l = (double *)orc_alloc(sizeof(double) * (size_t)(n_slots > 0 ? n_slots : 1));
     for (int g = 0; g < G; ++g) {
         double lse;
         orc_attend(n_slots, D, scale, q + (size_t)g * D, K, V, out + (size_t)g * D, l, &lse);
@@ -529,7 +542,7 @@ int orc_block_step(int Hq, int Hkv, int D, int n_tok, int bs, double scale, cons
 {
     const int G = Hq / Hkv;
     const int nb = (n_tok + bs - 1) / bs;
-    double *l = (double *)malloc(sizeof(double) * (size_t)(n_tok > 0 ? n_tok : 1));
+    double *l = (double *)orc_alloc(sizeof(double) * (size_t)(n_tok > 0 ? n_tok : 1));
     for (int h = 0; h < Hq; ++h) {
         const int kh = h / G;
         double lse;
@@ -572,12 +585,12 @@ void orc_duo_decode(int retrieval, int64_t t, int S, int W, int D, double scale,
         return;
     }
     const size_t cap = (size_t)(S + W + 1);
-    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * cap);
-    int64_t *cpos = (int64_t *)malloc(sizeof(int64_t) * cap);
+    int64_t *tok = (int64_t *)orc_alloc(sizeof(int64_t) * cap);
+    int64_t *cpos = (int64_t *)orc_alloc(sizeof(int64_t) * cap);
     int64_t qpos;
     const int n = orc_stream_window(t, S, W, tok, cpos, &qpos);
-    double *K = (double *)malloc(sizeof(double) * (size_t)n * D);
-    double *V = (double *)malloc(sizeof(double) * (size_t)n * D);
+    double *K = (double *)orc_alloc(sizeof(double) * (size_t)n * D);
+    double *V = (double *)orc_alloc(sizeof(double) * (size_t)n * D);
     for (int j = 0; j < n; ++j) {
         memcpy(K + (size_t)j * D, hist_k + (size_t)tok[j] * D, sizeof(double) * (size_t)D);
         memcpy(V + (size_t)j * D, hist_v + (size_t)tok[j] * D, sizeof(double) * (size_t)D);
@@ -612,7 +625,7 @@ int orc_block_prompt_select(int H, int N, int bs, const double *s, int budget_bl
                             int recent_blocks, double *score_blk, int32_t *keep)
 {
     const int nblk = (N + bs - 1) / bs;
-    double *sc = (double *)malloc(sizeof(double) * (size_t)(nblk > 0 ? nblk : 1));
+    double *sc = (double *)orc_alloc(sizeof(double) * (size_t)(nblk > 0 ? nblk : 1));
     for (int i = 0; i < nblk; ++i) sc[i] = 0.0;
     for (int h = 0; h < H; ++h)
         for (int t = 0; t < N; ++t) sc[t / bs] += s[(size_t)h * N + t];

@@ -447,3 +447,8 @@ def test_h2o_prompt_select_grouped_query(dtype, D, G):
             assert np.array_equal(oracle.h2o_prompt_select(sf[b, kh].astype(np.float64), L_local,
                                                            K_hh), ix[b, kh]), "stage-exact"
             assert np.array_equal(sc[b, kh], sf[b, kh][ix[b, kh]])
+            # end to end against the oracle's own selection: the recent quota exactly, the heavy
+            # hitters except where the oracle scores tie within the band of the K_hh-th
+            ref_idx = oracle.h2o_prompt_select(ref, L_local, K_hh)
+            assert list(ix[b, kh][K_hh:]) == list(ref_idx[K_hh:]) == list(range(N - L_local, N))
+            topk_sets_agree(ix[b, kh][:K_hh], ref_idx[:K_hh], ref[:N - L_local], K_hh)
