@@ -95,6 +95,35 @@ def test_snapkv_select_tensor_core_shapes(B, Hq, Hkv, D, N, L_obs, budget):
     _check_snapkv(q, K, N, L_obs, budget, 5, 1 / math.sqrt(D), kvc)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,D,N,L_obs,budget", [
+    (1, 8, 2, 128, 2500, 32, 300),      # one row block of 128 rows per KV head
+    (2, 8, 2, 64, 3000, 64, 500),       # two row blocks (heads of 64 rows), d_head 64
+    (8, 16, 8, 128, 700, 32, 150),      # 64 pairs, few key chunks
+    (1, 4, 1, 128, 40000, 32, 4000),    # one pair, many chunks per pass
+])
+def test_snapkv_tensor_core_repeated_on_one_workspace(B, Hq, Hkv, D, N, L_obs, budget):
+    """bf16 windows whose heads fill whole 128-row blocks (the column-sum pass walks each block's
+    key range backwards): three calls in a row on one workspace give the same bits, and the
+    selection matches the oracle as for the other shapes."""
+    dev = cuda_or_skip()
+    kvc = lib()
+    q = I.randn((B, Hq, L_obs, D), 400 + N, dev, torch.bfloat16)
+    K = I.randn((B, Hkv, N, D), 401 + N, dev, torch.bfloat16)
+    ws = kvc._zeroed_workspace(kvc.kvc_snapkv_select_workspace_bytes(B, Hq, Hkv, D, N, L_obs),
+                               dev)
+    runs = []
+    for _ in range(3):
+        scores = torch.empty((B, Hq, N - L_obs), device=dev)
+        idx = kvc.kvc_snapkv_select(q, K, seq_len=N, L_obs=L_obs, budget=budget,
+                                    scale=1 / math.sqrt(D), scores_out=scores, ws=ws)
+        assert kvc.kvc_device_status() == 0
+        runs.append((idx.cpu(), scores.cpu()))
+    for idx, scores in runs[1:]:
+        assert torch.equal(idx, runs[0][0]) and torch.equal(scores, runs[0][1])
+    pairs = [(0, 0), (B - 1, Hkv - 1)]
+    _check_snapkv(q, K, N, L_obs, budget, 5, 1 / math.sqrt(D), kvc, pairs=pairs)
+
+
 def test_snapkv_tiny_workload_bf16():
     dev = cuda_or_skip()
     kvc = lib()
