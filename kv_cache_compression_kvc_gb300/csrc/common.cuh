@@ -190,6 +190,15 @@ __device__ __forceinline__ void pdl_trigger()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Release / acquire ticket on a pair's counter (one thread, after a block barrier): the block's
+// partial state is visible to whichever block takes the last ticket.
+__device__ __forceinline__ int ticket_acq_rel(int *p)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ float ex2(float x)
 {
     float y;

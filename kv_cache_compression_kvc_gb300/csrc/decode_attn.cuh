@@ -443,7 +443,64 @@ decode_attn_kernel(const DecodeParams p)
     int cur_slots = 0;
     int cur_li = -1;           // whose length cur_slots holds (paged: the pairs of a sequence share it)
 
-    auto start_pair = [&](int q) {
+    // The loads a pair starts with -- its query rows and, with the factored rotation, the table
+    // rows of the lane's key offsets -- are issued before the previous pair's merge, whose
+    // barriers and ticket then hide their latency (the old pair's q and rotation registers are
+    // free by then).
+    constexpr int QW = VW * (int)sizeof(T) / 4;       // 32-bit words of a lane's half-row
+    constexpr int FU = FACT ? UNR : 1;
+    constexpr int FR = FACT ? P2 / 2 : 1;
+    struct PairFetch {
+        uint32_t qa[G][QW], qc[G][QW];                // q: first and second half, raw words
+        float4 rc[FU][FR], rs[FU][FR];                // factored rotation: cosines, sines
+    };
+    auto load_words = [](const T *src, uint32_t (&w)[QW]) {
+        if constexpr (QW == 4) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(src);
+            w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+        } else {
+            static_assert(QW == 2, "lane vector of 8 or 16 bytes");
+            const uint2 x = *reinterpret_cast<const uint2 *>(src);
+            w[0] = x.x; w[1] = x.y;
+        }
+    };
+    auto words_to_floats = [](const uint32_t (&w)[QW], float *f) {
+#pragma unroll
+        for (int i = 0; i < QW; ++i) {
+            if constexpr (sizeof(T) == 4) {
+                f[i] = __uint_as_float(w[i]);
+            } else {
+                f[2 * i] = bf16_lo(w[i]);
+                f[2 * i + 1] = bf16_hi(w[i]);
+            }
+        }
+    };
+    auto fetch_pair = [&](int q) -> PairFetch {
+        PairFetch f;
+        int b, kh;
+        pair_bk(q, b, kh);
+        const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)kh * G) * D;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            load_words(qb + (size_t)g * D + d0, f.qa[g]);
+            load_words(qb + (size_t)g * D + HALF + d0, f.qc[g]);
+        }
+        if constexpr (FACT) {
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int rk = TK - 1 - (warp * KPW * UNR + ks + u * KPW);
+                const float *row = p.cos_sin + (size_t)rk * D;
+#pragma unroll
+                for (int i2 = 0; i2 < P2; i2 += 2) {
+                    f.rc[u][i2 / 2] = __ldg(reinterpret_cast<const float4 *>(row + d0 + 2 * i2));
+                    f.rs[u][i2 / 2] =
+                        __ldg(reinterpret_cast<const float4 *>(row + HALF + d0 + 2 * i2));
+                }
+            }
+        }
+        return f;
+    };
+    auto start_pair = [&](int q, const PairFetch &f) {
         cur = q;
         const int li = PAGED ? q / p.Hkv : q;
         if (li != cur_li) {
@@ -452,12 +509,11 @@ decode_attn_kernel(const DecodeParams p)
         }
         int b, kh;
         pair_bk(q, b, kh);
-        const T *qb = static_cast<const T *>(p.q) + ((size_t)b * p.Hq + (size_t)kh * G) * D;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             float a[VW], c[VW];
-            load_cached<T, VW>(qb + (size_t)g * D + d0, a);
-            load_cached<T, VW>(qb + (size_t)g * D + HALF + d0, c);
+            words_to_floats(f.qa[g], a);
+            words_to_floats(f.qc[g], c);
 #pragma unroll
             for (int i = 0; i < P2; ++i) {
                 q1[g][i] = make_float2(a[2 * i] * p.scale_log2, a[2 * i + 1] * p.scale_log2);
@@ -473,13 +529,9 @@ decode_attn_kernel(const DecodeParams p)
         if constexpr (FACT) {
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
-                const int rk = TK - 1 - (warp * KPW * UNR + ks + u * KPW);
-                const float *row = p.cos_sin + (size_t)rk * D;
 #pragma unroll
                 for (int i2 = 0; i2 < P2; i2 += 2) {
-                    const float4 c4 = __ldg(reinterpret_cast<const float4 *>(row + d0 + 2 * i2));
-                    const float4 s4 =
-                        __ldg(reinterpret_cast<const float4 *>(row + HALF + d0 + 2 * i2));
+                    const float4 c4 = f.rc[u][i2 / 2], s4 = f.rs[u][i2 / 2];
                     const float2 cc[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
                     const float2 ss[2] = {make_float2(s4.x, s4.y), make_float2(s4.z, s4.w)};
 #pragma unroll
@@ -573,12 +625,13 @@ decode_attn_kernel(const DecodeParams p)
             }
         }
         if (nseg > 1 && seg_ok) {
-            __threadfence();
+            // the block barrier orders every thread's partial-state writes before thread 0's
+            // release; its acquire (and the barrier after it) orders the last block's reads of
+            // the other blocks' states after their writes
             __syncthreads();
-            if (threadIdx.x == 0) *sm_flag = (atomicAdd(&p.ws_cnt[q], 1) == nseg - 1);
+            if (threadIdx.x == 0) *sm_flag = (ticket_acq_rel(&p.ws_cnt[q]) == nseg - 1);
             __syncthreads();
             if (*sm_flag) {
-                __threadfence();
                 merge_pair_partials<G, D, kDecodeThreads>(p.ws_o, p.ws_ml, p.max_seg, q, nseg, p.out,
                                                     p.lse, rows0, sm_o, NW * G * D);
                 if (threadIdx.x == 0) p.ws_cnt[q] = 0;   // leave the ticket zeroed
@@ -592,8 +645,9 @@ decode_attn_kernel(const DecodeParams p)
         int q, j0;
         locate(i, q, j0);
         if (q != cur) {
+            const PairFetch pf = fetch_pair(q);
             if (cur >= 0) finish_pair(cur);
-            start_pair(q);
+            start_pair(q, pf);
         }
         if (!mbar_wait_abortable(bar_full + 8 * s, (i / NS) & 1, p.spin_limit, sm_abort)) {
             record_code(p.dev_code, kDevCodeTimeout);

@@ -117,14 +117,6 @@ struct MmaPlan {
     static constexpr int SMEM = 1024 + NS * STAGE_BYTES + BAR_BYTES + MERGE_BYTES + PREF_BYTES;
 };
 
-// Release / acquire ticket on a pair's counter (one thread, after a block barrier): the block's
-// partial state is visible to whichever block takes the last ticket.
-__device__ __forceinline__ int ticket_acq_rel(int *p)
-{
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
-    return old;
-}
 
 // Bulk copy global -> shared memory, completion counted in bytes on an mbarrier.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
