@@ -182,14 +182,16 @@ topk_rows_kernel(const float *score, int64_t score_stride, int n, int k, int tai
 // largest are selected as above.  The division comes after the max over the group: a correctly
 // rounded division by a positive constant is monotonic, so max_g(sum_g / PK) and
 // max_g(sum_g) / PK are the same float.  Radix digits are 10 bits wide (three passes cover the
-// bits in which pooled scores of one row differ), with one histogram per four warps.  A cluster of TKC_CL blocks shares the row.  Block c copies
-// the G column-sum rows of its slice into shared memory (cp.async, one round trip per
-// sub-chunk), pools them into order-preserving keys, and keeps the keys in shared memory.  Every
-// cross-block quantity -- the key range, each radix histogram, the per-block counts -- is pushed
-// with remote reductions into the shared memory of every block of the cluster, so after each
-// cluster barrier all blocks read the same totals locally and take the same decisions; a final
-// exchange of per-block counts gives each block the output offset of its slice, so indices still
-// come out ascending.
+// bits in which pooled scores of one row differ), with one histogram per four warps.  A cluster
+// of TKC_CL blocks shares the row.  Block c copies the G column-sum rows of its slice into
+// shared memory (16-byte cp.async where the rows allow, one round trip per sub-chunk), pools
+// them into order-preserving keys, and keeps the keys in shared memory.  The key range is pushed
+// with remote reductions into every block; for each radix pass every block writes its histogram
+// once, with vector remote stores, into the shared memory of block 0, which sums the eight,
+// finds the digit and writes the decision back into every block (two cluster barriers per pass,
+// 1024 words per block instead of a remote reduction per bin and block); a final exchange of
+// per-block counts gives each block the output offset of its slice, so indices still come out
+// ascending.
 constexpr int TKC_THREADS = 512;
 constexpr int TKC_WARPS = TKC_THREADS / 32;
 constexpr int TKC_CL = 8;              // blocks per row (portable cluster size)
@@ -217,10 +219,6 @@ __device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
     return a;
 }
-__device__ __forceinline__ void cl_red_add(uint32_t a, uint32_t v)
-{
-    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
 __device__ __forceinline__ void cl_red_min(uint32_t a, uint32_t v)
 {
     asm volatile("red.relaxed.cluster.shared::cluster.min.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
@@ -237,6 +235,16 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const float *src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const float *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cl_st_v4(uint32_t a, uint4 v)
+{
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -247,14 +255,20 @@ __device__ __forceinline__ void cp_async_wait_group()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// dynamic shared memory: seg keys, then two buffers of G rows of sub + PK - 1 pooling inputs
+// Pooling inputs are staged from the 16-byte boundary TKC_PAD columns before each sub-chunk:
+// a window row holds columns c0 - TKC_PAD .. c0 + sub + TKC_PAD - 1 (TKC_PAD >= (PK - 1) / 2).
+constexpr int TKC_PAD = 8;
+// dynamic shared memory: seg keys (seg a multiple of 4), two buffers of G window rows of
+// sub + 2 TKC_PAD inputs, then block 0's copy of every block's histogram [TKC_CL][TKC_BINS]
 template <int PK>
 __global__ void __launch_bounds__(TKC_THREADS)
 pool_topk_cluster_kernel(const float *s, int64_t s_row_stride, int G, int n, int k, int tail,
                          int32_t *idx, int64_t idx_stride, int seg, int sub)
 {
+    static_assert((PK - 1) / 2 <= TKC_PAD, "pooling halo inside the staged window");
     __shared__ uint32_t whist[TKC_HGROUPS][TKC_BINS];
-    __shared__ uint32_t cl_hist[4][TKC_BINS];   // summed histogram of each pass (every block)
+    __shared__ uint32_t cl_tot[TKC_BINS];       // block 0: the cluster's histogram of the pass
+    __shared__ uint32_t cl_dec[2];              // the pass's digit and keys above it (from block 0)
     __shared__ uint32_t cl_lohi[2];             // key range of the row (every block)
     __shared__ uint32_t cl_cnt[TKC_CL][2];      // (keys > T, keys == T) per block (every block)
     __shared__ uint32_t sh_bin, sh_above, sh_lo, sh_hi;
@@ -267,8 +281,9 @@ pool_topk_cluster_kernel(const float *s, int64_t s_row_stride, int G, int n, int
     const uint32_t rank = cl_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int32_t *out = idx + (size_t)row * idx_stride;
-    float *pin = reinterpret_cast<float *>(skeys + seg);   // [2][G][sub + PK - 1]
-    const int wlen = sub + PK - 1;
+    const int wlen = sub + 2 * TKC_PAD;
+    float *pin = reinterpret_cast<float *>(skeys + seg);   // [2][G][wlen]
+    uint32_t *all_hist = skeys + seg + 2 * G * wlen;        // block 0: [TKC_CL][TKC_BINS]
 
     if (rank == 0)
         for (int j = tid; j < tail; j += TKC_THREADS) out[k + j] = n + j;
@@ -280,7 +295,6 @@ pool_topk_cluster_kernel(const float *s, int64_t s_row_stride, int G, int n, int
         for (int j = beg + tid; j < end; j += TKC_THREADS) out[j] = j;
         return;
     }
-    for (int j = tid; j < 4 * TKC_BINS; j += TKC_THREADS) (&cl_hist[0][0])[j] = 0u;
     if (tid == 0) {
         cl_lohi[0] = 0xffffffffu;
         cl_lohi[1] = 0u;
@@ -292,19 +306,28 @@ pool_topk_cluster_kernel(const float *s, int64_t s_row_stride, int G, int n, int
     // ---- stage the pooled, group-max keys of this block's slice --------------------------------
     uint32_t lo = 0xffffffffu, hi = 0u;
     const float *srow = s + (size_t)row * G * s_row_stride;
-    // inputs c0 - r .. c0 + sub + r - 1 of every head into buffer `buf` (zeros outside the row);
-    // the next sub-chunk's copies are in flight while this one is pooled
+    // columns c0 - TKC_PAD .. c0 + sub + TKC_PAD - 1 of every head into buffer `buf` (zeros
+    // outside the row), in 16-byte copies where the rows are 16-byte aligned (c0 is a multiple
+    // of four); the next sub-chunk's copies are in flight while this one is pooled
+    const bool vec = (s_row_stride % 4 == 0) && ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);
     auto issue = [&](int c0, int buf) {
         float *dst0 = pin + (size_t)buf * G * wlen;
-        for (int g = 0; g < G; ++g) {
+        const int nq = wlen / 4;
+        for (int x4 = tid; x4 < G * nq; x4 += TKC_THREADS) {
+            const int g = x4 / nq, x = (x4 - g * nq) * 4;
             const float *src = srow + (size_t)g * s_row_stride;
-            float *dst = dst0 + g * wlen;
-            for (int x = tid; x < wlen; x += TKC_THREADS) {
-                const int ix = c0 - r + x;
-                if (ix >= 0 && ix < n)
-                    cp_async4(smem_addr(dst + x), src + ix);
-                else
-                    dst[x] = 0.f;
+            float *dst = dst0 + g * wlen + x;
+            const int ix = c0 - TKC_PAD + x;
+            if (vec && ix >= 0 && ix + 3 < n) {
+                cp_async16(smem_addr(dst), src + ix);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (ix + e >= 0 && ix + e < n)
+                        cp_async4(smem_addr(dst + e), src + ix + e);
+                    else
+                        dst[e] = 0.f;
+                }
             }
         }
         cp_async_commit();
@@ -323,7 +346,7 @@ pool_topk_cluster_kernel(const float *s, int64_t s_row_stride, int G, int n, int
         for (int i = c0 + tid; i < c1; i += TKC_THREADS) {
             float best = -INFINITY;
             for (int g = 0; g < G; ++g) {
-                const float *w = pbuf + g * wlen + (i - c0);   // inputs i - r .. i + r
+                const float *w = pbuf + g * wlen + (i - c0) + TKC_PAD - r;   // inputs i-r .. i+r
                 float acc = 0.f;
 #pragma unroll
                 for (int j = 0; j < PK; ++j) acc = __fadd_rn(acc, w[j]);
@@ -374,46 +397,64 @@ pool_topk_cluster_kernel(const float *s, int64_t s_row_stride, int G, int n, int
             if ((u & mask) == prefix) atomicAdd(&mine[(u >> shift) & dmask], 1u);
         }
         __syncthreads();
-        // this block's bin b goes to every block of the cluster
-        for (int bin = tid; bin < TKC_BINS; bin += TKC_THREADS) {
-            uint32_t c = 0;
+        // this block's histogram, once, into block 0's copy (four bins per vector store)
+        static_assert(TKC_BINS == 4 * 256 && TKC_THREADS >= 256, "one vector store per thread");
+        if (tid < TKC_BINS / 4) {
+            uint4 c = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int h = 0; h < TKC_HGROUPS; ++h) c += whist[h][bin];
-            if (c)
-#pragma unroll
-                for (int dst = 0; dst < TKC_CL; ++dst)
-                    cl_red_add(cl_map(&cl_hist[pass][bin], (uint32_t)dst), c);
+            for (int h = 0; h < TKC_HGROUPS; ++h) {
+                c.x += whist[h][4 * tid];
+                c.y += whist[h][4 * tid + 1];
+                c.z += whist[h][4 * tid + 2];
+                c.w += whist[h][4 * tid + 3];
+            }
+            cl_st_v4(cl_map(all_hist + rank * TKC_BINS + 4 * tid, 0u), c);
         }
         cl_sync();
-        if (warp == 0) {
-            // lane L owns bins 32L .. 32L+31; keys in bins above lane L's range
-            constexpr int PER = TKC_BINS / 32;
-            uint32_t c[PER], tot = 0;
+        if (rank == 0) {
+            for (int bin = tid; bin < TKC_BINS; bin += TKC_THREADS) {
+                uint32_t c = 0;
 #pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                c[j] = cl_hist[pass][lane * PER + j];
-                tot += c[j];
+                for (int b = 0; b < TKC_CL; ++b) c += all_hist[b * TKC_BINS + bin];
+                cl_tot[bin] = c;
             }
-            uint32_t incl = tot;
+            __syncthreads();
+            if (warp == 0) {
+                // lane L owns bins 32L .. 32L+31; keys in bins above lane L's range
+                constexpr int PER = TKC_BINS / 32;
+                uint32_t c[PER], tot = 0;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
-                if (lane + o < 32) incl += x;
-            }
-            uint32_t cum = incl - tot;
-#pragma unroll
-            for (int j = PER - 1; j >= 0; --j) {
-                if (cum < need && cum + c[j] >= need) {
-                    sh_bin = (uint32_t)(lane * PER + j);
-                    sh_above = cum;
+                for (int j = 0; j < PER; ++j) {
+                    c[j] = cl_tot[lane * PER + j];
+                    tot += c[j];
                 }
-                cum += c[j];
+                uint32_t incl = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
+                    if (lane + o < 32) incl += x;
+                }
+                uint32_t cum = incl - tot;
+#pragma unroll
+                for (int j = PER - 1; j >= 0; --j) {
+                    if (cum < need && cum + c[j] >= need) {
+                        sh_bin = (uint32_t)(lane * PER + j);
+                        sh_above = cum;
+                    }
+                    cum += c[j];
+                }
+            }
+            __syncthreads();
+            // the decision goes to every block of the cluster
+            if (tid < TKC_CL) {
+                cl_st(cl_map(&cl_dec[0], (uint32_t)tid), sh_bin);
+                cl_st(cl_map(&cl_dec[1], (uint32_t)tid), sh_above);
             }
         }
-        __syncthreads();
-        prefix |= sh_bin << shift;
+        cl_sync();
+        prefix |= cl_dec[0] << shift;
         mask |= dmask << shift;
-        need -= sh_above;
+        need -= cl_dec[1];
     }
     const uint32_t T = prefix;
 
@@ -493,9 +534,10 @@ cudaError_t launch_pool_topk_typed(const float *s, int64_t s_row_stride, int row
                                    int k, int tail, int32_t *idx, int64_t idx_stride,
                                    cudaStream_t stream, bool *used)
 {
-    const int seg = (n + TKC_CL - 1) / TKC_CL;
+    const int seg = ((n + TKC_CL - 1) / TKC_CL + 3) & ~3;   // multiple of 4 (aligned windows)
     const int sub = 2 * TKC_THREADS;            // pooled keys per sub-chunk (two per thread)
-    const size_t dyn = (size_t)seg * 4 + 2 * (size_t)G * (sub + PK - 1) * 4;
+    const size_t dyn = (size_t)seg * 4 + 2 * (size_t)G * (sub + 2 * TKC_PAD) * 4 +
+                       (size_t)TKC_CL * TKC_BINS * 4;
     if (dyn > (size_t)TKC_SMEM) return cudaSuccess;   // too long: the two-kernel path runs
     static bool configured[64] = {};
     int dev = 0;
