@@ -13,10 +13,11 @@
 // block to finish it (atomic ticket, no waiting) merges the states by log-sum-exp.
 //
 // Data movement.  K and V tiles (TK slots x d_head; 16 KB of keys per tile) stream from HBM into
-// an NS-stage shared-memory ring with cp.async.bulk issued by one thread, completion tracked by
-// mbarriers (transaction bytes); the block's eight warps compute from shared memory and release
-// each stage through a second mbarrier, after which the issuing thread refills it NS tiles
-// ahead.  Bytes in flight per SM come from the ring depth and the blocks per SM, not registers.
+// an NS-stage shared-memory ring with cp.async.bulk, completion tracked by mbarriers
+// (transaction bytes); the block's eight warps compute from shared memory and release each stage
+// through a second mbarrier, after which warp 0 refills it NS tiles ahead, the tile's copies
+// dealt out over its lanes.  Bytes in flight per SM come from the ring depth and the blocks per
+// SM, not registers.
 //
 // Arithmetic.  fp32 throughout, with Blackwell's packed fp32x2 FMA (two lanes of a float2 per
 // instruction) for the q.k dot products and the p*v accumulation.  A key row is read by
@@ -269,6 +270,39 @@ decode_attn_kernel(const DecodeParams p)
             j0 = (int)(t % p.NT) * TK;
         }
     };
+    // Walking this block's tiles in order: one division at the start, then the pair and first
+    // slot advance by one tile at a time.  DuoAttention's streaming pairs come first in its list,
+    // so it keeps locate(); so does the per-key rotation, whose registers are all taken.
+    constexpr bool CURSOR = !DUO && RM != 1;
+    struct TileCursor {
+        int i, q, j0;
+    };
+    auto cursor_start = [&]() -> TileCursor {
+        TileCursor c{0, 0, 0};
+        if constexpr (CURSOR) {
+            c.q = (int)(t_begin / p.NT);
+            c.j0 = (int)(t_begin % p.NT) * TK;
+        }
+        return c;
+    };
+    auto cursor_get = [&](const TileCursor &c, int &q, int &j0) {
+        if constexpr (!CURSOR) {
+            locate(c.i, q, j0);
+        } else {
+            q = c.q;
+            j0 = c.j0;
+        }
+    };
+    auto cursor_next = [&](TileCursor &c) {
+        ++c.i;
+        if constexpr (CURSOR) {
+            c.j0 += TK;
+            if (c.j0 >= p.NT * TK) {
+                c.j0 = 0;
+                ++c.q;
+            }
+        }
+    };
     // first tile and tile count of pair q in the even split (DuoAttention: retrieval pairs;
     // a streaming pair is one block's alone)
     auto pair_first = [&](int q) -> long long { return (long long)q * p.NT; };
@@ -303,14 +337,24 @@ decode_attn_kernel(const DecodeParams p)
         return p.n_valid;
     };
 
-    // ---- tile loader: thread 0 issues the bulk copies of tile i into stage i % NS ----------
+    // ---- tile loader: warp 0 issues the bulk copies of tile i into stage i % NS ------------
+    // Every lane of warp 0 walks the same tiles; a tile's copies (its K and V runs, the RoPE base
+    // row, or the page blocks it touches) are dealt out over the lanes, so issuing them costs
+    // one copy's issue time rather than the sum (each bulk copy takes a few hundred cycles to
+    // issue: 360 ns per tile for two copies, 790 ns for a paged tile's four, against ~500 ns of
+    // the issuing warp's own arithmetic), and lane 0 arrives on the stage's barrier with the byte
+    // count.  DuoAttention (two contiguous copies per tile) keeps one issuing thread, which
+    // leaves warp 0's other lanes free to start the next tile while it refills (97 % against
+    // 92.5 % of the HBM peak issued by the warp).
+    constexpr bool WARP_ISSUE = !DUO;
+    const bool LOADER = WARP_ISSUE ? warp == 0 : threadIdx.x == 0;
     const bool dense = (p.ss == D);
-    // The issuing thread keeps the slot count of the pair it is loading: one global read per
-    // pair, not one per tile on the critical path of every copy.
+    // The loader keeps the slot count of the pair it is loading: one global read per pair, not
+    // one per tile on the critical path of every copy.
     int iss_q = -1, iss_slots = 0;
     // Paged: it also keeps a window of kTabCache page-table entries of the sequence it is
-    // loading in shared memory, fetched together with cp.async (one round trip per window, not
-    // one per block on the critical path of every copy).
+    // loading in shared memory, fetched together with cp.async, one entry per lane (one round
+    // trip per window, not one per block on the critical path of every copy).
     int tab_b = -1, tab_lo = 0, tab_cnt = 0;
     auto table_entry = [&](int b, int lb) -> int {
         if (b != tab_b || lb < tab_lo || lb >= tab_lo + tab_cnt) {
@@ -320,20 +364,24 @@ decode_attn_kernel(const DecodeParams p)
             tab_lo = lb - lb % kTabCache;
             tab_cnt = min(kTabCache, p.max_blocks - tab_lo);
             const int32_t *src = p.table + (size_t)b * p.max_blocks + tab_lo;
-            for (int k = 0; k < tab_cnt; ++k)
+            static_assert(kTabCache <= 32, "one table entry per lane");
+            if (lane < tab_cnt)
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
-                             :: "r"(sbase + 128 + 4 * k), "l"(src + k) : "memory");
+                             :: "r"(sbase + 128 + 4 * lane), "l"(src + lane) : "memory");
             asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncwarp();
         }
         return reinterpret_cast<const int32_t *>(smem + 128)[lb - tab_lo];
     };
-    int last_issued = -1;      // the issuing thread's last tile (the drain after an abort)
+    int last_issued = -1;      // the loader's last tile (the drain after an abort)
+    TileCursor iss_cur = cursor_start();
     auto issue_tile = [&](int i) {
         if (p.starve) return;  // test hook: no loads, no arrivals (the waits run out)
         last_issued = i;
         const int s = i % NS;
         int q, j0;
-        locate(i, q, j0);
+        cursor_get(iss_cur, q, j0);
+        cursor_next(iss_cur);
         if (q != iss_q) {
             // paged: the pairs of a sequence share its length
             if (!PAGED || iss_q < 0 || q / p.Hkv != iss_q / p.Hkv) iss_slots = pair_slots(q);
@@ -363,26 +411,32 @@ decode_attn_kernel(const DecodeParams p)
             vb = static_cast<const T *>(p.v) + base;
         }
         if (rows == 0) {
-            mbar_arrive(full);
+            if (lane == 0) mbar_arrive(full);
             return;
         }
-        mbar_arrive_expect_tx(full, (uint32_t)(2 * rows * D * EB + SM::kRotBytes));
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(2 * rows * D * EB + SM::kRotBytes));
+        // the tile's copies, dealt out over the lanes in order
+        int job = 0;
+        auto copy = [&](uint32_t dst, const void *src, uint32_t bytes) {
+            if (((WARP_ISSUE ? job : 0) & 31) == lane) bulk_g2s(dst, src, bytes, full);
+            ++job;
+        };
         if constexpr (FACT) {
             // |base| <= max(TK - 1, qpos) < n_pos (checked on the host)
             const int row = min(abs(qpos - j0 - (TK - 1)), p.n_pos - 1);
-            bulk_g2s(vdst + SM::kTileBytes, p.cos_sin + (size_t)row * D, D * 4, full);
+            copy(vdst + SM::kTileBytes, p.cos_sin + (size_t)row * D, D * 4);
         }
         // copy rows [r_a, r_b) of the tile's work items, physically contiguous from slot j_a
         auto copy_run = [&](int r_a, int r_b, int j_a) {
             if (r_b <= r_a) return;
             const uint32_t off = (uint32_t)((r_a - j0) * D * EB);
             if (dense) {
-                bulk_g2s(kdst + off, kb + (size_t)j_a * D, (r_b - r_a) * D * EB, full);
-                bulk_g2s(vdst + off, vb + (size_t)j_a * D, (r_b - r_a) * D * EB, full);
+                copy(kdst + off, kb + (size_t)j_a * D, (r_b - r_a) * D * EB);
+                copy(vdst + off, vb + (size_t)j_a * D, (r_b - r_a) * D * EB);
             } else {
                 for (int r = 0; r < r_b - r_a; ++r) {
-                    bulk_g2s(kdst + off + r * D * EB, kb + (size_t)(j_a + r) * p.ss, D * EB, full);
-                    bulk_g2s(vdst + off + r * D * EB, vb + (size_t)(j_a + r) * p.ss, D * EB, full);
+                    copy(kdst + off + r * D * EB, kb + (size_t)(j_a + r) * p.ss, D * EB);
+                    copy(vdst + off + r * D * EB, vb + (size_t)(j_a + r) * p.ss, D * EB);
                 }
             }
         };
@@ -398,13 +452,13 @@ decode_attn_kernel(const DecodeParams p)
                 const int n = min(j1 - r, p.bs - off);
                 int phys = table_entry(b, lb);
                 if (phys < 0 || phys >= p.n_pool) {
-                    record_code(p.dev_code, 9 /* KVC_DEV_BAD_BLOCK */);
+                    if (lane == 0) record_code(p.dev_code, 9 /* KVC_DEV_BAD_BLOCK */);
                     phys = 0;
                 }
                 const size_t src = (size_t)phys * p.bs * D + (size_t)off * D;
                 const uint32_t bytes = (uint32_t)n * (uint32_t)(D * EB);
-                bulk_g2s(kdst + doff, kh_k + src, bytes, full);
-                bulk_g2s(vdst + doff, kh_v + src, bytes, full);
+                copy(kdst + doff, kh_k + src, bytes);
+                copy(vdst + doff, kh_v + src, bytes);
                 doff += bytes;
                 r += n;
                 off = 0;
@@ -422,7 +476,7 @@ decode_attn_kernel(const DecodeParams p)
             }
         }
     };
-    if (threadIdx.x == 0)
+    if (LOADER)
         for (int i = 0; i < NS && i < n_tiles; ++i) issue_tile(i);
     if (p.kv_settled) {
         pdl_trigger();
@@ -640,10 +694,12 @@ decode_attn_kernel(const DecodeParams p)
         __syncthreads();   // the merge area is reused by the next pair
     };
 
+    TileCursor cmp_cur = cursor_start();
     for (int i = 0; i < n_tiles; ++i) {
         const int s = i % NS;
         int q, j0;
-        locate(i, q, j0);
+        cursor_get(cmp_cur, q, j0);
+        cursor_next(cmp_cur);
         if (q != cur) {
             const PairFetch pf = fetch_pair(q);
             if (cur >= 0) finish_pair(cur);
@@ -814,16 +870,22 @@ decode_attn_kernel(const DecodeParams p)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        if (threadIdx.x == 0 && i + NS < n_tiles && *sm_abort == 0) {
+        if (LOADER && i + NS < n_tiles) {
             // every warp has released stage s: refill it with tile i + NS (a warp that gave up
             // on this stage set the abort flag before it released it, so the refill never lands
-            // on a load still in flight)
-            if (!mbar_wait_abortable(bar_empty + 8 * s, (i / NS) & 1, p.spin_limit, sm_abort)) {
-                record_code(p.dev_code, kDevCodeTimeout);
-                *sm_abort = 1;
-            } else if (*sm_abort == 0) {
-                issue_tile(i + NS);
+            // on a load still in flight); lane 0 waits, the loader issues
+            int go = 0;
+            if (lane == 0 && *sm_abort == 0) {
+                if (!mbar_wait_abortable(bar_empty + 8 * s, (i / NS) & 1, p.spin_limit,
+                                         sm_abort)) {
+                    record_code(p.dev_code, kDevCodeTimeout);
+                    *sm_abort = 1;
+                } else {
+                    go = *sm_abort == 0;
+                }
             }
+            if (WARP_ISSUE) go = __shfl_sync(0xffffffffu, go, 0);
+            if (go) issue_tile(i + NS);
         }
     }
     if (cur >= 0) finish_pair(cur);
