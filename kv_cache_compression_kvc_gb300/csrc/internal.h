@@ -158,7 +158,9 @@ struct ScoreParams {
     float col_mult;              // 1/L_obs (mean) or 1 (sum)
     float *s_out;                // [B][Hq][n_cols]
     float *row_ml;               // workspace [B*Hkv][n_chunks][R][2]
-    float *row_lse2;             // workspace [B*Hkv][R] (log2 units)
+    float *row_lse2;             // workspace [B*Hkv][R rounded up to 128]: each row's log2-sum-exp
+                                 // (CUDA-core path: stride R; tensor-core path: negated, stride
+                                 // R rounded up to 128, the padding zeroed)
     int32_t n_chunks;
     int32_t chunk;
 };

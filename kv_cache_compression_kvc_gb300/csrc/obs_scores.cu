@@ -297,7 +297,7 @@ ScorePlan score_plan(int B, int Hkv, int G, int N, int L_obs, int n_sm, size_t b
     auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
     pl.off_ml = align(base_off);
     pl.off_lse = align(pl.off_ml + (size_t)pairs * n_chunks * R * 2 * sizeof(float));
-    pl.bytes = align(pl.off_lse + (size_t)pairs * R * sizeof(float));
+    pl.bytes = align(pl.off_lse + (size_t)pairs * (mtiles * KTILE) * sizeof(float));
     return pl;
 }
 

@@ -138,6 +138,25 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[4][32])
     }
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 32 columns, issued without waiting (tmem_wait_ld before the registers are read).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, float (&v)[32])
+{
+    uint32_t *r = reinterpret_cast<uint32_t *>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 // 64 columns (two 32-column loads, one wait).
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[2][32])
 {
@@ -158,7 +177,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[2][32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 // sum_j exp2(v[j] * scale + off[j]) over 32 values with packed fp32x2 FMA and adds (two
-// independent chains); `off` is one value for all (off_u) or per element (off_v, 8-byte aligned).
+// independent chains); `off` is one value for all (off_u) or per element (off_v, 16-byte aligned).
 __device__ __forceinline__ float exp2_sum32(const float *v, float scale, float off_u,
                                             const float *off_v)
 {
@@ -166,8 +185,9 @@ __device__ __forceinline__ float exp2_sum32(const float *v, float scale, float o
     float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
-        const float2 o0 = off_v ? *reinterpret_cast<const float2 *>(off_v + j) : make_float2(off_u, off_u);
-        const float2 o1 = off_v ? *reinterpret_cast<const float2 *>(off_v + j + 2) : make_float2(off_u, off_u);
+        const float4 o = off_v ? *reinterpret_cast<const float4 *>(off_v + j)
+                               : make_float4(off_u, off_u, off_u, off_u);
+        const float2 o0 = make_float2(o.x, o.y), o1 = make_float2(o.z, o.w);
         float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), s2, o0);
         float2 y = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), s2, o1);
         x.x = ex2(x.x);
@@ -204,6 +224,132 @@ __device__ __forceinline__ void set_sync(int set)
     asm volatile("bar.sync %0, 128;" ::"r"(2 + set) : "memory");
 }
 
+// Column sums over one block of rows r0 .. r0 + rows_blk - 1 (tensor-memory columns from tcol,
+// 64 per read, or 32 with LD32: half the registers) for this thread's key.  (g_cur, acc_g) carry the sum of the head in progress; a
+// finished head's sum (times col_mult) goes to out[head * out_stride + out_idx] when out_ok.
+// nlse: the rows' negated log2-sum-exp.  The head g_a and row-in-head rem of each 32-row chunk
+// advance incrementally (heads have at least 32 rows, or there is one head).
+template <bool LD32 = false>
+__device__ __forceinline__ void colsum_rows(const ScoreParams &p, int first_pos, uint32_t tcol,
+                                            int r0, int rows_blk, int key, bool mask_tile,
+                                            const float *nlse, float *out, int out_stride,
+                                            int out_idx, bool out_ok, int &g_cur, float &acc_g)
+{
+    int g_a = r0 / p.L_obs;
+    int rem = r0 - g_a * p.L_obs;
+    float vt[2][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c * 32 >= rows_blk) break;
+        // 64 columns per tensor-memory read (one wait for two chunks)
+        if (LD32) {
+            tmem_ld32_async(tcol + c * 32, vt[0]);
+            tmem_wait_ld();
+        } else if ((c & 1) == 0) tmem_ld64(tcol + c * 32, vt);
+        const float *v = vt[LD32 ? 0 : (c & 1)];
+        const int rows_here = min(32, rows_blk - c * 32);
+        const int split = min(rows_here, p.L_obs - rem);      // rows in head g_a
+        if (g_a != g_cur) {                                   // flush the finished head
+            if (out_ok) out[(size_t)g_cur * out_stride + out_idx] = acc_g * p.col_mult;
+            acc_g = 0.f;
+            g_cur = g_a;
+        }
+        // rows see keys up to their positions; the smallest in the chunk is its first row, or
+        // the next head's first window row past a head boundary
+        const bool mask_c = mask_tile && key > first_pos + (split < rows_here ? 0 : rem);
+        if (split == 32 && !mask_c) {
+            acc_g += exp2_sum32(v, p.scale_log2, 0.f, nlse + c * 32);
+        } else {
+            float s_a = 0.f, s_b = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                float pr = ex2(fmaf(v[j], p.scale_log2, nlse[c * 32 + j]));
+                if (mask_c) {
+                    const int w = j < split ? rem + j : j - split;   // row inside its head
+                    if (key > first_pos + w) pr = 0.f;
+                }
+                if (j < split) s_a += pr;
+                else if (j < rows_here) s_b += pr;
+            }
+            acc_g += s_a;
+            if (split < rows_here) {                          // into head g_a + 1
+                if (out_ok) out[(size_t)g_cur * out_stride + out_idx] = acc_g * p.col_mult;
+                g_cur = g_a + 1;
+                acc_g = s_b;
+            }
+        }
+        rem += 32;
+        if (rem >= p.L_obs) {
+            rem -= p.L_obs;
+            ++g_a;
+        }
+    }
+}
+
+// Row statistics of one 128-key tile for this thread's row (accumulator lanes = rows): the
+// logits past the row's position (or past the prompt) are masked, then the running (max, sum
+// of exp2) in log2 units is updated.
+__device__ __forceinline__ void rowstats_tile(uint32_t taddr, int k0, int pos, int N,
+                                              float scale_log2, float &m_run, float &z_run)
+{
+    // this row sees keys up to its own position: mask only where the tile reaches past it (or
+    // past the prompt)
+    const bool need_mask = k0 + TC_ROWS - 1 > pos || k0 + TC_ROWS > N;
+    float v[4][32];
+    tmem_ld128(taddr, v);
+    if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int key = k0 + c * 32 + j;
+                if (key > pos || key >= N) v[c][j] = -INFINITY;
+            }
+    }
+    const float mx = fmaxf(fmaxf(max32(v[0]), max32(v[1])), fmaxf(max32(v[2]), max32(v[3])));
+    const float m_new = fmaxf(m_run, mx * scale_log2);
+    const float z = (exp2_sum32(v[0], scale_log2, -m_new, nullptr) +
+                     exp2_sum32(v[1], scale_log2, -m_new, nullptr)) +
+                    (exp2_sum32(v[2], scale_log2, -m_new, nullptr) +
+                     exp2_sum32(v[3], scale_log2, -m_new, nullptr));
+    z_run = z_run * ex2(m_run - m_new) + z;
+    m_run = m_new;
+}
+
+// The same update for 64 keys k0 .. k0 + 63 (one tensor-memory read), with a lazy running max:
+// the exp2 values are summed relative to the running max as it stands, without finding the
+// keys' max first; only when that sum comes out above 2^32 (a logit more than 32 above the
+// running max, and always on a row's first visible keys, whose running max is still kNegBig)
+// is their max taken and the sum rescaled to it.  z_run is then a sum relative to m_run that
+// may exceed 1, which every (m, z) merge downstream handles as it stands.
+__device__ __forceinline__ void rowstats_half_lazy(uint32_t taddr, int k0, int pos, int N,
+                                                   float scale_log2, float &m_run, float &z_run)
+{
+    const bool need_mask = k0 + 63 > pos || k0 + 64 > N;
+    float v[2][32];
+    tmem_ld64(taddr, v);
+    if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int key = k0 + c * 32 + j;
+                if (key > pos || key >= N) v[c][j] = -INFINITY;
+            }
+    }
+    const float z = exp2_sum32(v[0], scale_log2, -m_run, nullptr) +
+                    exp2_sum32(v[1], scale_log2, -m_run, nullptr);
+    if (z <= 4294967296.f) {
+        z_run += z;
+        return;
+    }
+    const float m_new = fmaxf(m_run, fmaxf(max32(v[0]), max32(v[1])) * scale_log2);
+    const float zn = exp2_sum32(v[0], scale_log2, -m_new, nullptr) +
+                     exp2_sum32(v[1], scale_log2, -m_new, nullptr);
+    z_run = z_run * ex2(m_run - m_new) + zn;
+    m_run = m_new;
+}
+
 struct TcParams {
     ScoreParams sp;       // shapes, scale, outputs, workspace (see internal.h)
     int32_t n_mtiles;     // row tiles of 128 per (batch, KV head)    (pass 1)
@@ -212,6 +358,8 @@ struct TcParams {
     int32_t col_chunks;   // pass 2 with a resident row block: key-tile chunks per row block
     int32_t col_chunk_tiles;
     int32_t n_work;       // work items of the launch (blocks take them round-robin)
+    int32_t n_fp;         // resident tile pairs per (pair, chunk) (tile-pair kernel)
+    int32_t n_sup;        // units per (pair, chunk): resident pairs i and n_fp - 1 - i together
     int32_t *dev_code;
 };
 
@@ -475,60 +623,6 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
         const int et = q4 * 32 + lane;            // this thread's lane (row or key)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        // Column sums over one block of rows r0 .. r0 + rows_blk - 1 (tensor-memory columns from
-        // tcol) for this thread's key.  (g_cur, acc_g) carry the sum of the head in progress; a
-        // finished head's sum is written.  nlse: the rows' negated log2-sum-exp.  The head g_a
-        // and row-in-head rem of each 32-row chunk advance incrementally (heads have at least
-        // 32 rows, or there is one head).
-        auto colsum_rows = [&](uint32_t tcol, int r0, int rows_blk, int key, bool mask_tile,
-                               const float *nlse, float *s_base, int &g_cur, float &acc_g) {
-            int g_a = r0 / p.L_obs;
-            int rem = r0 - g_a * p.L_obs;
-            float vt[2][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c * 32 >= rows_blk) break;
-                // 64 columns per tensor-memory read (one wait for two chunks)
-                if ((c & 1) == 0) tmem_ld64(tcol + c * 32, vt);
-                const float *v = vt[c & 1];
-                const int rows_here = min(32, rows_blk - c * 32);
-                const int split = min(rows_here, p.L_obs - rem);      // rows in head g_a
-                if (g_a != g_cur) {                                   // flush the finished head
-                    if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
-                    acc_g = 0.f;
-                    g_cur = g_a;
-                }
-                // rows see keys up to their positions; the smallest in the chunk is its first
-                // row, or the next head's first window row past a head boundary
-                const bool mask_c = mask_tile && key > first_pos + (split < rows_here ? 0 : rem);
-                if (split == 32 && !mask_c) {
-                    acc_g += exp2_sum32(v, p.scale_log2, 0.f, nlse + c * 32);
-                } else {
-                    float s_a = 0.f, s_b = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        float pr = ex2(fmaf(v[j], p.scale_log2, nlse[c * 32 + j]));
-                        if (mask_c) {
-                            const int w = j < split ? rem + j : j - split;   // row inside its head
-                            if (key > first_pos + w) pr = 0.f;
-                        }
-                        if (j < split) s_a += pr;
-                        else if (j < rows_here) s_b += pr;
-                    }
-                    acc_g += s_a;
-                    if (split < rows_here) {                          // into head g_a + 1
-                        if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
-                        g_cur = g_a + 1;
-                        acc_g = s_b;
-                    }
-                }
-                rem += 32;
-                if (rem >= p.L_obs) {
-                    rem -= p.L_obs;
-                    ++g_a;
-                }
-            }
-        };
         long long g = 0;
         int k = 0;
         // MODE 2: this thread's resident row, its negated log2-sum-exp, and whose it is
@@ -557,30 +651,8 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     const int ab = (int)(gg % TC_NACC);
                     mbar_wait(bar_acc_full + 8 * ab, (int)(gg / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
-                    const int k0 = (it.t_begin + i) * TC_ROWS;
-                    // this row sees keys up to its own position: mask only where the tile
-                    // reaches past it (or past the prompt)
-                    const bool need_mask = k0 + TC_ROWS - 1 > pos || k0 + TC_ROWS > p.N;
-                    float v[4][32];
-                    tmem_ld128(tmem_base + ab * 128 + lane_off, v);
-                    if (need_mask) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int key = k0 + c * 32 + j;
-                                if (key > pos || key >= p.N) v[c][j] = -INFINITY;
-                            }
-                    }
-                    const float mx = fmaxf(fmaxf(max32(v[0]), max32(v[1])),
-                                           fmaxf(max32(v[2]), max32(v[3])));
-                    const float m_new = fmaxf(m_run, mx * p.scale_log2);
-                    const float z = (exp2_sum32(v[0], p.scale_log2, -m_new, nullptr) +
-                                     exp2_sum32(v[1], p.scale_log2, -m_new, nullptr)) +
-                                    (exp2_sum32(v[2], p.scale_log2, -m_new, nullptr) +
-                                     exp2_sum32(v[3], p.scale_log2, -m_new, nullptr));
-                    z_run = z_run * ex2(m_run - m_new) + z;
-                    m_run = m_new;
+                    rowstats_tile(tmem_base + ab * 128 + lane_off, (it.t_begin + i) * TC_ROWS, pos,
+                                  p.N, p.scale_log2, m_run, z_run);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
@@ -637,8 +709,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     tc_fence_after();
                     int g_cur = it.fixed_row0 / p.L_obs;
                     float acc_g = 0.f;
-                    colsum_rows(tmem_base + ab * 128 + lane_off, it.fixed_row0, rows_blk, key,
-                                mask_tile, lse_buf, s_base, g_cur, acc_g);
+                    colsum_rows(p, first_pos, tmem_base + ab * 128 + lane_off, it.fixed_row0,
+                                rows_blk, key, mask_tile, lse_buf, s_base, p.n_cols, key,
+                                key < p.n_cols, g_cur, acc_g);
                     if (key < p.n_cols) s_base[(size_t)g_cur * p.n_cols + key] = acc_g * p.col_mult;
                     tc_fence_before();
                     __syncwarp();
@@ -647,7 +720,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             } else {
                 if (it.n_tiles == 0) continue;
                 const int key = it.ktile * TC_ROWS + et;
-                const float *lse_g = p.row_lse2 + (size_t)it.pair * R;
+                const float *lse_g = p.row_lse2 + (size_t)it.pair * tp.n_mtiles * TC_ROWS;
                 const bool mask_tile = it.ktile * TC_ROWS + TC_ROWS - 1 > first_pos;
                 float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols;
                 int g_cur = it.t_begin * TC_ROWS / p.L_obs;   // head of the first row handled
@@ -656,7 +729,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 // this thread's row of the set's next row block, loaded one block ahead
                 auto lse_of = [&](int i) -> float {
                     const int r = (it.t_begin + i) * TC_ROWS + et;
-                    return (i < it.n_tiles && r < R) ? -lse_g[r] : 0.f;
+                    return (i < it.n_tiles && r < R) ? lse_g[r] : 0.f;
                 };
                 const int i_first = (int)(((set - g) % NSETS + NSETS) % NSETS);
                 float lse_next = lse_of(i_first);
@@ -674,8 +747,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     mbar_wait(bar_acc_full + 8 * ab, (int)(gg / TC_NACC) & 1, tp.dev_code);
                     tc_fence_after();
                     ++n_mine;
-                    colsum_rows(tmem_base + ab * 128 + lane_off, r0, min(TC_ROWS, R - r0), key,
-                                mask_tile, lse_buf, s_base, g_cur, acc_g);
+                    colsum_rows(p, first_pos, tmem_base + ab * 128 + lane_off, r0,
+                                min(TC_ROWS, R - r0), key, mask_tile, lse_buf, s_base, p.n_cols,
+                                key, key < p.n_cols, g_cur, acc_g);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * ab);
@@ -694,6 +768,388 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             }
             g += it.n_tiles;
             if (it.n_tiles > 0) ++k;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+}
+
+// ---- resident tile pairs ------------------------------------------------------------------------
+// For windows of many 128-row tiles (H2O's whole-prompt window) a work item keeps TWO resident
+// tiles, a pair of window-row tiles for the row statistics (MODE 0) or a pair of key tiles for
+// the column sums (MODE 1), and streams the other operand once for both: each streamed tile
+// feeds two products (A = resident tile e, B = streamed tile, so the accumulator lanes are rows
+// in MODE 0 and keys in MODE 1), which doubles the product time per streamed byte.  Each tile
+// has two accumulators in tensor memory (its products alternate between them).  The epilogue
+// has four sets of four warps (four warps per SM sub-partition: the exp2 sums of a product need
+// that many to keep the special-function unit busy, one or two warps leave it mostly idle on
+// latency); sets (e, 0) and (e, 1) take every product of resident tile e, one 64-column half
+// each (keys in MODE 0, window rows in MODE 1), and at the end of an item they merge their
+// partial row states or column sums through shared memory.  In a causal window the item lengths grow with
+// the tile index, so a block takes the resident pairs i and n - 1 - i of one (pair, chunk) as
+// one unit and every unit costs about the same.  MODE 1 streams window-row blocks with their
+// negated row log-sum-exp values (a 512-byte bulk copy per block into a ring of its own,
+// released by the epilogue warps once read).
+constexpr int TP_LSE_SLOTS = 8;
+constexpr int TP_THREADS = 576;     // TMA warp, MMA warp, four epilogue sets of four warps
+constexpr int TP_MAX_G = 8;         // MODE 1: query heads per KV head (shared-memory partials)
+
+template <int D>
+struct TpPlan {
+    static constexpr int SUBS = D / 64;
+    static constexpr int TILE_BYTES = SUBS * TC_SUB_BYTES;
+    static constexpr int NS_RAW = (196 * 1024 - 2 * TILE_BYTES) / TILE_BYTES;
+    static constexpr int NS = NS_RAW > 8 ? 8 : NS_RAW;       // streamed tiles in flight
+    static_assert(NS >= 3, "resident tile pairs need three streamed stages");
+    static constexpr int LSE_BYTES = TP_LSE_SLOTS * TC_ROWS * 4;
+    // MODE 0: [2 tiles][128 rows][2] (m, z); MODE 1: [4 sets][G][128 keys] partial sums
+    static constexpr int PART_BYTES = 4 * TP_MAX_G * TC_ROWS * 4;
+    static constexpr int BAR_BYTES = 8 * (2 + 2 * NS + 2 * TC_NACC + 2 * TP_LSE_SLOTS) + 16;
+    static constexpr int SMEM_USED =
+        1024 + (2 + NS) * TILE_BYTES + LSE_BYTES + PART_BYTES + BAR_BYTES;
+    static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
+    static_assert(SMEM <= 227 * 1024, "tile-pair plan exceeds shared memory");
+};
+
+struct TpItem {
+    int pair, chunk, fp;      // (batch, KV head) pair, key chunk (MODE 0), resident tile pair
+    int n_fix;                // resident tiles: 1 or 2
+    int s_begin, n_str;       // first streamed tile, streamed tiles
+    int lo0, hi0, lo1, hi1;   // set s takes the streamed tiles lo_s <= i < hi_s
+    __device__ __forceinline__ int lo(int s) const { return s ? lo1 : lo0; }
+    __device__ __forceinline__ int hi(int s) const { return s ? hi1 : hi0; }
+};
+
+// Units: (pair, chunk, su) for MODE 0, (pair, su) for MODE 1; unit su covers the resident pairs
+// su and n_fp - 1 - su (one of them when they coincide).
+__device__ __forceinline__ int tp_subitems(const TcParams &tp, int u)
+{
+    const int su = u % tp.n_sup;
+    return tp.n_fp - 1 - su != su ? 2 : 1;
+}
+
+template <int MODE>
+__device__ __forceinline__ TpItem tp_item(const TcParams &tp, int u, int sub)
+{
+    const ScoreParams &p = tp.sp;
+    const int R = p.G * p.L_obs;
+    const int first_pos = p.N - p.L_obs;
+    const int su = u % tp.n_sup;
+    TpItem it{};
+    it.fp = sub == 0 ? su : tp.n_fp - 1 - su;
+    if (MODE == 0) {
+        it.pair = u / (tp.n_sup * p.n_chunks);
+        it.chunk = (u / tp.n_sup) % p.n_chunks;
+        it.s_begin = it.chunk * tp.chunk_tiles;
+        it.n_fix = (2 * it.fp + 1) * TC_ROWS < R ? 2 : 1;
+        // keys the rows of tile s can see: up to the largest position among them
+        auto need = [&](int s) {
+            const int r_lo = (2 * it.fp + s) * TC_ROWS;
+            const int r_hi = min(r_lo + TC_ROWS, R) - 1;
+            const int w_hi = (r_lo / p.L_obs != r_hi / p.L_obs) ? p.L_obs - 1 : r_hi % p.L_obs;
+            const int kt_needed = (first_pos + w_hi) / TC_ROWS + 1;
+            return max(0, min(it.s_begin + tp.chunk_tiles, kt_needed) - it.s_begin);
+        };
+        it.lo0 = it.lo1 = 0;
+        it.hi0 = need(0);
+        it.hi1 = it.n_fix == 2 ? need(1) : 0;
+        it.n_str = max(it.hi0, it.hi1);
+    } else {
+        it.pair = u / tp.n_sup;
+        it.n_fix = 2 * it.fp + 1 < tp.n_col_tiles ? 2 : 1;
+        const int n_rb = (R + TC_ROWS - 1) / TC_ROWS;
+        // row blocks whose rows can see key tile s: positions >= its first key (rows are sorted
+        // by position when G = 1)
+        auto first_rb = [&](int s) {
+            const int k0 = (2 * it.fp + s) * TC_ROWS;
+            return (p.G == 1 && k0 > first_pos) ? (k0 - first_pos) / TC_ROWS : 0;
+        };
+        it.s_begin = first_rb(0);
+        it.n_str = n_rb - it.s_begin;
+        it.lo0 = 0;
+        it.hi0 = it.n_str;
+        it.lo1 = it.n_fix == 2 ? first_rb(1) - it.s_begin : 0;
+        it.hi1 = it.n_fix == 2 ? it.n_str : 0;
+    }
+    return it;
+}
+
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t cnt)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(cnt) : "memory");
+}
+
+__device__ __forceinline__ void pair_sync(int id)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// Persistent blocks take units u = blockIdx.x, blockIdx.x + gridDim.x, ...; the three roles walk
+// the same item sequence.  The resident pair has one buffer, reloaded per item once the item's
+// last products are done (the epilogue still drains its last products meanwhile).
+template <int D, int MODE>
+__global__ void __launch_bounds__(TP_THREADS, 1)
+tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const TcParams tp)
+{
+    using PL = TpPlan<D>;
+    constexpr int SUBS = PL::SUBS, TILE_BYTES = PL::TILE_BYTES, NS = PL::NS;
+    constexpr int KSTEPS = D / 16;
+    constexpr int LS = TP_LSE_SLOTS;
+    const ScoreParams &p = tp.sp;
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t fixed0 = base;                          // two resident tiles
+    const uint32_t stage0 = base + 2 * TILE_BYTES;         // NS streamed tiles
+    const uint32_t lse0 = stage0 + NS * TILE_BYTES;        // LS x 128 floats (MODE 1)
+    const uint32_t part0 = lse0 + PL::LSE_BYTES;           // the sets' partial states
+    const uint32_t bars = part0 + PL::PART_BYTES;
+    const uint32_t bar_fix_full = bars;
+    const uint32_t bar_fix_empty = bar_fix_full + 8;
+    const uint32_t bar_full = bar_fix_empty + 8;           // NS
+    const uint32_t bar_empty = bar_full + 8 * NS;          // NS
+    const uint32_t bar_acc_full = bar_empty + 8 * NS;      // TC_NACC
+    const uint32_t bar_acc_empty = bar_acc_full + 8 * TC_NACC;   // TC_NACC
+    const uint32_t bar_lse_full = bar_acc_empty + 8 * TC_NACC;   // LS
+    const uint32_t bar_lse_empty = bar_lse_full + 8 * LS;        // LS
+    const uint32_t tmem_slot = bar_lse_empty + 8 * LS;
+    const float *sm_lse = reinterpret_cast<const float *>(smem_raw + (lse0 - raw));
+    float *sm_part = reinterpret_cast<float *>(smem_raw + (part0 - raw));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int R = p.G * p.L_obs;
+    const int first_pos = p.N - p.L_obs;
+    const int C = gridDim.x;
+    const int lse_stride = tp.n_mtiles * TC_ROWS;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_fix_full, 1);
+        mbar_init(bar_fix_empty, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < TC_NACC; ++a) {
+            mbar_init(bar_acc_full + 8 * a, 1);
+            mbar_init(bar_acc_empty + 8 * a, 8);   // the eight warps of the tile's two sets
+        }
+        for (int l = 0; l < LS; ++l) {
+            mbar_init(bar_lse_full + 8 * l, 1);
+            mbar_init(bar_lse_empty + 8 * l, 16);  // the warps of the (two or four) sets reading it
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         tmem_slot),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    uint32_t tmem_base;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot));
+
+    if (warp == 0 && lane == 0) {
+        // ================================ TMA producer ============================================
+        long long g = 0;
+        int nrl = 0;
+        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+            const int nsub = tp_subitems(tp, u);
+            for (int sub = 0; sub < nsub; ++sub) {
+                const TpItem it = tp_item<MODE>(tp, u, sub);
+                if (it.n_str == 0) continue;
+                const int b = it.pair / p.Hkv, kh = it.pair % p.Hkv;
+                const int qrow_group = (b * p.Hq + kh * p.G) * p.L_obs;
+                if (nrl > 0) mbar_wait(bar_fix_empty, (nrl - 1) & 1, tp.dev_code);
+                mbar_arrive_expect_tx(bar_fix_full, it.n_fix * TILE_BYTES);
+                for (int f = 0; f < it.n_fix; ++f)
+                    for (int a = 0; a < SUBS; ++a) {
+                        const uint32_t dst = fixed0 + f * TILE_BYTES + a * TC_SUB_BYTES;
+                        if (MODE == 0)
+                            tma_load_2d(dst, &qmap, a * 64,
+                                        qrow_group + (2 * it.fp + f) * TC_ROWS, bar_fix_full);
+                        else
+                            tma_load_4d(dst, &kmap, a * 64, (2 * it.fp + f) * TC_ROWS, kh, b,
+                                        bar_fix_full);
+                    }
+                ++nrl;
+                for (int i = 0; i < it.n_str; ++i, ++g) {
+                    const int s = (int)(g % NS);
+                    if (g >= NS) mbar_wait(bar_empty + 8 * s, (int)((g / NS) - 1) & 1, tp.dev_code);
+                    const uint32_t dst = stage0 + s * TILE_BYTES;
+                    mbar_arrive_expect_tx(bar_full + 8 * s, TILE_BYTES);
+                    for (int a = 0; a < SUBS; ++a) {
+                        if (MODE == 0)
+                            tma_load_4d(dst + a * TC_SUB_BYTES, &kmap, a * 64,
+                                        (it.s_begin + i) * TC_ROWS, kh, b, bar_full + 8 * s);
+                        else
+                            tma_load_2d(dst + a * TC_SUB_BYTES, &qmap, a * 64,
+                                        qrow_group + (it.s_begin + i) * TC_ROWS, bar_full + 8 * s);
+                    }
+                    if (MODE == 1) {
+                        // the row block's negated log2-sum-exp values (padded rows are zero)
+                        const int l = (int)(g % LS);
+                        if (g >= LS)
+                            mbar_wait(bar_lse_empty + 8 * l, (int)((g / LS) - 1) & 1, tp.dev_code);
+                        mbar_arrive_expect_tx(bar_lse_full + 8 * l, TC_ROWS * 4);
+                        bulk_g2s(lse0 + l * TC_ROWS * 4,
+                                 p.row_lse2 + (size_t)it.pair * lse_stride +
+                                     (size_t)(it.s_begin + i) * TC_ROWS,
+                                 TC_ROWS * 4, bar_lse_full + 8 * l);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ================================ MMA issuer ==============================================
+        long long g = 0;
+        int nrl = 0;
+        int uses0 = 0, uses1 = 0;             // accumulator uses per set
+        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+            const int nsub = tp_subitems(tp, u);
+            for (int sub = 0; sub < nsub; ++sub) {
+                const TpItem it = tp_item<MODE>(tp, u, sub);
+                if (it.n_str == 0) continue;
+                mbar_wait(bar_fix_full, nrl & 1, tp.dev_code);
+                ++nrl;
+                for (int i = 0; i < it.n_str; ++i, ++g) {
+                    const int s = (int)(g % NS);
+                    mbar_wait(bar_full + 8 * s, (int)(g / NS) & 1, tp.dev_code);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (i < it.lo(e) || i >= it.hi(e)) continue;
+                        const int k = e ? uses1++ : uses0++;
+                        const int acc = 2 * (k & 1) + e;
+                        if (k >= 2)
+                            mbar_wait(bar_acc_empty + 8 * acc, ((k >> 1) - 1) & 1, tp.dev_code);
+                        tc_fence_after();
+                        const uint32_t a_base = fixed0 + e * TILE_BYTES;
+                        const uint32_t b_base = stage0 + s * TILE_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < KSTEPS; ++kk) {
+                            const uint32_t off = (kk >> 2) * TC_SUB_BYTES + (kk & 3) * 32;
+                            umma_bf16(tmem_base + acc * 128, sw128_desc(a_base + off),
+                                      sw128_desc(b_base + off), kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(bar_acc_full + 8 * acc);
+                    }
+                    umma_commit(bar_empty + 8 * s);   // streamed stage free once both products end
+                }
+                umma_commit(bar_fix_empty);           // resident pair free after the item
+            }
+        }
+    } else if (warp >= 2) {
+        // ================================ epilogue ================================================
+        const int sg = (warp - 2) / 4;            // set
+        const int e = sg & 1;                     // resident tile e of every item ...
+        const int h = sg >> 1;                    // ... columns 64 h .. 64 h + 63 of its products
+        const int q4 = warp & 3;                  // TMEM lanes 32*q4 .. 32*q4+31
+        const int et = q4 * 32 + lane;            // this thread's lane (row or key)
+        const uint32_t tcol = tmem_base + e * 128 + h * 64 + ((uint32_t)(q4 * 32) << 16);
+        const int bar_id = 1 + e * 4 + q4;        // the two sets of tile e, this lane quarter
+        long long g = 0;
+        int k = 0;                                // products of tile e so far
+        for (int u = blockIdx.x; u < tp.n_work; u += C) {
+            const int nsub = tp_subitems(tp, u);
+            for (int sub = 0; sub < nsub; ++sub) {
+                const TpItem it = tp_item<MODE>(tp, u, sub);
+                if (e >= it.n_fix) {
+                    g += it.n_str;
+                    continue;
+                }
+                const int b = it.pair / p.Hkv, kh = it.pair % p.Hkv;
+                if (MODE == 0) {
+                    const int r = (2 * it.fp + e) * TC_ROWS + et;   // window row of the group
+                    const bool row_ok = r < R;
+                    const int pos = row_ok ? row_pos(p, r) : -1;
+                    float m_run = kNegBig, z_run = 0.f;
+                    for (int i = it.lo(e); i < it.hi(e); ++i, ++k) {
+                        const int acc = 2 * (k & 1) + e;
+                        mbar_wait(bar_acc_full + 8 * acc, (k >> 1) & 1, tp.dev_code);
+                        tc_fence_after();
+                        rowstats_half_lazy(tcol + (k & 1) * 256, (it.s_begin + i) * TC_ROWS + h * 64,
+                                           pos, p.N, p.scale_log2, m_run, z_run);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_acc_empty + 8 * acc);
+                    }
+                    // the second set hands its rows' states to the first, which merges and
+                    // writes them (an empty state where no key tile of the chunk reaches a row)
+                    float *mz = sm_part + (e * TC_ROWS + et) * 2;
+                    if (h == 1) {
+                        mz[0] = m_run;
+                        mz[1] = z_run;
+                    }
+                    pair_sync(bar_id);
+                    if (h == 0 && row_ok) {
+                        const float m1 = mz[0], z1 = mz[1];
+                        const float M = fmaxf(m_run, m1);
+                        float *dst =
+                            p.row_ml + (((size_t)it.pair * p.n_chunks + it.chunk) * R + r) * 2;
+                        dst[0] = M;
+                        dst[1] = z_run * ex2(m_run - M) + z1 * ex2(m1 - M);
+                    }
+                    pair_sync(bar_id);
+                } else {
+                    const bool other = it.n_fix == 2;     // does tile 1 take part?
+                    const int kt = 2 * it.fp + e;
+                    const int key = kt * TC_ROWS + et;
+                    const bool mask_tile = kt * TC_ROWS + TC_ROWS - 1 > first_pos;
+                    // this set's per-head partial sums of its key: [G][128]
+                    float *part = sm_part + (size_t)sg * TP_MAX_G * TC_ROWS;
+                    for (int gq = 0; gq < p.G; ++gq) part[gq * TC_ROWS + et] = 0.f;
+                    int g_cur = -1;
+                    float acc_g = 0.f;
+                    for (int i = it.lo(e); i < it.hi(e); ++i, ++k) {
+                        const long long gg = g + i;
+                        const int l = (int)(gg % LS);
+                        const int acc = 2 * (k & 1) + e;
+                        const int r0 = (it.s_begin + i) * TC_ROWS + h * 64;   // this half's rows
+                        const int rows = min(64, R - r0);
+                        mbar_wait(bar_lse_full + 8 * l, (int)(gg / LS) & 1, tp.dev_code);
+                        mbar_wait(bar_acc_full + 8 * acc, (k >> 1) & 1, tp.dev_code);
+                        tc_fence_after();
+                        if (rows > 0) {
+                            if (g_cur < 0) g_cur = r0 / p.L_obs;
+                            colsum_rows<true>(p, first_pos, tcol + (k & 1) * 256, r0, rows, key,
+                                        mask_tile, sm_lse + l * TC_ROWS + h * 64, part, TC_ROWS,
+                                        et, true, g_cur, acc_g);
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(bar_acc_empty + 8 * acc);
+                            // tile 0 takes every row block: its set also releases the slot for
+                            // tile 1 where tile 1 does not take this block
+                            const bool alone = e == 0 && !(other && i >= it.lo1);
+                            mbar_arrive_cnt(bar_lse_empty + 8 * l, alone ? 2u : 1u);
+                        }
+                    }
+                    if (g_cur >= 0) part[g_cur * TC_ROWS + et] = acc_g * p.col_mult;
+                    pair_sync(bar_id);
+                    if (h == 0 && key < p.n_cols) {
+                        const float *part1 = sm_part + (size_t)(sg + 2) * TP_MAX_G * TC_ROWS;
+                        float *s_base = p.s_out + (size_t)(b * p.Hq + kh * p.G) * p.n_cols + key;
+                        for (int gq = 0; gq < p.G; ++gq)
+                            s_base[(size_t)gq * p.n_cols] =
+                                part[gq * TC_ROWS + et] + part1[gq * TC_ROWS + et];
+                    }
+                    pair_sync(bar_id);
+                }
+                g += it.n_str;
+            }
         }
     }
 
@@ -757,13 +1213,20 @@ bool encode_4d(CUtensorMap *m, const void *ptr, uint64_t d, uint64_t n, uint64_t
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Each row's negated log2-sum-exp from pass 1's per-chunk (max, sum) states, stored with the row
+// count rounded up to 128 per pair (whole row blocks for the bulk copies; the padding is zero).
 __global__ void rowlse_tc_kernel(const ScoreParams p)
 {
     const int R = p.G * p.L_obs;
+    const int Rp = (R + TC_ROWS - 1) / TC_ROWS * TC_ROWS;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (long long)p.B * p.Hkv * R) return;
-    const long long bkh = i / R;
-    const int r = (int)(i % R);
+    if (i >= (long long)p.B * p.Hkv * Rp) return;
+    const long long bkh = i / Rp;
+    const int r = (int)(i % Rp);
+    if (r >= R) {
+        p.row_lse2[i] = 0.f;
+        return;
+    }
     float M = kNegBig;
     for (int c = 0; c < p.n_chunks; ++c)
         M = fmaxf(M, p.row_ml[((bkh * p.n_chunks + c) * R + r) * 2]);
@@ -772,7 +1235,7 @@ __global__ void rowlse_tc_kernel(const ScoreParams p)
         const float *s = p.row_ml + ((bkh * p.n_chunks + c) * R + r) * 2;
         Z += s[1] * exp2f(s[0] - M);
     }
-    p.row_lse2[bkh * R + r] = M + log2f(Z);
+    p.row_lse2[i] = -(M + log2f(Z));
 }
 
 template <int D>
@@ -793,6 +1256,13 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
                 cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
             if (e != cudaSuccess) return e;
         }
+        if constexpr (D <= 128) {
+            for (auto kf : {tc_pair_kernel<D, 0>, tc_pair_kernel<D, 1>}) {
+                cudaError_t e = cudaFuncSetAttribute(
+                    kf, cudaFuncAttributeMaxDynamicSharedMemorySize, TpPlan<D>::SMEM);
+                if (e != cudaSuccess) return e;
+            }
+        }
         configured[dev] = true;
     }
     int n_sm = 152;
@@ -806,6 +1276,8 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     tp.n_col_tiles = (sp.n_cols + TC_ROWS - 1) / TC_ROWS;
     tp.col_chunks = 1;
     tp.col_chunk_tiles = tp.n_col_tiles;
+    tp.n_fp = 0;
+    tp.n_sup = 0;
     tp.dev_code = dev_code;
     // one persistent block per SM (at most one per work item); round-robin items with a single
     // resident buffer would stall the pipeline at every item, so each gets its own block there
@@ -819,7 +1291,20 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     // several key chunks per row tile: contiguous items share the resident tile (where that buys
     // streamed stages: with d_head 256 two stages is all that fits either way)
     constexpr bool kContigPays = TcPlan<D, true>::NS > TcPlan<D, false>::NS;
-    if (kContigPays && sp.n_chunks >= 2)
+    // windows of several row tiles (up to d_head 128, where two resident tiles and three
+    // streamed stages fit): resident row-tile pairs
+    constexpr bool kPairs = D <= 128;
+    if (kPairs && tp.n_mtiles >= 2) {
+        if constexpr (kPairs) {
+            tp.n_fp = (tp.n_mtiles + 1) / 2;
+            tp.n_sup = (tp.n_fp + 1) / 2;
+            const long long work = pairs * sp.n_chunks * tp.n_sup;
+            if (work > 0x7fffffffLL) return cudaErrorInvalidValue;
+            tp.n_work = (int)work;
+            tc_pair_kernel<D, 0><<<(unsigned)(work < n_sm ? work : n_sm), TP_THREADS,
+                                   TpPlan<D>::SMEM, stream>>>(qm, km, tp);
+        }
+    } else if (kContigPays && sp.n_chunks >= 2)
         tc_scores_kernel<D, 0, true><<<grid(work0, true), TC_THREADS, SMEM, stream>>>(qm, km, tp);
     else
         tc_scores_kernel<D, 0, false><<<grid(work0, false), TC_THREADS, SMEM, stream>>>(qm, km, tp);
@@ -830,7 +1315,7 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
     // the column pass with resident rows folds each row's chunk states itself; with streamed
     // rows (or no column pass) the row log-sum-exp values are written first
     if (!rows_resident || tp.n_col_tiles == 0) {
-        const long long rows = pairs * R;
+        const long long rows = pairs * n_rb * TC_ROWS;
         rowlse_tc_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(sp);
         e = cudaGetLastError();
         if (e != cudaSuccess || tp.n_col_tiles == 0) return e;
@@ -851,6 +1336,16 @@ cudaError_t launch_tc_typed(const ScoreParams &sp, const CUtensorMap &qm, const 
         else
             tc_scores_kernel<D, 2, false><<<grid(work2, false), TC_THREADS, SMEM, stream>>>(qm, km,
                                                                                            tp);
+    } else if (kPairs && sp.G <= TP_MAX_G) {
+        // stream the row blocks past resident key-tile pairs
+        tp.n_fp = (tp.n_col_tiles + 1) / 2;
+        tp.n_sup = (tp.n_fp + 1) / 2;
+        const long long work = pairs * tp.n_sup;
+        if (work > 0x7fffffffLL) return cudaErrorInvalidValue;
+        tp.n_work = (int)work;
+        if constexpr (kPairs)
+            tc_pair_kernel<D, 1><<<(unsigned)(work < n_sm ? work : n_sm), TP_THREADS,
+                                   TpPlan<D>::SMEM, stream>>>(qm, km, tp);
     } else {
         const long long work1 = pairs * tp.n_col_tiles;
         if (work1 > 0x7fffffffLL) return cudaErrorInvalidValue;
