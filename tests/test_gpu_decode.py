@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, assert_close, assert_rel, cuda_or_skip, f64, lib
+from gpu_helpers import TOL, TOL_SPLIT_P, assert_close, assert_rel, cuda_or_skip, f64, lib
 from kv_cache_compression_kvc_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -50,7 +50,10 @@ def test_decode_matches_oracle_ragged(dtype, D, G):
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
     assert torch.equal(torch.nan_to_num(logits, 7.0), torch.nan_to_num(lg2, 7.0))
     ref, ref_lg, ref_lse = _oracle_decode(q, K, V, lens.cpu().numpy(), scale, G)
-    assert_close(out.cpu(), ref, TOL[dtype], "decode out")
+    # grouped bf16 heads run on the tensor cores (split-P product): the recorded bound there
+    err = assert_close(out.cpu(), ref, TOL_SPLIT_P if dtype == torch.bfloat16 and G >= 2
+                       else TOL[dtype], "decode out")
+    print(f"decode {dtype} D={D} G={G}: max abs error {err:.2e}")
     assert_close(lse.cpu(), ref_lse, 1e-4, "lse")
     lg = logits.cpu().numpy()
     for (b, h), r in ref_lg.items():
