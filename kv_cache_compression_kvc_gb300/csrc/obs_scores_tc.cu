@@ -213,6 +213,17 @@ __device__ __forceinline__ float max32(const float *x)
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
 
+// Before a block exits, its producer waits (bounded) for the last phase of each of the n ring
+// barriers it armed (`used` loads in all, load j on barrier j % n): in normal operation those
+// phases have long completed, but after a wait somewhere in the block ran out a copy could
+// otherwise still be writing into shared memory when the block exits.
+__device__ __forceinline__ void drain_loads(uint32_t bars, int n, long long used, int32_t *code)
+{
+    for (long long j = used > n ? used - n : 0; j < used; ++j)
+        if (!mbar_wait_ok(bars + 8 * (uint32_t)(j % n), (uint32_t)((j / n) & 1), kMbarSpinLimit))
+            record_code(code, kDevCodeTimeout);
+}
+
 // Named barriers: 1 over every epilogue warp that takes part (128 threads per set), 2 + set
 // over the four warps of one set.
 __device__ __forceinline__ void epilogue_sync(int nsets)
@@ -433,7 +444,7 @@ struct TcPlan {
     static constexpr int NS_CAP = CONTIG ? 8 : 4;
     static constexpr int NS = NS_RAW > NS_CAP ? NS_CAP : NS_RAW;   // streamed tiles in flight
     static_assert(NS >= 2, "tensor-core scoring needs two operand stages");
-    static constexpr int BAR_BYTES = 8 * (2 * NFIX + 2 * NS + 2 * TC_NACC) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 * NFIX + 2 * NS + 2 * TC_NACC + 2) + 16;
     static constexpr int SMEM_USED = 1024 + (NFIX + NS) * TILE_BYTES + BAR_BYTES +
                                      4 * TC_ROWS * 4 + 2 * TC_ROWS * 2 * 4 + 64;
     // every block allocates all of tensor memory: one block per SM, so at least half the SM's
@@ -474,7 +485,8 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const uint32_t bar_empty = bar_full + 8 * NS;         // NS
     const uint32_t bar_acc_full = bar_empty + 8 * NS;     // TC_NACC
     const uint32_t bar_acc_empty = bar_acc_full + 8 * TC_NACC;   // TC_NACC
-    const uint32_t tmem_slot = bar_acc_empty + 8 * TC_NACC;      // u32 written by tcgen05.alloc
+    const uint32_t bar_done = bar_acc_empty + 8 * TC_NACC;       // the MMA thread's last commit
+    const uint32_t tmem_slot = bar_done + 16;                    // u32 written by tcgen05.alloc
     float *sm_lse = reinterpret_cast<float *>(smem_raw + (tmem_slot + 16 - raw));   // [4][128]
     float *sm_mz = sm_lse + 4 * TC_ROWS;                  // [2][128][2] second set's states
 
@@ -505,6 +517,7 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             mbar_init(bar_acc_full + 8 * a, 1);
             mbar_init(bar_acc_empty + 8 * a, 4);   // the four warps of the set owning it
         }
+        mbar_init(bar_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -570,6 +583,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 }
             }
         }
+        // the last loads have landed before the block exits (see drain_loads)
+        drain_loads(bar_full, NS, g, tp.dev_code);
+        drain_loads(bar_fix_full, NFIX, nrl, tp.dev_code);
     } else if (warp == 1 && lane == 0) {
         // ================================ MMA issuer ==============================================
         long long g = 0;
@@ -617,6 +633,9 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             }
             if (next_id != -1 && next_id != id) umma_commit(bar_fix_empty + 8 * f);
         }
+        // every product issued has completed before the block frees tensor memory and exits
+        umma_commit(bar_done);
+        mbar_wait(bar_done, 0, tp.dev_code);
     } else if (warp >= 2 && (warp - 2) / 4 < NSETS) {
         // ================================ epilogue ================================================
         const int set = (warp - 2) / 4;           // global tiles g with g % NSETS == set
@@ -810,7 +829,7 @@ struct TpPlan {
     static constexpr int LSE_BYTES = TP_LSE_SLOTS * TC_ROWS * 4;
     // MODE 0: [2 tiles][128 rows][2] (m, z); MODE 1: [4 sets][G][128 keys] partial sums
     static constexpr int PART_BYTES = 4 * TP_MAX_G * TC_ROWS * 4;
-    static constexpr int BAR_BYTES = 8 * (2 + 2 * NS + 2 * TC_NACC + 2 * TP_LSE_SLOTS) + 16;
+    static constexpr int BAR_BYTES = 8 * (2 + 2 * NS + 2 * TC_NACC + 2 * TP_LSE_SLOTS + 2) + 16;
     static constexpr int SMEM_USED =
         1024 + (2 + NS) * TILE_BYTES + LSE_BYTES + PART_BYTES + BAR_BYTES;
     static constexpr int SMEM = SMEM_USED > 116 * 1024 ? SMEM_USED : 116 * 1024;
@@ -920,7 +939,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const uint32_t bar_acc_empty = bar_acc_full + 8 * TC_NACC;   // TC_NACC
     const uint32_t bar_lse_full = bar_acc_empty + 8 * TC_NACC;   // LS
     const uint32_t bar_lse_empty = bar_lse_full + 8 * LS;        // LS
-    const uint32_t tmem_slot = bar_lse_empty + 8 * LS;
+    const uint32_t bar_done = bar_lse_empty + 8 * LS;      // the MMA thread's last commit
+    const uint32_t tmem_slot = bar_done + 16;
     const float *sm_lse = reinterpret_cast<const float *>(smem_raw + (lse0 - raw));
     float *sm_part = reinterpret_cast<float *>(smem_raw + (part0 - raw));
 
@@ -946,6 +966,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(bar_lse_full + 8 * l, 1);
             mbar_init(bar_lse_empty + 8 * l, 16);  // the warps of the (two or four) sets reading it
         }
+        mbar_init(bar_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -1012,6 +1033,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
             }
         }
+        // the last loads have landed before the block exits (see drain_loads)
+        drain_loads(bar_full, NS, g, tp.dev_code);
+        drain_loads(bar_fix_full, 1, nrl, tp.dev_code);
+        if (MODE == 1) drain_loads(bar_lse_full, LS, g, tp.dev_code);
     } else if (warp == 1 && lane == 0) {
         // ================================ MMA issuer ==============================================
         long long g = 0;
@@ -1050,6 +1075,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 umma_commit(bar_fix_empty);           // resident pair free after the item
             }
         }
+        // every product issued has completed before the block frees tensor memory and exits
+        umma_commit(bar_done);
+        mbar_wait(bar_done, 0, tp.dev_code);
     } else if (warp >= 2) {
         // ================================ epilogue ================================================
         const int sg = (warp - 2) / 4;            // set
