@@ -1149,7 +1149,18 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         mbar_wait(bar_lse_full + 8 * l, (int)(gg / LS) & 1, tp.dev_code);
                         mbar_wait(bar_acc_full + 8 * acc, (k >> 1) & 1, tp.dev_code);
                         tc_fence_after();
-                        if (rows > 0) {
+                        // (warp-uniform: the tensor-memory loads below are .sync.aligned)
+                        if (p.G == 1 && rows == 64 &&
+                            __all_sync(0xffffffffu, key <= first_pos + r0)) {
+                            // one head, and every row of this half sees every key of the warp:
+                            // the 64 rows' probabilities summed with no head or mask bookkeeping
+                            float v[2][32];
+                            tmem_ld64(tcol + (k & 1) * 256, v);
+                            const float *nl = sm_lse + l * TC_ROWS + h * 64;
+                            acc_g += exp2_sum32(v[0], p.scale_log2, 0.f, nl) +
+                                     exp2_sum32(v[1], p.scale_log2, 0.f, nl + 32);
+                            g_cur = 0;
+                        } else if (rows > 0) {
                             if (g_cur < 0) g_cur = r0 / p.L_obs;
                             colsum_rows<true>(p, first_pos, tcol + (k & 1) * 256, r0, rows, key,
                                         mask_tile, sm_lse + l * TC_ROWS + h * 64, part, TC_ROWS,
