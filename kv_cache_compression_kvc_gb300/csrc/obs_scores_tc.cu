@@ -213,10 +213,14 @@ __device__ __forceinline__ float max32(const float *x)
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
 
-// Before a block exits, its producer waits (bounded) for the last phase of each of the n ring
-// barriers it armed (`used` loads in all, load j on barrier j % n): in normal operation those
-// phases have long completed, but after a wait somewhere in the block ran out a copy could
-// otherwise still be writing into shared memory when the block exits.
+// After a wait ran out (the device code is set), a block's producer waits (bounded) for the last
+// phase of each of the n ring barriers it armed (`used` loads in all, load j on barrier j % n),
+// so that no copy is still writing into shared memory when the block exits.  In normal
+// operation nothing is waited for: the drain is skipped.
+__device__ __forceinline__ bool timeout_recorded(const int32_t *code)
+{
+    return code != nullptr && *reinterpret_cast<const volatile int32_t *>(code) != 0;
+}
 __device__ __forceinline__ void drain_loads(uint32_t bars, int n, long long used, int32_t *code)
 {
     for (long long j = used > n ? used - n : 0; j < used; ++j)
@@ -533,6 +537,8 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     uint32_t tmem_base;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot));
 
+    long long loads_streamed = 0;               // the producer's counts (for the drain)
+    int loads_fixed = 0;
     if (warp == 0 && lane == 0) {
         // ================================ TMA producer ============================================
         long long g = 0;                            // streamed tiles so far
@@ -583,9 +589,8 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 }
             }
         }
-        // the last loads have landed before the block exits (see drain_loads)
-        drain_loads(bar_full, NS, g, tp.dev_code);
-        drain_loads(bar_fix_full, NFIX, nrl, tp.dev_code);
+        loads_streamed = g;
+        loads_fixed = nrl;
     } else if (warp == 1 && lane == 0) {
         // ================================ MMA issuer ==============================================
         long long g = 0;
@@ -633,9 +638,6 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             }
             if (next_id != -1 && next_id != id) umma_commit(bar_fix_empty + 8 * f);
         }
-        // every product issued has completed before the block frees tensor memory and exits
-        umma_commit(bar_done);
-        mbar_wait(bar_done, 0, tp.dev_code);
     } else if (warp >= 2 && (warp - 2) / 4 < NSETS) {
         // ================================ epilogue ================================================
         const int set = (warp - 2) / 4;           // global tiles g with g % NSETS == set
@@ -791,6 +793,18 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     }
 
     tc_fence_before();
+    __syncthreads();
+    // after a wait ran out: the last loads have landed and every product issued has completed
+    // before the block frees tensor memory and exits
+    if ((threadIdx.x == 0 || threadIdx.x == 32) && timeout_recorded(tp.dev_code)) {
+        if (threadIdx.x == 0) {
+            drain_loads(bar_full, NS, loads_streamed, tp.dev_code);
+            drain_loads(bar_fix_full, NFIX, loads_fixed, tp.dev_code);
+        } else {
+            umma_commit(bar_done);
+            mbar_wait(bar_done, 0, tp.dev_code);
+        }
+    }
     __syncthreads();
     tc_fence_after();
     if (warp == 1)
@@ -982,6 +996,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint32_t tmem_base;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot));
 
+    long long loads_streamed = 0;               // the producer's counts (for the drain)
+    int loads_fixed = 0;
     if (warp == 0 && lane == 0) {
         // ================================ TMA producer ============================================
         long long g = 0;
@@ -1033,10 +1049,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
             }
         }
-        // the last loads have landed before the block exits (see drain_loads)
-        drain_loads(bar_full, NS, g, tp.dev_code);
-        drain_loads(bar_fix_full, 1, nrl, tp.dev_code);
-        if (MODE == 1) drain_loads(bar_lse_full, LS, g, tp.dev_code);
+        loads_streamed = g;
+        loads_fixed = nrl;
     } else if (warp == 1 && lane == 0) {
         // ================================ MMA issuer ==============================================
         long long g = 0;
@@ -1075,9 +1089,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 umma_commit(bar_fix_empty);           // resident pair free after the item
             }
         }
-        // every product issued has completed before the block frees tensor memory and exits
-        umma_commit(bar_done);
-        mbar_wait(bar_done, 0, tp.dev_code);
     } else if (warp >= 2) {
         // ================================ epilogue ================================================
         const int sg = (warp - 2) / 4;            // set
@@ -1193,6 +1204,19 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
 
     tc_fence_before();
+    __syncthreads();
+    // after a wait ran out: the last loads have landed and every product issued has completed
+    // before the block frees tensor memory and exits
+    if ((threadIdx.x == 0 || threadIdx.x == 32) && timeout_recorded(tp.dev_code)) {
+        if (threadIdx.x == 0) {
+            drain_loads(bar_full, NS, loads_streamed, tp.dev_code);
+            drain_loads(bar_fix_full, 1, loads_fixed, tp.dev_code);
+            if (MODE == 1) drain_loads(bar_lse_full, LS, loads_streamed, tp.dev_code);
+        } else {
+            umma_commit(bar_done);
+            mbar_wait(bar_done, 0, tp.dev_code);
+        }
+    }
     __syncthreads();
     tc_fence_after();
     if (warp == 1)
