@@ -91,6 +91,17 @@ def test_snapkv_full_size_layer():
     Vc = torch.empty_like(Kc)
     lens = torch.zeros(B * Hkv, dtype=torch.int32, device=dev)
     kvc.kvc_compact_gather(k, v, idx, w.budget, Kc, Vc, len_dst=lens)
+    assert kvc.kvc_device_status() == 0
+    # compaction at full size, bit-exact: every pair's retained rows, in index order, and its
+    # length
+    assert lens.tolist() == [w.budget] * (B * Hkv)
+    sel = idx.long()
+    for b in range(B):
+        for h in range(Hkv):
+            assert torch.equal(Kc[b, h, :w.budget], k[b, h].index_select(0, sel[b, h])), \
+                f"compacted K ({b},{h})"
+            assert torch.equal(Vc[b, h, :w.budget], v[b, h].index_select(0, sel[b, h])), \
+                f"compacted V ({b},{h})"
     qs, ks, vs = I.decode_qkv(B, w.n_heads_q, Hkv, D, 2, w.seed, dev, w.dtype)
     ws = kvc.decode_workspace(B, w.n_heads_q, Hkv, D, cap, dev)
     worst = 0.0
