@@ -253,3 +253,18 @@ def test_workspace_queries_of_the_added_entry_points(kvc):
     assert kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, kvc.KVC_F32) > gqa
     assert kvc.kvc_h2o_prefill_gqa_workspace_bytes(B, Hkv, D, N, 7) == 0
     assert kvc.kvc_decode_attn_duo_workspace_bytes(1, 32, 32, 128, 100, 33) == 0
+
+
+@pytest.mark.parametrize("B,H,N", [(16, 32, 4096), (2, 3, 333), (1, 1, 129), (1, 2, 128)])
+def test_scoring_workspace_holds_whole_row_blocks(kvc, B, H, N):
+    """Host sizing of the prompt scoring: besides the column sums and at least one (max, sum)
+    state per window row, the workspace holds every row's log-sum-exp padded to whole 128-row
+    blocks (the column pass streams those values one 512-byte block at a time)."""
+    rows_padded = (N + 127) // 128 * 128
+    need = B * H * (N + 2 * N + rows_padded) * 4
+    assert kvc.kvc_h2o_prefill_workspace_bytes(B, H, 128, N) >= need
+    G, L_obs = 4, 64
+    if N > L_obs:
+        R = G * L_obs
+        need_s = B * H * ((N - L_obs) * (G + 1) + 2 * R + (R + 127) // 128 * 128) * 4
+        assert kvc.kvc_snapkv_select_workspace_bytes(B, H * G, H, 128, N, L_obs) >= need_s
