@@ -303,11 +303,13 @@ def test_h2o_bf16_ragged():
     _h2o_run(2, 3, 333, 128, 70, 35, 40, torch.bfloat16, 4321, kvc, dev, check_every=3)
 
 
-def test_h2o_bf16_multi_tile_prompt():
-    """A prompt of several 128-row tiles: causal row and column tiles on the tensor cores."""
+@pytest.mark.parametrize("D", [64, 128])
+def test_h2o_bf16_multi_tile_prompt(D):
+    """A prompt of several 128-row tiles: causal row and column tiles on the tensor cores
+    (resident tile pairs; at d_head 64 one 64-column sub-tile per tile)."""
     dev = cuda_or_skip()
     kvc = lib()
-    _h2o_run(1, 2, 700, 128, 200, 100, 6, torch.bfloat16, 987, kvc, dev, check_every=2)
+    _h2o_run(1, 2, 700, D, 200, 100, 6, torch.bfloat16, 987, kvc, dev, check_every=2)
 
 
 def test_h2o_evict_candidates_and_no_candidate_code():
