@@ -256,7 +256,7 @@ __device__ __forceinline__ void colsum_rows(const ScoreParams &p, int first_pos,
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         if (c * 32 >= rows_blk) break;
-        // 64 columns per tensor-memory read (one wait for two chunks)
+        // LD32: 32 columns per tensor-memory read; otherwise 64 (one wait for two chunks)
         if (LD32) {
             tmem_ld32_async(tcol + c * 32, vt[0]);
             tmem_wait_ld();
@@ -824,11 +824,11 @@ tc_scores_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 // that many to keep the special-function unit busy, one or two warps leave it mostly idle on
 // latency); sets (e, 0) and (e, 1) take every product of resident tile e, one 64-column half
 // each (keys in MODE 0, window rows in MODE 1), and at the end of an item they merge their
-// partial row states or column sums through shared memory.  In a causal window the item lengths grow with
-// the tile index, so a block takes the resident pairs i and n - 1 - i of one (pair, chunk) as
-// one unit and every unit costs about the same.  MODE 1 streams window-row blocks with their
-// negated row log-sum-exp values (a 512-byte bulk copy per block into a ring of its own,
-// released by the epilogue warps once read).
+// partial row states or column sums through shared memory.  In a causal window the item
+// lengths grow with the tile index, so a block takes the resident pairs i and n - 1 - i of one
+// (pair, chunk) as one unit and every unit costs about the same.  MODE 1 streams window-row
+// blocks with their negated row log-sum-exp values (a 512-byte bulk copy per block into a ring
+// of its own, released by the epilogue warps once read).
 constexpr int TP_LSE_SLOTS = 8;
 constexpr int TP_THREADS = 576;     // TMA warp, MMA warp, four epilogue sets of four warps
 constexpr int TP_MAX_G = 8;         // MODE 1: query heads per KV head (shared-memory partials)
